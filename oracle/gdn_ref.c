@@ -1,0 +1,175 @@
+/*
+ * Oracle: token-by-token fp64 gated delta rule (TEST INFRASTRUCTURE ONLY).
+ *
+ * Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline and
+ * reference legs may load this file's library. The CUDA path never links,
+ * includes or calls it, and it shares no code with the CUDA path.
+ *
+ * What it computes, per sequence n and value head hv (key head h = hv / HG,
+ * HG = Hv / H, the grouping of "Optimizing GDN Chunk Prefill on Intel AMX
+ * CPU", section 4):
+ *
+ *   S (dk x dv, one row per key dimension, fp64) = initial_state[n,hv]^T or 0
+ *   for each token t of sequence n:
+ *       alpha = exp(g[t,hv])                              decay
+ *       pred  = alpha * S^T k_t                           what S predicts for k_t
+ *       S     = alpha * S + beta[t,hv] * k_t (v_t - pred)^T   write the correction
+ *       o_t   = scale * S^T q_t                           read with the updated S
+ *   final_state[n,hv] = S^T
+ *
+ * This is the per-token update described in "Chunking Qwen3.5's gated
+ * DeltaNet for 1.5x faster prefill on Apple Silicon" (section "What is the
+ * gated delta rule in Qwen3.5?": decay, correction from the state's
+ * prediction for the key, write-back, read), with the state held as
+ * [dv, dk] at the boundary exactly as the AMX note's section 9 describes
+ * ("CPU / Triton-facing state: [N, Hv, V, K]"); the transpose here is the
+ * same layout bridge its tests use.
+ *
+ * Optional q/k L2 normalisation (AMX note, section 7): x / sqrt(sum x^2 + eps),
+ * done in fp64 before the recurrence. scale <= 0 or NaN means 1/sqrt(dk).
+ * cu_seqlens == NULL means one sequence covering all T rows. Rows outside
+ * [cu_seqlens[0], cu_seqlens[N]) are left untouched in out.
+ *
+ * Plain C11, no SIMD intrinsics, no fast-math. OpenMP is used only across
+ * independent (sequence, value head) lanes; each lane's arithmetic is serial
+ * and in a fixed order, so results do not depend on the thread count.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define GDN_REF_OK 0
+#define GDN_REF_BAD_ARG (-1)
+#define GDN_REF_NO_MEMORY (-2)
+
+static void l2_normalise(const double* x, double* y, int64_t d, double eps) {
+  double ss = 0.0;
+  for (int64_t i = 0; i < d; ++i) ss += x[i] * x[i];
+  double r = 1.0 / sqrt(ss + eps);
+  for (int64_t i = 0; i < d; ++i) y[i] = x[i] * r;
+}
+
+/* One (sequence, value-head) lane. S is dk x dv, row-major (S[i*dv + j]). */
+static void run_lane(int64_t t0, int64_t t1, int64_t H, int64_t Hv, int64_t dk,
+                     int64_t dv, int64_t h, int64_t hv, const double* q,
+                     const double* k, const double* v, const double* g,
+                     const double* beta, double scale, int qk_l2norm,
+                     double eps, double* S, double* pred, double* kt,
+                     double* qt, double* out) {
+  for (int64_t t = t0; t < t1; ++t) {
+    const double* kraw = k + (t * H + h) * dk;
+    const double* qraw = q + (t * H + h) * dk;
+    if (qk_l2norm) {
+      l2_normalise(kraw, kt, dk, eps);
+      l2_normalise(qraw, qt, dk, eps);
+    } else {
+      memcpy(kt, kraw, (size_t)dk * sizeof(double));
+      memcpy(qt, qraw, (size_t)dk * sizeof(double));
+    }
+    const double alpha = exp(g[t * Hv + hv]);
+    const double b = beta[t * Hv + hv];
+    const double* vt = v + (t * Hv + hv) * dv;
+
+    /* pred = alpha * S^T k */
+    for (int64_t j = 0; j < dv; ++j) pred[j] = 0.0;
+    for (int64_t i = 0; i < dk; ++i) {
+      const double ki = kt[i];
+      const double* Si = S + i * dv;
+      for (int64_t j = 0; j < dv; ++j) pred[j] += Si[j] * ki;
+    }
+    for (int64_t j = 0; j < dv; ++j) pred[j] *= alpha;
+
+    /* S = alpha * S + beta * k (v - pred)^T */
+    for (int64_t i = 0; i < dk; ++i) {
+      const double bki = b * kt[i];
+      double* Si = S + i * dv;
+      for (int64_t j = 0; j < dv; ++j) Si[j] = alpha * Si[j] + bki * (vt[j] - pred[j]);
+    }
+
+    /* o = scale * S^T q (after the update) */
+    double* ot = out + (t * Hv + hv) * dv;
+    for (int64_t j = 0; j < dv; ++j) ot[j] = 0.0;
+    for (int64_t i = 0; i < dk; ++i) {
+      const double qi = qt[i];
+      const double* Si = S + i * dv;
+      for (int64_t j = 0; j < dv; ++j) ot[j] += Si[j] * qi;
+    }
+    for (int64_t j = 0; j < dv; ++j) ot[j] *= scale;
+  }
+}
+
+int gdn_ref_forward(int64_t T, int64_t N, int64_t H, int64_t Hv, int64_t dk,
+                    int64_t dv, const double* q, const double* k,
+                    const double* v, const double* g, const double* beta,
+                    double scale, const double* initial_state,
+                    const int64_t* cu_seqlens, int qk_l2norm, double eps,
+                    double* out, double* final_state, int nthreads) {
+  if (T < 0 || N < 1 || H < 1 || Hv < 1 || dk < 1 || dv < 1) return GDN_REF_BAD_ARG;
+  if (Hv % H != 0) return GDN_REF_BAD_ARG;
+  if (!q || !k || !v || !g || !beta || !out) return GDN_REF_BAD_ARG;
+  if (!cu_seqlens && N != 1) return GDN_REF_BAD_ARG;
+  if (cu_seqlens) {
+    for (int64_t n = 0; n < N; ++n)
+      if (cu_seqlens[n] < 0 || cu_seqlens[n + 1] < cu_seqlens[n] || cu_seqlens[n + 1] > T)
+        return GDN_REF_BAD_ARG;
+  }
+  if (!(scale > 0.0)) scale = 1.0 / sqrt((double)dk); /* also catches NaN */
+  const int64_t HG = Hv / H;
+  const int64_t lanes = N * Hv;
+  int rc = GDN_REF_OK;
+
+#ifdef _OPENMP
+  if (nthreads < 1) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+  {
+    double* S = (double*)malloc((size_t)(dk * dv) * sizeof(double));
+    double* pred = (double*)malloc((size_t)dv * sizeof(double));
+    double* kt = (double*)malloc((size_t)dk * sizeof(double));
+    double* qt = (double*)malloc((size_t)dk * sizeof(double));
+    int ok = S && pred && kt && qt;
+    if (!ok) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      rc = GDN_REF_NO_MEMORY;
+    }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t lane = 0; lane < lanes; ++lane) {
+      if (!ok) continue;
+      const int64_t n = lane / Hv, hv = lane % Hv, h = hv / HG;
+      const int64_t t0 = cu_seqlens ? cu_seqlens[n] : 0;
+      const int64_t t1 = cu_seqlens ? cu_seqlens[n + 1] : T;
+      /* boundary layout [dv, dk] -> working layout [dk, dv] */
+      for (int64_t i = 0; i < dk; ++i)
+        for (int64_t j = 0; j < dv; ++j)
+          S[i * dv + j] = initial_state ? initial_state[((n * Hv + hv) * dv + j) * dk + i] : 0.0;
+      run_lane(t0, t1, H, Hv, dk, dv, h, hv, q, k, v, g, beta, scale, qk_l2norm, eps,
+               S, pred, kt, qt, out);
+      if (final_state)
+        for (int64_t i = 0; i < dk; ++i)
+          for (int64_t j = 0; j < dv; ++j)
+            final_state[((n * Hv + hv) * dv + j) * dk + i] = S[i * dv + j];
+    }
+    free(S);
+    free(pred);
+    free(kt);
+    free(qt);
+  }
+  return rc;
+}
+
+/* Threads the OpenMP runtime would use by default (1 without OpenMP). */
+int gdn_ref_max_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}

@@ -1,0 +1,51 @@
+"""The pins are strong enough: each plausible mistake planted in a copy of the
+C oracle (a dropped term, a wrong sign, index or layout) fails at least one pin.
+
+The mutants are compiled from a textual edit of oracle/gdn_ref.c into a
+temporary directory; the committed oracle is never modified.
+"""
+import os
+
+import pytest
+
+import oracle
+import oracle_pins as P
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "gdn_ref.c")
+
+MUTANTS = {
+    "pred_without_decay": ("pred[j] *= alpha;", "pred[j] *= 1.0;"),
+    "correction_sign": ("(vt[j] - pred[j])", "(vt[j] + pred[j])"),
+    "no_write_term": ("alpha * Si[j] + bki * (vt[j] - pred[j])", "alpha * Si[j]"),
+    "beta_dropped": ("const double bki = b * kt[i];", "const double bki = kt[i];"),
+    "decay_sign": ("exp(g[t * Hv + hv])", "exp(-g[t * Hv + hv])"),
+    "no_scale": ("ot[j] *= scale;", "ot[j] *= 1.0;"),
+    "gqa_modulo": ("h = hv / HG;", "h = hv % H;"),
+    "initial_state_transposed": ("initial_state[((n * Hv + hv) * dv + j) * dk + i]",
+                                 "initial_state[((n * Hv + hv) * dk + i) * dv + j]"),
+    "final_state_transposed": ("final_state[((n * Hv + hv) * dv + j) * dk + i]",
+                               "final_state[((n * Hv + hv) * dk + i) * dv + j]"),
+    "read_uses_query_of_key": ("ot[j] += Si[j] * qi;", "ot[j] += Si[j] * kt[i];"),
+    "decay_not_applied_to_state": ("Si[j] = alpha * Si[j] +", "Si[j] = Si[j] +"),
+    "l2norm_without_sqrt": ("1.0 / sqrt(ss + eps)", "1.0 / (ss + eps)"),
+    "default_scale_wrong": ("scale = 1.0 / sqrt((double)dk)", "scale = 1.0 / (double)dk"),
+    "sequence_start_ignored": ("cu_seqlens ? cu_seqlens[n] : 0", "0"),
+}
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_mutant_is_caught(name, tmp_path):
+    before, after = MUTANTS[name]
+    with open(SRC) as f:
+        text = f.read()
+    assert text.count(before) == 1, f"mutation site for {name} not unique"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(before, after))
+    lib = oracle.load_library(oracle.compile_library(str(src), str(tmp_path / "libm.so")))
+    failed = []
+    for pin in P.ALL_PINS:
+        try:
+            pin(lib)
+        except (AssertionError, ValueError):
+            failed.append(pin.__name__)
+    assert failed, f"no pin catches mutant {name}"
