@@ -1,0 +1,402 @@
+#!/usr/bin/env python
+"""Benchmark of the chunked gated-delta-rule prefill forward on one GB300.
+
+One step = one gdn_chunk_fwd call (chunk-table builder, intra-chunk kernel,
+inter-chunk scan) over the Qwen3.5-9B-shaped GQA prefill: one sequence of
+T=4096 tokens, H=16 key heads, Hv=32 value heads, dk=dv=128, bf16 q/k/v and
+output, fp32 g/beta/initial and final state. Inputs are seeded synthetic
+tensors already resident in HBM; a 512 MiB buffer is written between timed
+steps so that every step starts with a cold L2 (129 MB).
+
+Prints ONE JSON line (rank 0). ``--impl reference`` times the CPU oracle
+(fp64 token recurrence in C) on the host cores instead, on a bounded sample of
+the same workload. Under torchrun (N > 1) every rank runs an independent
+replica (the path has no exchange step); the slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GDN chunk-prefill tokens/s at T=4096 H16/Hv32 bf16; % of roofline"
+CHUNK = 64
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["gdn", "reference"], default="gdn")
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU time of the oracle baseline sample")
+    ap.add_argument("--clocks-file", default=None)
+    return ap.parse_args(argv)
+
+
+# --------------------------------------------------------------------- workload arithmetic
+def n_chunks(lengths):
+    return sum(-(-int(x) // CHUNK) for x in lengths)
+
+
+def algorithmic_bytes(x, out_bytes=2):
+    """Compulsory HBM bytes of one call: q, k, v, out, g, beta, initial and final states."""
+    esz = 2 if x["dtype"] == "bf16" else 4
+    T, H, Hv, dk, dv, N = x["n_tokens"], x["H"], x["Hv"], x["dk"], x["dv"], x["N"]
+    b = 2 * T * H * dk * esz + T * Hv * dv * esz + T * Hv * dv * out_bytes + 2 * T * Hv * 4
+    states = N * Hv * dk * dv * 4
+    b += states * (2 if x["initial_state"] is not None else 1)
+    return b
+
+
+def algorithmic_flops(x):
+    """FLOPs of the chunked method (q.k^T and k.k^T once per key head per chunk)."""
+    NT = n_chunks(x["lengths"])
+    C, dk, dv = CHUNK, x["dk"], x["dv"]
+    per_h = 2 * 2 * C * C * dk
+    per_hv = C ** 3 / 3 + 2 * C * C * dk + 2 * C * C * dv + 3 * 2 * C * dk * dv + 2 * C * C * dv
+    return NT * x["H"] * per_h + NT * x["Hv"] * per_hv
+
+
+def stage_bytes(x, out_bytes=2):
+    """Bytes each kernel must move given the intra/inter bridge it exchanges
+    (w bf16, u fp32, decay-masked q.k as a bf16 hi/lo pair, G fp32 per chunk row)."""
+    esz = 2 if x["dtype"] == "bf16" else 4
+    T, H, Hv, dk, dv, N = x["n_tokens"], x["H"], x["Hv"], x["dk"], x["dv"], x["N"]
+    NT = n_chunks(x["lengths"])
+    w_b = 2 if x["dtype"] == "bf16" else 4
+    bridge = NT * Hv * (CHUNK * dk * w_b + CHUNK * dv * 4 + CHUNK * CHUNK * 4 + CHUNK * 4)
+    qk = 2 * T * H * dk * esz
+    states = N * Hv * dk * dv * 4
+    s_in = states if x["initial_state"] is not None else 0
+    intra = qk + T * Hv * dv * esz + 2 * T * Hv * 4 + bridge
+    inter = qk + bridge + s_in + states + T * Hv * dv * out_bytes
+    return {"chunk_table": 8 * (x["N"] + 1 + x["nt_max"]), "intra": intra, "inter": inter}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# --------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int, path=None):
+        self.path = path or os.path.join(tempfile.gettempdir(), f"gdn_clocks_{os.getpid()}.csv")
+        self.gpu = gpu_index
+        self.proc = None
+
+    def start(self):
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------- CPU oracle
+def oracle_rate(x, seconds: float, max_tokens=None):
+    """Time the CPU oracle on the first T_s tokens of the workload (all heads).
+    T_s is sized from a short probe so the timed sample takes about `seconds`."""
+    import oracle
+    import torch
+
+    def run(ts):
+        cu = torch.tensor([0, ts], dtype=torch.int32)
+        sl = slice(0, ts)
+        s0 = x["initial_state"][:1] if x["initial_state"] is not None else None
+        t = time.perf_counter()
+        oracle.recurrent_forward(x["q"][sl], x["k"][sl], x["v"][sl], x["g"][sl], x["beta"][sl],
+                                 x["scale"], s0, cu)
+        return time.perf_counter() - t
+
+    oracle.build()
+    probe = min(64, x["n_tokens"])
+    dt = run(probe)
+    limit = max_tokens or x["n_tokens"]
+    ts = int(max(16, min(limit, probe * seconds / max(dt, 1e-6))))
+    ts = max(16, ts // 16 * 16)
+    dt = run(ts)
+    return ts / dt, ts, dt, oracle.max_threads()
+
+
+# --------------------------------------------------------------------- distributed plumbing
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def max_over_ranks(val: float, ws: int) -> float:
+    if ws == 1:
+        return val
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([val], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(ws: int):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# --------------------------------------------------------------------- arms
+def run_reference(args, ws, rank):
+    from gated_delta_rule_chunk_gb300.inputs import WORKLOADS, make_inputs
+    if rank != 0:
+        return None
+    x = make_inputs(args.workload)
+    budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
+    rate0, ts, dt, cores = oracle_rate(x, min(budget, args.cpu_seconds))
+    import oracle
+    import torch
+    cu = torch.tensor([0, ts], dtype=torch.int32)
+    sl = slice(0, ts)
+    s0 = x["initial_state"][:1] if x["initial_state"] is not None else None
+    times = []
+    for i in range(args.warmup + args.steps):
+        t = time.perf_counter()
+        oracle.recurrent_forward(x["q"][sl], x["k"][sl], x["v"][sl], x["g"][sl], x["beta"][sl],
+                                 x["scale"], s0, cu)
+        if i >= args.warmup:
+            times.append(time.perf_counter() - t)
+    ms = 1000.0 * statistics.mean(times)
+    value = ts / (ms / 1000.0)
+    sample = (f"first {ts} tokens of the {WORKLOADS[args.workload].name} workload, all "
+              f"{x['Hv']} value heads, per step")
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload].name, "T": x["T"], "H": x["H"],
+                   "Hv": x["Hv"], "dk": 128, "dv": 128, "chunk": CHUNK,
+                   "oracle": "fp64 token-by-token recurrence in C, OpenMP over (seq, head)"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+
+
+def run_gdn(args, ws, rank, local):
+    import torch
+    from gated_delta_rule_chunk_gb300 import binding as B
+    from gated_delta_rule_chunk_gb300.build import build
+    from gated_delta_rule_chunk_gb300.inputs import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    x = make_inputs(args.workload)
+    d = {k: (x[k].to(dev) if x.get(k) is not None else None)
+         for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
+    out = torch.empty(x["T"], x["Hv"], 128, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(x["N"], x["Hv"], 128, 128, dtype=torch.float32, device=dev)
+    desc = B.make_desc(x["T"], x["N"], x["H"], x["Hv"], d["q"].dtype, torch.bfloat16)
+    wsp = B.alloc_workspace(desc, dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(evs=None):
+        B.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"],
+                        d["initial_state"], d["cu_seqlens"], out=out, final_state=fin,
+                        workspace=wsp, stage_events=evs)
+
+    # events: start + the library's four stage events, per step
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    for row in evs:
+        for e in row:
+            e.record()          # creates the event; recorded again in the timed loop
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        flush.fill_(i & 255)
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, args.clocks_file)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_((i + 1) & 255)
+        evs[i][0].record(stream)
+        call([e.cuda_event for e in evs[i][1:]])
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    step_ms = [r[0].elapsed_time(r[4]) for r in evs]
+    st = {"chunk_table": [r[1].elapsed_time(r[2]) for r in evs],
+          "intra": [r[2].elapsed_time(r[3]) for r in evs],
+          "inter": [r[3].elapsed_time(r[4]) for r in evs]}
+    ms = statistics.mean(step_ms)
+    ms_max = max_over_ranks(ms, ws)
+    tokens = x["n_tokens"]
+    value = ws * tokens / (ms_max / 1000.0)
+
+    # ---------------------------------------------------------------- e2e through host buffers
+    host = {k: (x[k].pin_memory() if x.get(k) is not None else None)
+            for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    fin_h = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
+    e2e_ms = []
+    for i in range(3 + args.e2e_steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for key, t in host.items():
+            if t is not None:
+                d[key].copy_(t, non_blocking=True)
+        call()
+        out_h.copy_(out, non_blocking=True)
+        fin_h.copy_(fin, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = ws * tokens / (max_over_ranks(statistics.mean(e2e_ms), ws) / 1000.0)
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    sb = stage_bytes(x)
+    stage_mean = {k: statistics.mean(v) for k, v in st.items()}
+    dom = max(stage_mean, key=stage_mean.get)
+    dom_gbs = sb[dom] / (stage_mean[dom] / 1000.0) / 1e9
+    alg_b, alg_f = algorithmic_bytes(x), algorithmic_flops(x)
+    t_hbm = alg_b / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_f / (peaks["bf16_tflops"] * 1e12)
+    t_ns_hbm = alg_b / 8.0e12   # the 8 TB/s reading of the target
+    path_roof = {
+        "bound": "hbm" if t_hbm >= t_tc else "tensor",
+        "algorithmic_bytes": alg_b, "algorithmic_flops": alg_f,
+        "roofline_us_measured_peaks": 1e6 * max(t_hbm, t_tc),
+        "roofline_us_8tbs": 1e6 * max(t_ns_hbm, alg_f / (peaks["bf16_tflops"] * 1e12)),
+        "us_per_call": 1000.0 * ms,
+        "frac_of_measured": max(t_hbm, t_tc) / (ms / 1000.0),
+        "frac_of_8tbs": max(t_ns_hbm, t_tc) / (ms / 1000.0),
+    }
+    res = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload].name, "T": x["T"], "N": x["N"],
+                   "H": x["H"], "Hv": x["Hv"], "dk": 128, "dv": 128, "chunk": CHUNK,
+                   "qkv_dtype": "bf16", "out_dtype": "bf16", "g_beta_state_dtype": "fp32",
+                   "initial_state": x["initial_state"] is not None,
+                   "l2": "512 MiB buffer written between timed steps (L2 is 129 MB)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "inputs": "resident in HBM"},
+        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dom_gbs / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": sb[dom], "traffic": None},
+        "path_roofline": path_roof,
+        "stages_us": {k: 1000.0 * v for k, v in stage_mean.items()},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+        "gpu_launches": 3 * K,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        rate, ts, dt, cores = oracle_rate(x, args.cpu_seconds)
+        res["cpu_baseline"] = {
+            "value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {ts} tokens of the workload, all {x['Hv']} value heads "
+                      f"({dt:.1f} s of fp64 C on the host cores)"}
+    return res
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "gdn" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, ws, rank)
+        else:
+            res = run_gdn(args, ws, rank, local)
+        if rank == 0 and res is not None:
+            print(json.dumps(res), flush=True)
+    finally:
+        if ws > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

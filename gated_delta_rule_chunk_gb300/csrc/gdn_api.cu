@@ -1,0 +1,175 @@
+// Host side of the libgdn C ABI (include/gdn.h): argument validation,
+// workspace carve-up and the launch sequence. No allocation, no
+// synchronization, no device reads: every call only enqueues on `stream`.
+#include <math.h>
+
+#include <mutex>
+#include <set>
+#include <utility>
+
+#include "gdn_common.cuh"
+
+using namespace gdn;
+
+namespace gdn {
+
+void ensure_smem_limit(const void* kernel, int bytes) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
+      cudaSuccess)
+    done.insert({kernel, dev});
+}
+
+}  // namespace gdn
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+int check_desc_impl(const gdn_desc* d) {
+  if (!d) return GDN_ERR_NULL_ARG;
+  if (d->T < 0 || d->N < 1 || d->H < 1 || d->Hv < 1 || d->nt_max < 0) return GDN_ERR_BAD_SHAPE;
+  if (d->Hv % d->H != 0) return GDN_ERR_BAD_SHAPE;
+  if (d->dk != kDk || d->dv != kDv || d->chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
+  const bool dt_ok = (d->qkv_dtype == GDN_F32 || d->qkv_dtype == GDN_BF16) &&
+                     (d->out_dtype == GDN_F32 || d->out_dtype == GDN_BF16);
+  if (!dt_ok) return GDN_ERR_UNSUPPORTED;
+  if (d->flags & ~(uint32_t)(GDN_FLAG_QK_L2NORM | GDN_FLAG_BUILD_CHUNK_INDICES))
+    return GDN_ERR_UNSUPPORTED;
+  // Index arithmetic stays within 64-bit sizes and 32-bit grid limits.
+  if ((int64_t)d->T * d->Hv * kDv >= ((int64_t)1 << 40)) return GDN_ERR_BAD_SHAPE;
+  if (d->N > 65535 * 16 || d->Hv > 65535 || d->H > 65535) return GDN_ERR_BAD_SHAPE;
+  return GDN_OK;
+}
+
+int nt_max_of(const gdn_desc* d) {
+  return d->nt_max > 0 ? d->nt_max : gdn_nt_max(d->T, d->N, kChunk);
+}
+
+WsLayout layout_of(const gdn_desc* d) {
+  return ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), d->qkv_dtype == GDN_BF16,
+                   (d->flags & GDN_FLAG_QK_L2NORM) != 0);
+}
+
+}  // namespace
+
+extern "C" {
+
+int gdn_check_desc(const gdn_desc* desc) { return check_desc_impl(desc); }
+
+int32_t gdn_nt_max(int32_t T, int32_t N, int32_t chunk_size) {
+  if (T < 0 || N < 1 || chunk_size < 1) return -1;
+  return (int32_t)(((int64_t)T + chunk_size - 1) / chunk_size + N - 1);
+}
+
+size_t gdn_workspace_size(const gdn_desc* desc) {
+  if (check_desc_impl(desc) != GDN_OK) return 0;
+  return layout_of(desc).total;
+}
+
+int gdn_build_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T, int32_t nt_max,
+                            int32_t* chunk_indices, int32_t* chunk_offsets, int32_t* status,
+                            cudaStream_t stream) {
+  if (!chunk_offsets) return GDN_ERR_NULL_ARG;
+  if (N < 1 || T < 0 || nt_max < 0) return GDN_ERR_BAD_SHAPE;
+  if (!cu_seqlens && N != 1) return GDN_ERR_BAD_SHAPE;
+  if (!aligned(cu_seqlens, 4) || !aligned(chunk_indices, 8) || !aligned(chunk_offsets, 4) ||
+      !aligned(status, 4))
+    return GDN_ERR_MISALIGNED;
+  launch_chunk_table(cu_seqlens, N, T, nt_max, reinterpret_cast<int2*>(chunk_indices),
+                     chunk_offsets, nullptr, status, stream);
+  return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
+}
+
+int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void* v,
+                  const float* g, const float* beta, float scale, const float* initial_state,
+                  const int32_t* cu_seqlens, int32_t* chunk_indices, void* out,
+                  float* final_state, cudaStream_t stream) {
+  int rc = check_desc_impl(desc);
+  if (rc != GDN_OK) return rc;
+  const gdn_desc& d = *desc;
+  if (!q || !k || !v || !g || !beta || !out || !d.workspace) return GDN_ERR_NULL_ARG;
+  if (!cu_seqlens && d.N != 1) return GDN_ERR_BAD_SHAPE;
+  const bool build_into_caller = chunk_indices && (d.flags & GDN_FLAG_BUILD_CHUNK_INDICES);
+  const void* ptrs16[] = {q, k, v, g, beta, out, initial_state, final_state};
+  for (const void* p : ptrs16)
+    if (!aligned(p, 16)) return GDN_ERR_MISALIGNED;
+  if (!aligned(cu_seqlens, 4) || !aligned(chunk_indices, 8)) return GDN_ERR_MISALIGNED;
+  if (!aligned(d.workspace, 256)) return GDN_ERR_MISALIGNED;
+  const WsLayout L = layout_of(&d);
+  if (d.workspace_bytes < L.total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+
+  char* ws = static_cast<char*>(d.workspace);
+  const int nt_max = nt_max_of(&d);
+  const bool bf16 = d.qkv_dtype == GDN_BF16;
+  const bool l2 = (d.flags & GDN_FLAG_QK_L2NORM) != 0;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)kDk);  // also NaN
+  const float eps = d.l2norm_eps > 0.f ? d.l2norm_eps : 1e-6f;
+
+  Params p{};
+  p.T = d.T; p.N = d.N; p.H = d.H; p.Hv = d.Hv; p.HG = d.Hv / d.H; p.nt_max = nt_max;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.scale = scale;
+  p.s0 = initial_state; p.out = out; p.sT = final_state;
+  p.status = reinterpret_cast<int32_t*>(ws + L.status);
+  p.seq_info = reinterpret_cast<const int2*>(ws + L.seq_info);
+  p.chunk_offsets = reinterpret_cast<const int32_t*>(ws + L.chunk_offsets);
+  int2* table = chunk_indices ? reinterpret_cast<int2*>(chunk_indices)
+                              : reinterpret_cast<int2*>(ws + L.chunk_table);
+  p.chunk_table = table;
+  p.G = reinterpret_cast<float*>(ws + L.G);
+  p.w = ws + L.w;
+  p.u = reinterpret_cast<float*>(ws + L.u);
+  p.M = ws + L.M;
+  p.qrn = l2 ? reinterpret_cast<float*>(ws + L.qrn) : nullptr;
+  p.krn = l2 ? reinterpret_cast<float*>(ws + L.krn) : nullptr;
+  p.out_bf16 = d.out_dtype == GDN_BF16;
+
+  cudaEvent_t* ev = d.stage_events;
+  if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH_FAILED;
+  if (ev) cudaEventRecord(ev[0], stream);
+  if (l2) launch_l2norm(q, k, bf16, d.T, d.H, eps, const_cast<float*>(p.qrn),
+                        const_cast<float*>(p.krn), stream);
+  launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
+                     (!chunk_indices || build_into_caller) ? table : nullptr,
+                     const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
+                     p.status, stream);
+  if (ev) cudaEventRecord(ev[1], stream);
+  if (nt_max > 0) launch_simt_intra(p, bf16, stream);
+  if (ev) cudaEventRecord(ev[2], stream);
+  launch_simt_inter(p, bf16, stream);
+  if (ev) cudaEventRecord(ev[3], stream);
+  return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
+}
+
+int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t stream) {
+  int rc = check_desc_impl(desc);
+  if (rc != GDN_OK) return rc;
+  if (!host_status || !desc->workspace) return GDN_ERR_NULL_ARG;
+  const WsLayout L = layout_of(desc);
+  const char* ws = static_cast<const char*>(desc->workspace);
+  if (cudaMemcpyAsync(host_status, ws + L.status, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH_FAILED;
+  return GDN_OK;
+}
+
+const char* gdn_status_string(int status) {
+  switch (status) {
+    case GDN_OK: return "ok";
+    case GDN_ERR_NULL_ARG: return "a required pointer is NULL";
+    case GDN_ERR_BAD_SHAPE: return "invalid dimensions";
+    case GDN_ERR_UNSUPPORTED: return "unsupported head size, chunk size, dtype or flag";
+    case GDN_ERR_MISALIGNED: return "misaligned pointer";
+    case GDN_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case GDN_ERR_LAUNCH_FAILED: return "CUDA launch or copy failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

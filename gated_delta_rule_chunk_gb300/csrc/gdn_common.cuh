@@ -1,0 +1,100 @@
+// Shared definitions of the libgdn kernels: launch parameters, the workspace
+// layout and small device helpers. Nothing here computes the method itself.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/gdn.h"
+
+namespace gdn {
+
+constexpr int kChunk = 64;   // C: tokens per chunk
+constexpr int kDk = 128;     // key head dimension
+constexpr int kDv = 128;     // value head dimension
+
+// Everything a kernel needs, passed by value. Pointers are device pointers.
+struct Params {
+  int T, N, H, Hv, HG, nt_max;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  float scale;
+  const float* s0;           // [N, Hv, dv, dk] or null
+  void* out;                 // [T, Hv, dv]
+  float* sT;                 // [N, Hv, dv, dk] or null
+  int32_t* status;           // device status word
+  const int2* seq_info;      // [N] sanitized (start, length)
+  const int32_t* chunk_offsets;  // [N + 1]
+  const int2* chunk_table;   // [nt_max] (sequence, ordinal) or (-1, -1)
+  float* G;                  // [nt_max, Hv, 64] in-chunk cumulative log-decay
+  void* w;                   // [nt_max, Hv, 64, dk]
+  float* u;                  // [nt_max, Hv, 64, dv]
+  void* M;                   // [nt_max, Hv, 64, 64] (or hi/lo pair) decay-masked q.k
+  const float* qrn;          // [T, H] 1/||q|| or null
+  const float* krn;          // [T, H] 1/||k|| or null
+  int out_bf16;
+};
+
+// Byte offsets of the workspace regions (each 256-byte aligned).
+struct WsLayout {
+  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, qrn, krn, total;
+};
+
+__host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Layout for a problem; w is stored in the input precision path's format:
+// bf16 for bf16 inputs (4 bytes per element of M: a hi/lo bf16 pair) and fp32
+// for fp32 inputs (4 bytes per element of M as well).
+inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool bf16_path, bool l2norm) {
+  WsLayout L{};
+  size_t o = 0;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  L.status = take(64);
+  L.seq_info = take(sizeof(int2) * (size_t)N);
+  L.chunk_offsets = take(sizeof(int32_t) * (size_t)(N + 1));
+  L.chunk_table = take(sizeof(int2) * (size_t)nt_max);
+  const size_t slots = (size_t)nt_max * (size_t)Hv;
+  L.G = take(sizeof(float) * slots * kChunk);
+  L.w = take((bf16_path ? 2 : 4) * slots * kChunk * kDk);
+  L.u = take(sizeof(float) * slots * kChunk * kDv);
+  L.M = take(4 * slots * kChunk * kChunk);
+  L.qrn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
+  L.krn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
+  L.total = o;
+  return L;
+}
+
+__device__ __forceinline__ float to_f32(float x) { return x; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+__device__ __forceinline__ void set_status(int32_t* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// The (start, length) of sequence n and its first chunk slot.
+struct SeqView {
+  int start, len, first_slot;
+};
+
+__device__ __forceinline__ SeqView seq_view(const Params& p, int n) {
+  int2 si = p.seq_info[n];
+  return SeqView{si.x, si.y, p.chunk_offsets[n]};
+}
+
+// Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
+// that later calls (for example under CUDA-graph capture) make no attribute call.
+void ensure_smem_limit(const void* kernel, int bytes);
+
+// Kernel launchers (one translation unit each).
+void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,
+                        int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s);
+void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, float eps,
+                   float* qrn, float* krn, cudaStream_t s);
+void launch_simt_intra(const Params& p, bool bf16_inputs, cudaStream_t s);
+void launch_simt_inter(const Params& p, bool bf16_inputs, cudaStream_t s);
+
+}  // namespace gdn

@@ -1,0 +1,91 @@
+// K1: device-side chunk-index builder.
+//
+// FLA RFC "Graph capture support for prefill and training", section "Core
+// design": chunk-count-sized grids are launched at the static bound NT_max and
+// the (sequence id, chunk ordinal) table is filled on the device by a
+// searchsorted over the per-sequence chunk counts, with a sentinel in unused
+// slots, so no host synchronization is needed.
+//
+// One CTA of 1024 threads: (1) sanitize each sequence's [start, end) to
+// [0, T] and count its chunks, (2) exclusive-scan the counts into
+// chunk_offsets, (3) for every slot binary-search the sequence that owns it.
+#include "gdn_common.cuh"
+
+namespace gdn {
+
+__global__ void __launch_bounds__(1024)
+chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
+                   int2* __restrict__ table, int32_t* __restrict__ offsets,
+                   int2* __restrict__ seq_info, int32_t* status) {
+  __shared__ int warp_incl[32];
+  __shared__ int carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  if (tid == 0) carry_s = 0;
+  __syncthreads();
+  int bad = 0;
+  for (int base = 0; base < N; base += 1024) {
+    const int n = base + tid;
+    int cnt = 0;
+    if (n < N) {
+      const int a = cu ? cu[n] : 0;
+      const int b = cu ? cu[n + 1] : T;
+      const int s = min(max(a, 0), T);
+      const int e = min(max(b, s), T);
+      bad |= (a != s) | (b != e);
+      const int len = e - s;
+      cnt = (len + kChunk - 1) / kChunk;
+      if (seq_info) seq_info[n] = make_int2(s, len);
+    }
+    int x = cnt;  // inclusive warp scan
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_incl[wid] = x;
+    __syncthreads();
+    if (wid == 0) {
+      int ws = warp_incl[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, ws, o);
+        if (lane >= o) ws += y;
+      }
+      warp_incl[lane] = ws;
+    }
+    __syncthreads();
+    const int excl = carry_s + (wid ? warp_incl[wid - 1] : 0) + x - cnt;
+    if (n < N) offsets[n] = excl;
+    __syncthreads();
+    if (tid == 1023) carry_s = excl + cnt;
+    __syncthreads();
+  }
+  const int total = carry_s;
+  if (tid == 0) {
+    offsets[N] = total;
+    if (total > nt_max) set_status(status, GDN_DEV_CHUNK_OVERFLOW);
+  }
+  if (bad) set_status(status, GDN_DEV_BAD_CU_SEQLENS);
+  __syncthreads();  // offsets[] (global) visible to the whole block
+  if (!table) return;
+  for (int s = tid; s < nt_max; s += 1024) {
+    int2 r = make_int2(-1, -1);
+    if (s < total) {
+      // offsets[lo] <= s < offsets[hi]; offsets[0] = 0 and offsets[N] = total.
+      int lo = 0, hi = N;
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offsets[mid] <= s) lo = mid; else hi = mid;
+      }
+      r = make_int2(lo, s - offsets[lo]);
+    }
+    table[s] = r;
+  }
+}
+
+void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,
+                        int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s) {
+  chunk_table_kernel<<<1, 1024, 0, s>>>(cu, N, T, nt_max, table, offsets, seq_info, status);
+}
+
+}  // namespace gdn

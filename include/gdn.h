@@ -1,0 +1,209 @@
+/*
+ * gdn.h -- C ABI of libgdn: the chunked gated-delta-rule prefill forward
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per sequence n, value head hv, key head h = hv / (Hv / H);
+ * the per-head fp32 state S has one row per key dimension):
+ *
+ *   S_t = exp(g_t) * S_{t-1} + beta_t * k_t (v_t - exp(g_t) * S_{t-1}^T k_t)^T
+ *   o_t = scale * S_t^T q_t
+ *
+ * evaluated in chunks of C = 64 tokens: an intra-chunk stage parallel over
+ * [chunks, key heads] and an inter-chunk scan parallel over [sequences, value
+ * heads], the two-stage split of "Optimizing GDN Chunk Prefill on Intel AMX
+ * CPU" (sections 3-5). The per-token update is the one described in
+ * "Chunking Qwen3.5's gated DeltaNet for 1.5x faster prefill on Apple
+ * Silicon" (section "What is the gated delta rule in Qwen3.5?"). Varlen
+ * packing via cu_seqlens and the static [NT_max, 2] chunk table with
+ * sentinel slots follow the FLA RFC "Graph capture support for prefill and
+ * training" (section "Core design").
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller. The library
+ *     never allocates, frees or synchronizes; it enqueues work on `stream` and
+ *     returns. Nothing is read back to the host, so a call can be captured in
+ *     a CUDA graph (addresses are then fixed by the caller).
+ *   - Layouts are dense, row-major, innermost dimension last:
+ *       q, k            [T, H, dk]   (gdn_desc.qkv_dtype)
+ *       v               [T, Hv, dv]  (gdn_desc.qkv_dtype)
+ *       out             [T, Hv, dv]  (gdn_desc.out_dtype)
+ *       g, beta         [T, Hv]      fp32; g is the per-token log-decay (<= 0)
+ *       states          [N, Hv, dv, dk] fp32 (value-major, "[N, Hv, V, K]")
+ *       cu_seqlens      [N + 1] int32 prefix sums of sequence lengths
+ *       chunk_indices   [nt_max, 2] int32 (sequence id, chunk ordinal)
+ *       chunk_offsets   [N + 1] int32 (first slot of each sequence; [N] = total)
+ *   - Return value: GDN_OK (0) or a negative gdn_status. On an argument error
+ *     nothing is enqueued. Problems that only the data reveals (malformed
+ *     cu_seqlens, more chunks than nt_max, a bad caller-supplied chunk table)
+ *     never fault: the kernels clamp or skip and set bits of the device status
+ *     word (gdn_dev_status), which gdn_read_status copies back.
+ *   - Supported today: dk = dv = 128, chunk_size = 64, Hv % H == 0.
+ */
+#ifndef GDN_H_
+#define GDN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same definitions as the CUDA runtime's, so that this header stands alone. */
+typedef struct CUstream_st* cudaStream_t;
+typedef struct CUevent_st* cudaEvent_t;
+
+typedef enum gdn_dtype { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+typedef enum gdn_status {
+  GDN_OK = 0,
+  GDN_ERR_NULL_ARG = -1,          /* a required pointer is NULL */
+  GDN_ERR_BAD_SHAPE = -2,         /* T < 0, N < 1, H < 1, Hv % H != 0, nt_max < 0 */
+  GDN_ERR_UNSUPPORTED = -3,       /* valid but not built: dk/dv != 128, chunk_size != 64, dtype */
+  GDN_ERR_MISALIGNED = -4,        /* a pointer is not 16-byte aligned (workspace: 256 bytes) */
+  GDN_ERR_WORKSPACE_TOO_SMALL = -5,
+  GDN_ERR_LAUNCH_FAILED = -6      /* the CUDA runtime refused a launch or copy */
+} gdn_status;
+
+/* Bits of the device status word (OR-ed by the kernels, cleared per call). */
+typedef enum gdn_dev_status {
+  GDN_DEV_BAD_CU_SEQLENS = 1,     /* cu_seqlens not monotone or beyond T: clamped */
+  GDN_DEV_CHUNK_OVERFLOW = 2,     /* more chunks than nt_max: the excess is skipped */
+  GDN_DEV_BAD_CHUNK_TABLE = 4     /* caller table names a chunk that does not exist: skipped */
+} gdn_dev_status;
+
+enum {
+  GDN_FLAG_QK_L2NORM = 1u,            /* normalise q and k rows: x / sqrt(sum x^2 + eps) */
+  GDN_FLAG_BUILD_CHUNK_INDICES = 2u   /* fill the caller's chunk_indices buffer */
+};
+
+enum { GDN_NUM_STAGE_EVENTS = 4 };
+
+/*
+ * Problem descriptor (plain data; the pages' Python signature infers these
+ * from tensor shapes). Fields:
+ *   T            rows of q, k, v, g, beta, out (the token budget T_max when the
+ *                call is graph-captured; rows past cu_seqlens[N] are ignored and
+ *                their out rows are left untouched)
+ *   N            number of sequences (cu_seqlens has N + 1 entries; zero-length
+ *                sequences are allowed, e.g. padding up to N_max)
+ *   H, Hv        key/query heads and value heads; Hv must be a multiple of H
+ *   dk, dv       head dimensions (128 and 128)
+ *   chunk_size   64
+ *   nt_max       number of chunk slots; 0 selects cdiv(T, 64) + N - 1, which
+ *                bounds the chunk count of any cu_seqlens with N sequences
+ *                and at most T tokens
+ *   qkv_dtype    gdn_dtype of q, k, v; out_dtype: gdn_dtype of out
+ *   flags        GDN_FLAG_* bits
+ *   l2norm_eps   eps of the optional L2 norm; <= 0 selects 1e-6
+ *   workspace    device scratch of at least gdn_workspace_size(desc) bytes,
+ *                256-byte aligned, owned by the caller; it must not be used by
+ *                another call that may run at the same time
+ *   stage_events NULL, or an array of GDN_NUM_STAGE_EVENTS cudaEvent_t that
+ *                gdn_chunk_fwd records on `stream` before the first kernel and
+ *                after the chunk-table, intra-chunk and inter-chunk kernels
+ *                (for timing each stage; the library does not create them)
+ */
+typedef struct gdn_desc {
+  int32_t T;
+  int32_t N;
+  int32_t H;
+  int32_t Hv;
+  int32_t dk;
+  int32_t dv;
+  int32_t chunk_size;
+  int32_t nt_max;
+  int32_t qkv_dtype;
+  int32_t out_dtype;
+  uint32_t flags;
+  float l2norm_eps;
+  void* workspace;
+  size_t workspace_bytes;
+  cudaEvent_t* stage_events;
+} gdn_desc;
+
+/*
+ * Validate a descriptor's dimensions, dtypes and flags (host only; pointers
+ * other than the workspace are not looked at). Returns GDN_OK or the status
+ * gdn_chunk_fwd would return for it.
+ */
+int gdn_check_desc(const gdn_desc* desc);
+
+/*
+ * The chunk-slot bound nt_max = cdiv(T, chunk_size) + N - 1 of the FLA RFC
+ * ("Core design": the first sequence's partial chunk is covered by the cdiv
+ * term, every further sequence adds at most one). Returns -1 for T < 0 or N < 1.
+ */
+int32_t gdn_nt_max(int32_t T, int32_t N, int32_t chunk_size);
+
+/*
+ * Bytes of workspace gdn_chunk_fwd needs for this descriptor (the fields
+ * workspace and workspace_bytes are ignored). 0 if the descriptor is invalid.
+ * Size follows the static bound: it depends on T, N, nt_max, H, Hv and dtypes,
+ * not on the contents of cu_seqlens.
+ */
+size_t gdn_workspace_size(const gdn_desc* desc);
+
+/*
+ * Device-side chunk-index builder (FLA RFC, "Core design": a searchsorted
+ * routine fills a fixed [NT_max, 2] table and marks unused slots with a
+ * sentinel). For every slot s < nt_max it writes (n, c): the sequence n whose
+ * chunks cover slot s and the chunk ordinal c inside it (token start =
+ * cu_seqlens[n] + 64 c), slots ordered by sequence and then ordinal, and
+ * (-1, -1) in unused slots. chunk_offsets[n] receives the slot of sequence n's
+ * first chunk and chunk_offsets[N] the total number of chunks.
+ *   cu_seqlens     [N + 1] int32, or NULL for one sequence of T tokens
+ *   chunk_indices  [nt_max, 2] int32 output, or NULL to skip the table
+ *   chunk_offsets  [N + 1] int32 output (required)
+ *   status         one int32 of device memory the kernel ORs gdn_dev_status
+ *                  bits into (not cleared here), or NULL
+ * Malformed cu_seqlens are clamped to [0, T] and made monotone (status bit 1);
+ * chunks beyond nt_max are not written (status bit 2).
+ */
+int gdn_build_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T,
+                            int32_t nt_max, int32_t* chunk_indices,
+                            int32_t* chunk_offsets, int32_t* status,
+                            cudaStream_t stream);
+
+/*
+ * The chunked gated-delta-rule forward (the whole hot path: optional q/k
+ * L2-norm prologue, chunk-table builder, intra-chunk kernel, inter-chunk scan).
+ *   q, k, v        inputs (layouts above), dtype desc->qkv_dtype
+ *   g, beta        fp32 [T, Hv]
+ *   scale          output scale; <= 0 or NaN selects 1/sqrt(dk)
+ *   initial_state  fp32 [N, Hv, dv, dk] or NULL for zeros
+ *   cu_seqlens     int32 [N + 1] or NULL for one sequence of T tokens (N = 1)
+ *   chunk_indices  NULL: the table is built inside the workspace;
+ *                  non-NULL and GDN_FLAG_BUILD_CHUNK_INDICES set: the table is
+ *                  built into this caller buffer [nt_max, 2];
+ *                  non-NULL without the flag: the caller's table is read (it
+ *                  must list every real chunk once; sentinel rows are skipped)
+ *   out            [T, Hv, dv], dtype desc->out_dtype; rows outside the
+ *                  sequences are not written
+ *   final_state    fp32 [N, Hv, dv, dk] or NULL (not written). It may alias
+ *                  initial_state: each slice is read before it is written.
+ *                  A zero-length sequence gets its initial state (or zeros).
+ * Rows of a partial last chunk are masked (beta = 0, k = 0, g = 0 past the end
+ * of the sequence) and never stored.
+ */
+int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k,
+                  const void* v, const float* g, const float* beta, float scale,
+                  const float* initial_state, const int32_t* cu_seqlens,
+                  int32_t* chunk_indices, void* out, float* final_state,
+                  cudaStream_t stream);
+
+/*
+ * Enqueue an asynchronous copy of the device status word of the last call
+ * that used desc->workspace into *host_status (pinned host memory is best).
+ * The caller synchronizes the stream before reading it.
+ */
+int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t stream);
+
+/* Static description of a gdn_status value. */
+const char* gdn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H_ */

@@ -1,0 +1,141 @@
+"""libgdn loads, exports every symbol include/gdn.h declares, and validates
+arguments on the host (every call here fails validation before any CUDA call,
+so no GPU is needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from gated_delta_rule_chunk_gb300 import binding as B
+from gated_delta_rule_chunk_gb300.build import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return B.load_library()
+
+
+def declared_functions():
+    names = []
+    for hdr in os.listdir(os.path.join(ROOT, "include")):
+        if hdr.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", hdr)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names += re.findall(r"^\s*[\w\s\*]*?\b(gdn_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert "gdn_chunk_fwd" in names and len(names) >= 7
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(B.EXPORTED) <= set(names)
+
+
+def desc(**kw):
+    base = dict(T=4096, N=1, H=16, Hv=32, qkv_dtype=__import__("torch").bfloat16)
+    base.update(kw)
+    return B.make_desc(**base)
+
+
+def test_check_desc(lib):
+    assert B.gdn_check_desc(desc()) == 0
+    assert B.gdn_check_desc(desc(Hv=24, H=16)) == -2          # Hv % H != 0
+    assert B.gdn_check_desc(desc(N=0)) == -2
+    assert B.gdn_check_desc(desc(T=-1)) == -2
+    assert B.gdn_check_desc(desc(nt_max=-3)) == -2
+    assert B.gdn_check_desc(desc(dk=64, dv=64)) == -3          # not built
+    d = desc()
+    d.chunk_size = 32
+    assert B.gdn_check_desc(d) == -3
+    d = desc()
+    d.qkv_dtype = 7
+    assert B.gdn_check_desc(d) == -3
+    d = desc()
+    d.flags = 8
+    assert B.gdn_check_desc(d) == -3
+    assert lib.gdn_check_desc(None) == -1
+
+
+def test_nt_max_bound(lib):
+    assert B.gdn_nt_max(4096, 32) == 95
+    assert B.gdn_nt_max(4096, 1) == 64
+    assert B.gdn_nt_max(128, 1) == 2
+    assert B.gdn_nt_max(0, 1) == 0
+    assert B.gdn_nt_max(65, 3) == 4
+    assert B.gdn_nt_max(-1, 1) == -1 and B.gdn_nt_max(10, 0) == -1
+
+
+def test_workspace_size(lib):
+    import torch
+    a = B.gdn_workspace_size(desc())
+    b = B.gdn_workspace_size(desc(nt_max=128))
+    c = B.gdn_workspace_size(desc(qkv_dtype=torch.float32))
+    e = B.gdn_workspace_size(desc(flags=1))
+    assert 0 < a < b and a < c and a < e
+    # the bridge dominates: about 64 slots x 32 heads x 64 rows x (2 + 4 + 4 + ...) bytes
+    assert a >= 64 * 32 * 64 * (128 * 2 + 128 * 4 + 64 * 4)
+    assert B.gdn_workspace_size(desc(Hv=24)) == 0
+
+
+def _fwd(lib, d, q=16, k=16, v=16, g=16, beta=16, out=16, s0=None, fin=None, cu=None, ci=None):
+    f = lambda x: None if x is None else ctypes.c_void_p(x)
+    return lib.gdn_chunk_fwd(ctypes.byref(d), f(q), f(k), f(v), f(g), f(beta), 0.0, f(s0), f(cu),
+                             f(ci), f(out), f(fin), None)
+
+
+def test_fwd_rejects_before_enqueue(lib):
+    d = desc()
+    d.workspace = 4096
+    d.workspace_bytes = B.gdn_workspace_size(d)
+    assert _fwd(lib, d, q=None) == -1
+    assert _fwd(lib, d, out=None) == -1
+    dd = desc()
+    assert _fwd(lib, dd) == -1                                   # no workspace
+    assert _fwd(lib, desc(N=2, **{}), cu=None) in (-1, -2)
+    d2 = desc(N=2)
+    d2.workspace = 4096
+    d2.workspace_bytes = 1 << 40
+    assert _fwd(lib, d2, cu=None) == -2                          # N > 1 needs cu_seqlens
+    assert _fwd(lib, d, q=17) == -4                              # misaligned
+    assert _fwd(lib, d, s0=8) == -4
+    d3 = desc()
+    d3.workspace = 4096 + 128
+    d3.workspace_bytes = 1 << 40
+    assert _fwd(lib, d3) == -4                                   # workspace alignment
+    d4 = desc()
+    d4.workspace = 4096
+    d4.workspace_bytes = B.gdn_workspace_size(d4) - 1
+    assert _fwd(lib, d4) == -5
+    bad = desc(Hv=24)
+    assert _fwd(lib, bad) == -2
+
+
+def test_build_chunk_indices_rejects(lib):
+    f = ctypes.c_void_p
+    assert lib.gdn_build_chunk_indices(f(16), 2, 100, 5, f(16), None, None, None) == -1
+    assert lib.gdn_build_chunk_indices(None, 2, 100, 5, f(16), f(16), None, None) == -2
+    assert lib.gdn_build_chunk_indices(f(16), 0, 100, 5, f(16), f(16), None, None) == -2
+    assert lib.gdn_build_chunk_indices(f(18), 2, 100, 5, f(16), f(16), None, None) == -4
+
+
+def test_status_strings(lib):
+    for s in range(0, -7, -1):
+        assert B.status_string(s) not in ("", "unknown status")
+    assert B.status_string(-99) == "unknown status"
+
+
+def test_product_path_has_no_oracle_or_fallback():
+    """The package never imports the oracle and has no CPU fallback."""
+    pkg = os.path.join(ROOT, "gated_delta_rule_chunk_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith((".py", ".cu", ".cuh", ".h")):
+                text = open(os.path.join(dirpath, fn)).read()
+                assert "import oracle" not in text and "from oracle" not in text, fn
+                assert "gdn_ref" not in text, fn
