@@ -51,8 +51,11 @@ int nt_max_of(const gdn_desc* d) {
   return d->nt_max > 0 ? d->nt_max : gdn_nt_max(d->T, d->N, kChunk);
 }
 
+// The tensor-core path serves bf16 inputs; fp32 inputs take the SIMT path.
+bool uses_tc_path(const gdn_desc* d) { return false; }
+
 WsLayout layout_of(const gdn_desc* d) {
-  return ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), d->qkv_dtype == GDN_BF16,
+  return ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d),
                    (d->flags & GDN_FLAG_QK_L2NORM) != 0);
 }
 

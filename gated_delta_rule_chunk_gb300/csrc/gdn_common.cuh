@@ -46,10 +46,10 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Layout for a problem; w is stored in the input precision path's format:
-// bf16 for bf16 inputs (4 bytes per element of M: a hi/lo bf16 pair) and fp32
-// for fp32 inputs (4 bytes per element of M as well).
-inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool bf16_path, bool l2norm) {
+// Layout for a problem. The tensor-core path stores w in bf16 and M as a hi/lo
+// bf16 pair; the fp32 SIMT path stores both in fp32 (4 bytes per M element
+// either way).
+inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path, bool l2norm) {
   WsLayout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
@@ -59,7 +59,7 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool bf16_pat
   L.chunk_table = take(sizeof(int2) * (size_t)nt_max);
   const size_t slots = (size_t)nt_max * (size_t)Hv;
   L.G = take(sizeof(float) * slots * kChunk);
-  L.w = take((bf16_path ? 2 : 4) * slots * kChunk * kDk);
+  L.w = take((tc_path ? 2 : 4) * slots * kChunk * kDk);
   L.u = take(sizeof(float) * slots * kChunk * kDv);
   L.M = take(4 * slots * kChunk * kChunk);
   L.qrn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;

@@ -1,0 +1,264 @@
+// K2, bf16 inputs: fused intra-chunk kernel over [chunk slots, key heads].
+//
+// "Optimizing GDN Chunk Prefill on Intel AMX CPU", section 4: K K^T is
+// computed once per (chunk, key head) and reused by the value heads of the
+// group; per value head the decay/beta-scaled A, its triangular inverse and
+// w/u are formed without writing A to global memory. Section 8: triangular
+// work stays triangular (only the blocks on or below the diagonal of K K^T,
+// Q K^T, T K and T V are multiplied).
+//
+// Per (chunk, key head h), with rows past the end of the sequence masked
+// (k = q = v = 0, beta = 0, g = 0):
+//   P = K K^T, R = Q K^T                     (bf16 MMA, fp32 accumulate; exact products)
+//   per value head hv of the group:
+//     G = inclusive cumsum of g               (fp32, left to right)
+//     A_ij = beta_i exp(G_i - G_j) P_ij (j < i),  T = (I + A)^-1   (fp32, shared memory)
+//     w = (T diag(beta exp(G))) K             (bf16 operand, bf16 store)
+//     u = (T diag(beta)) V                    (T operand split into bf16 hi + lo, fp32 store)
+//     M = exp(G_i - G_j) R_ij (j <= i)        (stored as a bf16 hi/lo pair)
+// The bridge to the inter-chunk kernel is w, u, M and G per (slot, hv).
+// The hi/lo split keeps about 16 significant bits where a single bf16 rounding
+// would cost ~1e-2 of the output's rms (measured against the fp64 oracle).
+#include "gdn_common.cuh"
+#include "tri_inverse.cuh"
+#include "warp_mma.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int LDB = 136;   // bf16 stride of 128-wide tiles (272 B rows: conflict-free ldmatrix)
+constexpr int LDB64 = 72;  // bf16 stride of 64-wide tiles (144 B rows)
+constexpr int LDF = 68;    // fp32 stride of 64x64 product tiles
+constexpr int LDA = 65;    // fp32 stride of the triangular-solve tiles
+
+struct IntraSmem {
+  __nv_bfloat16 K[64 * LDB], Q[64 * LDB], V[64 * LDB];
+  float KK[64 * LDF], QK[64 * LDF];
+  float A[64 * LDA], T[64 * LDA], X[16 * LDA];
+  __nv_bfloat16 Tw[64 * LDB64], Tuh[64 * LDB64], Tul[64 * LDB64];
+  float G[64], B[64], E[64], KR[64];
+};
+
+__device__ __forceinline__ bool resolve(const Params& p, int slot, int& t0, int& L, int& wslot) {
+  const int2 e = p.chunk_table[slot];
+  if (e.x < 0) return false;  // sentinel: early exit
+  if (e.x >= p.N) {
+    set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
+    return false;
+  }
+  const SeqView sv = seq_view(p, e.x);
+  const int nch = (sv.len + kChunk - 1) / kChunk;
+  if (e.y < 0 || e.y >= nch) {
+    set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
+    return false;
+  }
+  wslot = sv.first_slot + e.y;
+  if (wslot >= p.nt_max) {
+    set_status(p.status, GDN_DEV_CHUNK_OVERFLOW);
+    return false;
+  }
+  t0 = sv.start + kChunk * e.y;
+  L = min(kChunk, sv.len - kChunk * e.y);
+  return true;
+}
+
+// 64 rows x 128 bf16 of a [T, heads, 128] tensor into a padded tile; rows >= L read as zero.
+__device__ __forceinline__ void load_rows(__nv_bfloat16* dst, const __nv_bfloat16* src, int t0,
+                                          int L, int heads, int head, int tid) {
+#pragma unroll
+  for (int it = 0; it < 8; ++it) {
+    const int idx = tid + it * 128;  // 1024 chunks of 16 bytes
+    const int i = idx >> 4, c = (idx & 15) * 8;
+    const bool ok = i < L;
+    const __nv_bfloat16* g = src + (((size_t)(ok ? t0 + i : t0) * heads + head) * kDk + c);
+    cp_async16(dst + i * LDB + c, g, ok);
+  }
+}
+
+__global__ void __launch_bounds__(128) tc_intra_kernel(Params p) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  IntraSmem& s = *reinterpret_cast<IntraSmem*>(smem_raw);
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int h = blockIdx.y;
+  int t0, L, wslot;
+  if (!resolve(p, blockIdx.x, t0, L, wslot)) return;
+  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
+  const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k);
+  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v);
+
+  load_rows(s.K, kg, t0, L, p.H, h, tid);
+  load_rows(s.Q, qg, t0, L, p.H, h, tid);
+  cp_async_commit();
+  if (tid < 64) {  // optional L2-norm factors (1 when off)
+    const bool ok = tid < L && p.krn;
+    s.KR[tid] = ok ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
+  }
+  cp_async_wait<0>();
+  __syncthreads();
+
+  // P = K K^T and R = Q K^T for this warp's 16 rows, column tiles on or below the diagonal.
+  {
+    const int r0 = 16 * warp;
+    float kk[8][4], qk[8][4];
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) kk[nt][e] = qk[nt][e] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      uint32_t ak[4], aq[4];
+      load_a(ak, s.K, LDB, r0, 16 * ks, lane);
+      load_a(aq, s.Q, LDB, r0, 16 * ks, lane);
+#pragma unroll
+      for (int np = 0; np < 4; ++np) {
+        if (np <= warp) {
+          uint32_t b[4];
+          load_b_nk(b, s.K, LDB, 16 * ks, 16 * np, lane);
+          mma_bf16(kk[2 * np], ak, b[0], b[1]);
+          mma_bf16(kk[2 * np + 1], ak, b[2], b[3]);
+          mma_bf16(qk[2 * np], aq, b[0], b[1]);
+          mma_bf16(qk[2 * np + 1], aq, b[2], b[3]);
+        }
+      }
+    }
+    const int g = lane >> 2, c = 2 * (lane & 3);
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+      const int col = 8 * nt + c;
+      *reinterpret_cast<float2*>(&s.KK[(r0 + g) * LDF + col]) = make_float2(kk[nt][0], kk[nt][1]);
+      *reinterpret_cast<float2*>(&s.KK[(r0 + g + 8) * LDF + col]) = make_float2(kk[nt][2], kk[nt][3]);
+      *reinterpret_cast<float2*>(&s.QK[(r0 + g) * LDF + col]) = make_float2(qk[nt][0], qk[nt][1]);
+      *reinterpret_cast<float2*>(&s.QK[(r0 + g + 8) * LDF + col]) = make_float2(qk[nt][2], qk[nt][3]);
+    }
+  }
+  __syncthreads();
+
+  for (int r = 0; r < p.HG; ++r) {
+    const int hv = h * p.HG + r;
+    const size_t sl = (size_t)wslot * p.Hv + hv;
+    load_rows(s.V, vg, t0, L, p.Hv, hv, tid);
+    cp_async_commit();
+    if (warp == 0) {  // gates and their in-chunk inclusive cumsum (64 rows, 2 per lane)
+      const size_t b0 = (size_t)(t0 + lane) * p.Hv + hv, b1 = (size_t)(t0 + lane + 32) * p.Hv + hv;
+      float g0 = lane < L ? p.g[b0] : 0.f, g1 = lane + 32 < L ? p.g[b1] : 0.f;
+      const float be0 = lane < L ? p.beta[b0] : 0.f, be1 = lane + 32 < L ? p.beta[b1] : 0.f;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y0 = __shfl_up_sync(0xffffffffu, g0, o);
+        const float y1 = __shfl_up_sync(0xffffffffu, g1, o);
+        if (lane >= o) { g0 += y0; g1 += y1; }
+      }
+      g1 += __shfl_sync(0xffffffffu, g0, 31);
+      s.G[lane] = g0;
+      s.G[lane + 32] = g1;
+      s.E[lane] = expf(g0);
+      s.E[lane + 32] = expf(g1);
+      s.B[lane] = be0;
+      s.B[lane + 32] = be1;
+      p.G[sl * 64 + lane] = g0;
+      p.G[sl * 64 + lane + 32] = g1;
+    }
+    __syncthreads();
+    __nv_bfloat16* Mh = static_cast<__nv_bfloat16*>(p.M) + sl * 2 * 64 * 64;
+    __nv_bfloat16* Ml = Mh + 64 * 64;
+    for (int idx = tid; idx < 64 * 64; idx += 128) {
+      const int i = idx >> 6, j = idx & 63;
+      const float dec = (j <= i) ? expf(s.G[i] - s.G[j]) : 0.f;
+      const float kr = s.KR[i] * s.KR[j];
+      s.A[i * LDA + j] = (j < i) ? s.B[i] * dec * kr * s.KK[i * LDF + j] : 0.f;
+      const float qr = p.qrn ? ((i < L) ? p.qrn[(size_t)(t0 + i) * p.H + h] : 1.f) * s.KR[j] : 1.f;
+      __nv_bfloat16 hi, lo;
+      split_bf16(dec * qr * s.QK[i * LDF + j], hi, lo);
+      Mh[idx] = hi;
+      Ml[idx] = lo;
+    }
+    __syncthreads();
+    tri_inverse_64(s.A, LDA, s.T, LDA, s.X, tid, 128);
+    for (int idx = tid; idx < 64 * 64; idx += 128) {
+      const int i = idx >> 6, j = idx & 63;
+      const float t = s.T[i * LDA + j] * s.B[j];
+      s.Tw[i * LDB64 + j] = __float2bfloat16_rn(t * s.E[j] * s.KR[j]);
+      __nv_bfloat16 hi, lo;
+      split_bf16(t, hi, lo);
+      s.Tuh[i * LDB64 + j] = hi;
+      s.Tul[i * LDB64 + j] = lo;
+    }
+    cp_async_wait<0>();
+    __syncthreads();
+
+    // w = Tw K and u = (Tuh + Tul) V for this warp's 16 rows; T is lower triangular,
+    // so only k-tiles 0..warp contribute.
+    const int r0 = 16 * warp, g = lane >> 2, c = 2 * (lane & 3);
+    {
+      float acc[16][4];
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        if (ks <= warp) {
+          uint32_t a[4];
+          load_a(a, s.Tw, LDB64, r0, 16 * ks, lane);
+#pragma unroll
+          for (int np = 0; np < 8; ++np) {
+            uint32_t b[4];
+            load_b_kn(b, s.K, LDB, 16 * ks, 16 * np, lane);
+            mma_bf16(acc[2 * np], a, b[0], b[1]);
+            mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
+          }
+        }
+      }
+      __nv_bfloat16* wo = static_cast<__nv_bfloat16*>(p.w) + sl * 64 * kDk;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int col = 8 * nt + c;
+        *reinterpret_cast<uint32_t*>(&wo[(r0 + g) * kDk + col]) = pack_bf16(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<uint32_t*>(&wo[(r0 + g + 8) * kDk + col]) = pack_bf16(acc[nt][2], acc[nt][3]);
+      }
+    }
+    {
+      float acc[16][4];
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks) {
+        if (ks <= warp) {
+          uint32_t ah[4], al[4];
+          load_a(ah, s.Tuh, LDB64, r0, 16 * ks, lane);
+          load_a(al, s.Tul, LDB64, r0, 16 * ks, lane);
+#pragma unroll
+          for (int np = 0; np < 8; ++np) {
+            uint32_t b[4];
+            load_b_kn(b, s.V, LDB, 16 * ks, 16 * np, lane);
+            mma_bf16(acc[2 * np], ah, b[0], b[1]);
+            mma_bf16(acc[2 * np + 1], ah, b[2], b[3]);
+            mma_bf16(acc[2 * np], al, b[0], b[1]);
+            mma_bf16(acc[2 * np + 1], al, b[2], b[3]);
+          }
+        }
+      }
+      float* uo = p.u + sl * 64 * kDv;
+#pragma unroll
+      for (int nt = 0; nt < 16; ++nt) {
+        const int col = 8 * nt + c;
+        *reinterpret_cast<float2*>(&uo[(r0 + g) * kDv + col]) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(&uo[(r0 + g + 8) * kDv + col]) = make_float2(acc[nt][2], acc[nt][3]);
+      }
+    }
+    __syncthreads();  // V, Tw, Tu are rewritten for the next value head
+  }
+}
+
+}  // namespace
+
+void launch_tc_intra(const Params& p, cudaStream_t s) {
+  const int smem = (int)sizeof(IntraSmem);
+  ensure_smem_limit((const void*)tc_intra_kernel, smem);
+  tc_intra_kernel<<<dim3(p.nt_max, p.H), 128, smem, s>>>(p);
+}
+
+}  // namespace gdn
