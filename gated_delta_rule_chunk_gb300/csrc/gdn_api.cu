@@ -52,7 +52,7 @@ int nt_max_of(const gdn_desc* d) {
 }
 
 // The tensor-core path serves bf16 inputs; fp32 inputs take the SIMT path.
-bool uses_tc_path(const gdn_desc* d) { return false; }
+bool uses_tc_path(const gdn_desc* d) { return d->qkv_dtype == GDN_BF16; }
 
 WsLayout layout_of(const gdn_desc* d) {
   return ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d),
@@ -143,9 +143,12 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
                      const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
                      p.status, stream);
   if (ev) cudaEventRecord(ev[1], stream);
-  if (nt_max > 0) launch_simt_intra(p, bf16, stream);
+  const bool tc = uses_tc_path(&d);
+  if (nt_max > 0) {
+    if (tc) launch_tc_intra(p, stream); else launch_simt_intra(p, false, stream);
+  }
   if (ev) cudaEventRecord(ev[2], stream);
-  launch_simt_inter(p, bf16, stream);
+  if (tc) launch_tc_inter(p, stream); else launch_simt_inter(p, false, stream);
   if (ev) cudaEventRecord(ev[3], stream);
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }

@@ -77,7 +77,7 @@ def test_workspace_size(lib):
     b = B.gdn_workspace_size(desc(nt_max=128))
     c = B.gdn_workspace_size(desc(qkv_dtype=torch.float32))
     e = B.gdn_workspace_size(desc(flags=1))
-    assert 0 < a < b and a <= c and a < e
+    assert 0 < a < b and a < c and a < e
     # the bridge dominates: about 64 slots x 32 heads x 64 rows x (2 + 4 + 4 + ...) bytes
     assert a >= 64 * 32 * 64 * (128 * 2 + 128 * 4 + 64 * 4)
     assert B.gdn_workspace_size(desc(Hv=24)) == 0
