@@ -1,0 +1,66 @@
+"""bench.py host logic without a GPU: the workload arithmetic, and the N > 1
+replica path over a world-size-2 gloo process group (barrier, max over ranks,
+rank 0 alone prints the reference arm's JSON line)."""
+import io
+import json
+import os
+import socket
+import sys
+from contextlib import redirect_stdout
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+from gated_delta_rule_chunk_gb300.inputs import make_inputs
+
+
+def test_headline_roofline_arithmetic():
+    x = make_inputs(2)
+    assert bench.algorithmic_bytes(x) == 105906176          # 25.9 KB/token
+    assert abs(bench.algorithmic_flops(x) - 21.65e9) < 0.01e9
+    assert bench.n_chunks(x["lengths"]) == 64
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _worker(rank, port, q):
+    os.environ.update(RANK=str(rank), LOCAL_RANK=str(rank), WORLD_SIZE="2",
+                      MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    import torch.distributed as dist
+    dist.init_process_group("gloo", rank=rank, world_size=2)
+    m = bench.max_over_ranks(float(rank + 1), 2)
+    bench.barrier(2)
+    dist.destroy_process_group()
+    buf = io.StringIO()
+    with redirect_stdout(buf):
+        bench.main(["--impl", "reference", "--workload", "0", "--steps", "1", "--warmup", "0",
+                    "--gpus", "2"])
+    q.put((rank, m, buf.getvalue()))
+
+
+def test_two_rank_replicas_over_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = dict()
+    for _ in range(2):
+        rank, m, out = q.get(timeout=300)
+        res[rank] = (m, out)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res[0][0] == 2.0 and res[1][0] == 2.0
+    assert res[1][1].strip() == ""
+    line = json.loads(res[0][1].strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["n_gpus"] == 2 and line["value"] > 0
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
