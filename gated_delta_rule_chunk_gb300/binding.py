@@ -26,7 +26,8 @@ DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table
 
 # Every entry point include/gdn.h declares.
 EXPORTED = ("gdn_check_desc", "gdn_nt_max", "gdn_workspace_size", "gdn_build_chunk_indices",
-            "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string")
+            "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string", "gdn_chunk_fwd_noalloc")
+GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
 class GdnError(RuntimeError):
@@ -71,6 +72,8 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_chunk_fwd.argtypes = [P(GdnDesc), vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
                                       vp, vp, vp, vp]
         lib.gdn_chunk_fwd.restype = ctypes.c_int
+        lib.gdn_chunk_fwd_noalloc.argtypes = lib.gdn_chunk_fwd.argtypes
+        lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.gdn_read_status.argtypes = [P(GdnDesc), vp, vp]
         lib.gdn_read_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -211,3 +214,33 @@ def gdn_read_status(desc: GdnDesc, stream=None) -> int:
         raise GdnError(rc, "gdn_read_status")
     (torch.cuda.current_stream() if stream is None else stream).synchronize()
     return int(host.item())
+
+
+def gdn_chunk_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                          beta: torch.Tensor, scale: Optional[float] = None,
+                          initial_state: Optional[torch.Tensor] = None,
+                          cu_seqlens: Optional[torch.Tensor] = None,
+                          out: Optional[torch.Tensor] = None,
+                          final_state: Optional[torch.Tensor] = None,
+                          out_dtype: Optional[torch.dtype] = None, stream=None):
+    """The forward pass through gdn_chunk_fwd_noalloc: the library's own static
+    scratch replaces the workspace (for callers that cannot allocate device
+    memory; here torch only provides the caller's inputs and outputs)."""
+    T, H, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    out_dtype = out_dtype or (out.dtype if out is not None else q.dtype)
+    desc = make_desc(T, N, H, Hv, q.dtype, out_dtype, dk=dk, dv=dv)
+    if out is None:
+        out = torch.empty(T, Hv, dv, dtype=out_dtype, device=q.device)
+    if final_state is None:
+        final_state = torch.empty(N, Hv, dv, dk, dtype=torch.float32, device=q.device)
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    rc = load_library().gdn_chunk_fwd_noalloc(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), None, _ptr(out), _ptr(final_state),
+        _stream_handle(stream))
+    if rc != 0:
+        raise GdnError(rc, "gdn_chunk_fwd_noalloc")
+    return out, final_state

@@ -199,6 +199,35 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k,
  */
 int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t stream);
 
+/*
+ * Size of the scratch array gdn_chunk_fwd_noalloc uses in place of a
+ * workspace (64 MiB, held on every GPU that loads the library until exit).
+ */
+enum { GDN_NOALLOC_SCRATCH_BYTES = 64 << 20 };
+
+/*
+ * gdn_chunk_fwd without a workspace, for callers that may not allocate device
+ * memory themselves (a framework that owns all device memory through its own
+ * arena, or a serving loop that cannot afford an allocation's device
+ * synchronization). The pages have no counterpart: this is a convenience of
+ * this library. Same arguments and results as gdn_chunk_fwd; desc->workspace
+ * and desc->workspace_bytes are ignored. The scratch is one file-scope device
+ * array of GDN_NOALLOC_SCRATCH_BYTES shared by every call in the process:
+ *   - a problem whose gdn_workspace_size exceeds it is rejected with
+ *     GDN_ERR_WORKSPACE_TOO_SMALL and nothing is enqueued (T = 1024 with
+ *     Hv = 32 fits; T = 4096 with Hv = 32 does not);
+ *   - calls that may overlap on the GPU (other streams or host threads) race
+ *     on the array: the caller must order them;
+ *   - the first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress), so make that first call outside stream capture.
+ * It calls no allocator (no cudaMalloc, cudaFree or library allocation).
+ */
+int gdn_chunk_fwd_noalloc(const gdn_desc* desc, const void* q, const void* k,
+                          const void* v, const float* g, const float* beta, float scale,
+                          const float* initial_state, const int32_t* cu_seqlens,
+                          int32_t* chunk_indices, void* out, float* final_state,
+                          cudaStream_t stream);
+
 /* Static description of a gdn_status value. */
 const char* gdn_status_string(int status);
 
