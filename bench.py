@@ -308,7 +308,7 @@ def run_gdn(args, ws, rank, local):
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = out_h.numel() * out_h.element_size() + fin_h.numel() * fin_h.element_size()
     e2e_ms = []
-    for i in range(3 + args.e2e_steps):
+    for i in range(3 + args.e2e_steps if args.e2e_steps > 0 else 0):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         for key, t in host.items():
@@ -321,7 +321,8 @@ def run_gdn(args, ws, rank, local):
         b.synchronize()
         if i >= 3:
             e2e_ms.append(a.elapsed_time(b))
-    e2e_val = ws * tokens / (max_over_ranks(statistics.mean(e2e_ms), ws) / 1000.0)
+    e2e_val = (ws * tokens / (max_over_ranks(statistics.mean(e2e_ms), ws) / 1000.0)
+               if e2e_ms else None)
 
     if rank != 0:
         return None
@@ -361,7 +362,8 @@ def run_gdn(args, ws, rank, local):
         "path_roofline": path_roof,
         "stages_us": {k: 1000.0 * v for k, v in stage_mean.items()},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": statistics.mean(e2e_ms)},
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms) if e2e_ms else None},
         "gpu_launches": 3 * K,
         "clocks": clk,
         "wall_s_timed_region": wall,

@@ -3,22 +3,26 @@
 // "Optimizing GDN Chunk Prefill on Intel AMX CPU", section 4: K K^T is
 // computed once per (chunk, key head) and reused by the value heads of the
 // group; per value head the decay/beta-scaled A, its triangular inverse and
-// w/u are formed without writing A to global memory. Section 8: triangular
-// work stays triangular (only the blocks on or below the diagonal of K K^T,
-// Q K^T, T K and T V are multiplied).
+// the products that need it are formed without writing A to global memory.
+// Section 8: triangular work stays triangular (only tiles on or below the
+// diagonal of K K^T, Q K^T and T K are multiplied).
 //
 // Per (chunk, key head h), with rows past the end of the sequence masked
-// (k = q = v = 0, beta = 0, g = 0):
-//   P = K K^T, R = Q K^T                     (bf16 MMA, fp32 accumulate; exact products)
+// (k = q = 0, beta = 0, g = 0):
+//   P = K K^T, R = Q K^T        (bf16 MMA, fp32 accumulate: exact products),
+//                                kept in registers across the value-head loop
 //   per value head hv of the group:
-//     G = inclusive cumsum of g               (fp32, left to right)
-//     A_ij = beta_i exp(G_i - G_j) P_ij (j < i),  T = (I + A)^-1   (fp32, shared memory)
-//     w = (T diag(beta exp(G))) K             (bf16 operand, bf16 store)
-//     u = (T diag(beta)) V                    (T operand split into bf16 hi + lo, fp32 store)
-//     M = exp(G_i - G_j) R_ij (j <= i)        (stored as a bf16 hi/lo pair)
-// The bridge to the inter-chunk kernel is w, u, M and G per (slot, hv).
-// The hi/lo split keeps about 16 significant bits where a single bf16 rounding
-// would cost ~1e-2 of the output's rms (measured against the fp64 oracle).
+//     G = inclusive in-chunk cumsum of g (fp32, left to right)
+//     A_ij = beta_i exp(G_i - G_j) P_ij (j < i);  T = (I + A)^-1 in place (fp32)
+//     w    = (T diag(beta exp(G))) K        (bf16 operand and store)
+//     u    = (T diag(beta)) V               (T operand split into bf16 hi + lo; fp32 store)
+//     M_ij = exp(G_i - G_j) R_ij (j <= i)   (stored as a bf16 hi/lo pair)
+// The hi/lo split keeps about 16 significant bits where one bf16 rounding
+// would cost ~1e-2 of the output's rms. MMA A-fragments of the scaled T are
+// built in registers straight from the fp32 T tile.
+//
+// Occupancy: ~75 KB of shared memory and 128 threads per CTA, so that several
+// CTAs share an SM and hide each other's latency.
 #include "gdn_common.cuh"
 #include "tri_inverse.cuh"
 #include "warp_mma.cuh"
@@ -27,16 +31,13 @@ namespace gdn {
 
 namespace {
 
-constexpr int LDB = 136;   // bf16 stride of 128-wide tiles (272 B rows: conflict-free ldmatrix)
-constexpr int LDB64 = 72;  // bf16 stride of 64-wide tiles (144 B rows)
-constexpr int LDF = 68;    // fp32 stride of 64x64 product tiles
-constexpr int LDA = 65;    // fp32 stride of the triangular-solve tiles
+constexpr int LDB = 136;  // bf16 stride of 128-wide tiles (272 B rows: conflict-free ldmatrix)
+constexpr int LDT = 68;   // fp32 stride of the A/T tile (16-byte rows)
 
 struct IntraSmem {
   __nv_bfloat16 K[64 * LDB], Q[64 * LDB], V[64 * LDB];
-  float KK[64 * LDF], QK[64 * LDF];
-  float A[64 * LDA], T[64 * LDA], X[16 * LDA];
-  __nv_bfloat16 Tw[64 * LDB64], Tuh[64 * LDB64], Tul[64 * LDB64];
+  float AT[64 * LDT];
+  float X[16 * LDT];
   float G[64], B[64], E[64], KR[64];
 };
 
@@ -76,68 +77,58 @@ __device__ __forceinline__ void load_rows(__nv_bfloat16* dst, const __nv_bfloat1
   }
 }
 
-__global__ void __launch_bounds__(128) tc_intra_kernel(Params p) {
+__global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   IntraSmem& s = *reinterpret_cast<IntraSmem*>(smem_raw);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = lane >> 2, c = 2 * (lane & 3);
   const int h = blockIdx.y;
   int t0, L, wslot;
   if (!resolve(p, blockIdx.x, t0, L, wslot)) return;
-  const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
-  const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k);
-  const __nv_bfloat16* vg = static_cast<const __nv_bfloat16*>(p.v);
 
-  load_rows(s.K, kg, t0, L, p.H, h, tid);
-  load_rows(s.Q, qg, t0, L, p.H, h, tid);
+  load_rows(s.K, static_cast<const __nv_bfloat16*>(p.k), t0, L, p.H, h, tid);
+  load_rows(s.Q, static_cast<const __nv_bfloat16*>(p.q), t0, L, p.H, h, tid);
   cp_async_commit();
   if (tid < 64) {  // optional L2-norm factors (1 when off)
-    const bool ok = tid < L && p.krn;
-    s.KR[tid] = ok ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
+    s.KR[tid] = (tid < L && p.krn) ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
+  }
+  const int r0 = 16 * warp;
+  float qra = 1.f, qrb = 1.f;  // 1/||q|| of this thread's two rows
+  if (p.qrn) {
+    qra = (r0 + g < L) ? p.qrn[(size_t)(t0 + r0 + g) * p.H + h] : 1.f;
+    qrb = (r0 + g + 8 < L) ? p.qrn[(size_t)(t0 + r0 + g + 8) * p.H + h] : 1.f;
   }
   cp_async_wait<0>();
   __syncthreads();
 
-  // P = K K^T and R = Q K^T for this warp's 16 rows, column tiles on or below the diagonal.
-  {
-    const int r0 = 16 * warp;
-    float kk[8][4], qk[8][4];
+  // P = K K^T and R = Q K^T, rows r0..r0+15, column tiles on or below the diagonal.
+  float kk[8][4], qk[8][4];
 #pragma unroll
-    for (int nt = 0; nt < 8; ++nt)
+  for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) kk[nt][e] = qk[nt][e] = 0.f;
+    for (int e = 0; e < 4; ++e) kk[nt][e] = qk[nt][e] = 0.f;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t ak[4], aq[4];
-      load_a(ak, s.K, LDB, r0, 16 * ks, lane);
-      load_a(aq, s.Q, LDB, r0, 16 * ks, lane);
+  for (int ks = 0; ks < 8; ++ks) {
+    uint32_t ak[4], aq[4];
+    load_a(ak, s.K, LDB, r0, 16 * ks, lane);
+    load_a(aq, s.Q, LDB, r0, 16 * ks, lane);
 #pragma unroll
-      for (int np = 0; np < 4; ++np) {
-        if (np <= warp) {
-          uint32_t b[4];
-          load_b_nk(b, s.K, LDB, 16 * ks, 16 * np, lane);
-          mma_bf16(kk[2 * np], ak, b[0], b[1]);
-          mma_bf16(kk[2 * np + 1], ak, b[2], b[3]);
-          mma_bf16(qk[2 * np], aq, b[0], b[1]);
-          mma_bf16(qk[2 * np + 1], aq, b[2], b[3]);
-        }
+    for (int np = 0; np < 4; ++np) {
+      if (np <= warp) {
+        uint32_t b[4];
+        load_b_nk(b, s.K, LDB, 16 * ks, 16 * np, lane);
+        mma_bf16(kk[2 * np], ak, b[0], b[1]);
+        mma_bf16(kk[2 * np + 1], ak, b[2], b[3]);
+        mma_bf16(qk[2 * np], aq, b[0], b[1]);
+        mma_bf16(qk[2 * np + 1], aq, b[2], b[3]);
       }
     }
-    const int g = lane >> 2, c = 2 * (lane & 3);
-#pragma unroll
-    for (int nt = 0; nt < 8; ++nt) {
-      const int col = 8 * nt + c;
-      *reinterpret_cast<float2*>(&s.KK[(r0 + g) * LDF + col]) = make_float2(kk[nt][0], kk[nt][1]);
-      *reinterpret_cast<float2*>(&s.KK[(r0 + g + 8) * LDF + col]) = make_float2(kk[nt][2], kk[nt][3]);
-      *reinterpret_cast<float2*>(&s.QK[(r0 + g) * LDF + col]) = make_float2(qk[nt][0], qk[nt][1]);
-      *reinterpret_cast<float2*>(&s.QK[(r0 + g + 8) * LDF + col]) = make_float2(qk[nt][2], qk[nt][3]);
-    }
   }
-  __syncthreads();
 
   for (int r = 0; r < p.HG; ++r) {
     const int hv = h * p.HG + r;
     const size_t sl = (size_t)wslot * p.Hv + hv;
-    load_rows(s.V, vg, t0, L, p.Hv, hv, tid);
+    load_rows(s.V, static_cast<const __nv_bfloat16*>(p.v), t0, L, p.Hv, hv, tid);
     cp_async_commit();
     if (warp == 0) {  // gates and their in-chunk inclusive cumsum (64 rows, 2 per lane)
       const size_t b0 = (size_t)(t0 + lane) * p.Hv + hv, b1 = (size_t)(t0 + lane + 32) * p.Hv + hv;
@@ -160,36 +151,35 @@ __global__ void __launch_bounds__(128) tc_intra_kernel(Params p) {
       p.G[sl * 64 + lane + 32] = g1;
     }
     __syncthreads();
-    __nv_bfloat16* Mh = static_cast<__nv_bfloat16*>(p.M) + sl * 2 * 64 * 64;
-    __nv_bfloat16* Ml = Mh + 64 * 64;
-    for (int idx = tid; idx < 64 * 64; idx += 128) {
-      const int i = idx >> 6, j = idx & 63;
-      const float dec = (j <= i) ? expf(s.G[i] - s.G[j]) : 0.f;
-      const float kr = s.KR[i] * s.KR[j];
-      s.A[i * LDA + j] = (j < i) ? s.B[i] * dec * kr * s.KK[i * LDF + j] : 0.f;
-      const float qr = p.qrn ? ((i < L) ? p.qrn[(size_t)(t0 + i) * p.H + h] : 1.f) * s.KR[j] : 1.f;
-      __nv_bfloat16 hi, lo;
-      split_bf16(dec * qr * s.QK[i * LDF + j], hi, lo);
-      Mh[idx] = hi;
-      Ml[idx] = lo;
-    }
-    __syncthreads();
-    tri_inverse_64(s.A, LDA, s.T, LDA, s.X, tid, 128);
-    for (int idx = tid; idx < 64 * 64; idx += 128) {
-      const int i = idx >> 6, j = idx & 63;
-      const float t = s.T[i * LDA + j] * s.B[j];
-      s.Tw[i * LDB64 + j] = __float2bfloat16_rn(t * s.E[j] * s.KR[j]);
-      __nv_bfloat16 hi, lo;
-      split_bf16(t, hi, lo);
-      s.Tuh[i * LDB64 + j] = hi;
-      s.Tul[i * LDB64 + j] = lo;
-    }
-    cp_async_wait<0>();
-    __syncthreads();
 
-    // w = Tw K and u = (Tuh + Tul) V for this warp's 16 rows; T is lower triangular,
-    // so only k-tiles 0..warp contribute.
-    const int r0 = 16 * warp, g = lane >> 2, c = 2 * (lane & 3);
+    // A (strictly lower, to shared memory) and M (hi/lo, to global) from the register tiles.
+    {
+      __nv_bfloat16* Mh = static_cast<__nv_bfloat16*>(p.M) + sl * 2 * 64 * 64;
+      __nv_bfloat16* Ml = Mh + 64 * 64;
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const int i = r0 + g + 8 * hh;
+        const float gi = s.G[i], bi = s.B[i] * s.KR[i], qi = hh ? qrb : qra;
+#pragma unroll
+        for (int nt = 0; nt < 8; ++nt) {
+          const int j = 8 * nt + c;
+          float a2[2], m2[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int jj = j + e;
+            const float dec = (jj <= i) ? expf(gi - s.G[jj]) : 0.f;
+            a2[e] = (jj < i) ? bi * dec * s.KR[jj] * kk[nt][2 * hh + e] : 0.f;
+            m2[e] = dec * qi * s.KR[jj] * qk[nt][2 * hh + e];
+          }
+          *reinterpret_cast<float2*>(&s.AT[i * LDT + j]) = make_float2(a2[0], a2[1]);
+          split2_store(Mh + i * 64 + j, Ml + i * 64 + j, m2[0], m2[1]);
+        }
+      }
+    }
+    __syncthreads();
+    tri_inverse_64_inplace(s.AT, LDT, s.X, tid, 128);
+
+    // w = (T diag(beta exp(G) krn)) K, rows r0..r0+15; T is lower triangular (k-tiles <= warp).
     {
       float acc[16][4];
 #pragma unroll
@@ -200,7 +190,12 @@ __global__ void __launch_bounds__(128) tc_intra_kernel(Params p) {
       for (int ks = 0; ks < 4; ++ks) {
         if (ks <= warp) {
           uint32_t a[4];
-          load_a(a, s.Tw, LDB64, r0, 16 * ks, lane);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {  // a0: (g, c) a1: (g+8, c) a2: (g, c+8) a3: (g+8, c+8)
+            const int i = r0 + g + 8 * (q4 & 1), j = 16 * ks + c + 8 * (q4 >> 1);
+            const float2 t = *reinterpret_cast<const float2*>(&s.AT[i * LDT + j]);
+            a[q4] = pack_bf16(t.x * s.B[j] * s.E[j] * s.KR[j], t.y * s.B[j + 1] * s.E[j + 1] * s.KR[j + 1]);
+          }
 #pragma unroll
           for (int np = 0; np < 8; ++np) {
             uint32_t b[4];
@@ -218,6 +213,9 @@ __global__ void __launch_bounds__(128) tc_intra_kernel(Params p) {
         *reinterpret_cast<uint32_t*>(&wo[(r0 + g + 8) * kDk + col]) = pack_bf16(acc[nt][2], acc[nt][3]);
       }
     }
+    // u = (T diag(beta)) V with the T operand split into bf16 hi + lo.
+    cp_async_wait<0>();
+    __syncthreads();
     {
       float acc[16][4];
 #pragma unroll
@@ -228,8 +226,17 @@ __global__ void __launch_bounds__(128) tc_intra_kernel(Params p) {
       for (int ks = 0; ks < 4; ++ks) {
         if (ks <= warp) {
           uint32_t ah[4], al[4];
-          load_a(ah, s.Tuh, LDB64, r0, 16 * ks, lane);
-          load_a(al, s.Tul, LDB64, r0, 16 * ks, lane);
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) {
+            const int i = r0 + g + 8 * (q4 & 1), j = 16 * ks + c + 8 * (q4 >> 1);
+            const float2 t = *reinterpret_cast<const float2*>(&s.AT[i * LDT + j]);
+            const float x0 = t.x * s.B[j], x1 = t.y * s.B[j + 1];
+            const __nv_bfloat162 hi = __floats2bfloat162_rn(x0, x1);
+            const float2 hf = __bfloat1622float2(hi);
+            const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+            ah[q4] = *reinterpret_cast<const uint32_t*>(&hi);
+            al[q4] = *reinterpret_cast<const uint32_t*>(&lo);
+          }
 #pragma unroll
           for (int np = 0; np < 8; ++np) {
             uint32_t b[4];
@@ -249,7 +256,7 @@ __global__ void __launch_bounds__(128) tc_intra_kernel(Params p) {
         *reinterpret_cast<float2*>(&uo[(r0 + g + 8) * kDv + col]) = make_float2(acc[nt][2], acc[nt][3]);
       }
     }
-    __syncthreads();  // V, Tw, Tu are rewritten for the next value head
+    __syncthreads();  // A/T and the gates are rewritten for the next value head
   }
 }
 
