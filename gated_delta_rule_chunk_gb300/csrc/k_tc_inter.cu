@@ -1,286 +1,321 @@
-// K3, bf16 inputs: fused inter-chunk scan over [sequences, value heads, dv blocks].
+// K3, bf16 inputs: fused inter-chunk scan over [sequences, value heads, dv blocks]
+// on the 5th-generation tensor cores (tcgen05, accumulators in TMEM).
 //
 // "Optimizing GDN Chunk Prefill on Intel AMX CPU", section 5: the state
 // contribution, the local-attention output and the state update are fused per
 // sequence and value head, walking the chunks in order with the fp32 state
-// updated in place; the [sequences, Hv] domain is chosen for parallelism over
-// [sequences, H]. "Chunking Qwen3.5's gated DeltaNet ... on Apple Silicon"
+// updated in place ([sequences, Hv] chosen over [sequences, H] for
+// parallelism). "Chunking Qwen3.5's gated DeltaNet ... on Apple Silicon"
 // (section "How do you parallelize a recurrence for prefill?"): the value
-// dimension of the state tile is blocked so that it stays on chip. Here a CTA
-// owns 32 value columns of one (sequence, value head): its 128x32 fp32 state
-// lives in registers as the accumulators of the state-update MMA for the whole
-// sequence.
+// dimension of the state is blocked so that the tile stays on chip. A CTA owns
+// 32 value columns of one (sequence, value head); thread d (0..127) holds row d
+// (key dimension) of that 128x32 fp32 state in registers for the whole sequence.
 //
-// Per chunk (S = chunk-start state, dk x 32):
-//   X     = w S_hi                          (chain; w and S_hi bf16)
-//   v_new = u - X                           (fp32)
-//   o     = scale (diag(exp(G)) Q (S_hi + S_lo) + (M_hi + M_lo)(vn_hi + vn_lo) - M_lo vn_lo)
-//   S    <- exp(G_L) S + K^T (vh_hi + vh_lo),  vh = diag(exp(G_L - G)) v_new
-// where x_hi + x_lo is a bf16 hi/lo split of an fp32 value (the lo*lo product
-// is dropped). S is split after every update; the next chunk's operands are
-// prefetched with cp.async while the current chunk is computed.
+// Per chunk (S = chunk-start state; x_hi + x_lo is a bf16 hi/lo split of fp32 x):
+//   group 1 (TMEM D1, D2):  [Q; w] S_hi,  [Q; w] S_lo          (M = 128, N = 32, K = 128)
+//     rows 64..127 of D1:   X = w S_hi;  v_new = u - X;  vh = exp(G_L - G) v_new
+//     rows 0..63 of D1+D2:  Q S
+//   group 2 (TMEM D3, D4):  K^T (vh_hi + vh_lo)                  (M = 128, N = 32, K = 64)
+//                           [M_hi; M_lo] (vn_hi + vn_lo)        (M = 128, N = 32, K = 64)
+//   S <- exp(G_L) S + D3;   o = scale (diag(exp(G)) Q S + D4[0:64] + D4[64:128])
+// One thread issues the MMAs; tcgen05.commit arrives on an mbarrier per result,
+// and every wait on those barriers is bounded (GDN_DEV_TIMEOUT on expiry). The
+// next chunk's operands are prefetched with cp.async into a second stage.
+// Shared-memory operands use the no-swizzle canonical layouts (umma.cuh).
 #include "gdn_common.cuh"
+#include "umma.cuh"
 #include "warp_mma.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int BV = 32;         // value columns of the state per CTA
-constexpr int LDB = 136;       // bf16 stride of 128-wide tiles
-constexpr int LDB64 = 72;      // bf16 stride of 64-wide tiles
-constexpr int LDS = BV + 8;    // bf16 stride of 32-wide tiles (80 B rows)
-constexpr int LDU = BV + 4;    // fp32 stride of the u tile
+constexpr int BV = 32;
+constexpr uint32_t kWaitIters = 1u << 22;
 
-struct Stage {
-  __nv_bfloat16 W[64 * LDB], Q[64 * LDB], K[64 * LDB];
-  __nv_bfloat16 Mh[64 * LDB64], Ml[64 * LDB64];
-  float U[64 * LDU];
-  float G[64], QR[64], KR[64], pad[64];
-};
+// One prefetch stage (bytes).
+constexpr uint32_t kAQ = 0;          // [Q; w]: 128 x 128 bf16, K-major (LBO 128, SBO 2048)
+constexpr uint32_t kKT = 32768;      // K^T:   128 (dk) x 64 (tokens), MN-major (LBO 2048, SBO 128)
+constexpr uint32_t kAM = 49152;      // [M_hi; M_lo]: 128 x 64, K-major (LBO 128, SBO 1024)
+constexpr uint32_t kU = 65536;       // u block: fp32 [64][32]
+constexpr uint32_t kG = 73728;       // G [64]
+constexpr uint32_t kQR = 73984;      // 1/||q|| [64] (1 when the L2 norm is off)
+constexpr uint32_t kKR = 74240;      // 1/||k|| [64]
+constexpr uint32_t kStage = 74752;
+// Operands written by the threads (B, MN-major, N = 32: LBO = 512, SBO = 128).
+constexpr uint32_t kSBh = 2 * kStage;    // S_hi: K = dk (128)
+constexpr uint32_t kSBl = kSBh + 8192;   // S_lo
+constexpr uint32_t kVHh = kSBl + 8192;   // vh_hi: K = tokens (64)
+constexpr uint32_t kVHl = kVHh + 4096;
+constexpr uint32_t kVNh = kVHl + 4096;   // vn_hi
+constexpr uint32_t kVNl = kVNh + 4096;
+constexpr uint32_t kX4 = kVNl + 4096;    // fp32 [64][32]: rows 64..127 of D4 handed to warps 0-1
+constexpr uint32_t kBar = kX4 + 8192;    // 4 mbarriers
+constexpr uint32_t kMisc = kBar + 32;    // TMEM base address, abort flag
+constexpr uint32_t kSmemBytes = kMisc + 16;
 
-struct InterSmem {
-  Stage st[2];
-  __nv_bfloat16 Sh[128 * LDS], Sl[128 * LDS];                        // [dk][BV]
-  __nv_bfloat16 Vnh[64 * LDS], Vnl[64 * LDS], Vhh[64 * LDS], Vhl[64 * LDS];  // [token][BV]
-};
+__device__ __forceinline__ uint32_t off_k(int r, int k, int kext) {  // K-major
+  return kmajor_offset(r, k, 128u, (uint32_t)kext * 16u);
+}
+__device__ __forceinline__ uint32_t off_mn(int r, int k, int rext) {  // MN-major
+  return mnmajor_offset(r, k, (uint32_t)rext * 16u, 128u);
+}
 
-__device__ __forceinline__ void load_chunk(Stage& st, const Params& p, int slot, int hv, int h,
-                                           int c0, int t0, int L, int tid) {
+// 8 bf16 -> 16 bytes
+__device__ __forceinline__ uint4 pack8(const float* x) {
+  uint4 u;
+  u.x = pack_bf16(x[0], x[1]);
+  u.y = pack_bf16(x[2], x[3]);
+  u.z = pack_bf16(x[4], x[5]);
+  u.w = pack_bf16(x[6], x[7]);
+  return u;
+}
+
+// Write 32 fp32 values of row r (r along N = 32, MN-major B operand with K
+// index k) as a bf16 hi/lo pair: 4 x 16-byte stores each.
+__device__ __forceinline__ void store_row_split(unsigned char* sm, uint32_t hi_off,
+                                                uint32_t lo_off, int k, const float (&x)[32]) {
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    float h[8], l[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      const __nv_bfloat16 hb = __float2bfloat16_rn(x[8 * a + e]);
+      h[e] = __bfloat162float(hb);
+      l[e] = x[8 * a + e] - h[e];
+    }
+    const uint32_t o = off_mn(8 * a, k, BV);
+    *reinterpret_cast<uint4*>(sm + hi_off + o) = pack8(h);
+    *reinterpret_cast<uint4*>(sm + lo_off + o) = pack8(l);
+  }
+}
+
+__device__ __forceinline__ void load_stage(unsigned char* st, const Params& p, int slot, int hv,
+                                           int h, int c0, int t0, int L, int tid) {
   const size_t sl = (size_t)slot * p.Hv + hv;
   const __nv_bfloat16* wg = static_cast<const __nv_bfloat16*>(p.w) + sl * 64 * kDk;
   const __nv_bfloat16* qg = static_cast<const __nv_bfloat16*>(p.q);
   const __nv_bfloat16* kg = static_cast<const __nv_bfloat16*>(p.k);
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int idx = tid + it * 128;
-    const int i = idx >> 4, c = (idx & 15) * 8;
-    const bool ok = i < L;
-    const size_t row = ((size_t)(ok ? t0 + i : t0) * p.H + h) * kDk + c;
-    cp_async16(&st.W[i * LDB + c], wg + i * kDk + c, true);
-    cp_async16(&st.Q[i * LDB + c], qg + row, ok);
-    cp_async16(&st.K[i * LDB + c], kg + row, ok);
-  }
   const __nv_bfloat16* mg = static_cast<const __nv_bfloat16*>(p.M) + sl * 2 * 64 * 64;
 #pragma unroll
-  for (int it = 0; it < 4; ++it) {
-    const int idx = tid + it * 128;  // 512 chunks per 64x64 bf16 tile
-    const int i = idx >> 3, c = (idx & 7) * 8;
-    cp_async16(&st.Mh[i * LDB64 + c], mg + i * 64 + c, true);
-    cp_async16(&st.Ml[i * LDB64 + c], mg + 64 * 64 + i * 64 + c, true);
-    cp_async16(&st.U[i * LDU + (idx & 7) * 4], p.u + (sl * 64 + i) * kDv + c0 + (idx & 7) * 4,
-               true);
+  for (int it = 0; it < 8; ++it) {
+    const int idx = tid + it * 128;  // 1024 16-byte chunks per 64 x 128 tile
+    const int i = idx >> 4, c = idx & 15;
+    const bool ok = i < L;
+    const size_t row = ((size_t)(ok ? t0 + i : t0) * p.H + h) * kDk + 8 * c;
+    cp_async16(st + kAQ + off_k(i, 8 * c, 128), qg + row, ok);             // Q rows 0..63
+    cp_async16(st + kAQ + off_k(64 + i, 8 * c, 128), wg + i * kDk + 8 * c, true);  // w rows
+    cp_async16(st + kKT + off_mn(8 * c, i, 128), kg + row, ok);            // K^T
+    const int mi = idx >> 3, mc = idx & 7;                                 // 128 rows x 8 chunks
+    cp_async16(st + kAM + off_k(mi, 8 * mc, 64), mg + mi * 64 + 8 * mc, true);
   }
-  if (tid < 16) cp_async16(&st.G[tid * 4], p.G + sl * 64 + tid * 4, true);
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int idx = tid + it * 128;  // 512 chunks: 64 rows x 8
+    const int i = idx >> 3, c = idx & 7;
+    cp_async16(st + kU + (i * 32 + 4 * c) * 4, p.u + (sl * 64 + i) * kDv + c0 + 4 * c, true);
+  }
+  if (tid < 16) cp_async16(st + kG + 16 * tid, p.G + sl * 64 + 4 * tid, true);
   if (tid >= 64) {
     const int i = tid - 64;
     const bool ok = i < L && p.qrn;
-    st.QR[i] = ok ? p.qrn[(size_t)(t0 + i) * p.H + h] : 1.f;
-    st.KR[i] = ok ? p.krn[(size_t)(t0 + i) * p.H + h] : 1.f;
+    reinterpret_cast<float*>(st + kQR)[i] = ok ? p.qrn[(size_t)(t0 + i) * p.H + h] : 1.f;
+    reinterpret_cast<float*>(st + kKR)[i] = ok ? p.krn[(size_t)(t0 + i) * p.H + h] : 1.f;
   }
 }
 
-__global__ void __launch_bounds__(128) tc_inter_kernel(Params p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  InterSmem& s = *reinterpret_cast<InterSmem*>(smem_raw);
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, c = 2 * (lane & 3);
+__device__ __forceinline__ void sync_all() {
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+__global__ void __launch_bounds__(128, 1) tc_inter_kernel(Params p) {
+  extern __shared__ __align__(1024) unsigned char sm[];
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc + 4);
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int n = blockIdx.x, hv = blockIdx.y, c0 = blockIdx.z * BV;
   const int h = hv / p.HG;
   const SeqView sv = seq_view(p, n);
   int nch = (sv.len + kChunk - 1) / kChunk;
   if (sv.first_slot + nch > p.nt_max) {
-    set_status(p.status, GDN_DEV_CHUNK_OVERFLOW);
+    if (tid == 0) set_status(p.status, GDN_DEV_CHUNK_OVERFLOW);
     nch = max(0, p.nt_max - sv.first_slot);
   }
   const size_t state_base = ((size_t)n * p.Hv + hv) * kDv * kDk;
 
-  // State rows (dk) 32*warp + 16*mt + {g, g+8}, columns 8*nt + c + {0,1}.
-  float S[2][4][4];
+  // Thread d = tid owns state row d (key dimension), 32 value columns.
+  float S[32];
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int row = 32 * warp + 16 * mt + g + (e >> 1) * 8, col = 8 * nt + c + (e & 1);
-        S[mt][nt][e] = p.s0 ? p.s0[state_base + (size_t)(c0 + col) * kDk + row] : 0.f;
-      }
-  auto store_split_state = [&]() {
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int row = 32 * warp + 16 * mt + g + hh * 8, col = 8 * nt + c;
-          split2_store(&s.Sh[row * LDS + col], &s.Sl[row * LDS + col], S[mt][nt][2 * hh],
-                       S[mt][nt][2 * hh + 1]);
-        }
-  };
-  store_split_state();
+  for (int j = 0; j < 32; ++j)
+    S[j] = p.s0 ? p.s0[state_base + (size_t)(c0 + j) * kDk + tid] : 0.f;
+  store_row_split(sm, kSBh, kSBl, tid, S);
 
-  if (nch > 0) load_chunk(s.st[0], p, sv.first_slot, hv, h, c0, sv.start, min(kChunk, sv.len), tid);
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 128);
+    tmem_relinquish();
+  }
+  if (tid == 0) {
+    for (int b = 0; b < 4; ++b) mbar_init(&bars[b], 1);
+    mbar_init_fence();
+    *abort_flag = 0;
+  }
+  if (nch > 0) load_stage(sm, p, sv.first_slot, hv, h, c0, sv.start, min(kChunk, sv.len), tid);
   cp_async_commit();
+  sync_all();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t lane_base = (uint32_t)(32 * warp) << 16;
+  const uint32_t D1 = tmem, D2 = tmem + 32, D3 = tmem + 64, D4 = tmem + 96;
+  const uint32_t id_g1 = idesc_bf16_f32(128, BV, false, true);
+  const uint32_t id_s = idesc_bf16_f32(128, BV, true, true);
+  const uint32_t sbase = smem_addr(sm);
+  float* X4 = reinterpret_cast<float*>(sm + kX4);
 
   for (int ci = 0; ci < nch; ++ci) {
+    const uint32_t ph = ci & 1;
+    unsigned char* st = sm + (ci & 1) * kStage;
+    const uint32_t st_a = sbase + (ci & 1) * kStage;
     const int t0 = sv.start + kChunk * ci;
     const int L = min(kChunk, sv.len - kChunk * ci);
-    if (ci + 1 < nch) {
-      const int t1 = t0 + kChunk;
-      load_chunk(s.st[(ci + 1) & 1], p, sv.first_slot + ci + 1, hv, h, c0, t1,
-                 min(kChunk, sv.len - kChunk * (ci + 1)), tid);
-    }
+    if (ci + 1 < nch)
+      load_stage(sm + ((ci + 1) & 1) * kStage, p, sv.first_slot + ci + 1, hv, h, c0,
+                 t0 + kChunk, min(kChunk, sv.len - kChunk * (ci + 1)), tid);
     cp_async_commit();
     cp_async_wait<1>();
-    __syncthreads();
-    Stage& st = s.st[ci & 1];
-    const int r0 = 16 * warp;
+    fence_async_smem();
+    sync_all();  // stage ci and the S split are visible to the tensor cores
+    if (*abort_flag) break;
 
-    // X = w S_hi (chain) and Q S = Q (S_hi + S_lo) (output), rows r0..r0+15.
-    float xa[4][4], qa[4][4];
+    if (tid == 0) {  // group 1: D1 = [Q; w] S_hi, D2 = [Q; w] S_lo
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(D1, sdesc(st_a + kAQ + 256 * ks, 128, 2048), sdesc(sbase + kSBh + 1024 * ks, 512, 128),
+                  id_g1, ks > 0);
+      umma_commit(&bars[0]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) xa[nt][e] = qa[nt][e] = 0.f;
+      for (int ks = 0; ks < 8; ++ks)
+        umma_bf16(D2, sdesc(st_a + kAQ + 256 * ks, 128, 2048), sdesc(sbase + kSBl + 1024 * ks, 512, 128),
+                  id_g1, ks > 0);
+      umma_commit(&bars[1]);
+    }
+    const float* G = reinterpret_cast<const float*>(st + kG);
+    const float gl = G[63];
+    float qs[32];
+    if (warp >= 2) {  // chain: token row i = tid - 64
+      const int i = tid - 64;
+      if (!mbar_wait(&bars[0], ph, kWaitIters)) *abort_flag = 1;
+      tc_fence_after();
+      float x[32];
+      tmem_ld32(D1 + lane_base, x);
+      tmem_ld_wait();
+      const float* U = reinterpret_cast<const float*>(st + kU) + i * 32;
+      const float fac = expf(gl - G[i]) * reinterpret_cast<const float*>(st + kKR)[i];
+      float vh[32];
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
-      uint32_t aw[4], aq[4];
-      load_a(aw, st.W, LDB, r0, 16 * ks, lane);
-      load_a(aq, st.Q, LDB, r0, 16 * ks, lane);
-#pragma unroll
-      for (int np = 0; np < 2; ++np) {
-        uint32_t bh[4], bl[4];
-        load_b_kn(bh, s.Sh, LDS, 16 * ks, 16 * np, lane);
-        load_b_kn(bl, s.Sl, LDS, 16 * ks, 16 * np, lane);
-        mma_bf16(xa[2 * np], aw, bh[0], bh[1]);
-        mma_bf16(xa[2 * np + 1], aw, bh[2], bh[3]);
-        mma_bf16(qa[2 * np], aq, bh[0], bh[1]);
-        mma_bf16(qa[2 * np + 1], aq, bh[2], bh[3]);
-        mma_bf16(qa[2 * np], aq, bl[0], bl[1]);
-        mma_bf16(qa[2 * np + 1], aq, bl[2], bl[3]);
+      for (int j = 0; j < 32; ++j) {
+        x[j] = U[j] - x[j];  // v_new
+        vh[j] = fac * x[j];
       }
-    }
-    // v_new = u - X; vh = exp(G_L - G) v_new * krn (row factors); both split hi/lo.
-    const float gl = st.G[63];
-    const float fa = expf(gl - st.G[r0 + g]) * st.KR[r0 + g];
-    const float fb = expf(gl - st.G[r0 + g + 8]) * st.KR[r0 + g + 8];
+      store_row_split(sm, kVNh, kVNl, i, x);
+      store_row_split(sm, kVHh, kVHl, i, vh);
+    } else {  // output rows i = tid: Q S = D1 + D2
+      if (!mbar_wait(&bars[1], ph, kWaitIters)) *abort_flag = 1;
+      tc_fence_after();
+      float a[32];
+      tmem_ld32(D1 + lane_base, qs);
+      tmem_ld32(D2 + lane_base, a);
+      tmem_ld_wait();
+      const float e = expf(G[tid]) * reinterpret_cast<const float*>(st + kQR)[tid];
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt) {
-      const int col = 8 * nt + c;
-      const float v0 = st.U[(r0 + g) * LDU + col] - xa[nt][0];
-      const float v1 = st.U[(r0 + g) * LDU + col + 1] - xa[nt][1];
-      const float v2 = st.U[(r0 + g + 8) * LDU + col] - xa[nt][2];
-      const float v3 = st.U[(r0 + g + 8) * LDU + col + 1] - xa[nt][3];
-      split2_store(&s.Vnh[(r0 + g) * LDS + col], &s.Vnl[(r0 + g) * LDS + col], v0, v1);
-      split2_store(&s.Vnh[(r0 + g + 8) * LDS + col], &s.Vnl[(r0 + g + 8) * LDS + col], v2, v3);
-      split2_store(&s.Vhh[(r0 + g) * LDS + col], &s.Vhl[(r0 + g) * LDS + col], fa * v0, fa * v1);
-      split2_store(&s.Vhh[(r0 + g + 8) * LDS + col], &s.Vhl[(r0 + g + 8) * LDS + col], fb * v2,
-                   fb * v3);
+      for (int j = 0; j < 32; ++j) qs[j] = (qs[j] + a[j]) * e;
     }
-    __syncthreads();
+    fence_async_smem();
+    sync_all();  // v_new / vh tiles visible to the tensor cores
 
-    // Output rows r0..r0+15: diag(exp(G) * qrn) Q S + M v_new (M causal: k-tiles <= warp).
+    if (tid == 0) {  // group 2: D3 = K^T (vh_hi + vh_lo), D4 = [M_hi; M_lo] (vn_hi + vn_lo)
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(D3, sdesc(st_a + kKT + 4096 * ks, 2048, 128), sdesc(sbase + kVHh + 1024 * ks, 512, 128),
+                  id_s, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(D3, sdesc(st_a + kKT + 4096 * ks, 2048, 128), sdesc(sbase + kVHl + 1024 * ks, 512, 128),
+                  id_s, 1);
+      umma_commit(&bars[2]);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(D4, sdesc(st_a + kAM + 256 * ks, 128, 1024), sdesc(sbase + kVNh + 1024 * ks, 512, 128),
+                  id_g1, ks > 0);
+#pragma unroll
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(D4, sdesc(st_a + kAM + 256 * ks, 128, 1024), sdesc(sbase + kVNl + 1024 * ks, 512, 128),
+                  id_g1, 1);
+      umma_commit(&bars[3]);
+    }
+    // S <- exp(G_L) S + K^T vh (row tid), then its split for the next chunk
     {
-      const float ea = expf(st.G[r0 + g]) * st.QR[r0 + g];
-      const float eb = expf(st.G[r0 + g + 8]) * st.QR[r0 + g + 8];
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        qa[nt][0] *= ea; qa[nt][1] *= ea; qa[nt][2] *= eb; qa[nt][3] *= eb;
-      }
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        if (ks <= warp) {
-          uint32_t mh[4], ml[4];
-          load_a(mh, st.Mh, LDB64, r0, 16 * ks, lane);
-          load_a(ml, st.Ml, LDB64, r0, 16 * ks, lane);
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            uint32_t bh[4], bl[4];
-            load_b_kn(bh, s.Vnh, LDS, 16 * ks, 16 * np, lane);
-            load_b_kn(bl, s.Vnl, LDS, 16 * ks, 16 * np, lane);
-            mma_bf16(qa[2 * np], mh, bh[0], bh[1]);
-            mma_bf16(qa[2 * np + 1], mh, bh[2], bh[3]);
-            mma_bf16(qa[2 * np], ml, bh[0], bh[1]);
-            mma_bf16(qa[2 * np + 1], ml, bh[2], bh[3]);
-            mma_bf16(qa[2 * np], mh, bl[0], bl[1]);
-            mma_bf16(qa[2 * np + 1], mh, bl[2], bl[3]);
-          }
-        }
-      }
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt) {
-        const int col = c0 + 8 * nt + c;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int row = r0 + g + 8 * hh;
-          if (row < L) {
-            const size_t oi = ((size_t)(t0 + row) * p.Hv + hv) * kDv + col;
-            const float o0 = p.scale * qa[nt][2 * hh], o1 = p.scale * qa[nt][2 * hh + 1];
-            if (p.out_bf16)
-              *reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + oi) = pack_bf16(o0, o1);
-            else
-              *reinterpret_cast<float2*>(static_cast<float*>(p.out) + oi) = make_float2(o0, o1);
-          }
-        }
-      }
-    }
-
-    // S <- exp(G_L) S + K^T (vh_hi + vh_lo); this warp owns dk rows 32*warp..+31.
-    {
+      if (!mbar_wait(&bars[2], ph, kWaitIters)) *abort_flag = 1;
+      tc_fence_after();
+      float inc[32];
+      tmem_ld32(D3 + lane_base, inc);
+      tmem_ld_wait();
       const float gam = expf(gl);
 #pragma unroll
-      for (int mt = 0; mt < 2; ++mt)
+      for (int j = 0; j < 32; ++j) S[j] = fmaf(gam, S[j], inc[j]);
+      store_row_split(sm, kSBh, kSBl, tid, S);
+    }
+    float mh[32];
+    if (!mbar_wait(&bars[3], ph, kWaitIters)) *abort_flag = 1;
+    tc_fence_after();
+    tmem_ld32(D4 + lane_base, mh);
+    tmem_ld_wait();
+    if (warp >= 2) {
+      float4* dst = reinterpret_cast<float4*>(X4 + (tid - 64) * 32);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+      for (int a = 0; a < 8; ++a) dst[a] = make_float4(mh[4 * a], mh[4 * a + 1], mh[4 * a + 2], mh[4 * a + 3]);
+    }
+    fence_async_smem();
+    sync_all();  // rows 64..127 of D4 visible to warps 0-1; all MMAs of this chunk done
+    if (warp < 2 && tid < L) {
+      const float4* lo = reinterpret_cast<const float4*>(X4 + tid * 32);
+      float o[32];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) S[mt][nt][e] *= gam;
+      for (int a = 0; a < 8; ++a) {
+        const float4 l4 = lo[a];
+        o[4 * a] = p.scale * (qs[4 * a] + mh[4 * a] + l4.x);
+        o[4 * a + 1] = p.scale * (qs[4 * a + 1] + mh[4 * a + 1] + l4.y);
+        o[4 * a + 2] = p.scale * (qs[4 * a + 2] + mh[4 * a + 2] + l4.z);
+        o[4 * a + 3] = p.scale * (qs[4 * a + 3] + mh[4 * a + 3] + l4.w);
+      }
+      const size_t oi = ((size_t)(t0 + tid) * p.Hv + hv) * kDv + c0;
+      if (p.out_bf16) {
+        uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + oi);
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        uint32_t bh[2][4], bl[2][4];
+        for (int a = 0; a < 4; ++a) dst[a] = pack8(o + 8 * a);
+      } else {
+        float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
 #pragma unroll
-        for (int np = 0; np < 2; ++np) {
-          load_b_kn(bh[np], s.Vhh, LDS, 16 * ks, 16 * np, lane);
-          load_b_kn(bl[np], s.Vhl, LDS, 16 * ks, 16 * np, lane);
-        }
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          uint32_t a[4];
-          load_a_trans(a, st.K, LDB, 32 * warp + 16 * mt, 16 * ks, lane);
-#pragma unroll
-          for (int np = 0; np < 2; ++np) {
-            mma_bf16(S[mt][2 * np], a, bh[np][0], bh[np][1]);
-            mma_bf16(S[mt][2 * np + 1], a, bh[np][2], bh[np][3]);
-            mma_bf16(S[mt][2 * np], a, bl[np][0], bl[np][1]);
-            mma_bf16(S[mt][2 * np + 1], a, bl[np][2], bl[np][3]);
-          }
-        }
+        for (int a = 0; a < 8; ++a) dst[a] = make_float4(o[4 * a], o[4 * a + 1], o[4 * a + 2], o[4 * a + 3]);
       }
     }
-    store_split_state();   // readers of the old split finished before the v_new barrier
-    __syncthreads();       // stage ci&1 and the v_new tiles are reused next
   }
   cp_async_wait<0>();
-
+  if (tid == 0 && *abort_flag) set_status(p.status, GDN_DEV_TIMEOUT);
+  sync_all();
+  if (warp == 0) tmem_dealloc(tmem, 128);
   if (p.sT) {
 #pragma unroll
-    for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-      for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int row = 32 * warp + 16 * mt + g + (e >> 1) * 8, col = 8 * nt + c + (e & 1);
-          p.sT[state_base + (size_t)(c0 + col) * kDk + row] = S[mt][nt][e];
-        }
+    for (int j = 0; j < 32; ++j) p.sT[state_base + (size_t)(c0 + j) * kDk + tid] = S[j];
   }
 }
 
 }  // namespace
 
 void launch_tc_inter(const Params& p, cudaStream_t s) {
-  const int smem = (int)sizeof(InterSmem);
-  ensure_smem_limit((const void*)tc_inter_kernel, smem);
-  tc_inter_kernel<<<dim3(p.N, p.Hv, kDv / BV), 128, smem, s>>>(p);
+  ensure_smem_limit((const void*)tc_inter_kernel, (int)kSmemBytes);
+  tc_inter_kernel<<<dim3(p.N, p.Hv, kDv / BV), 128, kSmemBytes, s>>>(p);
 }
 
 }  // namespace gdn

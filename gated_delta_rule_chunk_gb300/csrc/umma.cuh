@@ -91,11 +91,13 @@ __device__ __forceinline__ void tmem_ld_wait() {
 }
 
 // ---------------------------------------------------------------- descriptors
-// Shared-memory matrix descriptor, no swizzling, K-major "canonical" layout:
-// the operand is a grid of 8-row x 16-byte core matrices (each 128 contiguous
-// bytes, row r at byte 16 r); lbo = byte distance between core matrices that
-// are adjacent along K, sbo = byte distance between 8-row groups along M/N.
-__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+// Shared-memory matrix descriptor, no swizzling. The operand is a grid of core
+// matrices of 8 rows x 16 bytes (128 contiguous bytes, row r at byte 16 r).
+// K-major: a core-matrix row is 8 consecutive K elements of one M/N row.
+// MN-major: a core-matrix row is 8 consecutive M/N elements of one K index.
+// For both (measured on sm_103a): lbo = byte distance between core matrices
+// adjacent along K, sbo = byte distance between core matrices adjacent along M/N.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
   uint64_t d = 0;
   d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
   d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
@@ -104,19 +106,35 @@ __device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, uint32_t lbo, u
   return d;                // base offset 0, relative LBO, no swizzle
 }
 
-// Byte offset of element (r, k) of a bf16 operand stored in that layout.
+__device__ __forceinline__ uint64_t sdesc_kmajor(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  return sdesc(saddr, lbo, sbo);
+}
+
+// Byte offset of bf16 element (r, k) (r along M/N) in the K-major layout.
 __host__ __device__ __forceinline__ uint32_t kmajor_offset(int r, int k, uint32_t lbo,
                                                            uint32_t sbo) {
   return (uint32_t)(r >> 3) * sbo + (uint32_t)(k >> 3) * lbo + (uint32_t)(r & 7) * 16u +
          (uint32_t)(k & 7) * 2u;
 }
 
-// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, both operands
-// K-major, dense, M x N (M in {64, 128}, N a multiple of 8 (M = 64) or 16).
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Byte offset of bf16 element (r, k) (r along M/N) in the MN-major layout.
+__host__ __device__ __forceinline__ uint32_t mnmajor_offset(int r, int k, uint32_t lbo,
+                                                            uint32_t sbo) {
+  return (uint32_t)(r >> 3) * sbo + (uint32_t)(k >> 3) * lbo + (uint32_t)(k & 7) * 16u +
+         (uint32_t)(r & 7) * 2u;
+}
+
+// Instruction descriptor of kind::f16 with bf16 A and B, fp32 D, dense, M x N
+// (M in {64, 128}, N a multiple of 8 (M = 64) or 16). a_mn / b_mn select the
+// MN-major layout for that operand. With M = 128, row i of D is TMEM lane i; with
+// M = 64, rows 16q..16q+15 are lanes 32q..32q+15 (measured on sm_103a).
+__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn = false,
+                                                      bool b_mn = false) {
   return (1u << 4)                        // D format: f32
          | (1u << 7)                      // A format: bf16
          | (1u << 10)                     // B format: bf16
+         | ((a_mn ? 1u : 0u) << 15)       // A major-ness
+         | ((b_mn ? 1u : 0u) << 16)       // B major-ness
          | ((uint32_t)(N >> 3) << 17)     // N / 8
          | ((uint32_t)(M >> 4) << 24);    // M / 16
 }

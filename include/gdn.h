@@ -69,7 +69,8 @@ typedef enum gdn_status {
 typedef enum gdn_dev_status {
   GDN_DEV_BAD_CU_SEQLENS = 1,     /* cu_seqlens not monotone or beyond T: clamped */
   GDN_DEV_CHUNK_OVERFLOW = 2,     /* more chunks than nt_max: the excess is skipped */
-  GDN_DEV_BAD_CHUNK_TABLE = 4     /* caller table names a chunk that does not exist: skipped */
+  GDN_DEV_BAD_CHUNK_TABLE = 4,    /* caller table names a chunk that does not exist: skipped */
+  GDN_DEV_TIMEOUT = 8             /* a bounded on-chip wait gave up (results invalid) */
 } gdn_dev_status;
 
 enum {
