@@ -3,6 +3,8 @@
 // synchronization, no device reads: every call only enqueues on `stream`.
 #include <math.h>
 
+#include <cuda.h>
+
 #include <mutex>
 #include <set>
 #include <utility>
@@ -23,6 +25,38 @@ void ensure_smem_limit(const void* kernel, int bytes) {
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
       cudaSuccess)
     done.insert({kernel, dev});
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled through the runtime's driver entry point (no libcuda link).
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = []() -> EncodeTiledFn {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<EncodeTiledFn>(f);
+  }();
+  return fn;
+}
+
+bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kDk, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)kDk * 2, (cuuint64_t)heads * kDk * 2};
+  const cuuint32_t box[3] = {64, 1, 64};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace gdn
@@ -148,7 +182,11 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
     if (tc) launch_tc_intra(p, stream); else launch_simt_intra(p, false, stream);
   }
   if (ev) cudaEventRecord(ev[2], stream);
-  if (tc) launch_tc_inter(p, stream); else launch_simt_inter(p, false, stream);
+  if (tc) {
+    if (!launch_tc_inter(p, stream)) return GDN_ERR_LAUNCH_FAILED;
+  } else {
+    launch_simt_inter(p, false, stream);
+  }
   if (ev) cudaEventRecord(ev[3], stream);
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }

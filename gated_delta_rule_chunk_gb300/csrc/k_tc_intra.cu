@@ -21,6 +21,13 @@
 // would cost ~1e-2 of the output's rms. MMA A-fragments of the scaled T are
 // built in registers straight from the fp32 T tile.
 //
+// The bridge is written as the exact shared-memory images the inter-chunk
+// kernel's tensor cores read, so that kernel moves each with one bulk copy:
+//   w: two 64-column halves, each [64 rows][128 B] with the 128-byte swizzle
+//      (16-byte chunk c of row r stored at chunk c ^ (r % 8));
+//   M: [128 rows: hi then lo][128 B], same swizzle;
+//   u: [dv/32 blocks][64 rows][32 fp32], 16-byte chunk c of row r at c ^ (r % 8).
+//
 // Occupancy: ~75 KB of shared memory and 128 threads per CTA, so that several
 // CTAs share an SM and hide each other's latency.
 #include "gdn_common.cuh"
@@ -40,6 +47,15 @@ struct IntraSmem {
   float X[16 * LDT];
   float G[64], B[64], E[64], KR[64];
 };
+
+// Byte offset of bf16 element (r, k), k < 64, in a [rows][128 B] tile with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
+  return (uint32_t)r * 128u + ((uint32_t)((k >> 3) ^ (r & 7)) << 4) + (uint32_t)(k & 7) * 2u;
+}
+// Byte offset of fp32 element (r, j), j < 32, in a [rows][32] tile with 16-byte chunks swizzled.
+__device__ __forceinline__ uint32_t u_offset(int r, int j) {
+  return (uint32_t)r * 128u + ((uint32_t)((j >> 2) ^ (r & 7)) << 4) + (uint32_t)(j & 3) * 4u;
+}
 
 __device__ __forceinline__ bool resolve(const Params& p, int slot, int& t0, int& L, int& wslot) {
   const int2 e = p.chunk_table[slot];
@@ -154,8 +170,7 @@ __global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
 
     // A (strictly lower, to shared memory) and M (hi/lo, to global) from the register tiles.
     {
-      __nv_bfloat16* Mh = static_cast<__nv_bfloat16*>(p.M) + sl * 2 * 64 * 64;
-      __nv_bfloat16* Ml = Mh + 64 * 64;
+      unsigned char* Mimg = static_cast<unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2;
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
         const int i = r0 + g + 8 * hh;
@@ -172,7 +187,8 @@ __global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
             m2[e] = dec * qi * s.KR[jj] * qk[nt][2 * hh + e];
           }
           *reinterpret_cast<float2*>(&s.AT[i * LDT + j]) = make_float2(a2[0], a2[1]);
-          split2_store(Mh + i * 64 + j, Ml + i * 64 + j, m2[0], m2[1]);
+          split2_store(reinterpret_cast<__nv_bfloat16*>(Mimg + sw128_offset(i, j)),
+                       reinterpret_cast<__nv_bfloat16*>(Mimg + sw128_offset(64 + i, j)), m2[0], m2[1]);
         }
       }
     }
@@ -205,12 +221,13 @@ __global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
           }
         }
       }
-      __nv_bfloat16* wo = static_cast<__nv_bfloat16*>(p.w) + sl * 64 * kDk;
+      unsigned char* wimg = static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2;
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         const int col = 8 * nt + c;
-        *reinterpret_cast<uint32_t*>(&wo[(r0 + g) * kDk + col]) = pack_bf16(acc[nt][0], acc[nt][1]);
-        *reinterpret_cast<uint32_t*>(&wo[(r0 + g + 8) * kDk + col]) = pack_bf16(acc[nt][2], acc[nt][3]);
+        unsigned char* half = wimg + (col >> 6) * 8192;
+        *reinterpret_cast<uint32_t*>(half + sw128_offset(r0 + g, col & 63)) = pack_bf16(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<uint32_t*>(half + sw128_offset(r0 + g + 8, col & 63)) = pack_bf16(acc[nt][2], acc[nt][3]);
       }
     }
     // u = (T diag(beta)) V with the T operand split into bf16 hi + lo.
@@ -248,12 +265,13 @@ __global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
           }
         }
       }
-      float* uo = p.u + sl * 64 * kDv;
+      unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
 #pragma unroll
       for (int nt = 0; nt < 16; ++nt) {
         const int col = 8 * nt + c;
-        *reinterpret_cast<float2*>(&uo[(r0 + g) * kDv + col]) = make_float2(acc[nt][0], acc[nt][1]);
-        *reinterpret_cast<float2*>(&uo[(r0 + g + 8) * kDv + col]) = make_float2(acc[nt][2], acc[nt][3]);
+        unsigned char* blk = uimg + (col >> 5) * 64 * 32 * 4;
+        *reinterpret_cast<float2*>(blk + u_offset(r0 + g, col & 31)) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2*>(blk + u_offset(r0 + g + 8, col & 31)) = make_float2(acc[nt][2], acc[nt][3]);
       }
     }
     __syncthreads();  // A/T and the gates are rewritten for the next value head

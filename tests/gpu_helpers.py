@@ -26,11 +26,14 @@ def to_dev(x: dict, dev="cuda") -> dict:
     return out
 
 
-def run_gpu(x: dict, out_dtype=torch.float32, **kw):
+def run_gpu(x: dict, out_dtype=torch.float32, expect_status=0, **kw):
+    """Run the CUDA path through the C ABI; the device status word must be clean."""
     d = to_dev(x)
-    o, f = B.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"],
-                           d.get("initial_state"), d["cu_seqlens"], out_dtype=out_dtype, **kw)
-    torch.cuda.synchronize()
+    o, f, desc, _ = B.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"],
+                                    d.get("initial_state"), d["cu_seqlens"],
+                                    out_dtype=out_dtype, return_desc=True, **kw)
+    status = B.gdn_read_status(desc)
+    assert status == expect_status, f"device status {status:#x}"
     return o, f
 
 
