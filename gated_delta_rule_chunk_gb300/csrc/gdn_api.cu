@@ -162,6 +162,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.w = ws + L.w;
   p.u = reinterpret_cast<float*>(ws + L.u);
   p.M = ws + L.M;
+  p.k16 = L.k16 ? ws + L.k16 : nullptr;
   p.qrn = l2 ? reinterpret_cast<float*>(ws + L.qrn) : nullptr;
   p.krn = l2 ? reinterpret_cast<float*>(ws + L.krn) : nullptr;
   p.out_bf16 = d.out_dtype == GDN_BF16;

@@ -34,6 +34,7 @@ struct Params {
   void* w;                   // [nt_max, Hv, 64, dk]
   float* u;                  // [nt_max, Hv, 64, dv]
   void* M;                   // [nt_max, Hv, 64, 64] (or hi/lo pair) decay-masked q.k
+  void* k16;                 // [nt_max, H] fp16 images of the chunk's k tile (tensor-core path)
   const float* qrn;          // [T, H] 1/||q|| or null
   const float* krn;          // [T, H] 1/||k|| or null
   int out_bf16;
@@ -41,7 +42,7 @@ struct Params {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, qrn, krn, total;
+  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qrn, krn, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -62,6 +63,7 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
   L.w = take((tc_path ? 2 : 4) * slots * kChunk * kDk);
   L.u = take(sizeof(float) * slots * kChunk * kDv);
   L.M = take(4 * slots * kChunk * kChunk);
+  L.k16 = tc_path ? take((size_t)nt_max * H * kChunk * kDk * 2) : 0;
   L.qrn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
   L.krn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
   L.total = o;

@@ -26,7 +26,9 @@
 //   w: two 64-column halves, each [64 rows][128 B] with the 128-byte swizzle
 //      (16-byte chunk c of row r stored at chunk c ^ (r % 8));
 //   M: [128 rows: hi then lo][128 B], same swizzle;
-//   u: [dv/32 blocks][64 rows][32 fp32], 16-byte chunk c of row r at c ^ (r % 8).
+//   u: [dv/32 blocks][64 rows][32 fp32], 16-byte chunk c of row r at c ^ (r % 8);
+//   k (once per key head): fp16, scaled by 1/||k|| when the L2 norm is on, zero past
+//      the sequence end, two 64-column halves of [64 rows][128 B] with the 128-byte swizzle.
 //
 // Occupancy: ~75 KB of shared memory and 128 threads per CTA, so that several
 // CTAs share an SM and hide each other's latency.
@@ -116,6 +118,26 @@ __global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
   }
   cp_async_wait<0>();
   __syncthreads();
+
+  {  // fp16 image of the (normalised) k tile for the inter-chunk state update
+    unsigned char* kimg = static_cast<unsigned char*>(p.k16) + ((size_t)wslot * p.H + h) * 64 * kDk * 2;
+#pragma unroll
+    for (int it = 0; it < 8; ++it) {
+      const int idx = tid + it * 128;  // 1024 chunks of 8 elements
+      const int half = idx >> 9, t = (idx >> 3) & 63, ch = idx & 7;
+      const uint4 raw = *reinterpret_cast<const uint4*>(&s.K[t * LDB + half * 64 + ch * 8]);
+      const uint32_t* r = reinterpret_cast<const uint32_t*>(&raw);
+      uint4 v;
+      uint32_t* o = reinterpret_cast<uint32_t*>(&v);
+      const float sc = s.KR[t];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r[e]));
+        o[e] = pack_f16(f.x * sc, f.y * sc);
+      }
+      *reinterpret_cast<uint4*>(kimg + half * 8192 + t * 128 + ((ch ^ (t & 7)) << 4)) = v;
+    }
+  }
 
   // P = K K^T and R = Q K^T, rows r0..r0+15, column tiles on or below the diagonal.
   float kk[8][4], qk[8][4];
