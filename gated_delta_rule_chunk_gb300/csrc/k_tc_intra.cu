@@ -13,7 +13,8 @@
 //                                kept in registers across the value-head loop
 //   per value head hv of the group:
 //     G = inclusive in-chunk cumsum of g (fp32, left to right)
-//     A_ij = beta_i exp(G_i - G_j) P_ij (j < i);  T = (I + A)^-1 in place (fp32)
+//     A_ij = beta_i exp(G_i - G_j) P_ij (j < i);  T = (I + A)^-1 in place (fp32 diagonal
+//            blocks, off-diagonal blocks on tensor-core MMAs with split operands)
 //     w    = (T diag(beta exp(G))) K        (bf16 operand and store)
 //     u    = (T diag(beta)) V               (T operand split into bf16 hi + lo; fp32 store)
 //     M_ij = exp(G_i - G_j) R_ij (j <= i)   (stored as a bf16 hi/lo pair)
@@ -204,7 +205,7 @@ __global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int jj = j + e;
-            const float dec = (jj <= i) ? expf(gi - s.G[jj]) : 0.f;
+            const float dec = (jj <= i) ? __expf(gi - s.G[jj]) : 0.f;
             a2[e] = (jj < i) ? bi * dec * s.KR[jj] * kk[nt][2 * hh + e] : 0.f;
             m2[e] = dec * qi * s.KR[jj] * qk[nt][2 * hh + e];
           }
@@ -215,7 +216,7 @@ __global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
       }
     }
     __syncthreads();
-    tri_inverse_64_inplace(s.AT, LDT, s.X, tid, 128);
+    tri_inverse_64_tc(s.AT, LDT, s.X, tid);
 
     // w = (T diag(beta exp(G) krn)) K, rows r0..r0+15; T is lower triangular (k-tiles <= warp).
     {

@@ -99,3 +99,106 @@ __device__ inline void tri_inverse_64_inplace(float* AT, int ld, float* X, int t
 }
 
 }  // namespace gdn
+
+#include "warp_mma.cuh"
+
+namespace gdn {
+
+// fp32 pair -> bf16 hi pair and bf16 lo pair (x = hi + lo to about 16 bits).
+__device__ __forceinline__ void split_pack2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
+// Split A fragment (16 x 16 at (r0, c0)) of a row-major fp32 tile with stride ld.
+__device__ __forceinline__ void frag_a_split(const float* base, int ld, int r0, int c0, int lane,
+                                             uint32_t (&hi)[4], uint32_t (&lo)[4]) {
+  const int g = lane >> 2, c = 2 * (lane & 3);
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const float2 v = *reinterpret_cast<const float2*>(
+        &base[(r0 + g + 8 * (q & 1)) * ld + c0 + c + 8 * (q >> 1)]);
+    split_pack2(v.x, v.y, hi[q], lo[q]);
+  }
+}
+
+// Split B fragment (16 k x 8 n at (k0, n0)) of a row-major [k][n] fp32 tile.
+__device__ __forceinline__ void frag_b_split(const float* base, int ld, int k0, int n0, int lane,
+                                             uint32_t (&hi)[2], uint32_t (&lo)[2]) {
+  const int g = lane >> 2, c = 2 * (lane & 3);
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    const float x0 = base[(k0 + c + 8 * q) * ld + n0 + g];
+    const float x1 = base[(k0 + c + 8 * q + 1) * ld + n0 + g];
+    split_pack2(x0, x1, hi[q], lo[q]);
+  }
+}
+
+// D += A * B with both operands split into bf16 hi/lo (the lo*lo product dropped).
+__device__ __forceinline__ void mma_split3(float (&d)[4], const uint32_t (&ah)[4],
+                                           const uint32_t (&al)[4], const uint32_t (&bh)[2],
+                                           const uint32_t (&bl)[2]) {
+  mma_bf16(d, ah, bh[0], bh[1]);
+  mma_bf16(d, ah, bl[0], bl[1]);
+  mma_bf16(d, al, bh[0], bh[1]);
+}
+
+// In-place inverse of I + A (64 x 64, A strictly lower triangular with zeros on and
+// above the diagonal) for a CTA of 128 threads. The four diagonal 16 x 16 blocks are
+// inverted column by column (SIMT, fp32); block row a = 1..3 then needs two small
+// products, X = A[a, 0:a] T[0:a, 0:a] and T[a, 0:a] = -T[a, a] X, done on warp-level
+// tensor-core MMAs with the fp32 operands split into bf16 hi + lo (about 16
+// significant bits, fp32 accumulate). X: 16 rows x ld scratch.
+__device__ inline void tri_inverse_64_tc(float* AT, int ld, float* X, int tid) {
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = 2 * (lane & 3);
+  float col[16];
+  const int base = (tid >> 4) * 16, cc = tid & 15;
+  if (tid < 64) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        if (m < i) acc = fmaf(AT[(base + i) * ld + base + m], col[m], acc);
+      col[i] = (i < cc) ? 0.f : (i == cc ? 1.f : -acc);
+    }
+  }
+  __syncthreads();  // every diagonal block of A has been read
+  if (tid < 64) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) AT[(base + i) * ld + base + cc] = col[i];
+  }
+  __syncthreads();
+#pragma unroll
+  for (int a = 1; a < 4; ++a) {
+    const int r0 = 16 * a;
+    for (int nt = warp; nt < 2 * a; nt += 4) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int ks = 0; ks < a; ++ks) {
+        uint32_t ah[4], al[4], bh[2], bl[2];
+        frag_a_split(AT, ld, r0, 16 * ks, lane, ah, al);
+        frag_b_split(AT, ld, 16 * ks, 8 * nt, lane, bh, bl);
+        mma_split3(acc, ah, al, bh, bl);
+      }
+      *reinterpret_cast<float2*>(&X[g * ld + 8 * nt + c]) = make_float2(acc[0], acc[1]);
+      *reinterpret_cast<float2*>(&X[(g + 8) * ld + 8 * nt + c]) = make_float2(acc[2], acc[3]);
+    }
+    __syncthreads();
+    for (int nt = warp; nt < 2 * a; nt += 4) {
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      uint32_t ah[4], al[4], bh[2], bl[2];
+      frag_a_split(AT, ld, r0, r0, lane, ah, al);
+      frag_b_split(X, ld, 0, 8 * nt, lane, bh, bl);
+      mma_split3(acc, ah, al, bh, bl);
+      *reinterpret_cast<float2*>(&AT[(r0 + g) * ld + 8 * nt + c]) = make_float2(-acc[0], -acc[1]);
+      *reinterpret_cast<float2*>(&AT[(r0 + g + 8) * ld + 8 * nt + c]) = make_float2(-acc[2], -acc[3]);
+    }
+    __syncthreads();
+  }
+}
+
+}  // namespace gdn
