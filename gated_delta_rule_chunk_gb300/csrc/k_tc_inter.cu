@@ -15,19 +15,26 @@
 //   output (off the chain):
 //                     o = scale (diag(exp(G)) Q (S_hi + S_lo) + (M_hi + M_lo)(vn_hi + vn_lo))
 //
-// Warp roles (13 warps):
+// Warp roles (15 warps):
 //   * 8 chain warps run the serial recurrence on warp-level MMAs (lowest latency
 //     per dependent step); the state lives in their registers as fp32 MMA
 //     accumulators (warp w owns key rows 16w..16w+15). The state-update product
 //     uses fp16 operands (k as written by the intra kernel, vh rounded once), which
 //     keeps about 11 significant bits where bf16 would keep 8.
-//   * 1 producer warp issues every TMA copy (the q tile by tensor map with the
-//     128-byte swizzle; w, M, u, G and the fp16 k tile as bulk copies of images the
-//     intra kernel wrote in this kernel's layout) and the output MMAs on the 5th-generation tensor
-//     cores: D_QS = [Q; w] [S_hi | S_lo] and D_M = [M_hi; M_lo] [vn_hi | vn_lo]
-//     (M = 128, N = 64, fp32 accumulators in TMEM, double-buffered per chunk).
-//   * 4 output warps (one per TMEM lane quarter) finish chunk c's output while
-//     the chain works on chunk c + 1.
+//   * 1 load warp issues every TMA copy (the q tile by tensor map with the 128-byte
+//     swizzle; w, M, u, G and the fp16 k tile as bulk copies of images the intra
+//     kernel wrote in this kernel's layout).
+//   * 2 MMA warps (one thread each) issue the output MMAs on the 5th-generation
+//     tensor cores: D_QS = Q [S_hi | S_lo] and D_M = M_hi [vn_hi | vn_lo] +
+//     M_lo [vn_hi | vn_lo] (M = 64, N = 64, fp32 accumulators in TMEM, double-buffered
+//     per chunk; the two column halves are summed when the output is formed). What
+//     the chain reads (w, fp16 k, u, G) streams through a 3-slot ring so that each
+//     chunk's copies are issued two chunks ahead; q (double-buffered) and M (one
+//     buffer, refilled once the previous chunk's D_M is complete) feed only the
+//     output MMAs.
+//   * 4 output warps (one per TMEM lane quarter; rows 16q..16q+15 of an M = 64
+//     result sit in lanes 32q..32q+15) finish chunk c's output while the chain
+//     works on chunk c + 1.
 // Hand-offs use mbarriers; every wait is bounded (GDN_DEV_TIMEOUT on expiry).
 #include <cuda.h>
 
@@ -43,40 +50,50 @@ constexpr int BV = 32;
 constexpr uint32_t kWaitIters = 1u << 22;
 constexpr int kChainWarps = 8;
 constexpr int kOutWarps = 4;
-constexpr int kProducerWarp = kChainWarps + kOutWarps;
-constexpr int kThreads = (kProducerWarp + 1) * 32;
+constexpr int kLoadWarp = kChainWarps + kOutWarps;
+constexpr int kQsWarp = kLoadWarp + 1;  // issues D_QS; owns the TMEM allocation
+constexpr int kMWarp = kQsWarp + 1;     // issues D_M
+constexpr int kThreads = (kMWarp + 1) * 32;
 constexpr int kChainThreads = kChainWarps * 32;
 
-// One prefetch stage (bytes; 128-byte-swizzled tiles are 1024-byte aligned).
-constexpr uint32_t kAQ = 0;          // [Q; w]: two dk halves of [128 rows][128 B], K-major, swizzled
-constexpr uint32_t kKT = 32768;      // k (fp16 image): two dk halves of [64 tokens][128 B], swizzled
-constexpr uint32_t kAM = 49152;      // [M_hi; M_lo]: [128 rows][128 B], K-major, swizzled
-constexpr uint32_t kU = 65536;       // u block: fp32 [64][32], 16-byte chunks swizzled by row
-constexpr uint32_t kG = 73728;       // G [64]
-constexpr uint32_t kStage = 74752;   // 73 x 1024
-// Bytes the copies of one stage deliver: q tile (2 x 8 KB), w (2 x 8 KB), fp16 k (16 KB),
-// M (16 KB), u (8 KB), G (256 B).
-constexpr uint32_t kStageTx = 4 * 8192 + 16384 + 16384 + 8192 + 256;
+// Ring slot of the chain's operands (bytes; 128-byte-swizzled tiles are 1024-byte aligned).
+constexpr uint32_t kW = 0;           // w: two dk halves of [64 rows][128 B], K-major, swizzled
+constexpr uint32_t kK = 16384;       // k (fp16 image): two dk halves of [64 tokens][128 B], swizzled
+constexpr uint32_t kU = 32768;       // u block: fp32 [64][32], 16-byte chunks swizzled by row
+constexpr uint32_t kG = 40960;       // G [64]
+constexpr uint32_t kSlot = 41984;    // 41 x 1024
+constexpr int kRing = 3;
+constexpr uint32_t kTxRing = 2 * 8192 + 16384 + 8192 + 256;  // w, k, u, G
+// q (two buffers of two swizzled [64 rows][128 B] key-dim halves) and [M_hi; M_lo]
+// ([128 rows][128 B], swizzled) for the output MMAs.
+constexpr uint32_t kQ = kRing * kSlot;
+constexpr uint32_t kQsz = 16384;
+constexpr uint32_t kM = kQ + 2 * kQsz;
 // Operands written by the threads (no-swizzle MN-major core matrices: the K
 // group stride is the descriptor's lbo, sbo = 128 along N).
-constexpr uint32_t kSB = 2 * kStage;       // 2 x [S_hi | S_lo]: N = 64, K = 128 (key dim)
+constexpr uint32_t kSB = kM + 16384;       // 2 x [S_hi | S_lo]: N = 64, K = 128 (key dim)
 constexpr uint32_t kSBsz = 16384;
 constexpr uint32_t kVN = kSB + 2 * kSBsz;  // 2 x [vn_hi | vn_lo]: N = 64, K = 64 (tokens)
 constexpr uint32_t kVNsz = 8192;
 constexpr uint32_t kVH = kVN + 2 * kVNsz;  // vh (fp16): N = 32, K = 64 (tokens)
-constexpr uint32_t kX4 = kVH + 4096;       // fp32 [64][32]: rows 64..127 of D_M for the output
-constexpr uint32_t kBar = kX4 + 8192;      // 14 mbarriers
-constexpr uint32_t kMisc = kBar + 128;     // TMEM base address, abort flag
+constexpr uint32_t kBar = kVH + 4096;      // 19 mbarriers
+constexpr uint32_t kMisc = kBar + 256;     // TMEM base address, abort flag
 constexpr uint32_t kSmemBytes = kMisc + 16 + 1024;  // + room to align the base to 1024
 
-// mbarrier indices (double-buffered: chunk c uses index + (c & 1) with parity (c >> 1) & 1)
-constexpr int B_FULL = 0;   // stage copies landed (transaction count)
-constexpr int B_SBR = 2;    // S split of chunk c written (one arrival per chain warp)
-constexpr int B_VNR = 4;    // vn of chunk c written (one arrival per chain warp)
-constexpr int B_QSD = 6;    // D_QS of chunk c complete (tcgen05.commit)
-constexpr int B_MD = 8;     // D_M of chunk c complete (tcgen05.commit)
-constexpr int B_OD = 10;    // output warps done with the TMEM buffer of chunk c (per output warp)
-constexpr int B_CD = 12;    // chain warps done reading the stage of chunk c (per chain warp)
+// mbarrier indices. Ring barriers: chunk c uses slot c % 3 with parity (c / 3) & 1;
+// double-buffered barriers: index + (c & 1) with parity (c >> 1) & 1; B_MF: one
+// completion per chunk, parity c & 1.
+constexpr int B_FULL = 0;   // ring slot of chunk c landed (transaction count)
+constexpr int B_CD = 3;     // chain warps done reading the ring slot of chunk c (per chain warp)
+constexpr int B_QF = 6;     // q of chunk c landed
+constexpr int B_MF = 8;     // M of chunk c landed
+constexpr int B_XD = 9;     // chain warps finished X of chunk c (one arrival per chain warp);
+                            // each had written the S split of chunk c before
+constexpr int B_QSD = 11;   // D_QS of chunk c complete (tcgen05.commit)
+constexpr int B_MD = 13;    // D_M of chunk c complete (tcgen05.commit)
+constexpr int B_OD = 15;    // output warps done with the TMEM buffer of chunk c (per output warp)
+constexpr int kNumBars = 17;
+constexpr uint32_t kTmemCols = 256;
 
 // Byte offset of (n, k) in a no-swizzle MN-major tile with `kgrp` bytes per 8-deep K group.
 __device__ __forceinline__ uint32_t mn_off(int n, int k, uint32_t kgrp) {
@@ -105,10 +122,8 @@ __device__ __forceinline__ uint4 pack8_bf16(const float* x) {
 // bounded number of polls (raising the abort flag), and at once when the flag is
 // already raised, so that after a failure every role runs through its remaining
 // iterations without waiting and the CTA's barriers stay consistent.
-__device__ __forceinline__ bool wait_chunk(uint64_t* bars, int base, int c,
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity,
                                            volatile int* abort_flag) {
-  uint64_t* bar = &bars[base + (c & 1)];
-  const uint32_t parity = (uint32_t)((c >> 1) & 1);
   for (uint32_t i = 0; i < kWaitIters; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
@@ -116,26 +131,43 @@ __device__ __forceinline__ bool wait_chunk(uint64_t* bars, int base, int c,
   *abort_flag = 1;
   return false;
 }
+__device__ __forceinline__ bool wait_chunk(uint64_t* bars, int base, int c,
+                                           volatile int* abort_flag) {
+  return wait_phase(&bars[base + (c & 1)], (uint32_t)((c >> 1) & 1), abort_flag);
+}
+__device__ __forceinline__ bool wait_ring(uint64_t* bars, int base, int c,
+                                          volatile int* abort_flag) {
+  return wait_phase(&bars[base + c % kRing], (uint32_t)((c / kRing) & 1), abort_flag);
+}
 
-// Issued by one thread: every copy of chunk `slot` into stage `st`, counted on *full.
-__device__ __forceinline__ void issue_stage(unsigned char* st, uint64_t* full, const Params& p,
-                                            const CUtensorMap* tmq, int slot, int hv, int h,
-                                            int jb, int t0) {
+// Issued by one thread: the chain's copies of chunk `slot` into ring slot `st`.
+__device__ __forceinline__ void issue_ring(unsigned char* st, uint64_t* full, const Params& p,
+                                           int slot, int hv, int h, int jb) {
   const size_t sl = (size_t)slot * p.Hv + hv;
   const unsigned char* wimg = static_cast<const unsigned char*>(p.w) + sl * 64 * kDk * 2;
-  const unsigned char* mimg = static_cast<const unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2;
   const unsigned char* uimg = reinterpret_cast<const unsigned char*>(p.u + sl * 64 * kDv);
   const unsigned char* kimg =
       static_cast<const unsigned char*>(p.k16) + ((size_t)slot * p.H + h) * 64 * kDk * 2;
-  mbar_expect_tx(full, kStageTx);
-  tma_load_3d(st + kAQ, tmq, 0, h, t0, full);
-  tma_load_3d(st + kAQ + 16384, tmq, 64, h, t0, full);
-  bulk_load(st + kAQ + 8192, wimg, 8192, full);
-  bulk_load(st + kAQ + 16384 + 8192, wimg + 8192, 8192, full);
-  bulk_load(st + kKT, kimg, 16384, full);
-  bulk_load(st + kAM, mimg, 16384, full);
+  mbar_expect_tx(full, kTxRing);
+  bulk_load(st + kW, wimg, 16384, full);
+  bulk_load(st + kK, kimg, 16384, full);
   bulk_load(st + kU, uimg + jb * 8192, 8192, full);
   bulk_load(st + kG, p.G + sl * 64, 256, full);
+}
+
+// Issued by one thread: the two key-dim halves of chunk c's q tile (rows t0..t0+63).
+__device__ __forceinline__ void issue_q(unsigned char* dst, uint64_t* full, const CUtensorMap* tmq,
+                                        int h, int t0) {
+  mbar_expect_tx(full, 2 * 8192);
+  tma_load_3d(dst, tmq, 0, h, t0, full);
+  tma_load_3d(dst + 8192, tmq, 64, h, t0, full);
+}
+// Issued by one thread: the [M_hi; M_lo] image of chunk `slot`.
+__device__ __forceinline__ void issue_m(unsigned char* dst, uint64_t* full, const Params& p,
+                                        int slot, int hv) {
+  const size_t sl = (size_t)slot * p.Hv + hv;
+  mbar_expect_tx(full, 16384);
+  bulk_load(dst, static_cast<const unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2, 16384, full);
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -158,13 +190,15 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   const uint32_t sbase = smem_addr(sm);
   const int g = lane >> 2, c2 = 2 * (lane & 3);
 
-  if (warp == kProducerWarp) {
-    tmem_alloc(tmem_slot, 256);
+  if (warp == kQsWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   if (tid == 0) {
-    const uint32_t counts[7] = {1, kChainWarps, kChainWarps, 1, 1, kOutWarps, kChainWarps};
-    for (int b = 0; b < 14; ++b) mbar_init(&bars[b], counts[b >> 1]);
+    for (int b = 0; b < kNumBars; ++b) {
+      const bool per_chain = (b >= B_CD && b < B_QF) || (b >= B_XD && b < B_QSD);  // CD, XD
+      mbar_init(&bars[b], per_chain ? kChainWarps : (b >= B_OD ? kOutWarps : 1));
+    }
     mbar_init_fence();
     *abort_flag = 0;
   }
@@ -202,17 +236,13 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       fence_async_smem();
       __syncwarp();
     };
-    if (nch > 0) {
-      store_split_state(0);
-      if (lane == 0) mbar_arrive(&bars[B_SBR]);
-    }
+    if (nch > 0) store_split_state(0);
     named_sync(1, kChainThreads);
     for (int c = 0; c < nch; ++c) {
       const int b = c & 1;
-      unsigned char* st = sm + b * kStage;
-      const uint32_t st_a = sbase + b * kStage;
-      const int L = min(kChunk, sv.len - kChunk * c);
-      wait_chunk(bars, B_FULL, c, abort_flag);
+      unsigned char* st = sm + (c % kRing) * kSlot;
+      const uint32_t st_a = sbase + (c % kRing) * kSlot;
+      wait_ring(bars, B_FULL, c, abort_flag);
 
       // X = w S_hi: token rows 16mt.., columns 16np..16np+15
       float xa[2][4];
@@ -226,9 +256,9 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         uint32_t a[4], bb[4];
         const int i = lane >> 3;
         {
-          const int row = 64 + 16 * mt + (lane & 7) + (i & 1) * 8;  // w rows of [Q; w]
+          const int row = 16 * mt + (lane & 7) + (i & 1) * 8;
           const int col = (16 * ks + (i >> 1) * 8) & 63;
-          ldsm_x4_addr(a, st_a + kAQ + (ks >> 2) * 16384 + sw_chunk(row, col));
+          ldsm_x4_addr(a, st_a + kW + (ks >> 2) * 8192 + sw_chunk(row, col));
         }
         {
           const int nn = 16 * np + (i >> 1) * 8, kk = 16 * ks + (i & 1) * 8;
@@ -238,6 +268,10 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         mma_bf16(xa[0], a, bb[0], bb[1]);
         mma_bf16(xa[1], a, bb[2], bb[3]);
       }
+      // The output MMAs share the tensor datapath with the warp MMAs: D_QS of chunk c is
+      // issued now and runs while the chain forms v_new (no MMAs there).
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_XD + b]);
       // v_new = u - X; vn (bf16 hi|lo) for the output MMA; vh (fp16) for the state update.
       if (c >= 2) wait_chunk(bars, B_MD, c - 2, abort_flag);  // vn buffer b no longer read
       {
@@ -263,9 +297,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
           }
         }
       }
-      fence_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_VNR + b]);
+      fence_async_smem();  // vn visible to the tensor cores once this warp arrives on B_CD
       named_sync(1, kChainThreads);  // vh visible to every chain warp
 
       // S <- exp(G_L) S + K^T vh   (key rows 16*warp.., all 32 columns; fp16 operands)
@@ -275,7 +307,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) S[nt][e] *= gam;
-        const uint32_t kt = st_a + kKT + (warp >> 2) * 8192;
+        const uint32_t kt = st_a + kK + (warp >> 2) * 8192;
         const uint32_t vhb = sbase + kVH;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) {
@@ -297,14 +329,15 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
           }
         }
       }
+      // Ring slot of chunk c released; vn of chunk c complete. D_M of chunk c runs while
+      // the chain stores the split of the next state (no MMAs there).
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars[B_CD + c % kRing]);
       // split of S_{c+1} for the next chunk (its buffer was last read by D_QS of chunk c - 1)
       if (c + 1 < nch) {
         if (c >= 1) wait_chunk(bars, B_QSD, c - 1, abort_flag);
         store_split_state((c + 1) & 1);
-        if (lane == 0) mbar_arrive(&bars[B_SBR + ((c + 1) & 1)]);
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars[B_CD + b]);
       named_sync(1, kChainThreads);  // new split visible; vh may be rewritten
     }
     if (p.sT) {
@@ -316,119 +349,152 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
           p.sT[state_base + (size_t)(c0 + j) * kDk + d] = S[nt][e];
         }
     }
-  } else if (warp < kProducerWarp) {
+  } else if (warp < kLoadWarp) {
     // ------------------------------------------------------------------ output
     const int qd = warp - kChainWarps;  // TMEM lane quarter
     const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-    unsigned char* x4 = sm + kX4;
+    const int i = 16 * qd + (lane & 15);  // token row of this lane (lanes 16..31 idle)
     for (int c = 0; c < nch; ++c) {
       const int b = c & 1;
       const int t0 = sv.start + kChunk * c;
       const int L = min(kChunk, sv.len - kChunk * c);
       // row factor exp(G_i) / ||q_i|| straight from global memory (off the critical path)
-      const int ir = 32 * (qd & 1) + lane;
       const size_t sl = (size_t)(sv.first_slot + c) * p.Hv + hv;
-      const float grow = p.G[sl * 64 + ir];
-      const float qrow = (p.qrn && ir < L) ? p.qrn[(size_t)(t0 + ir) * p.H + h] : 1.f;
+      const float grow = p.G[sl * 64 + i];
+      const float qrow = (p.qrn && i < L) ? p.qrn[(size_t)(t0 + i) * p.H + h] : 1.f;
+      wait_chunk(bars, B_QSD, c, abort_flag);
       wait_chunk(bars, B_MD, c, abort_flag);
       tc_fence_after();
       const uint32_t dq = tmem + b * 128 + lane_base, dm = dq + 64;
-      float m[32], t[32], qs[32];
+      float m[32], qs[32], t[32];
       tmem_ld32(dm, m);
       tmem_ld32(dm + 32, t);
       tmem_ld_wait();
 #pragma unroll
-      for (int j = 0; j < 32; ++j) m[j] += t[j];  // M_x (vn_hi + vn_lo)
-      if (qd < 2) {
-        tmem_ld32(dq, qs);
-        tmem_ld32(dq + 32, t);
-        tmem_ld_wait();
+      for (int j = 0; j < 32; ++j) m[j] += t[j];  // M (vn_hi + vn_lo)
+      tmem_ld32(dq, qs);
+      tmem_ld32(dq + 32, t);
+      tmem_ld_wait();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) qs[j] += t[j];  // Q (S_hi + S_lo)
-      } else {
-#pragma unroll
-        for (int a = 0; a < 8; ++a)
-          *reinterpret_cast<float4*>(x4 + u_off(32 * (qd - 2) + lane, 4 * a)) =
-              make_float4(m[4 * a], m[4 * a + 1], m[4 * a + 2], m[4 * a + 3]);
-      }
+      for (int j = 0; j < 32; ++j) qs[j] += t[j];  // Q (S_hi + S_lo)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_OD + b]);
-      named_sync(2, kOutWarps * 32);  // rows 64..127 of D_M handed over
-      if (qd < 2) {
-        const int i = 32 * qd + lane;
-        if (i < L) {
-          const float e = expf(grow) * qrow;
-          float o[32];
+      if (lane < 16 && i < L) {
+        const float e = expf(grow) * qrow;
+        float o[32];
 #pragma unroll
-          for (int a = 0; a < 8; ++a) {
-            const float4 l4 = *reinterpret_cast<const float4*>(x4 + u_off(i, 4 * a));
-            o[4 * a] = p.scale * (e * qs[4 * a] + m[4 * a] + l4.x);
-            o[4 * a + 1] = p.scale * (e * qs[4 * a + 1] + m[4 * a + 1] + l4.y);
-            o[4 * a + 2] = p.scale * (e * qs[4 * a + 2] + m[4 * a + 2] + l4.z);
-            o[4 * a + 3] = p.scale * (e * qs[4 * a + 3] + m[4 * a + 3] + l4.w);
-          }
-          const size_t oi = ((size_t)(t0 + i) * p.Hv + hv) * kDv + c0;
-          if (p.out_bf16) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + oi);
+        for (int j = 0; j < 32; ++j) o[j] = p.scale * (e * qs[j] + m[j]);
+        const size_t oi = ((size_t)(t0 + i) * p.Hv + hv) * kDv + c0;
+        if (p.out_bf16) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + oi);
 #pragma unroll
-            for (int a = 0; a < 4; ++a) dst[a] = pack8_bf16(o + 8 * a);
-          } else {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
+          for (int a = 0; a < 4; ++a) dst[a] = pack8_bf16(o + 8 * a);
+        } else {
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.out) + oi);
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
-              dst[a] = make_float4(o[4 * a], o[4 * a + 1], o[4 * a + 2], o[4 * a + 3]);
-          }
+          for (int a = 0; a < 8; ++a)
+            dst[a] = make_float4(o[4 * a], o[4 * a + 1], o[4 * a + 2], o[4 * a + 3]);
         }
       }
-      named_sync(2, kOutWarps * 32);  // the exchange tile may be rewritten
     }
-  } else if (lane == 0) {
-    // ------------------------------------------------------------------ producer
-    const uint32_t id_o = idesc_bf16_f32(128, 64, false, true);
-    int issued = 0, committed = 0;  // stage loads issued; chunks whose D_M was committed
+  } else if (warp == kLoadWarp && lane == 0) {
+    // ------------------------------------------------------------------ loads
+    // ring chunks issued, q tiles issued, M tiles issued
+    int issued = 0, q_issued = 0, m_issued = 0;
+    for (int k = 0; k < min(nch, kRing - 1); ++k) {
+      issue_ring(sm + k * kSlot, &bars[B_FULL + k], p, sv.first_slot + k, hv, h, jb);
+      issued = k + 1;
+    }
+    for (int k = 0; k < min(nch, 2); ++k) {
+      issue_q(sm + kQ + k * kQsz, &bars[B_QF + k], &tmq, h, sv.start + kChunk * k);
+      q_issued = k + 1;
+    }
     if (nch > 0) {
-      issue_stage(sm, &bars[B_FULL], p, &tmq, sv.first_slot, hv, h, jb, sv.start);
-      issued = 1;
+      issue_m(sm + kM, &bars[B_MF], p, sv.first_slot, hv);
+      m_issued = 1;
     }
     for (int c = 0; c < nch; ++c) {
-      const int b = c & 1;
-      const uint32_t st_a = sbase + b * kStage;
       if (*abort_flag) break;
-      if (c + 1 < nch) {  // the other stage is free once chunk c - 1 is fully consumed
-        if (c >= 1) {
-          wait_chunk(bars, B_CD, c - 1, abort_flag);
-          wait_chunk(bars, B_MD, c - 1, abort_flag);
-        }
-        const int t1 = sv.start + kChunk * (c + 1);
-        issue_stage(sm + ((c + 1) & 1) * kStage, &bars[B_FULL + ((c + 1) & 1)], p, &tmq,
-                    sv.first_slot + c + 1, hv, h, jb, t1);
-        issued = c + 2;
+      if (c + kRing - 1 < nch) {  // ring slot of chunk c - 1 is free once the chain released it
+        if (c >= 1 && !wait_ring(bars, B_CD, c - 1, abort_flag)) break;
+        const int cn = c + kRing - 1;
+        issue_ring(sm + (cn % kRing) * kSlot, &bars[B_FULL + cn % kRing], p, sv.first_slot + cn,
+                   hv, h, jb);
+        issued = cn + 1;
       }
-      wait_chunk(bars, B_FULL, c, abort_flag);
-      wait_chunk(bars, B_SBR, c, abort_flag);
+      // q buffer of chunk c - 1 is free once its D_QS completed
+      if (c >= 1 && c + 1 < nch) {
+        if (!wait_chunk(bars, B_QSD, c - 1, abort_flag)) break;
+        issue_q(sm + kQ + ((c + 1) & 1) * kQsz, &bars[B_QF + ((c + 1) & 1)], &tmq, h,
+                sv.start + kChunk * (c + 1));
+        q_issued = c + 2;
+      }
+      // M is free once chunk c's D_M completed
+      if (c + 1 < nch) {
+        if (!wait_chunk(bars, B_MD, c, abort_flag)) break;
+        issue_m(sm + kM, &bars[B_MF], p, sv.first_slot + c + 1, hv);
+        m_issued = c + 2;
+      }
+    }
+    // Before the CTA retires: every copy this thread issued has landed (bounded waits).
+    for (int k = max(0, issued - kRing); k < issued; ++k)
+      mbar_wait(&bars[B_FULL + k % kRing], (uint32_t)((k / kRing) & 1), kWaitIters);
+    for (int k = max(0, q_issued - 2); k < q_issued; ++k)
+      mbar_wait(&bars[B_QF + (k & 1)], (uint32_t)((k >> 1) & 1), kWaitIters);
+    if (m_issued > 0) mbar_wait(&bars[B_MF], (uint32_t)((m_issued - 1) & 1), kWaitIters);
+  } else if (warp == kQsWarp && lane == 0) {
+    // ------------------------------------------------------------------ D_QS
+    // D_QS of chunk c = Q [S_hi | S_lo]; issued once the chain finished X of chunk c,
+    // so that it runs while the chain forms v_new (the output MMAs share the tensor
+    // datapath with the warp MMAs of the chain).
+    const uint32_t id_o = idesc_bf16_f32(64, 64, false, true);
+    int committed = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int b = c & 1;
+      if (*abort_flag) break;
+      wait_chunk(bars, B_QF, c, abort_flag);
+      wait_chunk(bars, B_XD, c, abort_flag);
       if (c >= 2) wait_chunk(bars, B_OD, c - 2, abort_flag);
       tc_fence_after();
+      const uint32_t q_a = sbase + kQ + b * kQsz;
       const uint32_t sbb = sbase + kSB + b * kSBsz;
-      const uint32_t dq = tmem + b * 128;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks)
-        umma_bf16(dq, sdesc_sw128(st_a + kAQ + (ks >> 2) * 16384 + 32 * (ks & 3), 16, 1024),
+        umma_bf16(tmem + b * 128, sdesc_sw128(q_a + (ks >> 2) * 8192 + 32 * (ks & 3), 16, 1024),
                   sdesc(sbb + 2048 * ks, 1024, 128), id_o, ks > 0);
       umma_commit(&bars[B_QSD + b]);
-      wait_chunk(bars, B_VNR, c, abort_flag);
+      committed = c + 1;
+    }
+    // Before the CTA retires: every MMA this thread issued has completed (bounded wait).
+    if (committed > 0)
+      mbar_wait(&bars[B_QSD + ((committed - 1) & 1)], (uint32_t)(((committed - 1) >> 1) & 1),
+                kWaitIters);
+  } else if (warp == kMWarp && lane == 0) {
+    // ------------------------------------------------------------------ D_M
+    // D_M of chunk c = M_hi [vn_hi | vn_lo] + M_lo [vn_hi | vn_lo]; issued once the
+    // chain finished the state update of chunk c, so that it runs while the chain
+    // stores the split of the next state.
+    const uint32_t id_o = idesc_bf16_f32(64, 64, false, true);
+    const uint32_t m_a = sbase + kM;
+    int committed = 0;
+    for (int c = 0; c < nch; ++c) {
+      const int b = c & 1;
+      if (*abort_flag) break;
+      wait_phase(&bars[B_MF], (uint32_t)(c & 1), abort_flag);
+      wait_ring(bars, B_CD, c, abort_flag);
+      if (c >= 2) wait_chunk(bars, B_OD, c - 2, abort_flag);
       tc_fence_after();
       const uint32_t vnb = sbase + kVN + b * kVNsz;
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks)
-        umma_bf16(dq + 64, sdesc_sw128(st_a + kAM + 32 * ks, 16, 1024),
-                  sdesc(vnb + 2048 * ks, 1024, 128), id_o, ks > 0);
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(tmem + b * 128 + 64, sdesc_sw128(m_a + 8192 * part + 32 * ks, 16, 1024),
+                    sdesc(vnb + 2048 * ks, 1024, 128), id_o, part > 0 || ks > 0);
       umma_commit(&bars[B_MD + b]);
       committed = c + 1;
     }
-    // Before the CTA retires: the copies and MMAs this thread issued complete (bounded).
-    for (int k = max(0, issued - 2); k < issued; ++k)
-      mbar_wait(&bars[B_FULL + (k & 1)], (uint32_t)((k >> 1) & 1), kWaitIters);
     if (committed > 0)
       mbar_wait(&bars[B_MD + ((committed - 1) & 1)], (uint32_t)(((committed - 1) >> 1) & 1),
                 kWaitIters);
@@ -438,7 +504,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   __syncthreads();
   tc_fence_after();
   if (tid == 0 && *abort_flag) set_status(p.status, GDN_DEV_TIMEOUT);
-  if (warp == kProducerWarp) tmem_dealloc(tmem, 256);
+  if (warp == kQsWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
