@@ -75,18 +75,52 @@ def algorithmic_flops(x):
 
 def stage_bytes(x, out_bytes=2):
     """Bytes each kernel must move given the intra/inter bridge it exchanges
-    (w bf16, u fp32, decay-masked q.k as a bf16 hi/lo pair, G fp32 per chunk row)."""
+    (per chunk and value head: w bf16, u fp32, decay-masked q.k as a bf16 hi/lo
+    pair, G fp32; per chunk and key head on the bf16 path: an fp16 copy of k,
+    which the inter kernel reads in place of k)."""
     esz = 2 if x["dtype"] == "bf16" else 4
     T, H, Hv, dk, dv, N = x["n_tokens"], x["H"], x["Hv"], x["dk"], x["dv"], x["N"]
     NT = n_chunks(x["lengths"])
     w_b = 2 if x["dtype"] == "bf16" else 4
     bridge = NT * Hv * (CHUNK * dk * w_b + CHUNK * dv * 4 + CHUNK * CHUNK * 4 + CHUNK * 4)
-    qk = 2 * T * H * dk * esz
+    k16 = NT * H * CHUNK * dk * 2 if x["dtype"] == "bf16" else 0
+    q = T * H * dk * esz
+    k = T * H * dk * esz
     states = N * Hv * dk * dv * 4
     s_in = states if x["initial_state"] is not None else 0
-    intra = qk + T * Hv * dv * esz + 2 * T * Hv * 4 + bridge
-    inter = qk + bridge + s_in + states + T * Hv * dv * out_bytes
+    intra = q + k + T * Hv * dv * esz + 2 * T * Hv * 4 + bridge + k16
+    inter = q + (k16 if k16 else k) + bridge + s_in + states + T * Hv * dv * out_bytes
     return {"chunk_table": 8 * (x["N"] + 1 + x["nt_max"]), "intra": intra, "inter": inter}
+
+
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of each
+# kernel on the T=4096 H=16 Hv=32 workload, from the ncu capture summarised in the
+# named profile, together with the SHA-1 of the kernel's source at capture time:
+# when the source has changed since, the figure no longer applies and is not reported.
+NCU_TRAFFIC = {
+    "inter": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_inter.cu",
+              "sha1": "41d43b926d39a4e76727a2bce7cf3701a61c66f4", "bytes": 195343872,
+              "profile": "profiles/tc_inter_kernel_T4096_H16_Hv32.md"},
+    "intra": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_intra.cu",
+              "sha1": "94e36e0bab9a9b5cf6923712e88c823420d57282", "bytes": 165812480,
+              "profile": "profiles/tc_intra_kernel_T4096_H16_Hv32.md"},
+}
+NCU_WORKLOAD = 2
+
+
+def ncu_traffic(stage: str, workload: int):
+    """Captured DRAM bytes per launch of `stage`, or None when no capture applies."""
+    import hashlib
+    e = NCU_TRAFFIC.get(stage)
+    if e is None or workload != NCU_WORKLOAD:
+        return None, None
+    try:
+        with open(os.path.join(ROOT, e["source"]), "rb") as f:
+            if hashlib.sha1(f.read()).hexdigest() != e["sha1"]:
+                return None, "kernel source changed since the capture"
+    except OSError:
+        return None, None
+    return e["bytes"], e["profile"]
 
 
 def load_peaks():
@@ -174,7 +208,11 @@ def oracle_rate(x, seconds: float, max_tokens=None):
     ts = int(max(16, min(limit, probe * seconds / max(dt, 1e-6))))
     ts = max(16, ts // 16 * 16)
     dt = run(ts)
-    return ts / dt, ts, dt, oracle.max_threads()
+    reps = 1
+    while dt < 0.8 * seconds and ts == limit:  # the whole workload is shorter: repeat it
+        dt += run(ts)
+        reps += 1
+    return reps * ts / dt, ts, dt, oracle.max_threads(), reps
 
 
 # --------------------------------------------------------------------- distributed plumbing
@@ -209,7 +247,7 @@ def run_reference(args, ws, rank):
         return None
     x = make_inputs(args.workload)
     budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
-    rate0, ts, dt, cores = oracle_rate(x, min(budget, args.cpu_seconds))
+    rate0, ts, dt, cores, _ = oracle_rate(x, min(budget, args.cpu_seconds))
     import oracle
     import torch
     cu = torch.tensor([0, ts], dtype=torch.int32)
@@ -331,6 +369,7 @@ def run_gdn(args, ws, rank, local):
     stage_mean = {k: statistics.mean(v) for k, v in st.items()}
     dom = max(stage_mean, key=stage_mean.get)
     dom_gbs = sb[dom] / (stage_mean[dom] / 1000.0) / 1e9
+    traffic, traffic_src = ncu_traffic(dom, args.workload)
     alg_b, alg_f = algorithmic_bytes(x), algorithmic_flops(x)
     t_hbm = alg_b / (peaks["hbm_gbs"] * 1e9)
     t_tc = alg_f / (peaks["bf16_tflops"] * 1e12)
@@ -358,7 +397,8 @@ def run_gdn(args, ws, rank, local):
         "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs,
                      "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dom_gbs / peaks["hbm_gbs"],
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                     "algorithmic_bytes_per_launch": sb[dom], "traffic": None},
+                     "algorithmic_bytes_per_launch": sb[dom], "traffic": traffic,
+                     "traffic_source": traffic_src},
         "path_roofline": path_roof,
         "stages_us": {k: 1000.0 * v for k, v in stage_mean.items()},
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
@@ -369,11 +409,12 @@ def run_gdn(args, ws, rank, local):
         "wall_s_timed_region": wall,
     }
     if not args.no_cpu_baseline:
-        rate, ts, dt, cores = oracle_rate(x, args.cpu_seconds)
+        rate, ts, dt, cores, reps = oracle_rate(x, args.cpu_seconds)
+        what = (f"the whole workload ({ts} tokens), all {x['Hv']} value heads, run {reps} times"
+                if reps > 1 else f"first {ts} tokens of the workload, all {x['Hv']} value heads")
         res["cpu_baseline"] = {
             "value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {ts} tokens of the workload, all {x['Hv']} value heads "
-                      f"({dt:.1f} s of fp64 C on the host cores)"}
+            "sample": f"{what} ({dt:.1f} s of fp64 C on the host cores)"}
     return res
 
 
