@@ -180,7 +180,11 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   if (ev) cudaEventRecord(ev[1], stream);
   const bool tc = uses_tc_path(&d);
   if (nt_max > 0) {
-    if (tc) launch_tc_intra(p, stream); else launch_simt_intra(p, false, stream);
+    if (tc) {
+      if (!launch_tc_intra(p, stream)) return GDN_ERR_LAUNCH_FAILED;
+    } else {
+      launch_simt_intra(p, false, stream);
+    }
   }
   if (ev) cudaEventRecord(ev[2], stream);
   if (tc) {

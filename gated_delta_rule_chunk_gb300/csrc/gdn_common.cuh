@@ -98,7 +98,7 @@ void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, float 
                    float* qrn, float* krn, cudaStream_t s);
 void launch_simt_intra(const Params& p, bool bf16_inputs, cudaStream_t s);
 void launch_simt_inter(const Params& p, bool bf16_inputs, cudaStream_t s);
-void launch_tc_intra(const Params& p, cudaStream_t s);
+bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
 
 // Encode a TMA tensor map over a bf16 [rows, heads, 128] tensor with a box of

@@ -4,56 +4,69 @@
 // computed once per (chunk, key head) and reused by the value heads of the
 // group; per value head the decay/beta-scaled A, its triangular inverse and
 // the products that need it are formed without writing A to global memory.
-// Section 8: triangular work stays triangular (only tiles on or below the
-// diagonal of K K^T, Q K^T and T K are multiplied).
+// Section 8: the triangular solve stays triangular.
 //
 // Per (chunk, key head h), with rows past the end of the sequence masked
-// (k = q = 0, beta = 0, g = 0):
-//   P = K K^T, R = Q K^T        (bf16 MMA, fp32 accumulate: exact products),
-//                                kept in registers across the value-head loop
+// (k = q = v = 0, beta = 0, g = 0):
+//   [P; R] = [K; Q] K^T          (one M = 128 tcgen05 MMA group, fp32 in TMEM:
+//                                 P = K K^T in TMEM lanes 0..63, R = Q K^T in 64..127)
 //   per value head hv of the group:
 //     G = inclusive in-chunk cumsum of g (fp32, left to right)
 //     A_ij = beta_i exp(G_i - G_j) P_ij (j < i);  T = (I + A)^-1 in place (fp32 diagonal
-//            blocks, off-diagonal blocks on tensor-core MMAs with split operands)
-//     w    = (T diag(beta exp(G))) K        (bf16 operand and store)
-//     u    = (T diag(beta)) V               (T operand split into bf16 hi + lo; fp32 store)
+//            blocks, off-diagonal blocks on warp MMAs with split operands)
+//     w    = (T diag(beta exp(G))) K   (bf16 T operand; tcgen05, M = 64, N = 128)
+//     u    = (T diag(beta)) V          (T operand split into bf16 hi + lo, two MMA groups
+//                                       into one accumulator)
 //     M_ij = exp(G_i - G_j) R_ij (j <= i)   (stored as a bf16 hi/lo pair)
-// The hi/lo split keeps about 16 significant bits where one bf16 rounding
-// would cost ~1e-2 of the output's rms. MMA A-fragments of the scaled T are
-// built in registers straight from the fp32 T tile.
+// (1/||k|| and 1/||q|| enter as fp32 row factors when the L2 norm is on.) The hi/lo
+// split keeps about 16 significant bits where one bf16 rounding would cost ~1e-2 of
+// the output's rms.
 //
 // The bridge is written as the exact shared-memory images the inter-chunk
-// kernel's tensor cores read, so that kernel moves each with one bulk copy:
+// kernel reads, so that kernel moves each with one bulk copy:
 //   w: two 64-column halves, each [64 rows][128 B] with the 128-byte swizzle
 //      (16-byte chunk c of row r stored at chunk c ^ (r % 8));
 //   M: [128 rows: hi then lo][128 B], same swizzle;
 //   u: [dv/32 blocks][64 rows][32 fp32], 16-byte chunk c of row r at c ^ (r % 8);
 //   k (once per key head): fp16, scaled by 1/||k|| when the L2 norm is on, zero past
 //      the sequence end, two 64-column halves of [64 rows][128 B] with the 128-byte swizzle.
+// Each image is assembled in shared memory and written with bulk copies (TMA), so
+// the warps never wait on scattered global stores; tiles come in by TMA tensor maps
+// (128-byte swizzle), which are also the tensor-core operand layouts.
 //
-// Occupancy: ~75 KB of shared memory and 128 threads per CTA, so that several
-// CTAs share an SM and hide each other's latency.
+// One CTA of 4 warps per (key head, chunk); ~99 KB of shared memory and 256 TMEM
+// columns, so two CTAs share an SM and hide each other's latency.
+#include <cuda.h>
+
 #include "gdn_common.cuh"
 #include "tri_inverse.cuh"
+#include "umma.cuh"
 #include "warp_mma.cuh"
 
 namespace gdn {
 
 namespace {
 
-constexpr int LDB = 136;  // bf16 stride of 128-wide tiles (272 B rows: conflict-free ldmatrix)
-constexpr int LDT = 68;   // fp32 stride of the A/T tile (16-byte rows)
+constexpr int LDT = 68;  // fp32 stride of the A/T tile (16-byte rows)
+constexpr uint32_t kWaitIters = 1u << 22;
+constexpr uint32_t kTmemCols = 256;
 
-struct IntraSmem {
-  __nv_bfloat16 K[64 * LDB], Q[64 * LDB], V[64 * LDB];
-  float AT[64 * LDT];
-  float X[16 * LDT];
-  float G[64], B[64], E[64], KR[64];
-};
+// Shared memory (bytes from a 1024-aligned base).
+constexpr uint32_t kKQ = 0;       // [K_h0 | Q_h0 | K_h1 | Q_h1], each [64 rows][128 B], swizzled;
+                                  // the Q halves later hold the M image and the u operands
+constexpr uint32_t kV = 32768;    // two buffers of [V_h0 | V_h1]
+constexpr uint32_t kAT = 65536;   // fp32 [64][LDT]: A, then T; staging of the k and w images
+constexpr uint32_t kX = kAT + 64 * LDT * 4;  // fp32 [16][LDT]: scratch of the inverse
+constexpr uint32_t kTW = 88064;   // bf16 [64][128 B], swizzled: T diag(beta exp(G)) (w operand)
+constexpr uint32_t kVec = kTW + 8192;        // 6 x fp32 [64] row vectors
+constexpr uint32_t kBar = kVec + 6 * 256;    // 7 mbarriers
+constexpr uint32_t kMisc = kBar + 64;        // TMEM base address, failure flag
+constexpr uint32_t kSmemBytes = kMisc + 16 + 1024;  // + room to align the base to 1024
+static_assert(kX + 16 * LDT * 4 <= kTW, "shared-memory layout overlaps");
 
-// Byte offset of bf16 element (r, k), k < 64, in a [rows][128 B] tile with the 128-byte swizzle.
-__device__ __forceinline__ uint32_t sw128_offset(int r, int k) {
-  return (uint32_t)r * 128u + ((uint32_t)((k >> 3) ^ (r & 7)) << 4) + (uint32_t)(k & 7) * 2u;
+// Byte offset of 16-byte chunk ch of row r in a [rows][128 B] tile with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw_off(int r, int ch) {
+  return (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4);
 }
 // Byte offset of fp32 element (r, j), j < 32, in a [rows][32] tile with 16-byte chunks swizzled.
 __device__ __forceinline__ uint32_t u_offset(int r, int j) {
@@ -83,230 +96,384 @@ __device__ __forceinline__ bool resolve(const Params& p, int slot, int& t0, int&
   return true;
 }
 
-// 64 rows x 128 bf16 of a [T, heads, 128] tensor into a padded tile; rows >= L read as zero.
-__device__ __forceinline__ void load_rows(__nv_bfloat16* dst, const __nv_bfloat16* src, int t0,
-                                          int L, int heads, int head, int tid) {
-#pragma unroll
-  for (int it = 0; it < 8; ++it) {
-    const int idx = tid + it * 128;  // 1024 chunks of 16 bytes
-    const int i = idx >> 4, c = (idx & 15) * 8;
-    const bool ok = i < L;
-    const __nv_bfloat16* g = src + (((size_t)(ok ? t0 + i : t0) * heads + head) * kDk + c);
-    cp_async16(dst + i * LDB + c, g, ok);
-  }
+// Bounded wait; on expiry the CTA's failure flag is raised (reported as GDN_DEV_TIMEOUT).
+__device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, volatile int* fail) {
+  if (!mbar_wait(bar, parity, kWaitIters)) *fail = 1;
 }
 
-__global__ void __launch_bounds__(128, 3) tc_intra_kernel(Params p) {
-  extern __shared__ __align__(16) unsigned char smem_raw[];
-  IntraSmem& s = *reinterpret_cast<IntraSmem*>(smem_raw);
+// Rows L..63 of a [64 rows][128 B] tile read as zero (the tile holds the rows that
+// follow the sequence, or padding, there).
+__device__ __forceinline__ void zero_tail(unsigned char* tile, int L, int tid) {
+  for (int idx = tid; idx < (64 - L) * 8; idx += 128)
+    *reinterpret_cast<uint4*>(tile + (uint32_t)(L + (idx >> 3)) * 128u + (idx & 7) * 16u) =
+        make_uint4(0u, 0u, 0u, 0u);
+}
+
+// Value-head tile of group member r (rows t0..t0+63) into V buffer r & 1.
+__device__ __forceinline__ void issue_v(unsigned char* sm, uint64_t* bars, const CUtensorMap* tmv,
+                                        int hv, int t0, int r) {
+  uint64_t* bar = &bars[1 + (r & 1)];
+  unsigned char* dst = sm + kV + (r & 1) * 16384;
+  mbar_expect_tx(bar, 16384);
+  tma_load_3d(dst, tmv, 0, hv, t0, bar);
+  tma_load_3d(dst + 8192, tmv, 64, hv, t0, bar);
+}
+
+__global__ void __launch_bounds__(128, 2)
+tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmk,
+                const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmv) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const uint32_t sbase = smem_addr(sm);
+  float* AT = reinterpret_cast<float*>(sm + kAT);
+  float* X = reinterpret_cast<float*>(sm + kX);
+  float* G = reinterpret_cast<float*>(sm + kVec);
+  float* Bt = G + 64;   // beta
+  float* KR = G + 128;  // 1/||k|| (1 when the norm is off)
+  float* FW = G + 192;  // beta exp(G) / ||k||: column factor of the w operand
+  // mbarriers: 0 k/q landed, 1-2 v buffers landed, 3 [P; R] done, 4 w done, 5 and 6 the
+  // two column halves of u done (one completion per value head for 4-6)
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
+  volatile int* fail = reinterpret_cast<volatile int*>(sm + kMisc + 4);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int g = lane >> 2, c = 2 * (lane & 3);
-  const int h = blockIdx.y;
+  // Key head fastest in the grid: CTAs resident together read all heads of the same
+  // tokens (contiguous rows of q, k and v) rather than one head of many chunks.
+  const int h = blockIdx.x;
   int t0, L, wslot;
-  if (!resolve(p, blockIdx.x, t0, L, wslot)) return;
+  if (!resolve(p, blockIdx.y, t0, L, wslot)) return;  // uniform over the CTA
 
-  load_rows(s.K, static_cast<const __nv_bfloat16*>(p.k), t0, L, p.H, h, tid);
-  load_rows(s.Q, static_cast<const __nv_bfloat16*>(p.q), t0, L, p.H, h, tid);
-  cp_async_commit();
-  if (tid < 64) {  // optional L2-norm factors (1 when off)
-    s.KR[tid] = (tid < L && p.krn) ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
   }
-  const int r0 = 16 * warp;
-  float qra = 1.f, qrb = 1.f;  // 1/||q|| of this thread's two rows
-  if (p.qrn) {
-    qra = (r0 + g < L) ? p.qrn[(size_t)(t0 + r0 + g) * p.H + h] : 1.f;
-    qrb = (r0 + g + 8 < L) ? p.qrn[(size_t)(t0 + r0 + g + 8) * p.H + h] : 1.f;
+  if (tid == 0) {
+    for (int b = 0; b < 7; ++b) mbar_init(&bars[b], 1);
+    mbar_init_fence();
+    *fail = 0;
+    mbar_expect_tx(&bars[0], 32768);
+    tma_load_3d(sm + kKQ, &tmk, 0, h, t0, &bars[0]);
+    tma_load_3d(sm + kKQ + 16384, &tmk, 64, h, t0, &bars[0]);
+    tma_load_3d(sm + kKQ + 8192, &tmq, 0, h, t0, &bars[0]);
+    tma_load_3d(sm + kKQ + 24576, &tmq, 64, h, t0, &bars[0]);
+    for (int r = 0; r < min(p.HG, 2); ++r) issue_v(sm, bars, &tmv, h * p.HG + r, t0, r);
   }
-  cp_async_wait<0>();
+  if (tid < 64) KR[tid] = (tid < L && p.krn) ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
+  // 1/||q|| of the row this thread forms M for (warps 2 and 3 own rows 0..63 of R)
+  const int qrow = 32 * (warp & 1) + lane;
+  const float qr = (warp >= 2 && p.qrn && qrow < L) ? p.qrn[(size_t)(t0 + qrow) * p.H + h] : 1.f;
+  tc_fence_before();
   __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
 
-  {  // fp16 image of the (normalised) k tile for the inter-chunk state update
-    unsigned char* kimg = static_cast<unsigned char*>(p.k16) + ((size_t)wslot * p.H + h) * 64 * kDk * 2;
+  // Gates of group member r and their in-chunk inclusive cumsum (warp 0, 2 rows per
+  // lane); the next member's g and beta are loaded one member ahead.
+  float gn0 = 0.f, gn1 = 0.f, bn0 = 0.f, bn1 = 0.f;
+  auto load_gates = [&](int r) {
+    const int hv = h * p.HG + r;
+    const size_t b0 = (size_t)(t0 + lane) * p.Hv + hv, b1 = (size_t)(t0 + lane + 32) * p.Hv + hv;
+    gn0 = lane < L ? p.g[b0] : 0.f;
+    gn1 = lane + 32 < L ? p.g[b1] : 0.f;
+    bn0 = lane < L ? p.beta[b0] : 0.f;
+    bn1 = lane + 32 < L ? p.beta[b1] : 0.f;
+  };
+  auto gates = [&](int r) {
+    const size_t sl = (size_t)wslot * p.Hv + h * p.HG + r;
+    float g0 = gn0, g1 = gn1;
+    const float be0 = bn0, be1 = bn1;
+    if (r + 1 < p.HG) load_gates(r + 1);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_up_sync(0xffffffffu, g0, o);
+      const float y1 = __shfl_up_sync(0xffffffffu, g1, o);
+      if (lane >= o) {
+        g0 += y0;
+        g1 += y1;
+      }
+    }
+    g1 += __shfl_sync(0xffffffffu, g0, 31);
+    G[lane] = g0;
+    G[lane + 32] = g1;
+    Bt[lane] = be0;
+    Bt[lane + 32] = be1;
+    FW[lane] = be0 * expf(g0) * KR[lane];
+    FW[lane + 32] = be1 * expf(g1) * KR[lane + 32];
+    p.G[sl * 64 + lane] = g0;
+    p.G[sl * 64 + lane + 32] = g1;
+  };
+  if (warp == 0) {
+    load_gates(0);
+    gates(0);  // while the k and q tiles are in flight
+  }
+
+  wait_or_flag(&bars[0], 0, fail);
+  if (L < kChunk) {
+    zero_tail(sm + kKQ, L, tid);
+    zero_tail(sm + kKQ + 8192, L, tid);
+    zero_tail(sm + kKQ + 16384, L, tid);
+    zero_tail(sm + kKQ + 24576, L, tid);
+  }
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0) {  // [P; R] = [K; Q] K^T
+    tc_fence_after();
+    const uint32_t id = idesc_bf16_f32(128, 64, false, false);
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const uint32_t a = sbase + kKQ + (ks >> 2) * 16384 + 32 * (ks & 3);
+      umma_bf16(tmem, sdesc_sw128(a, 16, 1024), sdesc_sw128(a, 16, 1024), id, ks > 0);
+    }
+    umma_commit(&bars[3]);
+  }
+
+  {  // fp16 image of the (normalised) k tile, assembled in the A/T region
+    const unsigned char* kt = sm + kKQ;
+    unsigned char* img = sm + kAT;
 #pragma unroll
     for (int it = 0; it < 8; ++it) {
       const int idx = tid + it * 128;  // 1024 chunks of 8 elements
       const int half = idx >> 9, t = (idx >> 3) & 63, ch = idx & 7;
-      const uint4 raw = *reinterpret_cast<const uint4*>(&s.K[t * LDB + half * 64 + ch * 8]);
-      const uint32_t* r = reinterpret_cast<const uint32_t*>(&raw);
+      const uint32_t off = (uint32_t)half * 16384u + sw_off(t, ch);
+      const uint4 raw = *reinterpret_cast<const uint4*>(kt + off);
+      const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
       uint4 v;
       uint32_t* o = reinterpret_cast<uint32_t*>(&v);
-      const float sc = s.KR[t];
+      const float sc = KR[t];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r[e]));
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rw[e]));
         o[e] = pack_f16(f.x * sc, f.y * sc);
       }
-      *reinterpret_cast<uint4*>(kimg + half * 8192 + t * 128 + ((ch ^ (t & 7)) << 4)) = v;
+      *reinterpret_cast<uint4*>(img + (uint32_t)half * 8192u + sw_off(t, ch)) = v;
     }
   }
-
-  // P = K K^T and R = Q K^T, rows r0..r0+15, column tiles on or below the diagonal.
-  float kk[8][4], qk[8][4];
-#pragma unroll
-  for (int nt = 0; nt < 8; ++nt)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) kk[nt][e] = qk[nt][e] = 0.f;
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    uint32_t ak[4], aq[4];
-    load_a(ak, s.K, LDB, r0, 16 * ks, lane);
-    load_a(aq, s.Q, LDB, r0, 16 * ks, lane);
-#pragma unroll
-    for (int np = 0; np < 4; ++np) {
-      if (np <= warp) {
-        uint32_t b[4];
-        load_b_nk(b, s.K, LDB, 16 * ks, 16 * np, lane);
-        mma_bf16(kk[2 * np], ak, b[0], b[1]);
-        mma_bf16(kk[2 * np + 1], ak, b[2], b[3]);
-        mma_bf16(qk[2 * np], aq, b[0], b[1]);
-        mma_bf16(qk[2 * np + 1], aq, b[2], b[3]);
-      }
-    }
+  fence_async_smem();
+  __syncthreads();
+  if (tid == 0) {
+    bulk_store(static_cast<unsigned char*>(p.k16) + ((size_t)wslot * p.H + h) * 64 * kDk * 2,
+               sm + kAT, 16384);
+    bulk_commit();
   }
 
   for (int r = 0; r < p.HG; ++r) {
     const int hv = h * p.HG + r;
     const size_t sl = (size_t)wslot * p.Hv + hv;
-    load_rows(s.V, static_cast<const __nv_bfloat16*>(p.v), t0, L, p.Hv, hv, tid);
-    cp_async_commit();
-    if (warp == 0) {  // gates and their in-chunk inclusive cumsum (64 rows, 2 per lane)
-      const size_t b0 = (size_t)(t0 + lane) * p.Hv + hv, b1 = (size_t)(t0 + lane + 32) * p.Hv + hv;
-      float g0 = lane < L ? p.g[b0] : 0.f, g1 = lane + 32 < L ? p.g[b1] : 0.f;
-      const float be0 = lane < L ? p.beta[b0] : 0.f, be1 = lane + 32 < L ? p.beta[b1] : 0.f;
-#pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y0 = __shfl_up_sync(0xffffffffu, g0, o);
-        const float y1 = __shfl_up_sync(0xffffffffu, g1, o);
-        if (lane >= o) { g0 += y0; g1 += y1; }
-      }
-      g1 += __shfl_sync(0xffffffffu, g0, 31);
-      s.G[lane] = g0;
-      s.G[lane + 32] = g1;
-      s.E[lane] = expf(g0);
-      s.E[lane + 32] = expf(g1);
-      s.B[lane] = be0;
-      s.B[lane + 32] = be1;
-      p.G[sl * 64 + lane] = g0;
-      p.G[sl * 64 + lane + 32] = g1;
-    }
+    const uint32_t par = (uint32_t)(r & 1);  // parity of this member's MMA barriers
+    if (r > 0 && warp == 0) gates(r);
+    if (tid == 0) bulk_wait_read<0>();  // staging regions read out by the previous copies
     __syncthreads();
+    if (r == 0) wait_or_flag(&bars[3], 0, fail);
+    tc_fence_after();
 
-    // A (strictly lower, to shared memory) and M (hi/lo, to global) from the register tiles.
+    // A (warps 0-1, rows of P) into A/T; M hi/lo image (warps 2-3, rows of R) into the Q
+    // halves. Branch-free: every decay factor is formed and the mask is a select (exp of
+    // a positive exponent above the diagonal may be inf; it is never used). Eight columns
+    // per step, not unrolled, to keep the kernel's code small.
     {
-      unsigned char* Mimg = static_cast<unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2;
+      const int i = 32 * (warp & 1) + lane;
+      const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+      const float gi = G[i];
+      const float rowf = warp < 2 ? Bt[i] * KR[i] : qr;
+#pragma unroll 2
+      for (int ch = 0; ch < 8; ++ch) {
+        const int j = 8 * ch;
+        float v[8];
+        tmem_ld8(trow + j, v);
+        const float4 ga = *reinterpret_cast<const float4*>(&G[j]);
+        const float4 gb = *reinterpret_cast<const float4*>(&G[j + 4]);
+        const float4 ka = *reinterpret_cast<const float4*>(&KR[j]);
+        const float4 kb = *reinterpret_cast<const float4*>(&KR[j + 4]);
+        const float gg[8] = {ga.x, ga.y, ga.z, ga.w, gb.x, gb.y, gb.z, gb.w};
+        const float kk[8] = {ka.x, ka.y, ka.z, ka.w, kb.x, kb.y, kb.z, kb.w};
+        float d[8];
 #pragma unroll
-      for (int hh = 0; hh < 2; ++hh) {
-        const int i = r0 + g + 8 * hh;
-        const float gi = s.G[i], bi = s.B[i] * s.KR[i], qi = hh ? qrb : qra;
+        for (int e = 0; e < 8; ++e) d[e] = __expf(gi - gg[e]) * rowf * kk[e];
+        tmem_ld_wait();
+        if (warp < 2) {  // strictly lower
 #pragma unroll
-        for (int nt = 0; nt < 8; ++nt) {
-          const int j = 8 * nt + c;
-          float a2[2], m2[2];
+          for (int e = 0; e < 8; ++e) d[e] = (j + e < i) ? d[e] * v[e] : 0.f;
+          *reinterpret_cast<float4*>(&AT[i * LDT + j]) = make_float4(d[0], d[1], d[2], d[3]);
+          *reinterpret_cast<float4*>(&AT[i * LDT + j + 4]) = make_float4(d[4], d[5], d[6], d[7]);
+        } else {  // lower, diagonal included
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int jj = j + e;
-            const float dec = (jj <= i) ? __expf(gi - s.G[jj]) : 0.f;
-            a2[e] = (jj < i) ? bi * dec * s.KR[jj] * kk[nt][2 * hh + e] : 0.f;
-            m2[e] = dec * qi * s.KR[jj] * qk[nt][2 * hh + e];
-          }
-          *reinterpret_cast<float2*>(&s.AT[i * LDT + j]) = make_float2(a2[0], a2[1]);
-          split2_store(reinterpret_cast<__nv_bfloat16*>(Mimg + sw128_offset(i, j)),
-                       reinterpret_cast<__nv_bfloat16*>(Mimg + sw128_offset(64 + i, j)), m2[0], m2[1]);
+          for (int e = 0; e < 8; ++e) d[e] = (j + e <= i) ? d[e] * v[e] : 0.f;
+          uint32_t hi[4], lo[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) split_pack2(d[2 * e], d[2 * e + 1], hi[e], lo[e]);
+          const uint32_t off = sw_off(i, ch);
+          *reinterpret_cast<uint4*>(sm + kKQ + 8192 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
+          *reinterpret_cast<uint4*>(sm + kKQ + 24576 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
       }
     }
+    fence_async_smem();
+    tc_fence_before();
     __syncthreads();
-    tri_inverse_64_tc(s.AT, LDT, s.X, tid);
+    if (tid == 0) {
+      unsigned char* mimg = static_cast<unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2;
+      bulk_store(mimg, sm + kKQ + 8192, 8192);
+      bulk_store(mimg + 8192, sm + kKQ + 24576, 8192);
+      bulk_commit();
+    }
+    tri_inverse_64_tc(AT, LDT, X, tid);  // ends with the CTA synchronized
 
-    // w = (T diag(beta exp(G) krn)) K, rows r0..r0+15; T is lower triangular (k-tiles <= warp).
-    {
-      float acc[16][4];
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
-#pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
-#pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        if (ks <= warp) {
-          uint32_t a[4];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {  // a0: (g, c) a1: (g+8, c) a2: (g, c+8) a3: (g+8, c+8)
-            const int i = r0 + g + 8 * (q4 & 1), j = 16 * ks + c + 8 * (q4 >> 1);
-            const float2 t = *reinterpret_cast<const float2*>(&s.AT[i * LDT + j]);
-            a[q4] = pack_bf16(t.x * s.B[j] * s.E[j] * s.KR[j], t.y * s.B[j + 1] * s.E[j + 1] * s.KR[j + 1]);
-          }
-#pragma unroll
-          for (int np = 0; np < 8; ++np) {
-            uint32_t b[4];
-            load_b_kn(b, s.K, LDB, 16 * ks, 16 * np, lane);
-            mma_bf16(acc[2 * np], a, b[0], b[1]);
-            mma_bf16(acc[2 * np + 1], a, b[2], b[3]);
-          }
-        }
-      }
-      unsigned char* wimg = static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2;
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int col = 8 * nt + c;
-        unsigned char* half = wimg + (col >> 6) * 8192;
-        *reinterpret_cast<uint32_t*>(half + sw128_offset(r0 + g, col & 63)) = pack_bf16(acc[nt][0], acc[nt][1]);
-        *reinterpret_cast<uint32_t*>(half + sw128_offset(r0 + g + 8, col & 63)) = pack_bf16(acc[nt][2], acc[nt][3]);
-      }
+    // This member's V tile (rows past the end zeroed) and the M image read out of the Q halves.
+    wait_or_flag(&bars[1 + (r & 1)], (uint32_t)((r >> 1) & 1), fail);
+    unsigned char* vt = sm + kV + (r & 1) * 16384;
+    if (L < kChunk) {
+      zero_tail(vt, L, tid);
+      zero_tail(vt + 8192, L, tid);
     }
-    // u = (T diag(beta)) V with the T operand split into bf16 hi + lo.
-    cp_async_wait<0>();
+    if (tid == 0) bulk_wait_read<0>();
     __syncthreads();
-    {
-      float acc[16][4];
+    // T operand images: T diag(beta exp(G) / ||k||) (bf16) and T diag(beta) as a bf16
+    // hi/lo pair (hi into the first Q half, lo into the second).
+#pragma unroll 1
+    for (int idx = tid; idx < 512; idx += 128) {
+      const int i = idx >> 3, ch = idx & 7, j0 = 8 * ch;
+      const float4 x0 = *reinterpret_cast<const float4*>(&AT[i * LDT + j0]);
+      const float4 x1 = *reinterpret_cast<const float4*>(&AT[i * LDT + j0 + 4]);
+      const float4 fa = *reinterpret_cast<const float4*>(&FW[j0]);
+      const float4 fb = *reinterpret_cast<const float4*>(&FW[j0 + 4]);
+      const float4 ba = *reinterpret_cast<const float4*>(&Bt[j0]);
+      const float4 bb = *reinterpret_cast<const float4*>(&Bt[j0 + 4]);
+      uint32_t th[4], tl[4];
+      split_pack2(x0.x * ba.x, x0.y * ba.y, th[0], tl[0]);
+      split_pack2(x0.z * ba.z, x0.w * ba.w, th[1], tl[1]);
+      split_pack2(x1.x * bb.x, x1.y * bb.y, th[2], tl[2]);
+      split_pack2(x1.z * bb.z, x1.w * bb.w, th[3], tl[3]);
+      const uint4 tw = make_uint4(pack_bf16(x0.x * fa.x, x0.y * fa.y), pack_bf16(x0.z * fa.z, x0.w * fa.w),
+                                  pack_bf16(x1.x * fb.x, x1.y * fb.y), pack_bf16(x1.z * fb.z, x1.w * fb.w));
+      const uint32_t off = sw_off(i, ch);
+      *reinterpret_cast<uint4*>(sm + kTW + off) = tw;
+      *reinterpret_cast<uint4*>(sm + kKQ + 8192 + off) = make_uint4(th[0], th[1], th[2], th[3]);
+      *reinterpret_cast<uint4*>(sm + kKQ + 24576 + off) = make_uint4(tl[0], tl[1], tl[2], tl[3]);
+    }
+    fence_async_smem();
+    __syncthreads();
+    // TMEM: [P; R] in columns 0..63, w in 128..255, the first half of u in 64..127; the
+    // second half of u reuses w's columns once w has been read out.
+    const uint32_t dw = tmem + 128, du0 = tmem + 64, du1 = tmem + 128;
+    const uint32_t vb = sbase + kV + (r & 1) * 16384;
+    const uint32_t id_w = idesc_bf16_f32(64, 128, false, true);
+    const uint32_t id_u = idesc_bf16_f32(64, 64, false, true);
+    auto issue_u_half = [&](uint32_t d, int half, uint64_t* bar) {
+      // u[:, 64 half ..] = T_hi V + T_lo V over the value columns of this half; B is the
+      // v tile read MN-major (N = value dim, K = tokens)
 #pragma unroll
-      for (int nt = 0; nt < 16; ++nt)
+      for (int part = 0; part < 2; ++part)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(d, sdesc_sw128(sbase + kKQ + 8192 + 16384 * part + 32 * ks, 16, 1024),
+                    sdesc_sw128(vb + 8192 * half + 2048 * ks, 8192, 1024), id_u, part > 0 || ks > 0);
+      umma_commit(bar);
+    };
+    if (tid == 0) {
+      tc_fence_after();
+      // w = TW K: B is the k tile read MN-major (N = key dim, K = tokens)
 #pragma unroll
-      for (int ks = 0; ks < 4; ++ks) {
-        if (ks <= warp) {
-          uint32_t ah[4], al[4];
+      for (int ks = 0; ks < 4; ++ks)
+        umma_bf16(dw, sdesc_sw128(sbase + kTW + 32 * ks, 16, 1024),
+                  sdesc_sw128(sbase + kKQ + 2048 * ks, 16384, 1024), id_w, ks > 0);
+      umma_commit(&bars[4]);
+      issue_u_half(du0, 0, &bars[5]);
+    }
+    wait_or_flag(&bars[4], par, fail);
+    tc_fence_after();
+    {  // w rows 16 warp .. 16 warp + 15 (TMEM lanes 32 warp ..), bf16, into the A/T region
+      const int i = 16 * warp + (lane & 15);
+      unsigned char* img = sm + kAT;
+#pragma unroll 2
+      for (int cb = 0; cb < 4; ++cb) {
+        float v[32];
+        tmem_ld32(dw + ((uint32_t)(32 * warp) << 16) + 32 * cb, v);
+        tmem_ld_wait();
+        if (lane < 16) {
 #pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) {
-            const int i = r0 + g + 8 * (q4 & 1), j = 16 * ks + c + 8 * (q4 >> 1);
-            const float2 t = *reinterpret_cast<const float2*>(&s.AT[i * LDT + j]);
-            const float x0 = t.x * s.B[j], x1 = t.y * s.B[j + 1];
-            const __nv_bfloat162 hi = __floats2bfloat162_rn(x0, x1);
-            const float2 hf = __bfloat1622float2(hi);
-            const __nv_bfloat162 lo = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-            ah[q4] = *reinterpret_cast<const uint32_t*>(&hi);
-            al[q4] = *reinterpret_cast<const uint32_t*>(&lo);
-          }
-#pragma unroll
-          for (int np = 0; np < 8; ++np) {
-            uint32_t b[4];
-            load_b_kn(b, s.V, LDB, 16 * ks, 16 * np, lane);
-            mma_bf16(acc[2 * np], ah, b[0], b[1]);
-            mma_bf16(acc[2 * np + 1], ah, b[2], b[3]);
-            mma_bf16(acc[2 * np], al, b[0], b[1]);
-            mma_bf16(acc[2 * np + 1], al, b[2], b[3]);
+          for (int q = 0; q < 4; ++q) {
+            const int col = 32 * cb + 8 * q;
+            const uint4 pk = make_uint4(pack_bf16(v[8 * q], v[8 * q + 1]),
+                                        pack_bf16(v[8 * q + 2], v[8 * q + 3]),
+                                        pack_bf16(v[8 * q + 4], v[8 * q + 5]),
+                                        pack_bf16(v[8 * q + 6], v[8 * q + 7]));
+            *reinterpret_cast<uint4*>(img + (col >> 6) * 8192 + sw_off(i, (col & 63) >> 3)) = pk;
           }
         }
       }
-      unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
-#pragma unroll
-      for (int nt = 0; nt < 16; ++nt) {
-        const int col = 8 * nt + c;
-        unsigned char* blk = uimg + (col >> 5) * 64 * 32 * 4;
-        *reinterpret_cast<float2*>(blk + u_offset(r0 + g, col & 31)) = make_float2(acc[nt][0], acc[nt][1]);
-        *reinterpret_cast<float2*>(blk + u_offset(r0 + g + 8, col & 31)) = make_float2(acc[nt][2], acc[nt][3]);
-      }
     }
-    __syncthreads();  // A/T and the gates are rewritten for the next value head
+    fence_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
+      bulk_commit();
+      tc_fence_after();
+      issue_u_half(du1, 1, &bars[6]);
+    }
+    unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
+    // u blocks (32 columns) of one half from TMEM to two staging tiles, then to global
+    auto u_out = [&](uint32_t d, unsigned char* s0, unsigned char* s1, int blk0) {
+      const int i = 16 * warp + (lane & 15);
+#pragma unroll 1
+      for (int b = 0; b < 2; ++b) {
+        float v[32];
+        tmem_ld32(d + ((uint32_t)(32 * warp) << 16) + 32 * b, v);
+        tmem_ld_wait();
+        unsigned char* blk = b ? s1 : s0;
+        if (lane < 16) {
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            *reinterpret_cast<float4*>(blk + u_offset(i, 4 * q)) =
+                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+        }
+      }
+      fence_async_smem();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        bulk_store(uimg + blk0 * 8192, s0, 8192);
+        bulk_store(uimg + (blk0 + 1) * 8192, s1, 8192);
+        bulk_commit();
+      }
+    };
+    // blocks 0, 1: staged in the first V half (read by the first u half only) and the
+    // w-operand image; blocks 2, 3: the second V half and the first Q half (T_hi)
+    wait_or_flag(&bars[5], par, fail);
+    tc_fence_after();
+    u_out(du0, vt, sm + kTW, 0);
+    wait_or_flag(&bars[6], par, fail);
+    tc_fence_after();
+    u_out(du1, vt + 8192, sm + kKQ + 8192, 2);
+    if (tid == 0 && r + 2 < p.HG) {  // this V buffer serves member r + 2 once the copies read it
+      bulk_wait_read<0>();
+      issue_v(sm, bars, &tmv, hv + 2, t0, r + 2);
+    }
   }
+
+  if (tid == 0) {
+    bulk_wait<0>();  // every image written
+    for (int r = max(0, p.HG - 2); r < p.HG; ++r)  // (all V loads were consumed; bounded)
+      mbar_wait(&bars[1 + (r & 1)], (uint32_t)((r >> 1) & 1), kWaitIters);
+    if (*fail) set_status(p.status, GDN_DEV_TIMEOUT);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
 
-void launch_tc_intra(const Params& p, cudaStream_t s) {
-  const int smem = (int)sizeof(IntraSmem);
-  ensure_smem_limit((const void*)tc_intra_kernel, smem);
-  tc_intra_kernel<<<dim3(p.nt_max, p.H), 128, smem, s>>>(p);
+bool launch_tc_intra(const Params& p, cudaStream_t s) {
+  CUtensorMap tmk, tmq, tmv;
+  const int rows = p.T > 0 ? p.T : 1;  // with T = 0 every slot is a sentinel
+  if (!encode_rows_tmap(&tmk, p.k, rows, p.H) || !encode_rows_tmap(&tmq, p.q, rows, p.H) ||
+      !encode_rows_tmap(&tmv, p.v, rows, p.Hv))
+    return false;
+  ensure_smem_limit((const void*)tc_intra_kernel, (int)kSmemBytes);
+  tc_intra_kernel<<<dim3(p.H, p.nt_max), 128, kSmemBytes, s>>>(p, tmk, tmq, tmv);
+  return true;
 }
 
 }  // namespace gdn
