@@ -26,7 +26,8 @@ DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table
 
 # Every entry point include/gdn.h declares.
 EXPORTED = ("gdn_check_desc", "gdn_nt_max", "gdn_workspace_size", "gdn_build_chunk_indices",
-            "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string", "gdn_chunk_fwd_noalloc")
+            "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string", "gdn_chunk_fwd_noalloc",
+            "gdn_recurrent_fwd")
 GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -74,6 +75,9 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_chunk_fwd.restype = ctypes.c_int
         lib.gdn_chunk_fwd_noalloc.argtypes = lib.gdn_chunk_fwd.argtypes
         lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.gdn_recurrent_fwd.argtypes = [P(GdnDesc), vp, vp, vp, vp, vp, ctypes.c_float, vp,
+                                          vp, vp, vp, vp]
+        lib.gdn_recurrent_fwd.restype = ctypes.c_int
         lib.gdn_read_status.argtypes = [P(GdnDesc), vp, vp]
         lib.gdn_read_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -203,6 +207,53 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
         raise GdnError(rc, "gdn_chunk_fwd")
     if return_desc:
         return out, final_state, desc, workspace
+    return out, final_state
+
+
+def gdn_recurrent_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                      beta: torch.Tensor, scale: Optional[float] = None,
+                      initial_state: Optional[torch.Tensor] = None,
+                      cu_seqlens: Optional[torch.Tensor] = None,
+                      output_final_state: bool = True, out_dtype: Optional[torch.dtype] = None,
+                      use_qk_l2norm: bool = False, l2norm_eps: float = 0.0,
+                      out: Optional[torch.Tensor] = None,
+                      final_state: Optional[torch.Tensor] = None,
+                      status: Optional[torch.Tensor] = None, stream=None,
+                      return_desc: bool = False):
+    """Token-serial forward (decode / speculative verify) through the C ABI.
+
+    Same tensors as gdn_chunk_fwd. `status`, if given, is a 256-byte-aligned
+    device buffer of at least 4 bytes that receives the device status word
+    (read it with gdn_read_status on the returned descriptor).
+    Returns (out, final_state) or (out, final_state, desc).
+    """
+    T, H, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    out_dtype = out_dtype or (out.dtype if out is not None else q.dtype)
+    desc = make_desc(T, N, H, Hv, q.dtype, out_dtype,
+                     flags=GDN_FLAG_QK_L2NORM if use_qk_l2norm else 0,
+                     l2norm_eps=l2norm_eps, dk=dk, dv=dv)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    if out is None:
+        out = torch.empty(T, Hv, dv, dtype=out_dtype, device=q.device)
+    if final_state is None and output_final_state:
+        final_state = torch.empty(N, Hv, dv, dk, dtype=torch.float32, device=q.device)
+    if status is not None:
+        desc.workspace = status.data_ptr()
+        desc.workspace_bytes = status.numel() * status.element_size()
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    rc = load_library().gdn_recurrent_fwd(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(out), _ptr(final_state),
+        _stream_handle(stream))
+    if rc != 0:
+        raise GdnError(rc, "gdn_recurrent_fwd")
+    if return_desc:
+        return out, final_state, desc
     return out, final_state
 
 

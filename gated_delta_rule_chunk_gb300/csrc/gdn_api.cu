@@ -196,6 +196,35 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 
+int gdn_recurrent_fwd(const gdn_desc* desc, const void* q, const void* k, const void* v,
+                      const float* g, const float* beta, float scale,
+                      const float* initial_state, const int32_t* cu_seqlens, void* out,
+                      float* final_state, cudaStream_t stream) {
+  int rc = check_desc_impl(desc);
+  if (rc != GDN_OK) return rc;
+  const gdn_desc& d = *desc;
+  if (!q || !k || !v || !g || !beta || !out) return GDN_ERR_NULL_ARG;
+  if (!cu_seqlens && d.N != 1) return GDN_ERR_BAD_SHAPE;
+  const void* ptrs16[] = {q, k, v, g, beta, out, initial_state, final_state};
+  for (const void* p : ptrs16)
+    if (!aligned(p, 16)) return GDN_ERR_MISALIGNED;
+  if (!aligned(cu_seqlens, 4) || !aligned(d.workspace, 256)) return GDN_ERR_MISALIGNED;
+  RecParams p{};
+  p.T = d.T; p.N = d.N; p.H = d.H; p.Hv = d.Hv; p.HG = d.Hv / d.H;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta;
+  p.scale = scale > 0.f ? scale : 1.0f / sqrtf((float)kDk);  // also NaN
+  p.eps = d.l2norm_eps > 0.f ? d.l2norm_eps : 1e-6f;
+  p.s0 = initial_state; p.out = out; p.sT = final_state; p.cu = cu_seqlens;
+  p.status = d.workspace ? static_cast<int32_t*>(d.workspace) : nullptr;
+  p.bf16_in = d.qkv_dtype == GDN_BF16;
+  p.out_bf16 = d.out_dtype == GDN_BF16;
+  p.l2norm = (d.flags & GDN_FLAG_QK_L2NORM) != 0;
+  if (p.status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH_FAILED;
+  if (d.T > 0) launch_recurrent(p, stream);
+  return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
+}
+
 int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t stream) {
   int rc = check_desc_impl(desc);
   if (rc != GDN_OK) return rc;

@@ -40,6 +40,23 @@ struct Params {
   int out_bf16;
 };
 
+// Parameters of the token-serial kernel (device pointers).
+struct RecParams {
+  int T, N, H, Hv, HG;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  float scale, eps;
+  const float* s0;      // [N, Hv, dv, dk] or null
+  void* out;            // [T, Hv, dv]
+  float* sT;            // [N, Hv, dv, dk] or null
+  const int32_t* cu;    // [N + 1] or null (one sequence of T rows)
+  int32_t* status;      // device status word or null
+  int bf16_in, out_bf16, l2norm;
+};
+
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
   size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qrn, krn, total;
@@ -100,6 +117,7 @@ void launch_simt_intra(const Params& p, bool bf16_inputs, cudaStream_t s);
 void launch_simt_inter(const Params& p, bool bf16_inputs, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
+void launch_recurrent(const RecParams& p, cudaStream_t s);
 
 // Encode a TMA tensor map over a bf16 [rows, heads, 128] tensor with a box of
 // 64 rows x 1 head x 64 elements and the 128-byte swizzle. False on failure.

@@ -43,7 +43,7 @@ class Workload:
     dv: int
     dtype: str                    # "f32" or "bf16" for q/k/v
     with_initial_state: bool
-    kind: str                     # "single", "varlen", "static_bound"
+    kind: str                     # "single", "varlen", "static_bound", "fixed"
     T: int = 0                    # single: sequence length
     n_seqs: int = 1               # varlen: number of sequences
     max_len: int = 0              # varlen: lengths ~ U[1, max_len]
@@ -51,6 +51,7 @@ class Workload:
     N_max: int = 0                # static_bound: padded sequence count
     n_real: int = 0               # static_bound: real sequences
     real_max_len: int = 0         # static_bound: lengths ~ U[1, real_max_len]
+    fixed_lens: tuple = ()        # fixed: the sequence lengths
 
 
 WORKLOADS = {
@@ -65,6 +66,11 @@ WORKLOADS = {
     4: Workload(4, "static-bound T_max=4096 N_max=32, 20 sequences, H=16 Hv=32 bf16", 16,
                 32, 128, 128, "bf16", True, "static_bound", T_max=4096, N_max=32,
                 n_real=20, real_max_len=204),
+    # token-serial (decode / speculative verify) workloads of the recurrent kernel
+    5: Workload(5, "decode step: 64 sequences x 1 token, H=16 Hv=32 d=128 bf16", 16, 32,
+                128, 128, "bf16", True, "fixed", fixed_lens=(1,) * 64),
+    6: Workload(6, "speculative verify: 8 sequences x 8 tokens, H=16 Hv=32 d=128 bf16", 16,
+                32, 128, 128, "bf16", True, "fixed", fixed_lens=(8,) * 8),
 }
 
 HEADLINE = 2
@@ -80,6 +86,8 @@ def draw_lengths(wl: Workload, gen: torch.Generator) -> list:
     """Sequence lengths of a workload (before any zero-length padding)."""
     if wl.kind == "single":
         return [wl.T]
+    if wl.kind == "fixed":
+        return list(wl.fixed_lens)
     if wl.kind == "varlen":
         out = []
         while len(out) < wl.n_seqs:
@@ -136,7 +144,7 @@ def make_inputs(wid: int = HEADLINE, seed: Optional[int] = None, T: Optional[int
     dtype = dtype or wl.dtype
     init = wl.with_initial_state if with_initial_state is None else with_initial_state
     if lengths is None:
-        if T is not None and wl.kind == "single":
+        if T is not None and wl.kind in ("single", "fixed"):
             lengths = [T]
         else:
             lengths = draw_lengths(wl, gen)

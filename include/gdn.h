@@ -229,6 +229,40 @@ int gdn_chunk_fwd_noalloc(const gdn_desc* desc, const void* q, const void* k,
                           int32_t* chunk_indices, void* out, float* final_state,
                           cudaStream_t stream);
 
+/*
+ * Token-serial forward of the same recurrence, for decode (one token per
+ * sequence) and speculative verification (a few tokens per sequence):
+ * "Chunking Qwen3.5's gated DeltaNet for 1.5x faster prefill on Apple Silicon",
+ * sections "How does decode run a sequential update on a GPU?" (one thread per
+ * value column of a head's fp32 state, held on chip for the whole call) and
+ * "Does the chunked kernel match the serial one?" (verification reproduces
+ * decode's numerics). Per token: decay exp(g), the state's prediction for k,
+ * the rank-1 correction with beta, then o = scale * S^T q (q and k
+ * L2-normalised first when GDN_FLAG_QK_L2NORM is set).
+ *
+ * Guarantee: a call over n tokens of a sequence performs, token by token, the
+ * same fp32 operations as n calls over one token each with the state passed
+ * along (final_state of one call as initial_state of the next), so outputs and
+ * states agree bit for bit.
+ *
+ * Arguments, layouts and ownership as gdn_chunk_fwd (q, k [T,H,dk]; v, out
+ * [T,Hv,dv]; g, beta fp32 [T,Hv]; states fp32 [N,Hv,dv,dk]; cu_seqlens int32
+ * [N+1] or NULL for one sequence of T rows; final_state may alias
+ * initial_state; either may be NULL). The descriptor is validated as for
+ * gdn_chunk_fwd; chunk_size, nt_max and flags other than GDN_FLAG_QK_L2NORM
+ * play no part. No workspace is needed: when desc->workspace is non-NULL its
+ * status word is cleared and receives GDN_DEV_BAD_CU_SEQLENS for a malformed
+ * cu_seqlens (clamped to [0, T]; a decreasing pair is an empty sequence), as
+ * gdn_read_status reports. Work grows linearly with the tokens of a sequence:
+ * long prompts belong to gdn_chunk_fwd. Errors: negative gdn_status before
+ * anything is enqueued (NULL q/k/v/g/beta/out, bad shape, misalignment: 16
+ * bytes for the tensors), GDN_ERR_LAUNCH_FAILED after a failed launch.
+ */
+int gdn_recurrent_fwd(const gdn_desc* desc, const void* q, const void* k, const void* v,
+                      const float* g, const float* beta, float scale,
+                      const float* initial_state, const int32_t* cu_seqlens, void* out,
+                      float* final_state, cudaStream_t stream);
+
 /* Static description of a gdn_status value. */
 const char* gdn_status_string(int status);
 

@@ -139,3 +139,25 @@ def test_product_path_has_no_oracle_or_fallback():
                 text = open(os.path.join(dirpath, fn)).read()
                 assert "import oracle" not in text and "from oracle" not in text, fn
                 assert "gdn_ref" not in text, fn
+
+
+def _rec(lib, d, q=4096, k=4096, v=4096, g=4096, beta=4096, s0=None, cu=4096, out=4096,
+         sT=None):
+    return lib.gdn_recurrent_fwd(ctypes.byref(d), q, k, v, g, beta, 0.0, s0, cu, out, sT, None)
+
+
+def test_recurrent_rejects_before_enqueue(lib):
+    """gdn_recurrent_fwd validates everything before touching the GPU."""
+    d = desc(N=1)
+    assert _rec(lib, d, q=None) == -1
+    assert _rec(lib, d, beta=None) == -1
+    assert _rec(lib, d, out=None) == -1
+    assert _rec(lib, desc(N=3), cu=None) == -2                   # N > 1 needs cu_seqlens
+    assert _rec(lib, d, v=4100) == -4                            # misaligned tensor
+    assert _rec(lib, d, sT=4104) == -4
+    assert _rec(lib, d, cu=4098) == -4
+    dw = desc(N=1)
+    dw.workspace = 4096 + 64                                     # status word alignment
+    assert _rec(lib, dw) == -4
+    assert _rec(lib, desc(Hv=24)) == -2
+    assert _rec(lib, desc(dk=64)) == -3
