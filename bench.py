@@ -279,6 +279,123 @@ def run_reference(args, ws, rank):
     }
 
 
+def recurrent_bytes(x, out_bytes=2):
+    """Bytes the token-serial kernel must move: each sequence's state read and written
+    once (fp32 [Hv, dv, dk]), q, k, v, g, beta read and out written per token."""
+    esz = 2 if x["dtype"] == "bf16" else 4
+    T, H, Hv, dk, dv, N = x["n_tokens"], x["H"], x["Hv"], x["dk"], x["dv"], x["N"]
+    states = N * Hv * dk * dv * 4
+    s_in = states if x["initial_state"] is not None else 0
+    return (s_in + states + 2 * T * H * dk * esz + T * Hv * dv * esz + 2 * T * Hv * 4
+            + T * Hv * dv * out_bytes)
+
+
+def run_recurrent(args, ws, rank, local):
+    """Decode / speculative-verify workloads through gdn_recurrent_fwd."""
+    import torch
+    from gated_delta_rule_chunk_gb300 import binding as B
+    from gated_delta_rule_chunk_gb300.build import build
+    from gated_delta_rule_chunk_gb300.inputs import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    x = make_inputs(args.workload)
+    d = {k: (x[k].to(dev) if x.get(k) is not None else None)
+         for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
+    out = torch.empty(x["T"], x["Hv"], 128, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(x["N"], x["Hv"], 128, 128, dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        B.gdn_recurrent_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"],
+                            d["initial_state"], d["cu_seqlens"], out=out, final_state=fin)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(args.warmup):
+        flush.fill_(i & 255)
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, args.clocks_file)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_((i + 1) & 255)
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    ms = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
+    ms_max = max_over_ranks(ms, ws)
+    tokens = x["n_tokens"]
+    value = ws * tokens / (ms_max / 1000.0)
+
+    # e2e: the step's tokens come from pinned host memory and the output goes back; the
+    # recurrent state stays resident on the device, as in a decode loop
+    host = {k: x[k].pin_memory() for k in ("q", "k", "v", "g", "beta", "cu_seqlens")}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size()
+    e2e_ms = []
+    for i in range(3 + args.e2e_steps if args.e2e_steps > 0 else 0):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for key, t in host.items():
+            d[key].copy_(t, non_blocking=True)
+        call()
+        out_h.copy_(out, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = (ws * tokens / (max_over_ranks(statistics.mean(e2e_ms), ws) / 1000.0)
+               if e2e_ms else None)
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    nbytes = recurrent_bytes(x)
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    res = {
+        "metric": "GDN token-serial decode/verify tokens/s (H16/Hv32 bf16, fp32 state)",
+        "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload].name, "N": x["N"],
+                   "tokens_per_sequence": x["lengths"][0], "H": x["H"], "Hv": x["Hv"],
+                   "dk": 128, "dv": 128, "qkv_dtype": "bf16", "out_dtype": "bf16",
+                   "initial_state": x["initial_state"] is not None,
+                   "l2": "512 MiB buffer written between timed steps (L2 is 129 MB)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "inputs": "resident in HBM"},
+        "roofline": {"bound": "hbm", "kernel": "recurrent", "achieved": gbs,
+                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms) if e2e_ms else None},
+        "gpu_launches": K,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        rate, ts, dt, cores, reps = oracle_rate(x, args.cpu_seconds)
+        res["cpu_baseline"] = {
+            "value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {ts} tokens as one sequence, all {x['Hv']} value heads, "
+                      f"run {reps} times ({dt:.1f} s of fp64 C on the host cores)"}
+    return res
+
+
 def run_gdn(args, ws, rank, local):
     import torch
     from gated_delta_rule_chunk_gb300 import binding as B
@@ -432,7 +549,11 @@ def main(argv=None):
         if args.impl == "reference":
             res = run_reference(args, ws, rank)
         else:
-            res = run_gdn(args, ws, rank, local)
+            from gated_delta_rule_chunk_gb300.inputs import WORKLOADS
+            if WORKLOADS[args.workload].kind == "fixed":
+                res = run_recurrent(args, ws, rank, local)
+            else:
+                res = run_gdn(args, ws, rank, local)
         if rank == 0 and res is not None:
             print(json.dumps(res), flush=True)
     finally:
