@@ -59,6 +59,19 @@ bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_state_tmap(void* tmap, const float* base, int rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {(cuuint64_t)kDk, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)kDk * 4};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<float*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace gdn
 
 namespace {
@@ -221,7 +234,7 @@ int gdn_recurrent_fwd(const gdn_desc* desc, const void* q, const void* k, const 
   p.l2norm = (d.flags & GDN_FLAG_QK_L2NORM) != 0;
   if (p.status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return GDN_ERR_LAUNCH_FAILED;
-  if (d.T > 0) launch_recurrent(p, stream);
+  if (d.T > 0 && !launch_recurrent(p, stream)) return GDN_ERR_LAUNCH_FAILED;
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 

@@ -117,10 +117,12 @@ void launch_simt_intra(const Params& p, bool bf16_inputs, cudaStream_t s);
 void launch_simt_inter(const Params& p, bool bf16_inputs, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
-void launch_recurrent(const RecParams& p, cudaStream_t s);
+bool launch_recurrent(const RecParams& p, cudaStream_t s);
 
 // Encode a TMA tensor map over a bf16 [rows, heads, 128] tensor with a box of
 // 64 rows x 1 head x 64 elements and the 128-byte swizzle. False on failure.
 bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads);
+// Same over an fp32 state [rows, 128]: box 32 rows x 32 elements, 128-byte swizzle.
+bool encode_state_tmap(void* tmap, const float* base, int rows);
 
 }  // namespace gdn
