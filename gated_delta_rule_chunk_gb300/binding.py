@@ -27,7 +27,7 @@ DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table
 # Every entry point include/gdn.h declares.
 EXPORTED = ("gdn_check_desc", "gdn_nt_max", "gdn_workspace_size", "gdn_build_chunk_indices",
             "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string", "gdn_chunk_fwd_noalloc",
-            "gdn_recurrent_fwd")
+            "gdn_recurrent_fwd", "gdn_conv_front")
 GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -78,6 +78,9 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_recurrent_fwd.argtypes = [P(GdnDesc), vp, vp, vp, vp, vp, ctypes.c_float, vp,
                                           vp, vp, vp, vp]
         lib.gdn_recurrent_fwd.restype = ctypes.c_int
+        lib.gdn_conv_front.argtypes = [P(GdnDesc), vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
+                                       i32, vp]
+        lib.gdn_conv_front.restype = ctypes.c_int
         lib.gdn_read_status.argtypes = [P(GdnDesc), vp, vp]
         lib.gdn_read_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -255,6 +258,46 @@ def gdn_recurrent_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torc
     if return_desc:
         return out, final_state, desc
     return out, final_state
+
+
+def gdn_conv_front(x: torch.Tensor, conv_w: torch.Tensor, H: int, Hv: int,
+                   conv_state: Optional[torch.Tensor] = None,
+                   cu_seqlens: Optional[torch.Tensor] = None, use_qk_l2norm: bool = False,
+                   l2norm_eps: float = 0.0, output_state: bool = True,
+                   conv_state_out: Optional[torch.Tensor] = None, n_snapshots: int = 0,
+                   status: Optional[torch.Tensor] = None, stream=None,
+                   return_desc: bool = False, q: Optional[torch.Tensor] = None,
+                   k: Optional[torch.Tensor] = None, v: Optional[torch.Tensor] = None):
+    """Front end through the C ABI: x [T, C] (C = 2*H*128 + Hv*128, bf16 or fp32),
+    conv_w fp32 [C, d_conv], conv_state fp32 [N, C, d_conv - 1] or None.
+    Returns (q, k, v, conv_state_out or None, snapshots or None[, desc])."""
+    T, C = x.shape
+    d_conv = conv_w.shape[1]
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    desc = make_desc(T, N, H, Hv, x.dtype, x.dtype,
+                     flags=GDN_FLAG_QK_L2NORM if use_qk_l2norm else 0, l2norm_eps=l2norm_eps)
+    for name, t in (("x", x), ("conv_w", conv_w)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    q = torch.empty(T, H, 128, dtype=x.dtype, device=x.device) if q is None else q
+    k = torch.empty(T, H, 128, dtype=x.dtype, device=x.device) if k is None else k
+    v = torch.empty(T, Hv, 128, dtype=x.dtype, device=x.device) if v is None else v
+    if conv_state_out is None and output_state:
+        conv_state_out = torch.empty(N, C, d_conv - 1, dtype=torch.float32, device=x.device)
+    snaps = (torch.empty(N, n_snapshots, C, d_conv - 1, dtype=torch.float32, device=x.device)
+             if n_snapshots > 0 else None)
+    if status is not None:
+        desc.workspace = status.data_ptr()
+        desc.workspace_bytes = status.numel() * status.element_size()
+    rc = load_library().gdn_conv_front(
+        ctypes.byref(desc), _ptr(x), _ptr(conv_w), int(d_conv), _ptr(conv_state),
+        _ptr(cu_seqlens), _ptr(q), _ptr(k), _ptr(v), _ptr(conv_state_out), _ptr(snaps),
+        int(n_snapshots), _stream_handle(stream))
+    if rc != 0:
+        raise GdnError(rc, "gdn_conv_front")
+    if return_desc:
+        return q, k, v, conv_state_out, snaps, desc
+    return q, k, v, conv_state_out, snaps
 
 
 def gdn_read_status(desc: GdnDesc, stream=None) -> int:

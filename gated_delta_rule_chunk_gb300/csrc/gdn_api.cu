@@ -238,6 +238,40 @@ int gdn_recurrent_fwd(const gdn_desc* desc, const void* q, const void* k, const 
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 
+int gdn_conv_front(const gdn_desc* desc, const void* x, const float* conv_w, int32_t d_conv,
+                   const float* conv_state_in, const int32_t* cu_seqlens, void* q, void* k,
+                   void* v, float* conv_state_out, float* snapshots, int32_t n_snapshots,
+                   cudaStream_t stream) {
+  int rc = check_desc_impl(desc);
+  if (rc != GDN_OK) return rc;
+  const gdn_desc& d = *desc;
+  if (!x || !conv_w || !q || !k || !v) return GDN_ERR_NULL_ARG;
+  if (d_conv < 1 || d_conv > 8 || n_snapshots < 0) return GDN_ERR_BAD_SHAPE;
+  if ((n_snapshots > 0) != (snapshots != nullptr)) return GDN_ERR_BAD_SHAPE;
+  if (!cu_seqlens && d.N != 1) return GDN_ERR_BAD_SHAPE;
+  const void* ptrs16[] = {x, q, k, v};
+  for (const void* p : ptrs16)
+    if (!aligned(p, 16)) return GDN_ERR_MISALIGNED;
+  const void* ptrs4[] = {conv_w, conv_state_in, conv_state_out, snapshots, cu_seqlens};
+  for (const void* p : ptrs4)
+    if (!aligned(p, 4)) return GDN_ERR_MISALIGNED;
+  if (!aligned(d.workspace, 256)) return GDN_ERR_MISALIGNED;
+  ConvParams p{};
+  p.T = d.T; p.N = d.N; p.H = d.H; p.Hv = d.Hv;
+  p.C = 2 * d.H * kDk + d.Hv * kDv;
+  p.d = d_conv; p.n_snap = n_snapshots;
+  p.x = x; p.w = conv_w; p.s_in = conv_state_in; p.s_out = conv_state_out; p.snaps = snapshots;
+  p.q = q; p.k = k; p.v = v; p.cu = cu_seqlens;
+  p.status = d.workspace ? static_cast<int32_t*>(d.workspace) : nullptr;
+  p.eps = d.l2norm_eps > 0.f ? d.l2norm_eps : 1e-6f;
+  p.bf16 = d.qkv_dtype == GDN_BF16;
+  p.l2norm = (d.flags & GDN_FLAG_QK_L2NORM) != 0;
+  if (p.status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH_FAILED;
+  launch_conv_front(p, stream);
+  return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
+}
+
 int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t stream) {
   int rc = check_desc_impl(desc);
   if (rc != GDN_OK) return rc;

@@ -57,6 +57,23 @@ struct RecParams {
   int bf16_in, out_bf16, l2norm;
 };
 
+// Parameters of the front-end kernels (device pointers).
+struct ConvParams {
+  int T, N, H, Hv, C, d, n_snap;
+  const void* x;        // [T, C] projection output (q | k | v channels)
+  const float* w;       // [C, d] conv taps
+  const float* s_in;    // [N, C, d - 1] or null (zeros)
+  float* s_out;         // [N, C, d - 1] or null
+  float* snaps;         // [N, n_snap, C, d - 1] or null
+  void* q;              // [T, H, dk]
+  void* k;              // [T, H, dk]
+  void* v;              // [T, Hv, dv]
+  const int32_t* cu;    // [N + 1] or null
+  int32_t* status;      // device status word or null
+  float eps;
+  int bf16, l2norm;
+};
+
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
   size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qrn, krn, total;
@@ -118,6 +135,7 @@ void launch_simt_inter(const Params& p, bool bf16_inputs, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
 bool launch_recurrent(const RecParams& p, cudaStream_t s);
+void launch_conv_front(const ConvParams& p, cudaStream_t s);
 
 // Encode a TMA tensor map over a bf16 [rows, heads, 128] tensor with a box of
 // 64 rows x 1 head x 64 elements and the 128-byte swizzle. False on failure.

@@ -177,3 +177,29 @@ def make_inputs(wid: int = HEADLINE, seed: Optional[int] = None, T: Optional[int
         T=rows, N=N, H=H, Hv=Hv, dk=dk, dv=dv, nt_max=nt_max, dtype=dtype,
         n_tokens=int(cu[-1]), lengths=lengths, wid=wid,
     )
+
+
+def make_conv_inputs(seed: int = 7, T: int = 64, H: int = 2, Hv: int = 4, d_conv: int = 4,
+                     lengths: Optional[list] = None, dtype: str = "bf16",
+                     with_state: bool = True, rows: Optional[int] = None,
+                     cu_offset: int = 0) -> dict:
+    """Inputs of the front end: the qkv projection output x [rows, C] ~ N(0, 1)
+    (C = 2*H*128 + Hv*128, rounded once to `dtype`), conv taps [C, d_conv] ~ N(0, 0.5)
+    fp32, conv states [N, C, d_conv - 1] ~ N(0, 1) fp32 (or None), cu_seqlens from
+    `lengths` (default one sequence of T rows) starting at row `cu_offset`."""
+    gen = _gen(seed)
+    lengths = [T] if lengths is None else [int(a) for a in lengths]
+    cu = [cu_offset]
+    for a in lengths:
+        cu.append(cu[-1] + a)
+    rows = rows if rows is not None else cu[-1]
+    C = 2 * H * 128 + Hv * 128
+    f64 = torch.float64
+    x = torch.randn(rows, C, generator=gen, dtype=f64)
+    w = 0.5 * torch.randn(C, d_conv, generator=gen, dtype=f64)
+    s0 = torch.randn(len(lengths), C, d_conv - 1, generator=gen, dtype=f64) if with_state else None
+    tdt = torch.float32 if dtype == "f32" else torch.bfloat16
+    return dict(x=x.to(tdt).contiguous(), w=w.float().contiguous(),
+                state=None if s0 is None else s0.float().contiguous(),
+                cu_seqlens=torch.tensor(cu, dtype=torch.int32), H=H, Hv=Hv, d_conv=d_conv,
+                T=rows, N=len(lengths), C=C, dtype=dtype)

@@ -263,6 +263,43 @@ int gdn_recurrent_fwd(const gdn_desc* desc, const void* q, const void* k, const 
                       const float* initial_state, const int32_t* cu_seqlens, void* out,
                       float* final_state, cudaStream_t stream);
 
+/*
+ * Front end: the qkv projection output of a gated-DeltaNet layer to q, k, v
+ * (the llama.cpp page, PrismML-Eng/llama.cpp pull 399, "What", item 1, and "How
+ * (exactness)"): per channel a causal depthwise convolution of width d_conv whose
+ * inputs are the d_conv - 1 inputs saved from before the sequence (the conv
+ * state) followed by the sequence's rows, summed in tap order
+ * (sum += w[j] * xx[t + j], j = 0 .. d_conv - 1, fp32, no bias), then SiLU, then,
+ * when GDN_FLAG_QK_L2NORM is set, each q and k head row divided by
+ * sqrt(sum x^2 + eps) (for gdn_chunk_fwd prefer leaving the flag off here and
+ * setting it there, where the norm stays an fp32 factor instead of a rounded copy).
+ *
+ *   x               [T, C] in desc->qkv_dtype, C = 2*H*dk + Hv*dv, channels q | k | v
+ *   conv_w          fp32 [C, d_conv], 1 <= d_conv <= 8
+ *   conv_state_in   fp32 [N, C, d_conv - 1] (oldest first) or NULL for zeros
+ *   cu_seqlens      int32 [N + 1] or NULL (one sequence of T rows); rows outside
+ *                   every sequence are not written
+ *   q, k            [T, H, dk]; v [T, Hv, dv]; desc->qkv_dtype (the x dtype)
+ *   conv_state_out  fp32 [N, C, d_conv - 1] or NULL: the last d_conv - 1 inputs of
+ *                   each sequence (old state entries when it is shorter); may alias
+ *                   conv_state_in
+ *   snapshots       fp32 [N, n_snapshots, C, d_conv - 1] or NULL: row s is the state
+ *                   after the sequence's token s (after its last token for s past
+ *                   the end), for rolling a speculative batch back; must not alias
+ *                   conv_state_in
+ *
+ * The descriptor is validated as for gdn_chunk_fwd (chunk_size, nt_max and
+ * out_dtype play no part). desc->workspace, when non-NULL, receives the status
+ * word (GDN_DEV_BAD_CU_SEQLENS for a malformed cu_seqlens, clamped to [0, T]).
+ * Errors: negative gdn_status before anything is enqueued (NULL x/conv_w/q/k/v,
+ * bad d_conv or n_snapshots, misalignment: 16 bytes for x, q, k, v),
+ * GDN_ERR_LAUNCH_FAILED after a failed launch.
+ */
+int gdn_conv_front(const gdn_desc* desc, const void* x, const float* conv_w, int32_t d_conv,
+                   const float* conv_state_in, const int32_t* cu_seqlens, void* q, void* k,
+                   void* v, float* conv_state_out, float* snapshots, int32_t n_snapshots,
+                   cudaStream_t stream);
+
 /* Static description of a gdn_status value. */
 const char* gdn_status_string(int status);
 

@@ -161,3 +161,22 @@ def test_recurrent_rejects_before_enqueue(lib):
     assert _rec(lib, dw) == -4
     assert _rec(lib, desc(Hv=24)) == -2
     assert _rec(lib, desc(dk=64)) == -3
+
+
+def test_conv_front_rejects_before_enqueue(lib):
+    """gdn_conv_front validates everything before touching the GPU."""
+    d = desc(N=1)
+    f = lambda **kw: lib.gdn_conv_front(
+        ctypes.byref(kw.pop("d", d)), kw.get("x", 4096), kw.get("w", 4096), kw.get("dc", 4),
+        kw.get("s0", None), kw.get("cu", None), kw.get("q", 4096), kw.get("k", 4096),
+        kw.get("v", 4096), kw.get("s1", None), kw.get("sn", None), kw.get("ns", 0), None)
+    assert f(x=None) == -1
+    assert f(w=None) == -1
+    assert f(v=None) == -1
+    assert f(dc=0) == -2 and f(dc=9) == -2
+    assert f(ns=2) == -2                       # snapshots requested without a buffer
+    assert f(sn=4096) == -2                    # a buffer without a count
+    assert f(d=desc(N=2)) == -2                # N > 1 needs cu_seqlens
+    assert f(q=4104) == -4 and f(x=4100) == -4
+    assert f(s1=4098) == -4
+    assert f(d=desc(Hv=24)) == -2
