@@ -396,6 +396,125 @@ def run_recurrent(args, ws, rank, local):
     return res
 
 
+def conv_bytes(c):
+    """Bytes the front end must move: x read, q/k/v written (same size), the taps,
+    the conv state read and written."""
+    esz = 2 if c["dtype"] == "bf16" else 4
+    T, C, d, N = c["T"], c["C"], c["d_conv"], c["N"]
+    states = N * C * (d - 1) * 4
+    return 2 * T * C * esz + C * d * 4 + 2 * states
+
+
+def run_conv(args, ws, rank, local):
+    """The front end (gdn_conv_front) on the Qwen3.5-9B-shaped prefill."""
+    import torch
+    from gated_delta_rule_chunk_gb300 import binding as B
+    from gated_delta_rule_chunk_gb300.build import build
+    from gated_delta_rule_chunk_gb300.inputs import WORKLOADS, make_conv_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    wl = WORKLOADS[args.workload]
+    c = make_conv_inputs(seed=1000 + args.workload, T=wl.T, H=wl.H, Hv=wl.Hv, d_conv=4)
+    x, w, s0 = c["x"].to(dev), c["w"].to(dev), c["state"].to(dev)
+    T, C = x.shape
+    q = torch.empty(T, wl.H, 128, dtype=x.dtype, device=dev)
+    k = torch.empty_like(q)
+    v = torch.empty(T, wl.Hv, 128, dtype=x.dtype, device=dev)
+    s1 = torch.empty_like(s0)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call():
+        B.gdn_conv_front(x, w, wl.H, wl.Hv, s0, None, conv_state_out=s1, q=q, k=k, v=v)
+
+    K = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K)]
+    for i in range(args.warmup):
+        flush.fill_(i & 255)
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, args.clocks_file)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_((i + 1) & 255)
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    ms = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
+    ms_max = max_over_ranks(ms, ws)
+    value = ws * T / (ms_max / 1000.0)
+    # e2e: x from pinned host memory, q/k/v back; the conv state stays resident
+    x_h = c["x"].pin_memory()
+    outs_h = [torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in (q, k, v)]
+    h2d = x_h.numel() * x_h.element_size()
+    d2h = sum(t.numel() * t.element_size() for t in outs_h)
+    e2e_ms = []
+    for i in range(3 + args.e2e_steps if args.e2e_steps > 0 else 0):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        x.copy_(x_h, non_blocking=True)
+        call()
+        for hh, dd in zip(outs_h, (q, k, v)):
+            hh.copy_(dd, non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = (ws * T / (max_over_ranks(statistics.mean(e2e_ms), ws) / 1000.0)
+               if e2e_ms else None)
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    nbytes = conv_bytes(c)
+    gbs = nbytes / (ms / 1000.0) / 1e9
+    res = {
+        "metric": "GDN front end (conv1d d=4 + SiLU over the qkv projection) tokens/s",
+        "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "T": T, "channels": C, "d_conv": 4, "H": wl.H,
+                   "Hv": wl.Hv, "qkv_dtype": "bf16", "conv_state": True,
+                   "l2": "512 MiB buffer written between timed steps (L2 is 129 MB)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "inputs": "resident in HBM"},
+        "roofline": {"bound": "hbm", "kernel": "conv", "achieved": gbs, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                     "algorithmic_bytes_per_launch": nbytes, "traffic": None},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms) if e2e_ms else None},
+        "gpu_launches": 2 * K,
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        from oracle.conv_front import conv_front
+        ts = min(T, 256)
+        t1 = time.perf_counter()
+        reps = 0
+        while time.perf_counter() - t1 < min(args.cpu_seconds, 5.0) or reps == 0:
+            conv_front(c["x"][:ts], c["w"], wl.H, wl.Hv, conv_state=c["state"])
+            reps += 1
+        dt = time.perf_counter() - t1
+        res["cpu_baseline"] = {"value": reps * ts / dt, "unit": "tokens/s", "cores": 1,
+                               "kind": "oracle",
+                               "sample": f"first {ts} rows, all {C} channels, run {reps} times "
+                                         f"({dt:.1f} s of fp64 NumPy on one core)"}
+    return res
+
+
 def run_gdn(args, ws, rank, local):
     import torch
     from gated_delta_rule_chunk_gb300 import binding as B
@@ -552,6 +671,8 @@ def main(argv=None):
             from gated_delta_rule_chunk_gb300.inputs import WORKLOADS
             if WORKLOADS[args.workload].kind == "fixed":
                 res = run_recurrent(args, ws, rank, local)
+            elif WORKLOADS[args.workload].kind == "conv":
+                res = run_conv(args, ws, rank, local)
             else:
                 res = run_gdn(args, ws, rank, local)
         if rank == 0 and res is not None:

@@ -86,6 +86,9 @@ __device__ __forceinline__ void input4(const ConvParams& p, int n, int start, in
   }
 }
 
+// D = d_conv as a compile-time constant: the tap loop and the window shift unroll
+// without predicates (the kernel is instruction-bound otherwise).
+template <int D>
 __global__ void __launch_bounds__(128) conv_kernel(ConvParams p) {
   const int tid = threadIdx.x;
   const int c = blockIdx.y * 512 + 4 * tid;  // first of this thread's 4 channels
@@ -93,67 +96,73 @@ __global__ void __launch_bounds__(128) conv_kernel(ConvParams p) {
   const int t0 = blockIdx.x * kTile;
   const int t1 = min(t0 + kTile, p.T);
   const bool qk = c < 2 * p.H * kDk;  // q or k channels (whole warps: heads are 128 wide)
-  float w[4][kMaxConv];
+  float w[4][D];
 #pragma unroll
   for (int e = 0; e < 4; ++e)
 #pragma unroll
-    for (int j = 0; j < kMaxConv; ++j) w[e][j] = j < p.d ? p.w[(size_t)(c + e) * p.d + j] : 0.f;
+    for (int j = 0; j < D; ++j) w[e][j] = p.w[(size_t)(c + e) * D + j];
 
   int n = seq_of(p, t0);
   int2 sb = n < p.N ? seq_bounds(p, n) : make_int2(p.T, p.T);
-  float win[kMaxConv][4];  // win[j]: input at row t - (d - 1) + j, j < d - 1
+  float win[D > 1 ? D - 1 : 1][4];  // win[j]: input at row t - (D - 1) + j
   auto fill = [&](int t) {
 #pragma unroll
-    for (int j = 0; j < kMaxConv - 1; ++j)
-      if (j < p.d - 1) input4(p, n, sb.x, t - (p.d - 1) + j, c, win[j]);
+    for (int j = 0; j < D - 1; ++j) input4(p, n, sb.x, t - (D - 1) + j, c, win[j]);
   };
   bool stale = true;  // the window is filled at the first row of each sequence run
-  for (int t = t0; t < t1; ++t) {
-    if (n >= p.N) break;             // rows past the last sequence are not part of any
-    if (t >= sb.y) {                 // next sequence (skipping empty ones)
-      while (n < p.N && seq_bounds(p, n).y <= t) ++n;
-      if (n >= p.N) break;
-      sb = seq_bounds(p, n);
-      stale = true;
-    }
-    if (t < sb.x) continue;          // a row before the sequence (no sequence owns it)
-    if (stale) {
-      fill(t);
-      stale = false;
-    }
-    float cur[4], y[4];
-    load4(p.x, (size_t)t * p.C + c, p.bf16, cur);
+  constexpr int G = 8;  // rows loaded together (memory-level parallelism)
+  for (int tb = t0; tb < t1; tb += G) {
+    float rowv[G][4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      float acc = 0.f;  // taps in order j = 0 .. d - 1 (the current row is tap d - 1)
+    for (int u = 0; u < G; ++u)
+      if (tb + u < t1) load4(p.x, (size_t)(tb + u) * p.C + c, p.bf16, rowv[u]);
 #pragma unroll
-      for (int j = 0; j < kMaxConv; ++j)
-        if (j < p.d) acc = fmaf(w[e][j], j < p.d - 1 ? win[j][e] : cur[e], acc);
-      y[e] = acc / (1.f + expf(-acc));
-    }
-    if (p.l2norm && qk) {
-      float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float r = 1.f / sqrtf(ss + p.eps);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) y[e] *= r;
-    }
-    // q [T,H,dk], k [T,H,dk], v [T,Hv,dv]: channel c is element c of row t of q, then k, v
-    const int qkc = p.H * kDk;
-    if (c < qkc)
-      store4(p.q, (size_t)t * qkc + c, p.bf16, y);
-    else if (c < 2 * qkc)
-      store4(p.k, (size_t)t * qkc + (c - qkc), p.bf16, y);
-    else
-      store4(p.v, (size_t)t * (p.Hv * kDv) + (c - 2 * qkc), p.bf16, y);
-    // slide the window (slot d - 2 takes the current row)
-#pragma unroll
-    for (int j = 0; j < kMaxConv - 1; ++j)
-      if (j < p.d - 1) {
-#pragma unroll
-        for (int e = 0; e < 4; ++e) win[j][e] = j + 1 < p.d - 1 ? win[j + 1][e] : cur[e];
+    for (int u = 0; u < G; ++u) {
+      const int t = tb + u;
+      if (t >= t1 || n >= p.N) break;  // rows past the last sequence are not part of any
+      if (t >= sb.y) {                  // next sequence (skipping empty ones)
+        while (n < p.N && seq_bounds(p, n).y <= t) ++n;
+        if (n >= p.N) break;
+        sb = seq_bounds(p, n);
+        stale = true;
       }
+      if (t < sb.x) continue;           // a row before the sequence (no sequence owns it)
+      if (stale) {
+        fill(t);
+        stale = false;
+      }
+      const float (&cur)[4] = rowv[u];
+      float y[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        float acc = 0.f;  // taps in order j = 0 .. D - 1 (the current row is tap D - 1)
+#pragma unroll
+        for (int j = 0; j < D - 1; ++j) acc = fmaf(w[e][j], win[j][e], acc);
+        acc = fmaf(w[e][D - 1], cur[e], acc);
+        y[e] = __fdividef(acc, 1.f + __expf(-acc));  // SiLU
+      }
+      if (p.l2norm && qk) {
+        float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        const float r = 1.f / sqrtf(ss + p.eps);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) y[e] *= r;
+      }
+      // q [T,H,dk], k [T,H,dk], v [T,Hv,dv]: channel c is element c of row t of q, then k, v
+      const int qkc = p.H * kDk;
+      if (c < qkc)
+        store4(p.q, (size_t)t * qkc + c, p.bf16, y);
+      else if (c < 2 * qkc)
+        store4(p.k, (size_t)t * qkc + (c - qkc), p.bf16, y);
+      else
+        store4(p.v, (size_t)t * (p.Hv * kDv) + (c - 2 * qkc), p.bf16, y);
+      // slide the window (slot D - 2 takes the current row)
+#pragma unroll
+      for (int j = 0; j < D - 1; ++j)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) win[j][e] = j + 1 < D - 1 ? win[j + 1][e] : cur[e];
+    }
   }
 }
 
@@ -207,8 +216,19 @@ __global__ void __launch_bounds__(128) state_kernel(ConvParams p) {
 
 void launch_conv_front(const ConvParams& p, cudaStream_t s) {
   const dim3 tiles((unsigned)((p.C + 511) / 512));
-  if (p.T > 0)
-    conv_kernel<<<dim3((unsigned)((p.T + kTile - 1) / kTile), tiles.x), 128, 0, s>>>(p);
+  if (p.T > 0) {
+    const dim3 grid((unsigned)((p.T + kTile - 1) / kTile), tiles.x);
+    switch (p.d) {
+      case 1: conv_kernel<1><<<grid, 128, 0, s>>>(p); break;
+      case 2: conv_kernel<2><<<grid, 128, 0, s>>>(p); break;
+      case 3: conv_kernel<3><<<grid, 128, 0, s>>>(p); break;
+      case 4: conv_kernel<4><<<grid, 128, 0, s>>>(p); break;
+      case 5: conv_kernel<5><<<grid, 128, 0, s>>>(p); break;
+      case 6: conv_kernel<6><<<grid, 128, 0, s>>>(p); break;
+      case 7: conv_kernel<7><<<grid, 128, 0, s>>>(p); break;
+      default: conv_kernel<8><<<grid, 128, 0, s>>>(p); break;
+    }
+  }
   if (p.N > 0) state_kernel<<<dim3((unsigned)p.N, tiles.x), 128, 0, s>>>(p);
 }
 

@@ -43,7 +43,7 @@ class Workload:
     dv: int
     dtype: str                    # "f32" or "bf16" for q/k/v
     with_initial_state: bool
-    kind: str                     # "single", "varlen", "static_bound", "fixed"
+    kind: str                     # "single", "varlen", "static_bound", "fixed", "conv"
     T: int = 0                    # single: sequence length
     n_seqs: int = 1               # varlen: number of sequences
     max_len: int = 0              # varlen: lengths ~ U[1, max_len]
@@ -71,6 +71,9 @@ WORKLOADS = {
                 128, 128, "bf16", True, "fixed", fixed_lens=(1,) * 64),
     6: Workload(6, "speculative verify: 8 sequences x 8 tokens, H=16 Hv=32 d=128 bf16", 16,
                 32, 128, 128, "bf16", True, "fixed", fixed_lens=(8,) * 8),
+    # front end (conv + SiLU over the qkv projection output; make_conv_inputs)
+    7: Workload(7, "front end: conv1d d=4 + SiLU over the qkv projection, T=4096 H=16 Hv=32 "
+                "bf16", 16, 32, 128, 128, "bf16", True, "conv", T=4096),
 }
 
 HEADLINE = 2
@@ -88,6 +91,8 @@ def draw_lengths(wl: Workload, gen: torch.Generator) -> list:
         return [wl.T]
     if wl.kind == "fixed":
         return list(wl.fixed_lens)
+    if wl.kind == "conv":
+        return [wl.T]
     if wl.kind == "varlen":
         out = []
         while len(out) < wl.n_seqs:
