@@ -5,8 +5,8 @@
 
 #include <cuda.h>
 
+#include <map>
 #include <mutex>
-#include <set>
 #include <utility>
 
 #include "gdn_common.cuh"
@@ -16,15 +16,17 @@ using namespace gdn;
 namespace gdn {
 
 void ensure_smem_limit(const void* kernel, int bytes) {
+  // largest limit set so far per (kernel, device); raised when a call needs more
   static std::mutex mu;
-  static std::set<std::pair<const void*, int>> done;
+  static std::map<std::pair<const void*, int>, int> done;
   int dev = 0;
   cudaGetDevice(&dev);
   std::lock_guard<std::mutex> lock(mu);
-  if (done.count({kernel, dev})) return;
+  auto it = done.find({kernel, dev});
+  if (it != done.end() && it->second >= bytes) return;
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) ==
       cudaSuccess)
-    done.insert({kernel, dev});
+    done[{kernel, dev}] = bytes;
 }
 
 using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
@@ -69,6 +71,22 @@ bool encode_state_tmap(void* tmap, const float* base, int rows) {
   return fn(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
             const_cast<float*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_2d_tmap(void* tmap, const void* base, bool bf16, int cols, int rows, int box_cols,
+                    int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t esz = bf16 ? 2 : 4;
+  const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)cols * esz};
+  const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(static_cast<CUtensorMap*>(tmap),
+            bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -268,7 +286,7 @@ int gdn_conv_front(const gdn_desc* desc, const void* x, const float* conv_w, int
   p.l2norm = (d.flags & GDN_FLAG_QK_L2NORM) != 0;
   if (p.status && cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return GDN_ERR_LAUNCH_FAILED;
-  launch_conv_front(p, stream);
+  if (!launch_conv_front(p, stream)) return GDN_ERR_LAUNCH_FAILED;
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 

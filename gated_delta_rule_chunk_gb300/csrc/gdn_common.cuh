@@ -135,11 +135,14 @@ void launch_simt_inter(const Params& p, bool bf16_inputs, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
 bool launch_recurrent(const RecParams& p, cudaStream_t s);
-void launch_conv_front(const ConvParams& p, cudaStream_t s);
+bool launch_conv_front(const ConvParams& p, cudaStream_t s);
 
 // Encode a TMA tensor map over a bf16 [rows, heads, 128] tensor with a box of
 // 64 rows x 1 head x 64 elements and the 128-byte swizzle. False on failure.
 bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads);
+// Plain 2-D tensor map over a row-major [rows, cols] bf16 or fp32 matrix (no swizzle).
+bool encode_2d_tmap(void* tmap, const void* base, bool bf16, int cols, int rows, int box_cols,
+                    int box_rows);
 // Same over an fp32 state [rows, 128]: box 32 rows x 32 elements, 128-byte swizzle.
 bool encode_state_tmap(void* tmap, const float* base, int rows);
 
