@@ -102,7 +102,7 @@ NCU_TRAFFIC = {
               "sha1": "41d43b926d39a4e76727a2bce7cf3701a61c66f4", "bytes": 195343872,
               "profile": "profiles/tc_inter_kernel_T4096_H16_Hv32.md"},
     "intra": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_intra.cu",
-              "sha1": "94e36e0bab9a9b5cf6923712e88c823420d57282", "bytes": 165812480,
+              "sha1": "3c8f81595559a68767530340128566c168a2e381", "bytes": 161003776,
               "profile": "profiles/tc_intra_kernel_T4096_H16_Hv32.md"},
 }
 NCU_WORKLOAD = 2
