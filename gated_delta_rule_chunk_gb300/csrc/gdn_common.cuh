@@ -107,6 +107,15 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
 __device__ __forceinline__ float to_f32(float x) { return x; }
 __device__ __forceinline__ float to_f32(__nv_bfloat16 x) { return __bfloat162float(x); }
 
+// Programmatic dependent launch: a kernel launched with the programmatic-serialization
+// attribute may start before its predecessor in the stream has finished; pdl_wait()
+// blocks until the predecessor has completed and its writes are visible (a no-op for
+// a kernel launched without the attribute); pdl_release() lets the successor start.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_release() {
+  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void set_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
@@ -124,6 +133,23 @@ __device__ __forceinline__ SeqView seq_view(const Params& p, int n) {
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
 // that later calls (for example under CUDA-graph capture) make no attribute call.
 void ensure_smem_limit(const void* kernel, int bytes);
+
+// Launch `kernel` on `s` with the programmatic-serialization attribute (see pdl_wait).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t s, Args&&... args) {
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args&&>(args)...);
+}
 
 // Kernel launchers (one translation unit each).
 void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,

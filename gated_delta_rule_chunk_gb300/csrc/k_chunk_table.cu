@@ -19,6 +19,7 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
                    int2* __restrict__ seq_info, int32_t* status) {
   __shared__ int warp_incl[32];
   __shared__ int carry_s;
+  pdl_release();  // the intra kernel may be scheduled now; it waits for this grid's writes
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
   if (tid == 0) carry_s = 0;
   __syncthreads();

@@ -180,12 +180,6 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x, hv = blockIdx.y, jb = blockIdx.z, c0 = jb * BV;
   const int h = hv / p.HG;
-  const SeqView sv = seq_view(p, n);
-  int nch = (sv.len + kChunk - 1) / kChunk;
-  if (sv.first_slot + nch > p.nt_max) {
-    if (tid == 0) set_status(p.status, GDN_DEV_CHUNK_OVERFLOW);
-    nch = max(0, p.nt_max - sv.first_slot);
-  }
   const size_t state_base = ((size_t)n * p.Hv + hv) * kDv * kDk;
   const uint32_t sbase = smem_addr(sm);
   const int g = lane >> 2, c2 = 2 * (lane & 3);
@@ -206,6 +200,13 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  pdl_wait();  // everything below reads what the chunk-table and intra kernels wrote
+  const SeqView sv = seq_view(p, n);
+  int nch = (sv.len + kChunk - 1) / kChunk;
+  if (sv.first_slot + nch > p.nt_max) {
+    if (tid == 0) set_status(p.status, GDN_DEV_CHUNK_OVERFLOW);
+    nch = max(0, p.nt_max - sv.first_slot);
+  }
 
   if (warp < kChainWarps) {
     // ------------------------------------------------------------------ chain
@@ -514,8 +515,8 @@ bool launch_tc_inter(const Params& p, cudaStream_t s) {
   const int rows = p.T > 0 ? p.T : 1;  // with T = 0 no tile is ever loaded
   if (!encode_rows_tmap(&tmq, p.q, rows, p.H)) return false;
   ensure_smem_limit((const void*)tc_inter_kernel, (int)kSmemBytes);
-  tc_inter_kernel<<<dim3(p.N, p.Hv, kDv / BV), kThreads, kSmemBytes, s>>>(p, tmq);
-  return true;
+  return launch_pdl(tc_inter_kernel, dim3(p.N, p.Hv, kDv / BV), dim3(kThreads), kSmemBytes, s, p,
+                    tmq) == cudaSuccess;
 }
 
 }  // namespace gdn

@@ -140,6 +140,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   // Key head fastest in the grid: CTAs resident together read all heads of the same
   // tokens (contiguous rows of q, k and v) rather than one head of many chunks.
   const int h = blockIdx.x;
+  pdl_wait();     // the chunk table (and the L2-norm factors) are written
+  pdl_release();  // the inter kernel may take SMs as this grid drains
   int t0, L, wslot;
   if (!resolve(p, blockIdx.y, t0, L, wslot)) return;  // uniform over the CTA
 
@@ -472,8 +474,8 @@ bool launch_tc_intra(const Params& p, cudaStream_t s) {
       !encode_rows_tmap(&tmv, p.v, rows, p.Hv))
     return false;
   ensure_smem_limit((const void*)tc_intra_kernel, (int)kSmemBytes);
-  tc_intra_kernel<<<dim3(p.H, p.nt_max), 128, kSmemBytes, s>>>(p, tmk, tmq, tmv);
-  return true;
+  return launch_pdl(tc_intra_kernel, dim3(p.H, p.nt_max), dim3(128), kSmemBytes, s, p, tmk,
+                    tmq, tmv) == cudaSuccess;
 }
 
 }  // namespace gdn
