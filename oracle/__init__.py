@@ -60,7 +60,7 @@ def _bind(path: str):
     i64, dbl, ptr = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p
     lib.gdn_ref_forward.argtypes = [i64, i64, i64, i64, i64, i64,
                                     ptr, ptr, ptr, ptr, ptr, dbl, ptr, ptr,
-                                    ctypes.c_int, dbl, ptr, ptr, ctypes.c_int]
+                                    ctypes.c_int, dbl, ptr, ptr, ctypes.c_int, ctypes.c_int]
     lib.gdn_ref_forward.restype = ctypes.c_int
     lib.gdn_ref_max_threads.argtypes = []
     lib.gdn_ref_max_threads.restype = ctypes.c_int
@@ -96,7 +96,8 @@ def recurrent_forward(q, k, v, g, beta, scale=None, initial_state=None,
     """Token-by-token fp64 gated delta rule (the oracle's definition).
 
     Shapes follow the library boundary: q, k [T, H, dk]; v [T, Hv, dv];
-    g, beta [T, Hv]; initial_state [N, Hv, dv, dk] (or None for zeros);
+    g, beta [T, Hv] (g may be [T, Hv, dk]: one log-decay per key channel);
+    initial_state [N, Hv, dv, dk] (or None for zeros);
     cu_seqlens [N+1] (or None for one sequence of T rows).
     Returns (out [T, Hv, dv], final_state [N, Hv, dv, dk] or None), fp64.
     ``out_init`` fills rows the recurrence does not touch (default zeros).
@@ -104,6 +105,9 @@ def recurrent_forward(q, k, v, g, beta, scale=None, initial_state=None,
     q, k, v, g, beta = (_f64(a) for a in (q, k, v, g, beta))
     T, H, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
+    per_channel = g.ndim == 3
+    if per_channel and g.shape != (T, Hv, dk):
+        raise ValueError("per-channel gates must be [T, Hv, dk]")
     if cu_seqlens is None:
         N, cu = 1, None
     else:
@@ -121,7 +125,7 @@ def recurrent_forward(q, k, v, g, beta, scale=None, initial_state=None,
     rc = lib.gdn_ref_forward(T, N, H, Hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
                              _ptr(beta), float(scale), _ptr(s0), _ptr(cu),
                              int(bool(qk_l2norm)), float(eps), _ptr(out), _ptr(fin),
-                             int(nthreads))
+                             int(nthreads), int(per_channel))
     if rc != 0:
         raise ValueError(f"gdn_ref_forward rejected its arguments (rc={rc})")
     return out, fin

@@ -19,6 +19,17 @@ contribution, the local attention output and the state update), with the
 plus sign of (I + A) fixed by the derivation. The triangular system is
 solved with SciPy's ``solve_triangular`` (a library primitive); nothing is
 blocked, fused or reordered beyond the closed form above.
+
+Per-channel gates (g of shape [T, Hv, dk]): G_i becomes a vector over the key
+dimension and every scalar ratio gamma_i / gamma_j moves inside the dot
+products, one factor per key channel d:
+
+    A_ij = beta_i * sum_d k_id k_jd exp(G_id - G_jd)        for j < i,
+    (I + A) X = diag(beta) V - diag(beta) (exp(G) * K) S,
+    o_i  = scale * [(exp(G_i) * q_i)^T S + sum_{j<=i} (sum_d q_id k_jd exp(G_id - G_jd)) x_j],
+    S'   = diag(exp(G_L)) S + (exp(G_L - G) * K)^T X,
+
+which reduces to the scalar form when all channels carry the same gate.
 """
 from __future__ import annotations
 
@@ -65,8 +76,12 @@ def chunked_forward(q, k, v, g, beta, scale=None, initial_state=None,
                 Q = q[c0:c1, h]
                 V = v[c0:c1, hv]             # [L, dv]
                 b = beta[c0:c1, hv]          # [L]
-                G = np.cumsum(g[c0:c1, hv])  # inclusive, within the chunk
                 L = c1 - c0
+                if g.ndim == 3:
+                    S, o, X = _channel_chunk(K, Q, V, b, g[c0:c1, hv], S)
+                    out[c0:c1, hv] = scale * o
+                    continue
+                G = np.cumsum(g[c0:c1, hv])  # inclusive, within the chunk
                 ii, jj = np.meshgrid(np.arange(L), np.arange(L), indexing="ij")
                 ratio = np.exp(np.where(jj <= ii, G[:, None] - G[None, :], -np.inf))
                 A = np.where(jj < ii, b[:, None] * ratio * (K @ K.T), 0.0)
@@ -77,3 +92,20 @@ def chunked_forward(q, k, v, g, beta, scale=None, initial_state=None,
                 S = np.exp(G[-1]) * S + (np.exp(G[-1] - G)[:, None] * K).T @ X
             final[n, hv] = S.T
     return out, final
+
+
+def _channel_chunk(K, Q, V, b, g, S):
+    """One chunk with per-channel gates g [L, dk]; returns (S', o / scale, X)."""
+    L = K.shape[0]
+    G = np.cumsum(g, axis=0)                                  # [L, dk]
+    ii, jj = np.meshgrid(np.arange(L), np.arange(L), indexing="ij")
+    diff = np.where((jj <= ii)[:, :, None], G[:, None, :] - G[None, :, :], -np.inf)
+    ratio = np.exp(diff)                                      # [L, L, dk], 0 above the diagonal
+    KK = np.einsum("id,jd,ijd->ij", K, K, ratio)
+    QK = np.einsum("id,jd,ijd->ij", Q, K, ratio)
+    A = np.where(jj < ii, b[:, None] * KK, 0.0)
+    rhs = b[:, None] * V - b[:, None] * ((np.exp(G) * K) @ S)
+    X = solve_triangular(np.eye(L) + A, rhs, lower=True, unit_diagonal=True)
+    o = (np.exp(G) * Q) @ S + QK @ X
+    S = np.exp(G[-1])[:, None] * S + (np.exp(G[-1][None, :] - G) * K).T @ X
+    return S, o, X

@@ -17,6 +17,15 @@
  *       o_t   = scale * S^T q_t                           read with the updated S
  *   final_state[n,hv] = S^T
  *
+ * With per-channel gates (g_per_channel != 0; g is then [T, Hv, dk]) the
+ * decay is a diagonal matrix over the key dimension, one factor per row of S:
+ *       pred  = (diag(alpha_t) S)^T k_t
+ *       S     = diag(alpha_t) S + beta[t,hv] * k_t (v_t - pred)^T
+ * which is the scalar case when all dk factors are equal. This is the reading
+ * of the per-channel ("KDA") gate the graph-capture RFC for the GDN/KDA chunk
+ * paths lists beside GDN (section "What needs to change", the KDA forward
+ * kernels): the same delta-rule write, with a gate per key channel.
+ *
  * This is the per-token update described in "Chunking Qwen3.5's gated
  * DeltaNet for 1.5x faster prefill on Apple Silicon" (section "What is the
  * gated delta rule in Qwen3.5?": decay, correction from the state's
@@ -58,8 +67,8 @@ static void run_lane(int64_t t0, int64_t t1, int64_t H, int64_t Hv, int64_t dk,
                      int64_t dv, int64_t h, int64_t hv, const double* q,
                      const double* k, const double* v, const double* g,
                      const double* beta, double scale, int qk_l2norm,
-                     double eps, double* S, double* pred, double* kt,
-                     double* qt, double* out) {
+                     double eps, int g_per_channel, double* S, double* pred,
+                     double* kt, double* qt, double* out) {
   for (int64_t t = t0; t < t1; ++t) {
     const double* kraw = k + (t * H + h) * dk;
     const double* qraw = q + (t * H + h) * dk;
@@ -70,24 +79,27 @@ static void run_lane(int64_t t0, int64_t t1, int64_t H, int64_t Hv, int64_t dk,
       memcpy(kt, kraw, (size_t)dk * sizeof(double));
       memcpy(qt, qraw, (size_t)dk * sizeof(double));
     }
-    const double alpha = exp(g[t * Hv + hv]);
+    /* per-channel gates: alpha is folded into each row below and is 1 here */
+    const double* gk = g_per_channel ? g + (t * Hv + hv) * dk : NULL;
+    const double alpha = gk ? 1.0 : exp(g[t * Hv + hv]);
     const double b = beta[t * Hv + hv];
     const double* vt = v + (t * Hv + hv) * dv;
 
-    /* pred = alpha * S^T k */
+    /* pred = alpha * S^T k, or (diag(alpha_i) S)^T k with per-channel gates */
     for (int64_t j = 0; j < dv; ++j) pred[j] = 0.0;
     for (int64_t i = 0; i < dk; ++i) {
-      const double ki = kt[i];
+      const double ki = gk ? exp(gk[i]) * kt[i] : kt[i];
       const double* Si = S + i * dv;
       for (int64_t j = 0; j < dv; ++j) pred[j] += Si[j] * ki;
     }
     for (int64_t j = 0; j < dv; ++j) pred[j] *= alpha;
 
-    /* S = alpha * S + beta * k (v - pred)^T */
+    /* S = alpha * S + beta * k (v - pred)^T, alpha per row with per-channel gates */
     for (int64_t i = 0; i < dk; ++i) {
       const double bki = b * kt[i];
+      const double ai = gk ? exp(gk[i]) : alpha;
       double* Si = S + i * dv;
-      for (int64_t j = 0; j < dv; ++j) Si[j] = alpha * Si[j] + bki * (vt[j] - pred[j]);
+      for (int64_t j = 0; j < dv; ++j) Si[j] = ai * Si[j] + bki * (vt[j] - pred[j]);
     }
 
     /* o = scale * S^T q (after the update) */
@@ -107,7 +119,7 @@ int gdn_ref_forward(int64_t T, int64_t N, int64_t H, int64_t Hv, int64_t dk,
                     const double* v, const double* g, const double* beta,
                     double scale, const double* initial_state,
                     const int64_t* cu_seqlens, int qk_l2norm, double eps,
-                    double* out, double* final_state, int nthreads) {
+                    double* out, double* final_state, int nthreads, int g_per_channel) {
   if (T < 0 || N < 1 || H < 1 || Hv < 1 || dk < 1 || dv < 1) return GDN_REF_BAD_ARG;
   if (Hv % H != 0) return GDN_REF_BAD_ARG;
   if (!q || !k || !v || !g || !beta || !out) return GDN_REF_BAD_ARG;
@@ -151,7 +163,7 @@ int gdn_ref_forward(int64_t T, int64_t N, int64_t H, int64_t Hv, int64_t dk,
         for (int64_t j = 0; j < dv; ++j)
           S[i * dv + j] = initial_state ? initial_state[((n * Hv + hv) * dv + j) * dk + i] : 0.0;
       run_lane(t0, t1, H, Hv, dk, dv, h, hv, q, k, v, g, beta, scale, qk_l2norm, eps,
-               S, pred, kt, qt, out);
+               g_per_channel, S, pred, kt, qt, out);
       if (final_state)
         for (int64_t i = 0; i < dk; ++i)
           for (int64_t j = 0; j < dv; ++j)

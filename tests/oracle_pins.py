@@ -12,6 +12,8 @@ AssertionError when the oracle disagrees with what the mathematics fixes:
   causal linear attention, a masked (Q K^T * D) V product;
 * closed form 2: beta = 1 with unit keys makes S_t^T k_t = v_t exactly;
 * invariants: beta = 0 leaves the state to decay only (S_t = exp(cum g) S_0);
+* per-channel gates: exact rationals, the chunked form, uniform gates = scalar
+  gates, and beta = 0 decaying each key row by its own cumulative gate;
 * GQA pairing h = hv / (Hv / H) against explicitly repeated key heads;
 * split/resume and varlen isolation (bitwise);
 * L2-norm prologue against pre-normalised inputs; the default scale.
@@ -240,6 +242,108 @@ def pin_l2norm_and_scale(lib):
     assert np.array_equal(o_def, o_exp) and np.array_equal(o_nan, o_exp)
 
 
+# ---------------------------------------------------------------- per-channel gates
+def channel_gates(rng, T, Hv, dk):
+    """Log-decays per key channel, each channel with its own typical magnitude."""
+    mu = rng.uniform(-1.0, 4.0, size=dk)
+    return -np.log1p(np.exp(-(rng.standard_normal((T, Hv, dk)) + mu)))
+
+
+def _exact_lane_channel(q, k, v, alpha, beta, s0, scale):
+    """S_t = (I - b k k^T) diag(alpha_t) S + b k v^T in exact rationals."""
+    dk, dv = len(k[0]), len(v[0])
+    S = [[s0[i][j] for j in range(dv)] for i in range(dk)]
+    outs = []
+    for t in range(len(k)):
+        a, b, kt, vt, qt = alpha[t], beta[t], k[t], v[t], q[t]
+        D = [[a[i] * S[i][j] for j in range(dv)] for i in range(dk)]
+        S = [[D[i][j] - b * kt[i] * sum(kt[m] * D[m][j] for m in range(dk)) + b * kt[i] * vt[j]
+              for j in range(dv)] for i in range(dk)]
+        outs.append([scale * sum(S[i][j] * qt[i] for i in range(dk)) for j in range(dv)])
+    return outs, S
+
+
+def pin_channel_exact_rationals(lib):
+    rng = np.random.default_rng(15)
+    H, Hv, dk, dv = 1, 2, 4, 3
+    lengths = [4, 3]
+    T = sum(lengths)
+    dy = lambda: Fraction(int(rng.integers(-8, 9)), 8)
+    q = [[[dy() for _ in range(dk)] for _ in range(H)] for _ in range(T)]
+    k = [[[dy() for _ in range(dk)] for _ in range(H)] for _ in range(T)]
+    v = [[[dy() for _ in range(dv)] for _ in range(Hv)] for _ in range(T)]
+    alphas = [Fraction(1, 4), Fraction(1, 2), Fraction(3, 4), Fraction(7, 8), Fraction(1, 1)]
+    alpha = [[[alphas[int(rng.integers(0, len(alphas)))] for _ in range(dk)] for _ in range(Hv)]
+             for _ in range(T)]
+    beta = [[Fraction(int(rng.integers(0, 9)), 8) for _ in range(Hv)] for _ in range(T)]
+    s0 = [[[[dy() for _ in range(dk)] for _ in range(dv)] for _ in range(Hv)] for _ in lengths]
+    scale = Fraction(3, 4)
+    f = lambda x: np.array(x, dtype=np.float64)
+    cu = np.concatenate([[0], np.cumsum(lengths)]).astype(np.int64)
+    out, fin = oracle.recurrent_forward(
+        f(q), f(k), f(v), np.log(f(alpha)), f(beta), float(scale), f(s0), cu, lib=lib)
+    for n in range(len(lengths)):
+        t0, t1 = int(cu[n]), int(cu[n + 1])
+        for hv in range(Hv):
+            h = hv // (Hv // H)
+            s0_kv = [[s0[n][hv][j][i] for j in range(dv)] for i in range(dk)]
+            outs, S = _exact_lane_channel(
+                [q[t][h] for t in range(t0, t1)], [k[t][h] for t in range(t0, t1)],
+                [v[t][hv] for t in range(t0, t1)], [alpha[t][hv] for t in range(t0, t1)],
+                [beta[t][hv] for t in range(t0, t1)], s0_kv, scale)
+            for t in range(t0, t1):
+                for j in range(dv):
+                    ex = float(outs[t - t0][j])
+                    assert abs(out[t, hv, j] - ex) <= 1e-13 * max(1.0, abs(ex)), (t, hv, j)
+            for i in range(dk):
+                for j in range(dv):
+                    ex = float(S[i][j])
+                    assert abs(fin[n, hv, j, i] - ex) <= 1e-13 * max(1.0, abs(ex)), (n, hv, i, j)
+
+
+def pin_channel_chunked(lib):
+    rng = np.random.default_rng(16)
+    for T in (1, 63, 64, 65, 130):
+        c = rand_case(rng, T, 2, 4, 16, 8)
+        c["g"] = channel_gates(rng, T, 4, 16)
+        o1, f1 = run(lib, c)
+        o2, f2 = chunked_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["scale"],
+                                 c["initial_state"], c["cu_seqlens"])
+        assert rel(o1, o2) <= 1e-12 and rel(f1, f2) <= 1e-12, T
+    lengths = [70, 1, 0, 66]
+    c = rand_case(rng, sum(lengths) + 3, 1, 2, 8, 12, lengths=lengths)
+    c["g"] = channel_gates(rng, c["q"].shape[0], 2, 8)
+    o1, f1 = run(lib, c)
+    o2, f2 = chunked_forward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["scale"],
+                             c["initial_state"], c["cu_seqlens"])
+    assert rel(o1, o2) <= 1e-12 and rel(f1, f2) <= 1e-12
+
+
+def pin_channel_uniform_is_scalar(lib):
+    """The same gate on every key channel is the scalar gate."""
+    rng = np.random.default_rng(17)
+    c = rand_case(rng, 50, 2, 4, 8, 6, lengths=[20, 30])
+    o1, f1 = run(lib, c)
+    o2, f2 = run(lib, dict(c, g=np.repeat(c["g"][:, :, None], 8, axis=2)))
+    assert rel(o1, o2) <= 1e-13 and rel(f1, f2) <= 1e-13
+
+
+def pin_channel_beta_zero(lib):
+    """beta = 0: key row d of the state decays by exp(sum of its own gates)."""
+    rng = np.random.default_rng(18)
+    c = rand_case(rng, 21, 1, 2, 8, 5)
+    c["beta"] = np.zeros_like(c["beta"])
+    c["g"] = channel_gates(rng, 21, 2, 8)
+    out, fin = run(lib, c)
+    for hv in range(2):
+        cum = np.cumsum(c["g"][:, hv], axis=0)              # [T, dk]
+        S0 = c["initial_state"][0, hv]                      # [dv, dk]
+        expect = c["scale"] * (np.exp(cum) * c["q"][:, 0]) @ S0.T
+        assert rel(out[:, hv], expect) <= 1e-12
+        assert rel(fin[0, hv], S0 * np.exp(cum[-1])[None, :]) <= 1e-12
+
+
 ALL_PINS = [pin_exact_rationals, pin_chunked, pin_orthonormal_keys, pin_overwrite,
             pin_beta_zero, pin_gqa_pairing, pin_split_resume, pin_varlen_isolation,
-            pin_l2norm_and_scale]
+            pin_l2norm_and_scale, pin_channel_exact_rationals, pin_channel_chunked,
+            pin_channel_uniform_is_scalar, pin_channel_beta_zero]

@@ -16,7 +16,7 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "gdn_ref.c")
 MUTANTS = {
     "pred_without_decay": ("pred[j] *= alpha;", "pred[j] *= 1.0;"),
     "correction_sign": ("(vt[j] - pred[j])", "(vt[j] + pred[j])"),
-    "no_write_term": ("alpha * Si[j] + bki * (vt[j] - pred[j])", "alpha * Si[j]"),
+    "no_write_term": ("ai * Si[j] + bki * (vt[j] - pred[j])", "ai * Si[j]"),
     "beta_dropped": ("const double bki = b * kt[i];", "const double bki = kt[i];"),
     "decay_sign": ("exp(g[t * Hv + hv])", "exp(-g[t * Hv + hv])"),
     "no_scale": ("ot[j] *= scale;", "ot[j] *= 1.0;"),
@@ -26,7 +26,11 @@ MUTANTS = {
     "final_state_transposed": ("final_state[((n * Hv + hv) * dv + j) * dk + i]",
                                "final_state[((n * Hv + hv) * dk + i) * dv + j]"),
     "read_uses_query_of_key": ("ot[j] += Si[j] * qi;", "ot[j] += Si[j] * kt[i];"),
-    "decay_not_applied_to_state": ("Si[j] = alpha * Si[j] +", "Si[j] = Si[j] +"),
+    "decay_not_applied_to_state": ("Si[j] = ai * Si[j] +", "Si[j] = Si[j] +"),
+    "channel_pred_without_decay": ("gk ? exp(gk[i]) * kt[i] : kt[i]", "kt[i]"),
+    "channel_state_decay_first_channel": ("gk ? exp(gk[i]) : alpha", "gk ? exp(gk[0]) : alpha"),
+    "channel_gate_stride": ("g + (t * Hv + hv) * dk", "g + (t * Hv + hv)"),
+    "channel_gate_sign": ("const double ai = gk ? exp(gk[i])", "const double ai = gk ? exp(-gk[i])"),
     "l2norm_without_sqrt": ("1.0 / sqrt(ss + eps)", "1.0 / (ss + eps)"),
     "default_scale_wrong": ("scale = 1.0 / sqrt((double)dk)", "scale = 1.0 / (double)dk"),
     "sequence_start_ignored": ("cu_seqlens ? cu_seqlens[n] : 0", "0"),
