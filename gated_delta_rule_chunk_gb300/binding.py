@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(_PKG, "libgdn.so")
 GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_BUILD_CHUNK_INDICES = 2
+GDN_FLAG_CHANNEL_GATES = 4
 GDN_NUM_STAGE_EVENTS = 4
 DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table"}
 
@@ -173,15 +174,18 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   stage_events=None, return_desc: bool = False):
     """Chunked gated-delta-rule forward through the C ABI.
 
-    q, k [T, H, 128]; v [T, Hv, 128] (fp32 or bf16, CUDA, contiguous); g, beta
-    fp32 [T, Hv]; initial_state fp32 [N, Hv, 128, 128] or None; cu_seqlens int32
-    [N + 1] or None. Returns (out [T, Hv, 128], final_state or None).
+    q, k [T, H, d]; v [T, Hv, d] with d = 128 or 64 (fp32 or bf16, CUDA,
+    contiguous); beta fp32 [T, Hv]; g fp32 [T, Hv] (one gate per token) or
+    [T, Hv, d] (one gate per key channel); initial_state fp32 [N, Hv, d, d] or
+    None; cu_seqlens int32 [N + 1] or None. Returns (out [T, Hv, d], final_state
+    or None).
     """
     T, H, dk = q.shape
     Hv, dv = v.shape[1], v.shape[2]
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     flags = (GDN_FLAG_QK_L2NORM if use_qk_l2norm else 0) | (
-        GDN_FLAG_BUILD_CHUNK_INDICES if build_chunk_indices else 0)
+        GDN_FLAG_BUILD_CHUNK_INDICES if build_chunk_indices else 0) | (
+        GDN_FLAG_CHANNEL_GATES if g.dim() == 3 else 0)
     out_dtype = out_dtype or (out.dtype if out is not None else q.dtype)
     desc = make_desc(T, N, H, Hv, q.dtype, out_dtype, nt_max=nt_max, flags=flags,
                      l2norm_eps=l2norm_eps, dk=dk, dv=dv)
@@ -324,7 +328,8 @@ def gdn_chunk_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: 
     Hv, dv = v.shape[1], v.shape[2]
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     out_dtype = out_dtype or (out.dtype if out is not None else q.dtype)
-    desc = make_desc(T, N, H, Hv, q.dtype, out_dtype, dk=dk, dv=dv)
+    desc = make_desc(T, N, H, Hv, q.dtype, out_dtype, dk=dk, dv=dv,
+                     flags=GDN_FLAG_CHANNEL_GATES if g.dim() == 3 else 0)
     if out is None:
         out = torch.empty(T, Hv, dv, dtype=out_dtype, device=q.device)
     if final_state is None:

@@ -100,11 +100,13 @@ int check_desc_impl(const gdn_desc* d) {
   if (!d) return GDN_ERR_NULL_ARG;
   if (d->T < 0 || d->N < 1 || d->H < 1 || d->Hv < 1 || d->nt_max < 0) return GDN_ERR_BAD_SHAPE;
   if (d->Hv % d->H != 0) return GDN_ERR_BAD_SHAPE;
-  if (d->dk != kDk || d->dv != kDv || d->chunk_size != kChunk) return GDN_ERR_UNSUPPORTED;
+  if (d->dk != d->dv || (d->dk != 128 && d->dk != 64) || d->chunk_size != kChunk)
+    return GDN_ERR_UNSUPPORTED;
   const bool dt_ok = (d->qkv_dtype == GDN_F32 || d->qkv_dtype == GDN_BF16) &&
                      (d->out_dtype == GDN_F32 || d->out_dtype == GDN_BF16);
   if (!dt_ok) return GDN_ERR_UNSUPPORTED;
-  if (d->flags & ~(uint32_t)(GDN_FLAG_QK_L2NORM | GDN_FLAG_BUILD_CHUNK_INDICES))
+  if (d->flags &
+      ~(uint32_t)(GDN_FLAG_QK_L2NORM | GDN_FLAG_BUILD_CHUNK_INDICES | GDN_FLAG_CHANNEL_GATES))
     return GDN_ERR_UNSUPPORTED;
   // Index arithmetic stays within 64-bit sizes and 32-bit grid limits.
   if ((int64_t)d->T * d->Hv * kDv >= ((int64_t)1 << 40)) return GDN_ERR_BAD_SHAPE;
@@ -116,12 +118,20 @@ int nt_max_of(const gdn_desc* d) {
   return d->nt_max > 0 ? d->nt_max : gdn_nt_max(d->T, d->N, kChunk);
 }
 
-// The tensor-core path serves bf16 inputs; fp32 inputs take the SIMT path.
-bool uses_tc_path(const gdn_desc* d) { return d->qkv_dtype == GDN_BF16; }
+bool channel_gates(const gdn_desc* d) { return (d->flags & GDN_FLAG_CHANNEL_GATES) != 0; }
+
+// The tensor-core path serves bf16 inputs with dk = 128 and a scalar gate; every
+// other case (fp32 inputs, dk = 64, per-channel gates) takes the fp32 SIMT path.
+bool uses_tc_path(const gdn_desc* d) {
+  return d->qkv_dtype == GDN_BF16 && d->dk == kDk && !channel_gates(d);
+}
+
+// The token-serial and front-end kernels are built for dk = dv = 128 and scalar gates.
+bool serial_shape_ok(const gdn_desc* d) { return d->dk == kDk && !channel_gates(d); }
 
 WsLayout layout_of(const gdn_desc* d) {
   return ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d),
-                   (d->flags & GDN_FLAG_QK_L2NORM) != 0);
+                   (d->flags & GDN_FLAG_QK_L2NORM) != 0, d->dk);
 }
 
 }  // namespace
@@ -176,7 +186,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   const int nt_max = nt_max_of(&d);
   const bool bf16 = d.qkv_dtype == GDN_BF16;
   const bool l2 = (d.flags & GDN_FLAG_QK_L2NORM) != 0;
-  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)kDk);  // also NaN
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)d.dk);  // also NaN
   const float eps = d.l2norm_eps > 0.f ? d.l2norm_eps : 1e-6f;
 
   Params p{};
@@ -189,11 +199,14 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   int2* table = chunk_indices ? reinterpret_cast<int2*>(chunk_indices)
                               : reinterpret_cast<int2*>(ws + L.chunk_table);
   p.chunk_table = table;
-  p.G = reinterpret_cast<float*>(ws + L.G);
+  p.G = L.G ? reinterpret_cast<float*>(ws + L.G) : nullptr;
   p.w = ws + L.w;
   p.u = reinterpret_cast<float*>(ws + L.u);
   p.M = ws + L.M;
   p.k16 = L.k16 ? ws + L.k16 : nullptr;
+  p.qt = L.qt ? reinterpret_cast<float*>(ws + L.qt) : nullptr;
+  p.kt = L.kt ? reinterpret_cast<float*>(ws + L.kt) : nullptr;
+  p.gam = L.gam ? reinterpret_cast<float*>(ws + L.gam) : nullptr;
   p.qrn = l2 ? reinterpret_cast<float*>(ws + L.qrn) : nullptr;
   p.krn = l2 ? reinterpret_cast<float*>(ws + L.krn) : nullptr;
   p.out_bf16 = d.out_dtype == GDN_BF16;
@@ -202,7 +215,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return GDN_ERR_LAUNCH_FAILED;
   if (ev) cudaEventRecord(ev[0], stream);
-  if (l2) launch_l2norm(q, k, bf16, d.T, d.H, eps, const_cast<float*>(p.qrn),
+  if (l2) launch_l2norm(q, k, bf16, d.T, d.H, d.dk, eps, const_cast<float*>(p.qrn),
                         const_cast<float*>(p.krn), stream);
   launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
                      (!chunk_indices || build_into_caller) ? table : nullptr,
@@ -213,15 +226,15 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   if (nt_max > 0) {
     if (tc) {
       if (!launch_tc_intra(p, stream)) return GDN_ERR_LAUNCH_FAILED;
-    } else {
-      launch_simt_intra(p, false, stream);
+    } else if (!launch_gen_intra(p, d.dk, channel_gates(&d), bf16, stream)) {
+      return GDN_ERR_LAUNCH_FAILED;
     }
   }
   if (ev) cudaEventRecord(ev[2], stream);
   if (tc) {
     if (!launch_tc_inter(p, stream)) return GDN_ERR_LAUNCH_FAILED;
-  } else {
-    launch_simt_inter(p, false, stream);
+  } else if (!launch_gen_inter(p, d.dk, stream)) {
+    return GDN_ERR_LAUNCH_FAILED;
   }
   if (ev) cudaEventRecord(ev[3], stream);
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
@@ -233,6 +246,7 @@ int gdn_recurrent_fwd(const gdn_desc* desc, const void* q, const void* k, const 
                       float* final_state, cudaStream_t stream) {
   int rc = check_desc_impl(desc);
   if (rc != GDN_OK) return rc;
+  if (!serial_shape_ok(desc)) return GDN_ERR_UNSUPPORTED;
   const gdn_desc& d = *desc;
   if (!q || !k || !v || !g || !beta || !out) return GDN_ERR_NULL_ARG;
   if (!cu_seqlens && d.N != 1) return GDN_ERR_BAD_SHAPE;
@@ -262,6 +276,7 @@ int gdn_conv_front(const gdn_desc* desc, const void* x, const float* conv_w, int
                    cudaStream_t stream) {
   int rc = check_desc_impl(desc);
   if (rc != GDN_OK) return rc;
+  if (desc->dk != kDk) return GDN_ERR_UNSUPPORTED;
   const gdn_desc& d = *desc;
   if (!x || !conv_w || !q || !k || !v) return GDN_ERR_NULL_ARG;
   if (d_conv < 1 || d_conv > 8 || n_snapshots < 0) return GDN_ERR_BAD_SHAPE;

@@ -35,6 +35,9 @@ struct Params {
   float* u;                  // [nt_max, Hv, 64, dv]
   void* M;                   // [nt_max, Hv, 64, 64] (or hi/lo pair) decay-masked q.k
   void* k16;                 // [nt_max, H] fp16 images of the chunk's k tile (tensor-core path)
+  float* qt;                 // [nt_max, Hv, dk, 64] (exp(G) q)^T        (SIMT path)
+  float* kt;                 // [nt_max, Hv, 64, dk] exp(G_L - G) k      (SIMT path)
+  float* gam;                // [nt_max, Hv, dk] exp(G_L)                (SIMT path)
   const float* qrn;          // [T, H] 1/||q|| or null
   const float* krn;          // [T, H] 1/||k|| or null
   int out_bf16;
@@ -76,15 +79,17 @@ struct ConvParams {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qrn, krn, total;
+  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qt, kt, gam, qrn, krn,
+      total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Layout for a problem. The tensor-core path stores w in bf16 and M as a hi/lo
-// bf16 pair; the fp32 SIMT path stores both in fp32 (4 bytes per M element
-// either way).
-inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path, bool l2norm) {
+// Layout for a problem with head size D. The tensor-core path (D = 128) stores w
+// in bf16, M as a hi/lo bf16 pair and the in-chunk gate sums G; the fp32 SIMT
+// path stores w^T, u, M^T and the decayed q / k images and exp(G_L) in fp32.
+inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path, bool l2norm,
+                          int D = kDk) {
   WsLayout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
@@ -93,11 +98,14 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
   L.chunk_offsets = take(sizeof(int32_t) * (size_t)(N + 1));
   L.chunk_table = take(sizeof(int2) * (size_t)nt_max);
   const size_t slots = (size_t)nt_max * (size_t)Hv;
-  L.G = take(sizeof(float) * slots * kChunk);
-  L.w = take((tc_path ? 2 : 4) * slots * kChunk * kDk);
-  L.u = take(sizeof(float) * slots * kChunk * kDv);
+  L.G = tc_path ? take(sizeof(float) * slots * kChunk) : 0;
+  L.w = take((tc_path ? 2 : 4) * slots * kChunk * D);
+  L.u = take(sizeof(float) * slots * kChunk * D);
   L.M = take(4 * slots * kChunk * kChunk);
   L.k16 = tc_path ? take((size_t)nt_max * H * kChunk * kDk * 2) : 0;
+  L.qt = tc_path ? 0 : take(sizeof(float) * slots * kChunk * D);
+  L.kt = tc_path ? 0 : take(sizeof(float) * slots * kChunk * D);
+  L.gam = tc_path ? 0 : take(sizeof(float) * slots * D);
   L.qrn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
   L.krn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
   L.total = o;
@@ -154,10 +162,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 // Kernel launchers (one translation unit each).
 void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,
                         int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s);
-void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, float eps,
+void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, int D, float eps,
                    float* qrn, float* krn, cudaStream_t s);
-void launch_simt_intra(const Params& p, bool bf16_inputs, cudaStream_t s);
-void launch_simt_inter(const Params& p, bool bf16_inputs, cudaStream_t s);
+bool launch_gen_intra(const Params& p, int D, bool channel_gates, bool bf16_inputs, cudaStream_t s);
+bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
 bool launch_recurrent(const RecParams& p, cudaStream_t s);

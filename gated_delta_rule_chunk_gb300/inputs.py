@@ -13,7 +13,10 @@ Distributions (the Qwen3.5-style workloads; all draws in fp64 on a CPU
   then a no-op, so the optional prologue stays off for these workloads);
 * v ~ N(0, 1);
 * g = log(sigmoid(x)) with x ~ N(2, 1), per (token, value head), evaluated as
-  -log1p(exp(-x)) so that it never rounds to log(1) = 0 or overflows;
+  -log1p(exp(-x)) so that it never rounds to log(1) = 0 or overflows; with
+  per-channel gates the same draw is made independently per key channel,
+  g [T, Hv, dk] (optionally with a per-channel offset added to x, drawn once
+  from U[lo, hi], to spread the channels' decay rates);
 * beta = sigmoid(y), y ~ N(0, 1);
 * initial states ~ N(0, 0.02) (0.02 read as the standard deviation), fp32,
   layout [N, Hv, dv, dk];
@@ -52,6 +55,7 @@ class Workload:
     n_real: int = 0               # static_bound: real sequences
     real_max_len: int = 0         # static_bound: lengths ~ U[1, real_max_len]
     fixed_lens: tuple = ()        # fixed: the sequence lengths
+    gate: str = "scalar"          # "scalar" (g [T, Hv]) or "channel" (g [T, Hv, dk])
 
 
 WORKLOADS = {
@@ -74,6 +78,11 @@ WORKLOADS = {
     # front end (conv + SiLU over the qkv projection output; make_conv_inputs)
     7: Workload(7, "front end: conv1d d=4 + SiLU over the qkv projection, T=4096 H=16 Hv=32 "
                 "bf16", 16, 32, 128, 128, "bf16", True, "conv", T=4096),
+    # head size 64 and per-channel gates (the fp32 SIMT chunk kernels)
+    8: Workload(8, "head size 64 GQA prefill T=4096 H=16 Hv=32 d=64 bf16", 16, 32, 64, 64,
+                "bf16", True, "single", T=4096),
+    9: Workload(9, "per-channel gates GQA prefill T=4096 H=16 Hv=32 d=128 bf16", 16, 32, 128,
+                128, "bf16", True, "single", T=4096, gate="channel"),
 }
 
 HEADLINE = 2
@@ -132,12 +141,16 @@ def gates(x: torch.Tensor) -> torch.Tensor:
 def make_inputs(wid: int = HEADLINE, seed: Optional[int] = None, T: Optional[int] = None,
                 H: Optional[int] = None, Hv: Optional[int] = None,
                 lengths: Optional[list] = None, dtype: Optional[str] = None,
-                with_initial_state: Optional[bool] = None, normalise_qk: bool = True) -> dict:
+                with_initial_state: Optional[bool] = None, normalise_qk: bool = True,
+                d: Optional[int] = None, channel_gates: Optional[bool] = None,
+                gate_offsets: Optional[tuple] = None) -> dict:
     """Draw one workload's inputs on the CPU.
 
     Overrides (T, H, Hv, lengths, dtype, with_initial_state) let tests build
-    smaller cases with the same distributions. Returns a dict of CPU tensors:
-    q, k [T,H,dk]; v [T,Hv,dv]; g, beta [T,Hv] fp32; initial_state
+    smaller cases with the same distributions; d sets dk = dv, channel_gates the
+    gate kind, gate_offsets (lo, hi) the per-channel offset range. Returns a dict
+    of CPU tensors: q, k [T,H,dk]; v [T,Hv,dv]; g [T,Hv] or [T,Hv,dk] and beta
+    [T,Hv] fp32; initial_state
     [N,Hv,dv,dk] fp32 or None; cu_seqlens int32 [N+1]; plus scalars
     scale, T, N, H, Hv, dk, dv, nt_max, n_tokens (valid rows) and lengths.
     """
@@ -145,7 +158,8 @@ def make_inputs(wid: int = HEADLINE, seed: Optional[int] = None, T: Optional[int
     gen = _gen(1000 + wid if seed is None else seed)
     H = H or wl.H
     Hv = Hv or wl.Hv
-    dk, dv = wl.dk, wl.dv
+    dk, dv = (d, d) if d is not None else (wl.dk, wl.dv)
+    chan = (wl.gate == "channel") if channel_gates is None else channel_gates
     dtype = dtype or wl.dtype
     init = wl.with_initial_state if with_initial_state is None else with_initial_state
     if lengths is None:
@@ -168,7 +182,14 @@ def make_inputs(wid: int = HEADLINE, seed: Optional[int] = None, T: Optional[int
     if normalise_qk:
         q, k = unit_rows(q), unit_rows(k)
     v = torch.randn(rows, Hv, dv, generator=gen, dtype=f64)
-    g = gates(torch.randn(rows, Hv, generator=gen, dtype=f64) + 2.0)
+    if chan:
+        x = torch.randn(rows, Hv, dk, generator=gen, dtype=f64) + 2.0
+        if gate_offsets is not None:
+            lo, hi = gate_offsets
+            x = x + (lo + (hi - lo) * torch.rand(dk, generator=gen, dtype=f64))
+        g = gates(x)
+    else:
+        g = gates(torch.randn(rows, Hv, generator=gen, dtype=f64) + 2.0)
     beta = torch.sigmoid(torch.randn(rows, Hv, generator=gen, dtype=f64))
     s0 = (0.02 * torch.randn(N, Hv, dv, dk, generator=gen, dtype=f64)) if init else None
     tdt = torch.float32 if dtype == "f32" else torch.bfloat16
@@ -180,7 +201,7 @@ def make_inputs(wid: int = HEADLINE, seed: Optional[int] = None, T: Optional[int
         initial_state=None if s0 is None else s0.float().contiguous(),
         cu_seqlens=cu, scale=1.0 / math.sqrt(dk),
         T=rows, N=N, H=H, Hv=Hv, dk=dk, dv=dv, nt_max=nt_max, dtype=dtype,
-        n_tokens=int(cu[-1]), lengths=lengths, wid=wid,
+        n_tokens=int(cu[-1]), lengths=lengths, wid=wid, channel_gates=chan,
     )
 
 

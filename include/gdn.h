@@ -28,6 +28,8 @@
  *       v               [T, Hv, dv]  (gdn_desc.qkv_dtype)
  *       out             [T, Hv, dv]  (gdn_desc.out_dtype)
  *       g, beta         [T, Hv]      fp32; g is the per-token log-decay (<= 0)
+ *                       (g is [T, Hv, dk] with GDN_FLAG_CHANNEL_GATES: one
+ *                       log-decay per key channel, decaying that row of S)
  *       states          [N, Hv, dv, dk] fp32 (value-major, "[N, Hv, V, K]")
  *       cu_seqlens      [N + 1] int32 prefix sums of sequence lengths
  *       chunk_indices   [nt_max, 2] int32 (sequence id, chunk ordinal)
@@ -37,7 +39,12 @@
  *     cu_seqlens, more chunks than nt_max, a bad caller-supplied chunk table)
  *     never fault: the kernels clamp or skip and set bits of the device status
  *     word (gdn_dev_status), which gdn_read_status copies back.
- *   - Supported today: dk = dv = 128, chunk_size = 64, Hv % H == 0.
+ *   - Supported: dk = dv = 128 or dk = dv = 64 (the head sizes of "Optimizing
+ *     GDN Chunk Prefill on Intel AMX CPU", section 9), chunk_size = 64,
+ *     Hv % H == 0, scalar or per-channel gates. bf16 inputs with dk = 128 and
+ *     scalar gates run on the tensor-core kernels; every other case runs on the
+ *     fp32 SIMT kernels of the same intra/inter split. gdn_recurrent_fwd and
+ *     gdn_conv_front take dk = dv = 128 and scalar gates only.
  */
 #ifndef GDN_H_
 #define GDN_H_
@@ -59,7 +66,7 @@ typedef enum gdn_status {
   GDN_OK = 0,
   GDN_ERR_NULL_ARG = -1,          /* a required pointer is NULL */
   GDN_ERR_BAD_SHAPE = -2,         /* T < 0, N < 1, H < 1, Hv % H != 0, nt_max < 0 */
-  GDN_ERR_UNSUPPORTED = -3,       /* valid but not built: dk/dv != 128, chunk_size != 64, dtype */
+  GDN_ERR_UNSUPPORTED = -3,       /* valid but not built: head size, chunk_size != 64, dtype, flag */
   GDN_ERR_MISALIGNED = -4,        /* a pointer is not 16-byte aligned (workspace: 256 bytes) */
   GDN_ERR_WORKSPACE_TOO_SMALL = -5,
   GDN_ERR_LAUNCH_FAILED = -6      /* the CUDA runtime refused a launch or copy */
@@ -75,7 +82,8 @@ typedef enum gdn_dev_status {
 
 enum {
   GDN_FLAG_QK_L2NORM = 1u,            /* normalise q and k rows: x / sqrt(sum x^2 + eps) */
-  GDN_FLAG_BUILD_CHUNK_INDICES = 2u   /* fill the caller's chunk_indices buffer */
+  GDN_FLAG_BUILD_CHUNK_INDICES = 2u,  /* fill the caller's chunk_indices buffer */
+  GDN_FLAG_CHANNEL_GATES = 4u         /* g is [T, Hv, dk]: a gate per key channel */
 };
 
 enum { GDN_NUM_STAGE_EVENTS = 4 };
@@ -89,7 +97,7 @@ enum { GDN_NUM_STAGE_EVENTS = 4 };
  *   N            number of sequences (cu_seqlens has N + 1 entries; zero-length
  *                sequences are allowed, e.g. padding up to N_max)
  *   H, Hv        key/query heads and value heads; Hv must be a multiple of H
- *   dk, dv       head dimensions (128 and 128)
+ *   dk, dv       head dimensions: dk = dv = 128 or dk = dv = 64
  *   chunk_size   64
  *   nt_max       number of chunk slots; 0 selects cdiv(T, 64) + N - 1, which
  *                bounds the chunk count of any cu_seqlens with N sequences
@@ -170,7 +178,7 @@ int gdn_build_chunk_indices(const int32_t* cu_seqlens, int32_t N, int32_t T,
  * The chunked gated-delta-rule forward (the whole hot path: optional q/k
  * L2-norm prologue, chunk-table builder, intra-chunk kernel, inter-chunk scan).
  *   q, k, v        inputs (layouts above), dtype desc->qkv_dtype
- *   g, beta        fp32 [T, Hv]
+ *   g, beta        fp32 [T, Hv] (g: [T, Hv, dk] with GDN_FLAG_CHANNEL_GATES)
  *   scale          output scale; <= 0 or NaN selects 1/sqrt(dk)
  *   initial_state  fp32 [N, Hv, dv, dk] or NULL for zeros
  *   cu_seqlens     int32 [N + 1] or NULL for one sequence of T tokens (N = 1)
@@ -249,7 +257,8 @@ int gdn_chunk_fwd_noalloc(const gdn_desc* desc, const void* q, const void* k,
  * [T,Hv,dv]; g, beta fp32 [T,Hv]; states fp32 [N,Hv,dv,dk]; cu_seqlens int32
  * [N+1] or NULL for one sequence of T rows; final_state may alias
  * initial_state; either may be NULL). The descriptor is validated as for
- * gdn_chunk_fwd; chunk_size, nt_max and flags other than GDN_FLAG_QK_L2NORM
+ * gdn_chunk_fwd, and dk = dv = 128 with scalar gates is required
+ * (GDN_ERR_UNSUPPORTED otherwise); chunk_size, nt_max and the other flags
  * play no part. No workspace is needed: when desc->workspace is non-NULL its
  * status word is cleared and receives GDN_DEV_BAD_CU_SEQLENS for a malformed
  * cu_seqlens (clamped to [0, T]; a decreasing pair is an empty sequence), as
@@ -288,8 +297,9 @@ int gdn_recurrent_fwd(const gdn_desc* desc, const void* q, const void* k, const 
  *                   the end), for rolling a speculative batch back; must not alias
  *                   conv_state_in
  *
- * The descriptor is validated as for gdn_chunk_fwd (chunk_size, nt_max and
- * out_dtype play no part). desc->workspace, when non-NULL, receives the status
+ * The descriptor is validated as for gdn_chunk_fwd, and dk = dv = 128 is
+ * required (GDN_ERR_UNSUPPORTED otherwise; chunk_size, nt_max, out_dtype and
+ * GDN_FLAG_CHANNEL_GATES play no part). desc->workspace, when non-NULL, receives the status
  * word (GDN_DEV_BAD_CU_SEQLENS for a malformed cu_seqlens, clamped to [0, T]).
  * Errors: negative gdn_status before anything is enqueued (NULL x/conv_w/q/k/v,
  * bad d_conv or n_snapshots, misalignment: 16 bytes for x, q, k, v),

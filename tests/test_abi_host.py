@@ -49,7 +49,10 @@ def test_check_desc(lib):
     assert B.gdn_check_desc(desc(N=0)) == -2
     assert B.gdn_check_desc(desc(T=-1)) == -2
     assert B.gdn_check_desc(desc(nt_max=-3)) == -2
-    assert B.gdn_check_desc(desc(dk=64, dv=64)) == -3          # not built
+    assert B.gdn_check_desc(desc(dk=64, dv=64)) == 0           # head size 64
+    assert B.gdn_check_desc(desc(dk=64, dv=128)) == -3         # dk != dv: not built
+    assert B.gdn_check_desc(desc(dk=96, dv=96)) == -3
+    assert B.gdn_check_desc(desc(flags=B.GDN_FLAG_CHANNEL_GATES)) == 0
     d = desc()
     d.chunk_size = 32
     assert B.gdn_check_desc(d) == -3
@@ -81,6 +84,11 @@ def test_workspace_size(lib):
     # the bridge dominates: about 64 slots x 32 heads x 64 rows x (2 + 4 + 4 + ...) bytes
     assert a >= 64 * 32 * 64 * (128 * 2 + 128 * 4 + 64 * 4)
     assert B.gdn_workspace_size(desc(Hv=24)) == 0
+    # the SIMT path (head size 64, per-channel gates) keeps fp32 w^T, u, M^T, the
+    # decayed q and k images and exp(G_L): 4 * (64 * (4 d) + 64 * 64 + d) bytes per slot
+    for dd, fl in ((64, 0), (128, B.GDN_FLAG_CHANNEL_GATES)):
+        n = B.gdn_workspace_size(desc(dk=dd, dv=dd, flags=fl))
+        assert n >= 64 * 32 * 4 * (64 * 4 * dd + 64 * 64 + dd)
 
 
 def _fwd(lib, d, q=16, k=16, v=16, g=16, beta=16, out=16, s0=None, fin=None, cu=None, ci=None):
@@ -161,6 +169,8 @@ def test_recurrent_rejects_before_enqueue(lib):
     assert _rec(lib, dw) == -4
     assert _rec(lib, desc(Hv=24)) == -2
     assert _rec(lib, desc(dk=64)) == -3
+    assert _rec(lib, desc(dk=64, dv=64)) == -3                   # built for d = 128 only
+    assert _rec(lib, desc(flags=B.GDN_FLAG_CHANNEL_GATES)) == -3
 
 
 def test_conv_front_rejects_before_enqueue(lib):
@@ -180,3 +190,4 @@ def test_conv_front_rejects_before_enqueue(lib):
     assert f(q=4104) == -4 and f(x=4100) == -4
     assert f(s1=4098) == -4
     assert f(d=desc(Hv=24)) == -2
+    assert f(d=desc(dk=64, dv=64)) == -3       # built for d = 128 only
