@@ -58,19 +58,49 @@ def algorithmic_bytes(x, out_bytes=2):
     """Compulsory HBM bytes of one call: q, k, v, out, g, beta, initial and final states."""
     esz = 2 if x["dtype"] == "bf16" else 4
     T, H, Hv, dk, dv, N = x["n_tokens"], x["H"], x["Hv"], x["dk"], x["dv"], x["N"]
-    b = 2 * T * H * dk * esz + T * Hv * dv * esz + T * Hv * dv * out_bytes + 2 * T * Hv * 4
+    g_b = T * Hv * (dk if x.get("channel_gates") else 1) * 4
+    b = 2 * T * H * dk * esz + T * Hv * dv * esz + T * Hv * dv * out_bytes + g_b + T * Hv * 4
     states = N * Hv * dk * dv * 4
     b += states * (2 if x["initial_state"] is not None else 1)
     return b
 
 
 def algorithmic_flops(x):
-    """FLOPs of the chunked method (q.k^T and k.k^T once per key head per chunk)."""
+    """FLOPs of the chunked method (q.k^T and k.k^T once per key head per chunk; with
+    per-channel gates the decay sits inside those products, so once per value head)."""
     NT = n_chunks(x["lengths"])
     C, dk, dv = CHUNK, x["dk"], x["dv"]
     per_h = 2 * 2 * C * C * dk
     per_hv = C ** 3 / 3 + 2 * C * C * dk + 2 * C * C * dv + 3 * 2 * C * dk * dv + 2 * C * C * dv
-    return NT * x["H"] * per_h + NT * x["Hv"] * per_hv
+    heads_qk = x["Hv"] if x.get("channel_gates") else x["H"]
+    return NT * heads_qk * per_h + NT * x["Hv"] * per_hv
+
+
+def gdn_metric(workload: int) -> str:
+    from gated_delta_rule_chunk_gb300.inputs import HEADLINE, WORKLOADS
+    if workload == HEADLINE:
+        return METRIC
+    return f"GDN chunk-prefill tokens/s, {WORKLOADS[workload].name}; % of roofline"
+
+
+def stage_flops(x):
+    """FLOPs of the intra kernel (A and M products, triangular inverse, w and u) and of
+    the scan (w S, q S, M v_new and the state update), counted as in algorithmic_flops."""
+    NT = n_chunks(x["lengths"])
+    C, dk, dv = CHUNK, x["dk"], x["dv"]
+    heads_qk = x["Hv"] if x.get("channel_gates") else x["H"]
+    intra = NT * heads_qk * 2 * 2 * C * C * dk + NT * x["Hv"] * (C ** 3 / 3 + 2 * C * C * (dk + dv))
+    inter = NT * x["Hv"] * (3 * 2 * C * dk * dv + 2 * C * C * dv)
+    return {"chunk_table": 0.0, "intra": intra, "inter": inter}
+
+
+# fp32 FMA peak of the SIMT kernels: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz (max SM clock)
+SIMT_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
+
+
+def uses_tc_path(x):
+    """The bf16 tensor-core kernels serve d = 128 with scalar gates; the rest is SIMT."""
+    return x["dtype"] == "bf16" and x["dk"] == 128 and not x.get("channel_gates")
 
 
 def stage_bytes(x, out_bytes=2):
@@ -81,15 +111,21 @@ def stage_bytes(x, out_bytes=2):
     esz = 2 if x["dtype"] == "bf16" else 4
     T, H, Hv, dk, dv, N = x["n_tokens"], x["H"], x["Hv"], x["dk"], x["dv"], x["N"]
     NT = n_chunks(x["lengths"])
-    w_b = 2 if x["dtype"] == "bf16" else 4
-    bridge = NT * Hv * (CHUNK * dk * w_b + CHUNK * dv * 4 + CHUNK * CHUNK * 4 + CHUNK * 4)
-    k16 = NT * H * CHUNK * dk * 2 if x["dtype"] == "bf16" else 0
     q = T * H * dk * esz
     k = T * H * dk * esz
     states = N * Hv * dk * dv * 4
     s_in = states if x["initial_state"] is not None else 0
-    intra = q + k + T * Hv * dv * esz + 2 * T * Hv * 4 + bridge + k16
-    inter = q + (k16 if k16 else k) + bridge + s_in + states + T * Hv * dv * out_bytes
+    g_b = T * Hv * (dk if x.get("channel_gates") else 1) * 4
+    if uses_tc_path(x):
+        bridge = NT * Hv * (CHUNK * dk * 2 + CHUNK * dv * 4 + CHUNK * CHUNK * 4 + CHUNK * 4)
+        k16 = NT * H * CHUNK * dk * 2
+        intra = q + k + T * Hv * dv * esz + g_b + T * Hv * 4 + bridge + k16
+        inter = q + k16 + bridge + s_in + states + T * Hv * dv * out_bytes
+    else:
+        # per chunk and value head, fp32: w^T, u, M^T, exp(G) q, exp(G_L - G) k, exp(G_L)
+        bridge = NT * Hv * (4 * CHUNK * dk * 4 + CHUNK * CHUNK * 4 + dk * 4)
+        intra = q + k + T * Hv * dv * esz + g_b + T * Hv * 4 + bridge
+        inter = bridge + s_in + states + T * Hv * dv * out_bytes
     return {"chunk_table": 8 * (x["N"] + 1 + x["nt_max"]), "intra": intra, "inter": inter}
 
 
@@ -265,12 +301,13 @@ def run_reference(args, ws, rank):
     sample = (f"first {ts} tokens of the {WORKLOADS[args.workload].name} workload, all "
               f"{x['Hv']} value heads, per step")
     return {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "impl": "reference", "metric": gdn_metric(args.workload), "value": value,
+        "unit": "tokens/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload].name, "T": x["T"], "H": x["H"],
-                   "Hv": x["Hv"], "dk": 128, "dv": 128, "chunk": CHUNK,
+                   "Hv": x["Hv"], "dk": x["dk"], "dv": x["dv"], "chunk": CHUNK,
                    "oracle": "fp64 token-by-token recurrence in C, OpenMP over (seq, head)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": sample},
@@ -529,9 +566,11 @@ def run_gdn(args, ws, rank, local):
     x = make_inputs(args.workload)
     d = {k: (x[k].to(dev) if x.get(k) is not None else None)
          for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
-    out = torch.empty(x["T"], x["Hv"], 128, dtype=torch.bfloat16, device=dev)
-    fin = torch.empty(x["N"], x["Hv"], 128, 128, dtype=torch.float32, device=dev)
-    desc = B.make_desc(x["T"], x["N"], x["H"], x["Hv"], d["q"].dtype, torch.bfloat16)
+    D = x["dk"]
+    out = torch.empty(x["T"], x["Hv"], D, dtype=torch.bfloat16, device=dev)
+    fin = torch.empty(x["N"], x["Hv"], D, D, dtype=torch.float32, device=dev)
+    desc = B.make_desc(x["T"], x["N"], x["H"], x["Hv"], d["q"].dtype, torch.bfloat16, dk=D, dv=D,
+                       flags=B.GDN_FLAG_CHANNEL_GATES if x.get("channel_gates") else 0)
     wsp = B.alloc_workspace(desc, dev)
     flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
@@ -634,22 +673,39 @@ def run_gdn(args, ws, rank, local):
         "frac_of_measured": max(t_hbm, t_tc) / (ms / 1000.0),
         "frac_of_8tbs": max(t_ns_hbm, t_tc) / (ms / 1000.0),
     }
+    tc = uses_tc_path(x)
+    if tc:
+        roof = {"bound": "hbm", "kernel": dom, "achieved": dom_gbs,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dom_gbs / peaks["hbm_gbs"],
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": sb[dom], "traffic": traffic,
+                "traffic_source": traffic_src}
+    else:
+        # the fp32 SIMT kernels: FMA-pipe bound; peak from the unit counts and clock
+        sf = stage_flops(x)
+        achieved = sf[dom] / (stage_mean[dom] / 1000.0) / 1e12
+        roof = {"bound": "alu", "kernel": dom, "achieved": achieved, "peak": SIMT_FP32_TFLOPS,
+                "unit": "TFLOP/s", "frac": achieved / SIMT_FP32_TFLOPS,
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz",
+                "algorithmic_flops_per_launch": sf[dom],
+                "hbm_frac": dom_gbs / peaks["hbm_gbs"], "algorithmic_bytes_per_launch": sb[dom],
+                "traffic": traffic, "traffic_source": traffic_src}
+    metric = gdn_metric(args.workload)
     res = {
-        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
+        "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K,
         "warmup": args.warmup, "ms_per_step": ms_max, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if tc else "f32",
+        "data": "synthetic",
         "config": {"workload": WORKLOADS[args.workload].name, "T": x["T"], "N": x["N"],
-                   "H": x["H"], "Hv": x["Hv"], "dk": 128, "dv": 128, "chunk": CHUNK,
+                   "H": x["H"], "Hv": x["Hv"], "dk": x["dk"], "dv": x["dv"], "chunk": CHUNK,
+                   "gates": "per key channel" if x.get("channel_gates") else "per token",
+                   "kernels": "tensor-core (tcgen05) intra + scan" if tc else "fp32 SIMT intra + scan",
                    "qkv_dtype": "bf16", "out_dtype": "bf16", "g_beta_state_dtype": "fp32",
                    "initial_state": x["initial_state"] is not None,
                    "l2": "512 MiB buffer written between timed steps (L2 is 129 MB)",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "inputs": "resident in HBM"},
-        "roofline": {"bound": "hbm", "kernel": dom, "achieved": dom_gbs,
-                     "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dom_gbs / peaks["hbm_gbs"],
-                     "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
-                     "algorithmic_bytes_per_launch": sb[dom], "traffic": traffic,
-                     "traffic_source": traffic_src},
+        "roofline": roof,
         "path_roofline": path_roof,
         "stages_us": {k: 1000.0 * v for k, v in stage_mean.items()},
         "us_per_call_with_stage_events": 1000.0 * staged_ms,

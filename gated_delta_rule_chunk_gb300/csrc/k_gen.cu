@@ -144,16 +144,23 @@ __global__ void __launch_bounds__(kThr) gen_intra_kernel(Params p) {
     }
     for (int idx = tid; idx < 64 * 65; idx += kThr) A[idx] = 0.f;
     for (int idx = tid; idx < 64 * 64; idx += kThr) TT[idx] = 0.f;
-    if constexpr (CH) {
-      for (int d = tid; d < D; d += kThr) {  // inclusive cumsum along the chunk, per channel
+    if constexpr (CH) {  // gate rows in (coalesced), zero past the chunk end
+      for (int idx = tid; idx < 64 * D; idx += kThr) {
+        const int i = idx / D;
+        Gc[idx] = i < L ? p.g[((size_t)(t0 + i) * p.Hv + hv) * D + idx % D] : 0.f;
+      }
+    }
+    __syncthreads();
+    if constexpr (CH) {  // inclusive cumsum along the chunk, one thread per channel
+      for (int d = tid; d < D; d += kThr) {
         float acc = 0.f;
+#pragma unroll 8
         for (int i = 0; i < 64; ++i) {
-          if (i < L) acc += p.g[((size_t)(t0 + i) * p.Hv + hv) * D + d];
+          acc += Gc[i * D + d];
           Gc[i * D + d] = acc;
         }
       }
     }
-    __syncthreads();
     if (!CH && tid == 0) {  // inclusive cumsum, left to right
       float acc = 0.f;
       for (int i = 0; i < 64; ++i) {

@@ -9,8 +9,10 @@ method.
 Contents
 --------
 * ``gdn_ref.c`` -- the definition: a plain fp64 token-by-token recurrence in
-  C (see its header for the equations and the pages they follow).
-  ``recurrent_forward`` below is its ctypes wrapper.
+  C (see its header for the equations and the pages they follow), and the
+  exact adjoint of each of its steps for the backward pass.
+  ``recurrent_forward`` and ``recurrent_backward`` below are their ctypes
+  wrappers.
 * ``chunked.py`` -- an independent fp64 NumPy/SciPy chunked formulation, used
   only as a pin of the token recurrence (a different algorithm for the same
   function).
@@ -62,6 +64,10 @@ def _bind(path: str):
                                     ptr, ptr, ptr, ptr, ptr, dbl, ptr, ptr,
                                     ctypes.c_int, dbl, ptr, ptr, ctypes.c_int, ctypes.c_int]
     lib.gdn_ref_forward.restype = ctypes.c_int
+    lib.gdn_ref_backward.argtypes = [i64, i64, i64, i64, i64, i64,
+                                     ptr, ptr, ptr, ptr, ptr, dbl, ptr, ptr, ptr, ptr,
+                                     ptr, ptr, ptr, ptr, ptr, ptr, ctypes.c_int]
+    lib.gdn_ref_backward.restype = ctypes.c_int
     lib.gdn_ref_max_threads.argtypes = []
     lib.gdn_ref_max_threads.restype = ctypes.c_int
     return lib
@@ -129,6 +135,40 @@ def recurrent_forward(q, k, v, g, beta, scale=None, initial_state=None,
     if rc != 0:
         raise ValueError(f"gdn_ref_forward rejected its arguments (rc={rc})")
     return out, fin
+
+
+def recurrent_backward(q, k, v, g, beta, scale=None, initial_state=None, cu_seqlens=None,
+                       d_out=None, d_final=None, nthreads=0, lib=None):
+    """Gradients of the token recurrence (scalar gates, no L2 norm) in fp64.
+
+    d_out [T, Hv, dv] is the gradient with respect to out, d_final [N, Hv, dv, dk]
+    (or None) with respect to final_state. Returns a dict with dq, dk [T, H, dk],
+    dv [T, Hv, dv], dg, dbeta [T, Hv] and d_initial [N, Hv, dv, dk]; rows outside
+    the sequences get zeros."""
+    q, k, v, g, beta, d_out = (_f64(a) for a in (q, k, v, g, beta, d_out))
+    T, H, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    if g.ndim != 2:
+        raise ValueError("the backward takes one gate per token and value head")
+    if cu_seqlens is None:
+        N, cu = 1, None
+    else:
+        cu = np.ascontiguousarray(np.asarray(
+            cu_seqlens.cpu().numpy() if hasattr(cu_seqlens, "cpu") else cu_seqlens,
+            dtype=np.int64))
+        N = cu.shape[0] - 1
+    s0, dfin = _f64(initial_state), _f64(d_final)
+    out = dict(dq=np.zeros((T, H, dk)), dk=np.zeros((T, H, dk)), dv=np.zeros((T, Hv, dv)),
+               dg=np.zeros((T, Hv)), dbeta=np.zeros((T, Hv)), d_initial=np.zeros((N, Hv, dv, dk)))
+    lib = lib or load_library()
+    rc = lib.gdn_ref_backward(T, N, H, Hv, dk, dv, _ptr(q), _ptr(k), _ptr(v), _ptr(g),
+                              _ptr(beta), float(scale or 0.0), _ptr(s0), _ptr(cu), _ptr(d_out),
+                              _ptr(dfin), _ptr(out["dq"]), _ptr(out["dk"]), _ptr(out["dv"]),
+                              _ptr(out["dg"]), _ptr(out["dbeta"]), _ptr(out["d_initial"]),
+                              int(nthreads))
+    if rc != 0:
+        raise ValueError(f"gdn_ref_backward rejected its arguments (rc={rc})")
+    return out
 
 
 def max_threads(lib=None) -> int:

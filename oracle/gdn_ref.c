@@ -185,3 +185,206 @@ int gdn_ref_max_threads(void) {
   return 1;
 #endif
 }
+
+/*
+ * Backward of the token recurrence above (scalar gates): the exact adjoint of
+ * each step, applied from the last token to the first. Given d_out [T,Hv,dv]
+ * (the gradient of a loss with respect to out) and d_final [N,Hv,dv,dk] (with
+ * respect to final_state, NULL for none), it writes the gradients with respect
+ * to every input: dq, dk [T,H,dk] (summed over the value heads that share a key
+ * head), dv [T,Hv,dv], dg, dbeta [T,Hv] and d_initial [N,Hv,dv,dk] (NULL: not
+ * written). q/k L2 normalisation is not part of this function.
+ *
+ * One forward step, with alpha = exp(g_t), b = beta_t:
+ *     D = alpha S_prev;  pred = D^T k;  delta = v - pred;
+ *     S = D + b k delta^T;  o = scale S^T q
+ * and its adjoint, with dS the gradient flowing into S:
+ *     dS += scale q do^T;            dq  = scale S do
+ *     dD  = dS;  db = k^T dS delta;  dk  = b dS delta;  ddelta = b dS^T k
+ *     dv  = ddelta;  dpred = -ddelta
+ *     dD += k dpred^T;               dk += D dpred
+ *     dS_prev = alpha dD;            dg  = alpha <S_prev, dD>
+ * The states the adjoint needs are recomputed: S is stored every 64 tokens on
+ * the way forward and each 64-token segment is replayed before its adjoint.
+ */
+static void lane_backward(int64_t t0, int64_t t1, int64_t H, int64_t Hv, int64_t dk,
+                          int64_t dv, int64_t h, int64_t hv, const double* q,
+                          const double* k, const double* v, const double* g,
+                          const double* beta, double scale, const double* dout,
+                          double* S, double* ckpt, double* seg, double* dS, double* dD,
+                          double* tmp_v, double* tmp_k, double* dq, double* dk_out,
+                          double* dv_out, double* dg, double* dbeta) {
+  const int64_t n = t1 - t0, KV = dk * dv;
+  const int64_t nseg = (n + 63) / 64;
+  /* forward, keeping the state at the start of each 64-token segment */
+  for (int64_t s = 0; s < nseg; ++s) {
+    memcpy(ckpt + s * KV, S, (size_t)KV * sizeof(double));
+    const int64_t a = t0 + 64 * s, e = a + 64 < t1 ? a + 64 : t1;
+    for (int64_t t = a; t < e; ++t) {
+      const double alpha = exp(g[t * Hv + hv]), b = beta[t * Hv + hv];
+      const double* kt = k + (t * H + h) * dk;
+      const double* vt = v + (t * Hv + hv) * dv;
+      for (int64_t j = 0; j < dv; ++j) tmp_v[j] = 0.0;
+      for (int64_t i = 0; i < dk; ++i)
+        for (int64_t j = 0; j < dv; ++j) tmp_v[j] += alpha * S[i * dv + j] * kt[i];
+      for (int64_t i = 0; i < dk; ++i)
+        for (int64_t j = 0; j < dv; ++j)
+          S[i * dv + j] = alpha * S[i * dv + j] + b * kt[i] * (vt[j] - tmp_v[j]);
+    }
+  }
+  /* adjoint, segment by segment from the end; dS holds the incoming gradient */
+  for (int64_t s = nseg - 1; s >= 0; --s) {
+    const int64_t a = t0 + 64 * s, e = a + 64 < t1 ? a + 64 : t1;
+    /* replay: seg[m] = state after token a + m - 1 (seg[0] = segment start) */
+    memcpy(seg, ckpt + s * KV, (size_t)KV * sizeof(double));
+    for (int64_t t = a; t < e; ++t) {
+      const double* Sp = seg + (t - a) * KV;
+      double* Sn = seg + (t - a + 1) * KV;
+      const double alpha = exp(g[t * Hv + hv]), b = beta[t * Hv + hv];
+      const double* kt = k + (t * H + h) * dk;
+      const double* vt = v + (t * Hv + hv) * dv;
+      for (int64_t j = 0; j < dv; ++j) tmp_v[j] = 0.0;
+      for (int64_t i = 0; i < dk; ++i)
+        for (int64_t j = 0; j < dv; ++j) tmp_v[j] += alpha * Sp[i * dv + j] * kt[i];
+      for (int64_t i = 0; i < dk; ++i)
+        for (int64_t j = 0; j < dv; ++j)
+          Sn[i * dv + j] = alpha * Sp[i * dv + j] + b * kt[i] * (vt[j] - tmp_v[j]);
+    }
+    for (int64_t t = e - 1; t >= a; --t) {
+      const double* Sp = seg + (t - a) * KV;      /* S_prev */
+      const double* St = seg + (t - a + 1) * KV;  /* S after token t */
+      const double alpha = exp(g[t * Hv + hv]), b = beta[t * Hv + hv];
+      const double* kt = k + (t * H + h) * dk;
+      const double* qt = q + (t * H + h) * dk;
+      const double* vt = v + (t * Hv + hv) * dv;
+      const double* dot = dout + (t * Hv + hv) * dv;
+      double* dqt = dq + (t * H + h) * dk;
+      double* dkt = dk_out + (t * H + h) * dk;
+      double* dvt = dv_out + (t * Hv + hv) * dv;
+      /* read: dS += scale q do^T; dq += scale S do */
+      for (int64_t i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < dv; ++j) {
+          dS[i * dv + j] += scale * qt[i] * dot[j];
+          acc += St[i * dv + j] * dot[j];
+        }
+        dqt[i] += scale * acc;
+      }
+      /* delta = v - (alpha S_prev)^T k, recomputed */
+      for (int64_t j = 0; j < dv; ++j) tmp_v[j] = 0.0;
+      for (int64_t i = 0; i < dk; ++i)
+        for (int64_t j = 0; j < dv; ++j) tmp_v[j] += alpha * Sp[i * dv + j] * kt[i];
+      for (int64_t j = 0; j < dv; ++j) tmp_v[j] = vt[j] - tmp_v[j];  /* delta */
+      /* write: db = k^T dS delta; dk = b dS delta; ddelta = b dS^T k */
+      double db = 0.0;
+      for (int64_t i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < dv; ++j) acc += dS[i * dv + j] * tmp_v[j];
+        tmp_k[i] = acc;                       /* (dS delta)_i */
+        db += kt[i] * acc;
+      }
+      dbeta[t * Hv + hv] = db;
+      for (int64_t i = 0; i < dk; ++i) dkt[i] += b * tmp_k[i];
+      for (int64_t j = 0; j < dv; ++j) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < dk; ++i) acc += dS[i * dv + j] * kt[i];
+        dvt[j] = b * acc;                     /* dv = ddelta; dpred = -ddelta */
+      }
+      /* dD = dS + k dpred^T; dk += D dpred with D = alpha S_prev */
+      for (int64_t i = 0; i < dk; ++i) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < dv; ++j) {
+          dD[i * dv + j] = dS[i * dv + j] - kt[i] * dvt[j];
+          acc += alpha * Sp[i * dv + j] * dvt[j];
+        }
+        dkt[i] -= acc;
+      }
+      /* decay: dg = alpha <S_prev, dD>; dS_prev = alpha dD */
+      double da = 0.0;
+      for (int64_t i = 0; i < KV; ++i) {
+        da += Sp[i] * dD[i];
+        dS[i] = alpha * dD[i];
+      }
+      dg[t * Hv + hv] = alpha * da;
+    }
+  }
+}
+
+int gdn_ref_backward(int64_t T, int64_t N, int64_t H, int64_t Hv, int64_t dk, int64_t dv,
+                     const double* q, const double* k, const double* v, const double* g,
+                     const double* beta, double scale, const double* initial_state,
+                     const int64_t* cu_seqlens, const double* d_out, const double* d_final,
+                     double* dq, double* dk_out, double* dv_out, double* dg, double* dbeta,
+                     double* d_initial, int nthreads) {
+  if (T < 0 || N < 1 || H < 1 || Hv < 1 || dk < 1 || dv < 1) return GDN_REF_BAD_ARG;
+  if (Hv % H != 0) return GDN_REF_BAD_ARG;
+  if (!q || !k || !v || !g || !beta || !d_out || !dq || !dk_out || !dv_out || !dg || !dbeta)
+    return GDN_REF_BAD_ARG;
+  if (!cu_seqlens && N != 1) return GDN_REF_BAD_ARG;
+  if (cu_seqlens)
+    for (int64_t n = 0; n < N; ++n)
+      if (cu_seqlens[n] < 0 || cu_seqlens[n + 1] < cu_seqlens[n] || cu_seqlens[n + 1] > T)
+        return GDN_REF_BAD_ARG;
+  if (!(scale > 0.0)) scale = 1.0 / sqrt((double)dk);
+  const int64_t HG = Hv / H, KV = dk * dv;
+  int64_t max_len = 0;
+  for (int64_t n = 0; n < N; ++n) {
+    const int64_t len = cu_seqlens ? cu_seqlens[n + 1] - cu_seqlens[n] : T;
+    if (len > max_len) max_len = len;
+  }
+  const int64_t max_seg = (max_len + 63) / 64 + 1;
+  memset(dq, 0, (size_t)(T * H * dk) * sizeof(double));
+  memset(dk_out, 0, (size_t)(T * H * dk) * sizeof(double));
+  memset(dv_out, 0, (size_t)(T * Hv * dv) * sizeof(double));
+  memset(dg, 0, (size_t)(T * Hv) * sizeof(double));
+  memset(dbeta, 0, (size_t)(T * Hv) * sizeof(double));
+  int rc = GDN_REF_OK;
+  /* value heads of one key head write the same dq/dk rows: one task per
+     (sequence, key head), its value heads in order */
+  const int64_t tasks = N * H;
+#ifdef _OPENMP
+  if (nthreads < 1) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+#endif
+  {
+    double* S = (double*)malloc((size_t)KV * sizeof(double));
+    double* ckpt = (double*)malloc((size_t)(max_seg * KV) * sizeof(double));
+    double* seg = (double*)malloc((size_t)(65 * KV) * sizeof(double));
+    double* dS = (double*)malloc((size_t)KV * sizeof(double));
+    double* dD = (double*)malloc((size_t)KV * sizeof(double));
+    double* tv = (double*)malloc((size_t)dv * sizeof(double));
+    double* tk = (double*)malloc((size_t)dk * sizeof(double));
+    int ok = S && ckpt && seg && dS && dD && tv && tk;
+    if (!ok) {
+#ifdef _OPENMP
+#pragma omp atomic write
+#endif
+      rc = GDN_REF_NO_MEMORY;
+    }
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+    for (int64_t task = 0; task < tasks; ++task) {
+      if (!ok) continue;
+      const int64_t n = task / H, h = task % H;
+      const int64_t first = cu_seqlens ? cu_seqlens[n] : 0;
+      const int64_t end = cu_seqlens ? cu_seqlens[n + 1] : T;
+      for (int64_t hv = h * HG; hv < (h + 1) * HG; ++hv) {
+        for (int64_t i = 0; i < dk; ++i)
+          for (int64_t j = 0; j < dv; ++j) {
+            const size_t at = (size_t)(((n * Hv + hv) * dv + j) * dk + i);
+            S[i * dv + j] = initial_state ? initial_state[at] : 0.0;
+            dS[i * dv + j] = d_final ? d_final[at] : 0.0;
+          }
+        lane_backward(first, end, H, Hv, dk, dv, h, hv, q, k, v, g, beta, scale, d_out, S, ckpt,
+                      seg, dS, dD, tv, tk, dq, dk_out, dv_out, dg, dbeta);
+        if (d_initial)
+          for (int64_t i = 0; i < dk; ++i)
+            for (int64_t j = 0; j < dv; ++j)
+              d_initial[((n * Hv + hv) * dv + j) * dk + i] = dS[i * dv + j];
+      }
+    }
+    free(S); free(ckpt); free(seg); free(dS); free(dD); free(tv); free(tk);
+  }
+  return rc;
+}

@@ -347,3 +347,101 @@ ALL_PINS = [pin_exact_rationals, pin_chunked, pin_orthonormal_keys, pin_overwrit
             pin_beta_zero, pin_gqa_pairing, pin_split_resume, pin_varlen_isolation,
             pin_l2norm_and_scale, pin_channel_exact_rationals, pin_channel_chunked,
             pin_channel_uniform_is_scalar, pin_channel_beta_zero]
+
+
+# ---------------------------------------------------------------- backward
+def _loss_and_grads(lib, c, do, dfin):
+    grads = oracle.recurrent_backward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["scale"],
+                                      c["initial_state"], c["cu_seqlens"], do, dfin, lib=lib)
+
+    def loss(**over):
+        a = dict(c)
+        a.update(over)
+        out, fin = run(lib, a)
+        return float((out * do).sum() + (fin * dfin).sum())
+
+    return grads, loss
+
+
+def pin_backward_finite_differences(lib):
+    """Every gradient entry against a central difference of L = <do, out> + <dfin, final>."""
+    rng = np.random.default_rng(21)
+    c = rand_case(rng, 9, 1, 2, 3, 2, lengths=[5, 4])
+    do = rng.standard_normal(c["v"].shape)
+    dfin = rng.standard_normal(c["initial_state"].shape)
+    grads, loss = _loss_and_grads(lib, c, do, dfin)
+    eps = 1e-6
+    for name, key in (("q", "dq"), ("k", "dk"), ("v", "dv"), ("g", "dg"), ("beta", "dbeta"),
+                      ("initial_state", "d_initial")):
+        base = c[name]
+        for idx in np.ndindex(base.shape):
+            plus, minus = base.copy(), base.copy()
+            plus[idx] += eps
+            minus[idx] -= eps
+            fd = (loss(**{name: plus}) - loss(**{name: minus})) / (2 * eps)
+            got = grads[key][idx]
+            assert abs(got - fd) <= 1e-6 * max(1.0, abs(fd)), (name, idx, got, fd)
+
+
+def _torch_token_loss(q, k, v, g, beta, s0, scale, cu, H, Hv, do, dfin):
+    """The token recurrence written as a plain torch loop (for autograd)."""
+    import torch
+    HG = Hv // H
+    loss = torch.zeros((), dtype=torch.float64)
+    for n in range(len(cu) - 1):
+        for hv in range(Hv):
+            h = hv // HG
+            S = s0[n, hv].T
+            for t in range(int(cu[n]), int(cu[n + 1])):
+                a = torch.exp(g[t, hv])
+                pred = a * (S.T @ k[t, h])
+                S = a * S + beta[t, hv] * torch.outer(k[t, h], v[t, hv] - pred)
+                loss = loss + scale * ((S.T @ q[t, h]) * do[t, hv]).sum()
+            loss = loss + (S.T * dfin[n, hv]).sum()
+    return loss
+
+
+def pin_backward_autograd(lib):
+    """The adjoint against torch autograd of an independently written token loop."""
+    import torch
+    rng = np.random.default_rng(22)
+    c = rand_case(rng, 70, 2, 4, 8, 6, lengths=[66, 0, 4])
+    do = rng.standard_normal(c["v"].shape)
+    dfin = rng.standard_normal(c["initial_state"].shape)
+    grads, _ = _loss_and_grads(lib, c, do, dfin)
+    names = ("q", "k", "v", "g", "beta", "initial_state")
+    ts = {n: torch.tensor(c[n], dtype=torch.float64, requires_grad=True) for n in names}
+    loss = _torch_token_loss(ts["q"], ts["k"], ts["v"], ts["g"], ts["beta"], ts["initial_state"],
+                             c["scale"], c["cu_seqlens"], 2, 4, torch.tensor(do),
+                             torch.tensor(dfin))
+    loss.backward()
+    for n, key in zip(names, ("dq", "dk", "dv", "dg", "dbeta", "d_initial")):
+        assert rel(grads[key], ts[n].grad.numpy()) <= 1e-12, n
+
+
+def pin_backward_closed_forms(lib):
+    """beta = 0 and g = 0: out = scale S0^T q, so dq = scale S0 do, dS0 = scale sum q do^T
+    + dfin, dk = dv = 0; and dbeta = k^T dS (v - S0^T k) at every token."""
+    rng = np.random.default_rng(23)
+    c = rand_case(rng, 12, 1, 1, 4, 3)
+    c["beta"] = np.zeros_like(c["beta"])
+    c["g"] = np.zeros_like(c["g"])
+    do = rng.standard_normal(c["v"].shape)
+    dfin = rng.standard_normal(c["initial_state"].shape)
+    grads, _ = _loss_and_grads(lib, c, do, dfin)
+    S0 = c["initial_state"][0, 0]          # [dv, dk]
+    q, k, v = c["q"][:, 0], c["k"][:, 0], c["v"][:, 0]
+    np.testing.assert_allclose(grads["dq"][:, 0], c["scale"] * do[:, 0] @ S0, atol=1e-13)
+    assert np.abs(grads["dk"]).max() <= 1e-13 and np.abs(grads["dv"]).max() <= 1e-13
+    dS = dfin[0, 0] + c["scale"] * do[:, 0].T @ q          # [dv, dk], constant in t
+    np.testing.assert_allclose(grads["d_initial"][0, 0], dS, atol=1e-12)
+    # the state never changes, so the gradient into token t's state is the sum of
+    # the reads from t onwards plus dfin
+    for t in range(12):
+        dSt = dfin[0, 0] + c["scale"] * do[t:, 0].T @ q[t:]   # [dv, dk]
+        delta = v[t] - S0 @ k[t]
+        np.testing.assert_allclose(grads["dbeta"][t, 0], delta @ dSt @ k[t], atol=1e-12)
+
+
+BACKWARD_PINS = [pin_backward_finite_differences, pin_backward_autograd,
+                 pin_backward_closed_forms]

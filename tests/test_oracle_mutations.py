@@ -1,5 +1,6 @@
 """The pins are strong enough: each plausible mistake planted in a copy of the
-C oracle (a dropped term, a wrong sign, index or layout) fails at least one pin.
+C oracle (a dropped term, a wrong sign, index or layout, in the forward or in
+its adjoint) fails at least one pin.
 
 The mutants are compiled from a textual edit of oracle/gdn_ref.c into a
 temporary directory; the committed oracle is never modified.
@@ -18,7 +19,7 @@ MUTANTS = {
     "correction_sign": ("(vt[j] - pred[j])", "(vt[j] + pred[j])"),
     "no_write_term": ("ai * Si[j] + bki * (vt[j] - pred[j])", "ai * Si[j]"),
     "beta_dropped": ("const double bki = b * kt[i];", "const double bki = kt[i];"),
-    "decay_sign": ("exp(g[t * Hv + hv])", "exp(-g[t * Hv + hv])"),
+    "decay_sign": ("gk ? 1.0 : exp(g[t * Hv + hv])", "gk ? 1.0 : exp(-g[t * Hv + hv])"),
     "no_scale": ("ot[j] *= scale;", "ot[j] *= 1.0;"),
     "gqa_modulo": ("h = hv / HG;", "h = hv % H;"),
     "initial_state_transposed": ("initial_state[((n * Hv + hv) * dv + j) * dk + i]",
@@ -32,8 +33,20 @@ MUTANTS = {
     "channel_gate_stride": ("g + (t * Hv + hv) * dk", "g + (t * Hv + hv)"),
     "channel_gate_sign": ("const double ai = gk ? exp(gk[i])", "const double ai = gk ? exp(-gk[i])"),
     "l2norm_without_sqrt": ("1.0 / sqrt(ss + eps)", "1.0 / (ss + eps)"),
-    "default_scale_wrong": ("scale = 1.0 / sqrt((double)dk)", "scale = 1.0 / (double)dk"),
-    "sequence_start_ignored": ("cu_seqlens ? cu_seqlens[n] : 0", "0"),
+    "default_scale_wrong": ("scale = 1.0 / sqrt((double)dk); /* also catches NaN */",
+                            "scale = 1.0 / (double)dk; /* also catches NaN */"),
+    "sequence_start_ignored": ("t0 = cu_seqlens ? cu_seqlens[n] : 0", "t0 = 0"),
+    # backward (adjoint) mistakes
+    "bwd_no_read_gradient": ("dS[i * dv + j] += scale * qt[i] * dot[j];",
+                             "dS[i * dv + j] += 0.0 * qt[i] * dot[j];"),
+    "bwd_dq_from_old_state": ("acc += St[i * dv + j] * dot[j];", "acc += Sp[i * dv + j] * dot[j];"),
+    "bwd_dk_without_prediction_term": ("dkt[i] -= acc;", "dkt[i] += 0.0 * acc;"),
+    "bwd_dpred_sign": ("dD[i * dv + j] = dS[i * dv + j] - kt[i] * dvt[j];",
+                       "dD[i * dv + j] = dS[i * dv + j] + kt[i] * dvt[j];"),
+    "bwd_dg_without_alpha": ("dg[t * Hv + hv] = alpha * da;", "dg[t * Hv + hv] = da;"),
+    "bwd_dbeta_dropped": ("dbeta[t * Hv + hv] = db;", "dbeta[t * Hv + hv] = 0.0;"),
+    "bwd_state_gradient_not_decayed": ("dS[i] = alpha * dD[i];", "dS[i] = dD[i];"),
+    "bwd_dv_without_beta": ("dvt[j] = b * acc;", "dvt[j] = acc;"),
 }
 
 
@@ -47,7 +60,7 @@ def test_mutant_is_caught(name, tmp_path):
     src.write_text(text.replace(before, after))
     lib = oracle.load_library(oracle.compile_library(str(src), str(tmp_path / "libm.so")))
     failed = []
-    for pin in P.ALL_PINS:
+    for pin in P.ALL_PINS + P.BACKWARD_PINS:
         try:
             pin(lib)
         except (AssertionError, ValueError):

@@ -95,3 +95,20 @@ def test_chunk_table_never_exceeds_bound(seed):
     _, offs, total = build_chunk_table(cu, nt_max_bound(4096, 32))
     assert total <= nt_max_bound(4096, 32)
     assert total == sum(cdiv(int(b - a), 64) for a, b in zip(cu[:-1], cu[1:]))
+
+
+@pytest.mark.parametrize("pin", P.BACKWARD_PINS, ids=lambda f: f.__name__)
+def test_backward_pin(lib, pin):
+    pin(lib)
+
+
+def test_backward_is_independent_of_thread_count(lib):
+    rng = np.random.default_rng(24)
+    c = P.rand_case(rng, 140, 2, 4, 8, 8, lengths=[70, 70])
+    do = rng.standard_normal(c["v"].shape)
+    a = oracle.recurrent_backward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["scale"],
+                                  c["initial_state"], c["cu_seqlens"], do, None, nthreads=1)
+    b = oracle.recurrent_backward(c["q"], c["k"], c["v"], c["g"], c["beta"], c["scale"],
+                                  c["initial_state"], c["cu_seqlens"], do, None, nthreads=3)
+    for key in a:
+        assert np.array_equal(a[key], b[key]), key
