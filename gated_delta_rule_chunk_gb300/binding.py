@@ -28,7 +28,7 @@ DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table
 # Every entry point include/gdn.h declares.
 EXPORTED = ("gdn_check_desc", "gdn_nt_max", "gdn_workspace_size", "gdn_build_chunk_indices",
             "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string", "gdn_chunk_fwd_noalloc",
-            "gdn_recurrent_fwd", "gdn_conv_front")
+            "gdn_recurrent_fwd", "gdn_conv_front", "gdn_bwd_workspace_size", "gdn_chunk_bwd")
 GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
 
@@ -82,6 +82,11 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_conv_front.argtypes = [P(GdnDesc), vp, vp, i32, vp, vp, vp, vp, vp, vp, vp,
                                        i32, vp]
         lib.gdn_conv_front.restype = ctypes.c_int
+        lib.gdn_bwd_workspace_size.argtypes = [P(GdnDesc)]
+        lib.gdn_bwd_workspace_size.restype = ctypes.c_size_t
+        lib.gdn_chunk_bwd.argtypes = [P(GdnDesc), vp, vp, vp, vp, vp, ctypes.c_float, vp, vp,
+                                      vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        lib.gdn_chunk_bwd.restype = ctypes.c_int
         lib.gdn_read_status.argtypes = [P(GdnDesc), vp, vp]
         lib.gdn_read_status.restype = ctypes.c_int
         lib.gdn_status_string.argtypes = [ctypes.c_int]
@@ -302,6 +307,58 @@ def gdn_conv_front(x: torch.Tensor, conv_w: torch.Tensor, H: int, Hv: int,
     if return_desc:
         return q, k, v, conv_state_out, snaps, desc
     return q, k, v, conv_state_out, snaps
+
+
+def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Tensor,
+                  beta: torch.Tensor, d_out: torch.Tensor, scale: Optional[float] = None,
+                  initial_state: Optional[torch.Tensor] = None,
+                  cu_seqlens: Optional[torch.Tensor] = None,
+                  d_final_state: Optional[torch.Tensor] = None,
+                  chunk_indices: Optional[torch.Tensor] = None, nt_max: int = 0,
+                  workspace: Optional[torch.Tensor] = None, stream=None,
+                  return_desc: bool = False):
+    """Backward of gdn_chunk_fwd through the C ABI (scalar gates, no L2 norm).
+
+    Same inputs as the forward call plus d_out [T, Hv, d] (fp32 or bf16) and
+    d_final_state fp32 [N, Hv, d, d] or None. Returns a dict of fp32 gradients
+    dq, dk [T, H, d], dv [T, Hv, d], dg, dbeta [T, Hv] and d_initial_state
+    [N, Hv, d, d]."""
+    T, H, dk = q.shape
+    Hv, dv = v.shape[1], v.shape[2]
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    desc = make_desc(T, N, H, Hv, q.dtype, d_out.dtype, nt_max=nt_max, dk=dk, dv=dv,
+                     flags=GDN_FLAG_CHANNEL_GATES if g.dim() == 3 else 0)
+    for name, t in (("q", q), ("k", k), ("v", v), ("g", g), ("beta", beta), ("d_out", d_out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous CUDA tensor")
+    dev = q.device
+    f32 = torch.float32
+    grads = dict(dq=torch.zeros(T, H, dk, dtype=f32, device=dev),
+                 dk=torch.zeros(T, H, dk, dtype=f32, device=dev),
+                 dv=torch.zeros(T, Hv, dv, dtype=f32, device=dev),
+                 dg=torch.zeros(T, Hv, dtype=f32, device=dev),
+                 dbeta=torch.zeros(T, Hv, dtype=f32, device=dev),
+                 d_initial_state=torch.empty(N, Hv, dv, dk, dtype=f32, device=dev))
+    if workspace is None:
+        n = int(load_library().gdn_bwd_workspace_size(ctypes.byref(desc)))
+        if n == 0:
+            raise GdnError(load_library().gdn_check_desc(ctypes.byref(desc)), "bwd workspace")
+        workspace = torch.empty(n, dtype=torch.uint8, device=dev)
+    desc.workspace = workspace.data_ptr()
+    desc.workspace_bytes = workspace.numel()
+    if scale is None:
+        scale = 1.0 / math.sqrt(dk)
+    rc = load_library().gdn_chunk_bwd(
+        ctypes.byref(desc), _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), float(scale),
+        _ptr(initial_state), _ptr(cu_seqlens), _ptr(chunk_indices), _ptr(d_out),
+        _ptr(d_final_state), _ptr(grads["dq"]), _ptr(grads["dk"]), _ptr(grads["dv"]),
+        _ptr(grads["dg"]), _ptr(grads["dbeta"]), _ptr(grads["d_initial_state"]),
+        _stream_handle(stream))
+    if rc != 0:
+        raise GdnError(rc, "gdn_chunk_bwd")
+    if return_desc:
+        return grads, desc, workspace
+    return grads
 
 
 def gdn_read_status(desc: GdnDesc, stream=None) -> int:

@@ -134,6 +134,44 @@ WsLayout layout_of(const gdn_desc* d) {
                    (d->flags & GDN_FLAG_QK_L2NORM) != 0, d->dk);
 }
 
+// Workspace of the backward pass: the SIMT forward's layout, then the chunk-start
+// states and v_new it keeps, then the backward intermediates (per slot = chunk slot *
+// Hv + value head).
+struct BwdLayout {
+  WsLayout fwd;
+  size_t hs, vn, dvn, dhs, dos, dw, ys, sdot, ttdw, dqp, dkp, total;
+};
+
+BwdLayout bwd_layout_of(const gdn_desc* d) {
+  BwdLayout B{};
+  B.fwd = ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), false, false, d->dk);
+  size_t o = B.fwd.total;
+  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  const size_t slots = (size_t)nt_max_of(d) * d->Hv, D = (size_t)d->dk;
+  const size_t mat = sizeof(float) * slots * kChunk * D, st = sizeof(float) * slots * D * D;
+  B.hs = take(st);
+  B.vn = take(mat);
+  B.dvn = take(mat);
+  B.dhs = take(st);
+  B.dos = take(mat);
+  B.dw = take(mat);
+  B.ys = take(mat);
+  B.sdot = take(sizeof(float) * slots);
+  B.ttdw = take(mat);
+  B.dqp = take(mat);
+  B.dkp = take(mat);
+  B.total = o;
+  return B;
+}
+
+// The backward pass takes scalar gates and no q/k L2 norm.
+int check_bwd_desc_impl(const gdn_desc* d) {
+  const int rc = check_desc_impl(d);
+  if (rc != GDN_OK) return rc;
+  if (d->flags & (GDN_FLAG_CHANNEL_GATES | GDN_FLAG_QK_L2NORM)) return GDN_ERR_UNSUPPORTED;
+  return GDN_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -237,6 +275,79 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
     return GDN_ERR_LAUNCH_FAILED;
   }
   if (ev) cudaEventRecord(ev[3], stream);
+  return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
+}
+
+size_t gdn_bwd_workspace_size(const gdn_desc* desc) {
+  if (check_bwd_desc_impl(desc) != GDN_OK) return 0;
+  return bwd_layout_of(desc).total;
+}
+
+int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void* v,
+                  const float* g, const float* beta, float scale, const float* initial_state,
+                  const int32_t* cu_seqlens, int32_t* chunk_indices, const void* d_out,
+                  const float* d_final_state, float* dq, float* dk, float* dv, float* dg,
+                  float* dbeta, float* d_initial_state, cudaStream_t stream) {
+  int rc = check_bwd_desc_impl(desc);
+  if (rc != GDN_OK) return rc;
+  const gdn_desc& d = *desc;
+  if (!q || !k || !v || !g || !beta || !d_out || !dq || !dk || !dv || !dg || !dbeta ||
+      !d.workspace)
+    return GDN_ERR_NULL_ARG;
+  if (!cu_seqlens && d.N != 1) return GDN_ERR_BAD_SHAPE;
+  const bool build_into_caller = chunk_indices && (d.flags & GDN_FLAG_BUILD_CHUNK_INDICES);
+  const void* ptrs16[] = {q, k, v, g, beta, d_out, initial_state, d_final_state,
+                          dq, dk, dv, dg, dbeta, d_initial_state};
+  for (const void* p : ptrs16)
+    if (!aligned(p, 16)) return GDN_ERR_MISALIGNED;
+  if (!aligned(cu_seqlens, 4) || !aligned(chunk_indices, 8)) return GDN_ERR_MISALIGNED;
+  if (!aligned(d.workspace, 256)) return GDN_ERR_MISALIGNED;
+  const BwdLayout B = bwd_layout_of(&d);
+  if (d.workspace_bytes < B.total) return GDN_ERR_WORKSPACE_TOO_SMALL;
+
+  char* ws = static_cast<char*>(d.workspace);
+  const WsLayout& L = B.fwd;
+  const int nt_max = nt_max_of(&d), D = d.dk;
+  const bool bf16 = d.qkv_dtype == GDN_BF16;
+  if (!(scale > 0.f)) scale = 1.0f / sqrtf((float)D);  // also NaN
+  auto f32 = [&](size_t off) { return reinterpret_cast<float*>(ws + off); };
+
+  // forward recompute: the SIMT intra kernel and the scan, keeping S and v_new per chunk
+  Params p{};
+  p.T = d.T; p.N = d.N; p.H = d.H; p.Hv = d.Hv; p.HG = d.Hv / d.H; p.nt_max = nt_max;
+  p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.scale = scale;
+  p.s0 = initial_state; p.out = nullptr; p.sT = nullptr;
+  p.status = reinterpret_cast<int32_t*>(ws + L.status);
+  p.seq_info = reinterpret_cast<const int2*>(ws + L.seq_info);
+  p.chunk_offsets = reinterpret_cast<const int32_t*>(ws + L.chunk_offsets);
+  int2* table = chunk_indices ? reinterpret_cast<int2*>(chunk_indices)
+                              : reinterpret_cast<int2*>(ws + L.chunk_table);
+  p.chunk_table = table;
+  p.w = ws + L.w; p.u = f32(L.u); p.M = ws + L.M;
+  p.qt = f32(L.qt); p.kt = f32(L.kt); p.gam = f32(L.gam);
+  p.hs = f32(B.hs); p.vn_out = f32(B.vn);
+  if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH_FAILED;
+  launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
+                     (!chunk_indices || build_into_caller) ? table : nullptr,
+                     const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
+                     p.status, stream);
+  if (nt_max > 0 && !launch_gen_intra(p, D, false, bf16, stream)) return GDN_ERR_LAUNCH_FAILED;
+  if (!launch_gen_inter(p, D, stream)) return GDN_ERR_LAUNCH_FAILED;
+
+  BwdParams b{};
+  b.T = d.T; b.N = d.N; b.H = d.H; b.Hv = d.Hv; b.HG = p.HG; b.nt_max = nt_max;
+  b.q = q; b.k = k; b.v = v; b.g = g; b.beta = beta; b.scale = scale;
+  b.dout = d_out; b.dout_bf16 = d.out_dtype == GDN_BF16; b.dfin = d_final_state;
+  b.dq = dq; b.dk = dk; b.dv = dv; b.dg = dg; b.dbeta = dbeta; b.dh0 = d_initial_state;
+  b.status = p.status; b.seq_info = p.seq_info; b.chunk_offsets = p.chunk_offsets;
+  b.chunk_table = table;
+  b.wT = f32(L.w); b.kt = p.kt; b.qt = p.qt; b.MT = f32(L.M); b.gam = p.gam;
+  b.hs = p.hs; b.vn = p.vn_out;
+  b.dvn = f32(B.dvn); b.dhs = f32(B.dhs); b.dos = f32(B.dos); b.dw = f32(B.dw);
+  b.ys = f32(B.ys); b.sdot = f32(B.sdot); b.ttdw = f32(B.ttdw);
+  b.dqp = f32(B.dqp); b.dkp = f32(B.dkp);
+  if (!launch_bwd(b, D, bf16, stream)) return GDN_ERR_LAUNCH_FAILED;
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 

@@ -38,9 +38,54 @@ struct Params {
   float* qt;                 // [nt_max, Hv, dk, 64] (exp(G) q)^T        (SIMT path)
   float* kt;                 // [nt_max, Hv, 64, dk] exp(G_L - G) k      (SIMT path)
   float* gam;                // [nt_max, Hv, dk] exp(G_L)                (SIMT path)
+  float* hs;                 // [nt_max, Hv, dv, dk] chunk-start states, or null (backward)
+  float* vn_out;             // [nt_max, Hv, 64, dv] v_new, or null (backward)
   const float* qrn;          // [T, H] 1/||q|| or null
   const float* krn;          // [T, H] 1/||k|| or null
   int out_bf16;
+};
+
+// Parameters of the backward kernels (device pointers; fp32 SIMT arithmetic). Per-slot
+// arrays are indexed by slot = chunk slot * Hv + value head.
+struct BwdParams {
+  int T, N, H, Hv, HG, nt_max;
+  const void* q;
+  const void* k;
+  const void* v;
+  const float* g;
+  const float* beta;
+  float scale;
+  const void* dout;          // [T, Hv, dv], bf16 when dout_bf16 else fp32
+  int dout_bf16;
+  const float* dfin;         // [N, Hv, dv, dk] gradient of the final state, or null
+  float* dq;                 // [T, H, dk]
+  float* dk;                 // [T, H, dk]
+  float* dv;                 // [T, Hv, dv]
+  float* dg;                 // [T, Hv]
+  float* dbeta;              // [T, Hv]
+  float* dh0;                // [N, Hv, dv, dk] gradient of the initial state, or null
+  int32_t* status;
+  const int2* seq_info;
+  const int32_t* chunk_offsets;
+  const int2* chunk_table;
+  // forward quantities (the general path's layout)
+  const float* wT;           // [slot][D][64] w^T
+  const float* kt;           // [slot][64][D] exp(G_L - G) k
+  const float* qt;           // [slot][D][64] (exp(G) q)^T
+  const float* MT;           // [slot][64][64] M^T
+  const float* gam;          // [slot][D] exp(G_L)
+  const float* hs;           // [slot][D][D] chunk-start state, [dv][dk]
+  const float* vn;           // [slot][64][D] v_new
+  // backward intermediates
+  float* dvn;                // [slot][64][D] gradient of v_new
+  float* dhs;                // [slot][D][D] gradient of the next chunk-start state, [dv][dk]
+  float* dos;                // [slot][64][D] dO S^T
+  float* dw;                 // [slot][64][D] gradient of w: -dv_new S^T
+  float* ys;                 // [slot][64][D] v_new dS_next^T
+  float* sdot;               // [slot] <S, dS_next>
+  float* ttdw;               // [slot][64][D] T^T dw
+  float* dqp;                // [slot][64][D] this value head's part of dq
+  float* dkp;                // [slot][64][D] this value head's part of dk
 };
 
 // Parameters of the token-serial kernel (device pointers).
@@ -133,7 +178,8 @@ struct SeqView {
   int start, len, first_slot;
 };
 
-__device__ __forceinline__ SeqView seq_view(const Params& p, int n) {
+template <typename P>
+__device__ __forceinline__ SeqView seq_view(const P& p, int n) {
   int2 si = p.seq_info[n];
   return SeqView{si.x, si.y, p.chunk_offsets[n]};
 }
@@ -166,6 +212,7 @@ void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, int D,
                    float* qrn, float* krn, cudaStream_t s);
 bool launch_gen_intra(const Params& p, int D, bool channel_gates, bool bf16_inputs, cudaStream_t s);
 bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
+bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
 bool launch_recurrent(const RecParams& p, cudaStream_t s);

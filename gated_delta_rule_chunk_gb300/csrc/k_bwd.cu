@@ -1,0 +1,603 @@
+// Backward pass of the chunked gated delta rule (scalar gates), fp32 SIMT.
+//
+// The stage names follow the backward kernels listed in the FLA graph-capture
+// RFC ("What needs to change", GDN bwd: the state-gradient scan, the local dv
+// and dq/dk/dw/dg gradients and the WY-representation gradient). Per sequence
+// and value head, with the chunk quantities of the forward (chunk-start state
+// S, T = (I + A)^-1, w, u, v_new, M = Gamma * (Q K^T) and the decayed images
+// Qt = exp(G) Q, Kt = exp(G_L - G) K), the gradient of
+//   v_new = u - w S,   o = scale (Qt S + M v_new),   S' = exp(G_L) S + Kt^T v_new
+// runs a reverse scan over the chunks (dS holds the gradient of the next
+// chunk-start state):
+//   dv_new = Kt dS + scale M^T dO,   dS <- exp(G_L) dS + scale Qt^T dO - w^T dv_new
+// and then, per chunk, with dw = -dv_new S^T, Z = dv_new (beta V)^T + dw (beta exp(G) K)^T
+// and dA = -(T^T Z T^T) on the strict lower triangle:
+//   dv   = beta * (T^T dv_new)
+//   dq   = scale exp(G) * (dO S^T) + (dP * Gamma) K,           dP = scale dO v_new^T (j <= i)
+//   dk   = (dP * Gamma)^T Q + exp(G_L - G) * (v_new dS^T) + beta exp(G) * (T^T dw)
+//          + (dAt + dAt^T) K,                                  dAt = dA * beta_i Gamma_ij
+//   dbeta_i = (T^T dv_new)_i . v_i + exp(G_i) (T^T dw)_i . k_i + sum_j dA_ij Gamma_ij k_i . k_j
+//   dG   from every exp(G) factor (rows and columns of Gamma, exp(G), exp(G_L));
+//   dg   = reverse in-chunk cumsum of dG,  dS_0 = the scan's last dS.
+// Each step is the derivative of one forward equation; together they equal the
+// token-by-token adjoint of the recurrence.
+#include "gdn_common.cuh"
+#include "simt_tile.cuh"
+#include "tri_inverse.cuh"
+
+namespace gdn {
+
+namespace {
+
+constexpr int kThr = 256;
+
+template <int D>
+constexpr int bv_of() { return D == 128 ? 32 : 16; }
+
+__device__ __forceinline__ float ld_dout(const BwdParams& p, size_t idx) {
+  return p.dout_bf16 ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(p.dout)[idx])
+                     : reinterpret_cast<const float*>(p.dout)[idx];
+}
+
+// ---------------------------------------------------------------- reverse scan
+template <int D>
+constexpr size_t scan_floats() {
+  constexpr int BV = bv_of<D>(), SLD = BV + 4, LQ = D + 4;
+  return (size_t)D * SLD + D * 68 + 64 * 68 + 2 * 64 * LQ + 2 * 64 * BV + D;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThr) bwd_scan_kernel(BwdParams p) {
+  constexpr int BV = bv_of<D>(), SLD = BV + 4, LQ = D + 4, RN = BV / 16;
+  extern __shared__ __align__(16) float sm[];
+  float* dS = sm;                  // [D][SLD] gradient of the next chunk-start state
+  float* KtT = dS + D * SLD;       // [D][68]  Kt^T
+  float* Mr = KtT + D * 68;        // [64][68] M (row-major)
+  float* Qr = Mr + 64 * 68;        // [64][LQ] Qt (token-major)
+  float* Wr = Qr + 64 * LQ;        // [64][LQ] w (token-major)
+  float* dO = Wr + 64 * LQ;        // [64][BV]
+  float* dV = dO + 64 * BV;        // [64][BV] dv_new
+  float* gm = dV + 64 * BV;        // [D]
+
+  const int tid = threadIdx.x;
+  const int n = blockIdx.x, hv = blockIdx.y, c0 = blockIdx.z * BV;
+  const SeqView sv = seq_view(p, n);
+  int nch = (sv.len + kChunk - 1) / kChunk;
+  if (sv.first_slot + nch > p.nt_max) {
+    if (tid == 0) set_status(p.status, GDN_DEV_CHUNK_OVERFLOW);
+    nch = max(0, p.nt_max - sv.first_slot);
+  }
+  const size_t sbase = ((size_t)n * p.Hv + hv) * D * D;
+  for (int idx = tid; idx < D * BV; idx += kThr) {
+    const int d = idx / BV, j = idx % BV;
+    dS[d * SLD + j] = p.dfin ? p.dfin[sbase + (size_t)(c0 + j) * D + d] : 0.f;
+  }
+  for (int c = nch - 1; c >= 0; --c) {
+    const size_t sl = (size_t)(sv.first_slot + c) * p.Hv + hv;
+    const int t0 = sv.start + kChunk * c;
+    const int L = min(kChunk, sv.len - kChunk * c);
+    for (int idx = tid; idx < 64 * D; idx += kThr) {
+      const int r = idx / D, f = idx % D;          // Kt rows, lanes along features
+      KtT[f * 68 + r] = p.kt[sl * 64 * D + idx];
+      const int fq = idx / 64, t = idx % 64;       // Qt^T and w^T rows, lanes along tokens
+      Qr[t * LQ + fq] = p.qt[sl * 64 * D + idx];
+      Wr[t * LQ + fq] = p.wT[sl * 64 * D + idx];
+    }
+    for (int idx = tid; idx < 64 * 64; idx += kThr) {
+      const int i = idx >> 6, t = idx & 63;        // M^T[i][t] = M[t][i]
+      Mr[t * 68 + i] = p.MT[sl * 4096 + idx];
+    }
+    for (int idx = tid; idx < 64 * BV; idx += kThr) {
+      const int i = idx / BV, j = idx % BV;
+      dO[idx] = i < L ? ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + c0 + j) : 0.f;
+    }
+    for (int d = tid; d < D; d += kThr) gm[d] = p.gam[sl * D + d];
+    __syncthreads();
+    {  // the incoming gradient is this chunk's dS_next; keep it for the chunk kernels
+      float* dh = p.dhs + sl * D * D;
+      for (int idx = tid; idx < D * BV; idx += kThr) {
+        const int j = idx / D, d = idx % D;
+        dh[(size_t)(c0 + j) * D + d] = dS[d * SLD + j];
+      }
+    }
+    {  // dv_new = Kt dS + scale M^T dO (M[t][i] is zero for t < i)
+      const int i0 = (tid >> 4) * 4, n0 = (tid & 15) * RN;
+      float a[4][RN], b[4][RN];
+      zero(a);
+      zero(b);
+      fma_tile<4, RN>(a, KtT, 68, dS, SLD, i0, n0, 0, D);
+      fma_tile<4, RN>(b, Mr, 68, dO, BV, i0, n0, i0, 64);
+      float* gout = p.dvn + sl * 64 * D + c0;
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int cc = 0; cc < RN; ++cc) {
+          const float x = fmaf(p.scale, b[r][cc], a[r][cc]);
+          dV[(i0 + r) * BV + n0 + cc] = x;
+          gout[(size_t)(i0 + r) * D + n0 + cc] = x;
+        }
+    }
+    __syncthreads();
+    // dS <- exp(G_L) dS + scale Qt^T dO - w^T dv_new (each entry owned by one thread)
+    for (int t = tid; t < (D / 4) * 16; t += kThr) {
+      const int d0 = (t >> 4) * 4, n0 = (t & 15) * RN;
+      float a[4][RN], b[4][RN];
+      zero(a);
+      zero(b);
+      fma_tile<4, RN>(a, Qr, LQ, dO, BV, d0, n0, 0, 64);
+      fma_tile<4, RN>(b, Wr, LQ, dV, BV, d0, n0, 0, 64);
+#pragma unroll
+      for (int r = 0; r < 4; ++r)
+#pragma unroll
+        for (int cc = 0; cc < RN; ++cc) {
+          float& s = dS[(d0 + r) * SLD + n0 + cc];
+          s = fmaf(gm[d0 + r], s, fmaf(p.scale, a[r][cc], -b[r][cc]));
+        }
+    }
+    __syncthreads();
+  }
+  __syncthreads();  // an empty sequence skips the loop: dS was written by other threads
+  if (p.dh0)
+    for (int idx = tid; idx < D * BV; idx += kThr) {
+      const int j = idx / D, d = idx % D;
+      p.dh0[sbase + (size_t)(c0 + j) * D + d] = dS[d * SLD + j];
+    }
+}
+
+// ---------------------------------------------------------------- contractions with S, dS
+template <int D>
+constexpr size_t state_floats() { return (size_t)3 * D * 68 + 2 * 32 * D + kThr / 32; }
+
+// dos = dO S^T, dw = -dv_new S^T, ys = v_new dS_next^T (contractions over dv) and
+// sdot = <S, dS_next>, per (chunk slot, value head).
+template <int D>
+__global__ void __launch_bounds__(kThr) bwd_state_kernel(BwdParams p) {
+  constexpr int RN = D / 16;
+  extern __shared__ __align__(16) float sm[];
+  float* dOT = sm;                 // [D][68] dO^T
+  float* vnT = dOT + D * 68;       // [D][68] v_new^T
+  float* dvT = vnT + D * 68;       // [D][68] dv_new^T
+  float* Sb = dvT + D * 68;        // [32][D] rows of S ([dv][dk])
+  float* dSb = Sb + 32 * D;        // [32][D] rows of dS_next
+  float* red = dSb + 32 * D;       // [8] warp partials
+
+  const int tid = threadIdx.x, hv = blockIdx.y;
+  int t0, L, wslot;
+  if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
+  const size_t sl = (size_t)wslot * p.Hv + hv;
+  for (int idx = tid; idx < 64 * D; idx += kThr) {
+    const int i = idx / D, f = idx % D;
+    dOT[f * 68 + i] = i < L ? ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + f) : 0.f;
+    vnT[f * 68 + i] = p.vn[sl * 64 * D + idx];
+    dvT[f * 68 + i] = p.dvn[sl * 64 * D + idx];
+  }
+  const int i0 = (tid >> 4) * 4, d0 = (tid & 15) * RN;
+  float aos[4][RN], aw[4][RN], ay[4][RN];
+  zero(aos);
+  zero(aw);
+  zero(ay);
+  float sd = 0.f;
+  const float4* hs4 = reinterpret_cast<const float4*>(p.hs + sl * D * D);
+  const float4* dh4 = reinterpret_cast<const float4*>(p.dhs + sl * D * D);
+  for (int nb = 0; nb < D / 32; ++nb) {
+    __syncthreads();  // previous blocks consumed (and the transposes above written)
+    for (int idx = tid; idx < 32 * D / 4; idx += kThr) {
+      const float4 a = hs4[nb * 8 * D + idx], b = dh4[nb * 8 * D + idx];
+      reinterpret_cast<float4*>(Sb)[idx] = a;
+      reinterpret_cast<float4*>(dSb)[idx] = b;
+      sd += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+    }
+    __syncthreads();
+#pragma unroll 2
+    for (int r = 0; r < 32; ++r) {
+      const int f = nb * 32 + r;
+      float xo[4], xw[4], xy[4], bs[RN], bd[RN];
+      ldv<4>(dOT + f * 68 + i0, xo);
+      ldv<4>(dvT + f * 68 + i0, xw);
+      ldv<4>(vnT + f * 68 + i0, xy);
+#pragma unroll
+      for (int h = 0; h < RN; h += 4) {
+        float t4[4], u4[4];
+        ldv<4>(Sb + r * D + d0 + h, t4);
+        ldv<4>(dSb + r * D + d0 + h, u4);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          bs[h + e] = t4[e];
+          bd[h + e] = u4[e];
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < RN; ++b) {
+          aos[a][b] = fmaf(xo[a], bs[b], aos[a][b]);
+          aw[a][b] = fmaf(xw[a], bs[b], aw[a][b]);
+          ay[a][b] = fmaf(xy[a], bd[b], ay[a][b]);
+        }
+    }
+  }
+#pragma unroll
+  for (int a = 0; a < 4; ++a) {
+    const size_t row = sl * 64 * D + (size_t)(i0 + a) * D + d0;
+#pragma unroll
+    for (int b = 0; b < RN; ++b) {
+      p.dos[row + b] = aos[a][b];
+      p.dw[row + b] = -aw[a][b];
+      p.ys[row + b] = ay[a][b];
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
+  if ((tid & 31) == 0) red[tid >> 5] = sd;
+  __syncthreads();
+  if (tid == 0) {
+    float s = 0.f;
+    for (int w = 0; w < kThr / 32; ++w) s += red[w];
+    p.sdot[sl] = s;
+  }
+}
+
+// ---------------------------------------------------------------- per-chunk gradients
+constexpr int kLd = 68;    // row stride of the 64 x 64 matrices and feature-major blocks
+constexpr int kLt = 36;    // row stride of the token-major 64 x 32 blocks
+
+constexpr size_t chunk_floats() {
+  return (size_t)7 * 64 * kLd + 16 * kLd + 4 * 32 * kLd + 2 * 64 * kLt + 8 * 64 + 4 * 64 * 8;
+}
+
+// Load a [64 x 32] block of a token-major source as feature-major [32][kLd] (rows of the
+// chunk past L are zero). get(i, f) returns the value of token i, feature f.
+template <typename Get>
+__device__ __forceinline__ void load_fm(float* dst, int L, int tid, Get get) {
+  for (int idx = tid; idx < 64 * 32; idx += kThr) {
+    const int i = idx >> 5, f = idx & 31;
+    dst[f * kLd + i] = i < L ? get(i, f) : 0.f;
+  }
+}
+template <typename Get>
+__device__ __forceinline__ void load_tm(float* dst, int L, int tid, Get get) {
+  for (int idx = tid; idx < 64 * 32; idx += kThr) {
+    const int i = idx >> 5, f = idx & 31;
+    dst[i * kLt + f] = i < L ? get(i, f) : 0.f;
+  }
+}
+
+template <typename TIn, int D>
+__global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
+  extern __shared__ __align__(16) float sm[];
+  float* Tm = sm;                  // T = (I + A)^-1, row-major
+  float* Tt = Tm + 64 * kLd;       // T^T
+  float* GK = Tt + 64 * kLd;       // Gamma * K K^T (strict lower); later dAt + dAt^T
+  float* Mm = GK + 64 * kLd;       // Gamma * Q K^T (lower incl.)
+  float* dP = Mm + 64 * kLd;       // scale dO v_new^T (lower incl.); later dP * Gamma
+  float* Zm = dP + 64 * kLd;       // Z; later dA
+  float* Tp = Zm + 64 * kLd;       // scratch: Z^T T; later (dP * Gamma)^T
+  float* Xs = Tp + 64 * kLd;       // [16][kLd] scratch of the inverse
+  float* B0 = Xs + 16 * kLd;       // [32][kLd] feature-major blocks
+  float* B1 = B0 + 32 * kLd;
+  float* B2 = B1 + 32 * kLd;
+  float* B3 = B2 + 32 * kLd;
+  float* R0 = B3 + 32 * kLd;       // [64][kLt] token-major blocks
+  float* R1 = R0 + 64 * kLt;
+  float* G = R1 + 64 * kLt;        // [64] in-chunk cumulative gate
+  float* eG = G + 64;              // exp(G)
+  float* eL = eG + 64;             // exp(G_L - G)
+  float* bt = eL + 64;             // beta
+  float* dGv = bt + 64;            // dG
+  float* dBv = dGv + 64;           // dbeta
+  float* rsk = dBv + 64;           // (T^T dw)_i . k_i
+  float* wsum = rsk + 64;          // W_i = exp(G_L - G_i) k_i . (v_new dS^T)_i
+  float* pv = wsum + 64;           // [64][8] partial row dots (T^T dv_new) . v
+  float* pk = pv + 64 * 8;         // [64][8] partial row dots (T^T dw) . k
+  float* pq = pk + 64 * 8;         // [64][8] partial row dots q . (dO S^T)
+  float* pw = pq + 64 * 8;         // [64][8] partial row dots k . (v_new dS^T)
+
+  const int tid = threadIdx.x, hv = blockIdx.y, h = hv / p.HG;
+  int t0, L, wslot;
+  if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
+  const size_t sl = (size_t)wslot * p.Hv + hv;
+  auto kin = [&](int i, int f) { return ld_in<TIn>(p.k, ((size_t)(t0 + i) * p.H + h) * D + f); };
+  auto qin = [&](int i, int f) { return ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + f); };
+  auto vin = [&](int i, int f) { return ld_in<TIn>(p.v, ((size_t)(t0 + i) * p.Hv + hv) * D + f); };
+
+  if (tid < 64) {
+    const bool ok = tid < L;
+    G[tid] = ok ? p.g[(size_t)(t0 + tid) * p.Hv + hv] : 0.f;
+    bt[tid] = ok ? p.beta[(size_t)(t0 + tid) * p.Hv + hv] : 0.f;
+  }
+  for (int idx = tid; idx < 64 * kLd; idx += kThr) Tm[idx] = 0.f;
+  __syncthreads();
+  if (tid == 0) {
+    float acc = 0.f;
+    for (int i = 0; i < 64; ++i) {
+      acc += G[i];
+      G[i] = acc;
+    }
+  }
+  __syncthreads();
+  if (tid < 64) {
+    eG[tid] = expf(G[tid]);
+    eL[tid] = expf(G[63] - G[tid]);
+  }
+  // ---------------- K K^T and Q K^T (feature blocks of 32)
+  const int ti = (tid >> 4) * 4, tj = (tid & 15) * 4;  // 4 x 4 tile of a 64 x 64 matrix
+  {
+    float akk[4][4], aqk[4][4];
+    zero(akk);
+    zero(aqk);
+    for (int fb = 0; fb < D / 32; ++fb) {
+      __syncthreads();
+      load_fm(B0, L, tid, [&](int i, int f) { return kin(i, fb * 32 + f); });
+      load_fm(B1, L, tid, [&](int i, int f) { return qin(i, fb * 32 + f); });
+      __syncthreads();
+      if (tj <= ti) {
+        fma_tile<4, 4>(akk, B0, kLd, B0, kLd, ti, tj, 0, 32);
+        fma_tile<4, 4>(aqk, B1, kLd, B0, kLd, ti, tj, 0, 32);
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int i = ti + a, j = tj + b;
+        const float gam = j <= i ? expf(G[i] - G[j]) : 0.f;
+        GK[i * kLd + j] = j < i ? gam * akk[a][b] : 0.f;
+        Mm[i * kLd + j] = gam * aqk[a][b];
+        Tm[i * kLd + j] = j < i ? bt[i] * gam * akk[a][b] : 0.f;  // A
+      }
+  }
+  __syncthreads();
+  tri_inverse_64_inplace(Tm, kLd, Xs, tid, kThr);  // Tm = T, ends synchronized
+  for (int idx = tid; idx < 64 * 64; idx += kThr) {
+    const int i = idx >> 6, j = idx & 63;
+    Tt[j * kLd + i] = Tm[i * kLd + j];
+  }
+  // ---------------- value features: dP, Z1, T^T dv_new (dv and the dbeta part)
+  float az[4][4];
+  zero(az);
+  {
+    float adp[4][4];
+    zero(adp);
+    const int j0 = (tid >> 3) * 2, n0 = (tid & 7) * 4;  // 2 x 4 tile of a 64 x 32 block
+    float rv[2] = {0.f, 0.f};
+    for (int fb = 0; fb < D / 32; ++fb) {
+      __syncthreads();
+      const int f0 = fb * 32;
+      load_fm(B0, L, tid, [&](int i, int f) {
+        return ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + f0 + f); });
+      load_fm(B1, 64, tid, [&](int i, int f) { return p.vn[sl * 64 * D + (size_t)i * D + f0 + f]; });
+      load_fm(B2, 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + f0 + f]; });
+      load_fm(B3, L, tid, [&](int i, int f) { return vin(i, f0 + f); });
+      load_tm(R0, 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + f0 + f]; });
+      __syncthreads();
+      if (tj <= ti) fma_tile<4, 4>(adp, B0, kLd, B1, kLd, ti, tj, 0, 32);
+      fma_tile<4, 4>(az, B2, kLd, B3, kLd, ti, tj, 0, 32);
+      float tu[2][4];
+      zero(tu);
+      fma_tile<2, 4>(tu, Tm, kLd, R0, kLt, j0, n0, j0, 64);  // T[i][j] = 0 for i < j
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int j = j0 + a;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          rv[a] = fmaf(tu[a][b], B3[(n0 + b) * kLd + j], rv[a]);
+          if (j < L) p.dv[((size_t)(t0 + j) * p.Hv + hv) * D + f0 + n0 + b] = bt[j] * tu[a][b];
+        }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) pv[(j0 + a) * 8 + (tid & 7)] = rv[a];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) dP[(ti + a) * kLd + tj + b] = (tj + b <= ti + a) ? p.scale * adp[a][b] : 0.f;
+  }
+  // ---------------- key features: Z2, T^T dw (the dk and dbeta / dG parts)
+  {
+    const int j0 = (tid >> 3) * 2, n0 = (tid & 7) * 4;
+    float rk[2] = {0.f, 0.f};
+    for (int fb = 0; fb < D / 32; ++fb) {
+      __syncthreads();
+      const int f0 = fb * 32;
+      load_fm(B0, 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + f0 + f]; });
+      load_fm(B1, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
+      load_tm(R0, 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + f0 + f]; });
+      __syncthreads();
+      {  // Z2[i][j] = sum_d dw[i][d] exp(G_j) k[j][d]: scale column j after the sum
+        float z2[4][4];
+        zero(z2);
+        fma_tile<4, 4>(z2, B0, kLd, B1, kLd, ti, tj, 0, 32);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int b = 0; b < 4; ++b) az[a][b] = fmaf(eG[tj + b], z2[a][b], az[a][b]);
+      }
+      float tw[2][4];
+      zero(tw);
+      fma_tile<2, 4>(tw, Tm, kLd, R0, kLt, j0, n0, j0, 64);
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int j = j0 + a;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          rk[a] = fmaf(tw[a][b], B1[(n0 + b) * kLd + j], rk[a]);
+          p.ttdw[sl * 64 * D + (size_t)j * D + f0 + n0 + b] = tw[a][b];
+        }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) pk[(j0 + a) * 8 + (tid & 7)] = rk[a];
+  }
+  // Z = (Z1 + Z2) diag(beta)
+#pragma unroll
+  for (int a = 0; a < 4; ++a)
+#pragma unroll
+    for (int b = 0; b < 4; ++b) Zm[(ti + a) * kLd + tj + b] = bt[tj + b] * az[a][b];
+  __syncthreads();
+  {  // Tp = Z^T T   (T[i][j] = 0 for i < j)
+    float acc[4][4];
+    zero(acc);
+    fma_tile<4, 4>(acc, Zm, kLd, Tm, kLd, ti, tj, tj, 64);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) Tp[(ti + a) * kLd + tj + b] = acc[a][b];
+  }
+  __syncthreads();
+  {  // dA[j][m] = -sum_l Tp[l][j] T[m][l] on the strict lower triangle (T[m][l] = 0 for l > m)
+    float acc[4][4];
+    zero(acc);
+    if (tj <= ti) fma_tile<4, 4>(acc, Tp, kLd, Tt, kLd, ti, tj, 0, tj + 4);
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) Zm[(ti + a) * kLd + tj + b] = (tj + b < ti + a) ? -acc[a][b] : 0.f;
+  }
+  __syncthreads();
+  // ---------------- row and column sums: dbeta and dG parts from A and from dP
+  if (tid < 64) {
+    const int i = tid;
+    float db = 0.f, dg = 0.f;
+    for (int j = 0; j < 64; ++j) {
+      const float da = Zm[i * kLd + j], gk = GK[i * kLd + j];
+      db = fmaf(da, gk, db);
+      dg = fmaf(da, bt[i] * gk, dg);                      // row of dA * A
+      dg = fmaf(dP[i * kLd + j], Mm[i * kLd + j], dg);    // row of dP * M
+      dg -= Zm[j * kLd + i] * bt[j] * GK[j * kLd + i];    // column of dA * A
+      dg -= dP[j * kLd + i] * Mm[j * kLd + i];            // column of dP * M
+    }
+    float sv = 0.f, sk = 0.f;
+    for (int c = 0; c < 8; ++c) {
+      sv += pv[i * 8 + c];
+      sk += pk[i * 8 + c];
+    }
+    rsk[i] = sk;
+    dBv[i] = sv + eG[i] * sk + db;
+    dGv[i] = dg + bt[i] * eG[i] * sk;
+  }
+  __syncthreads();
+  // PG = dP * Gamma (lower incl.), Tp = PG^T, GK = dAt + dAt^T with dAt = dA * beta_i Gamma_ij
+  for (int idx = tid; idx < 64 * 64; idx += kThr) {
+    const int i = idx >> 6, j = idx & 63;
+    const float gij = j <= i ? expf(G[i] - G[j]) : 0.f;
+    const float gji = i <= j ? expf(G[j] - G[i]) : 0.f;
+    const float pg = dP[i * kLd + j] * gij;
+    Tp[j * kLd + i] = pg;
+    GK[i * kLd + j] = Zm[i * kLd + j] * bt[i] * gij + Zm[j * kLd + i] * bt[j] * gji;
+  }
+  __syncthreads();
+  for (int idx = tid; idx < 64 * 64; idx += kThr) {
+    const int i = idx >> 6, j = idx & 63;
+    dP[i * kLd + j] = Tp[j * kLd + i];
+  }
+  // ---------------- key features again: dq and dk parts of this value head
+  {
+    const int i0 = (tid >> 3) * 2, d0 = (tid & 7) * 4;
+    float rq[2] = {0.f, 0.f}, rw[2] = {0.f, 0.f};
+    for (int fb = 0; fb < D / 32; ++fb) {
+      __syncthreads();
+      const int f0 = fb * 32;
+      load_tm(R0, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
+      load_tm(R1, L, tid, [&](int i, int f) { return qin(i, f0 + f); });
+      __syncthreads();
+      float aq[2][4], ak[2][4];
+      zero(aq);
+      zero(ak);
+      fma_tile<2, 4>(aq, Tp, kLd, R0, kLt, i0, d0, 0, i0 + 2);   // (PG K)[i]: j <= i
+      fma_tile<2, 4>(ak, dP, kLd, R1, kLt, i0, d0, i0, 64);      // (PG^T Q)[i]: l >= i
+      fma_tile<2, 4>(ak, GK, kLd, R0, kLt, i0, d0, 0, 64);       // (dAt + dAt^T) K
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        const int i = i0 + a;
+        const size_t row = sl * 64 * D + (size_t)i * D + f0 + d0;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          const float os = p.dos[row + b], y = p.ys[row + b], tw = p.ttdw[row + b];
+          const float qv = R1[i * kLt + d0 + b], kv = R0[i * kLt + d0 + b];
+          rq[a] = fmaf(qv, os, rq[a]);
+          rw[a] = fmaf(kv, y, rw[a]);
+          p.dqp[row + b] = fmaf(p.scale * eG[i], os, aq[a][b]);
+          p.dkp[row + b] = ak[a][b] + eL[i] * y + bt[i] * eG[i] * tw;
+        }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 2; ++a) {
+      pq[(i0 + a) * 8 + (tid & 7)] = rq[a];
+      pw[(i0 + a) * 8 + (tid & 7)] = rw[a];
+    }
+  }
+  __syncthreads();
+  if (tid < 64) {
+    const int i = tid;
+    float sq = 0.f, sw = 0.f;
+    for (int c = 0; c < 8; ++c) {
+      sq += pq[i * 8 + c];
+      sw += pw[i * 8 + c];
+    }
+    wsum[i] = eL[i] * sw;
+    dGv[i] += p.scale * eG[i] * sq - eL[i] * sw;
+  }
+  __syncthreads();
+  if (tid == 0) {  // exp(G_L) terms go to the last row (G is flat past the chunk end)
+    float s = 0.f;
+    for (int i = 0; i < 64; ++i) s += wsum[i];
+    dGv[63] += s + expf(G[63]) * p.sdot[sl];
+    float acc = 0.f;  // dg = reverse in-chunk cumsum of dG
+    for (int i = 63; i >= 0; --i) {
+      acc += dGv[i];
+      if (i < L) {
+        p.dg[(size_t)(t0 + i) * p.Hv + hv] = acc;
+        p.dbeta[(size_t)(t0 + i) * p.Hv + hv] = dBv[i];
+      }
+    }
+  }
+}
+
+// dq, dk = sum over the value heads of each key head group (fixed order)
+template <int D>
+__global__ void __launch_bounds__(kThr) bwd_reduce_kernel(BwdParams p) {
+  const int tid = threadIdx.x, h = blockIdx.y;
+  int t0, L, wslot;
+  if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
+  for (int idx = tid; idx < L * D; idx += kThr) {
+    const int i = idx / D, d = idx % D;
+    float sq = 0.f, sk = 0.f;
+    for (int r = 0; r < p.HG; ++r) {
+      const size_t at = ((size_t)wslot * p.Hv + h * p.HG + r) * 64 * D + idx;
+      sq += p.dqp[at];
+      sk += p.dkp[at];
+    }
+    const size_t o = ((size_t)(t0 + i) * p.H + h) * D + d;
+    p.dq[o] = sq;
+    p.dk[o] = sk;
+  }
+}
+
+template <typename TIn, int D>
+bool launch_bwd_t(const BwdParams& p, cudaStream_t s) {
+  constexpr int BV = bv_of<D>();
+  const int s1 = (int)(scan_floats<D>() * sizeof(float));
+  const int s2 = (int)(state_floats<D>() * sizeof(float));
+  const int s3 = (int)(chunk_floats() * sizeof(float));
+  ensure_smem_limit((const void*)bwd_scan_kernel<D>, s1);
+  ensure_smem_limit((const void*)bwd_state_kernel<D>, s2);
+  ensure_smem_limit((const void*)bwd_chunk_kernel<TIn, D>, s3);
+  bwd_scan_kernel<D><<<dim3(p.N, p.Hv, D / BV), kThr, s1, s>>>(p);
+  if (p.nt_max > 0) {
+    bwd_state_kernel<D><<<dim3(p.nt_max, p.Hv), kThr, s2, s>>>(p);
+    bwd_chunk_kernel<TIn, D><<<dim3(p.nt_max, p.Hv), kThr, s3, s>>>(p);
+    bwd_reduce_kernel<D><<<dim3(p.nt_max, p.H), kThr, 0, s>>>(p);
+  }
+  return cudaPeekAtLastError() == cudaSuccess;
+}
+
+}  // namespace
+
+bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s) {
+  if (D == 128)
+    return bf16_inputs ? launch_bwd_t<__nv_bfloat16, 128>(p, s) : launch_bwd_t<float, 128>(p, s);
+  return bf16_inputs ? launch_bwd_t<__nv_bfloat16, 64>(p, s) : launch_bwd_t<float, 64>(p, s);
+}
+
+}  // namespace gdn

@@ -20,6 +20,7 @@
 // both factors <= 1; entries inside one 16-row block exponentiate G_i - G_j
 // directly. No factor ever exceeds 1, so no gate value can overflow.
 #include "gdn_common.cuh"
+#include "simt_tile.cuh"
 #include "tri_inverse.cuh"
 #include "umma.cuh"
 
@@ -29,75 +30,6 @@ namespace {
 
 constexpr int kThr = 256;
 constexpr uint32_t kGenWaitIters = 1u << 22;
-
-template <typename TIn>
-__device__ __forceinline__ float ld_in(const void* base, size_t idx) {
-  return to_f32(reinterpret_cast<const TIn*>(base)[idx]);
-}
-
-template <int R>
-__device__ __forceinline__ void ldv(const float* p, float (&v)[R]) {
-  if constexpr (R == 4) {
-    const float4 t = *reinterpret_cast<const float4*>(p);
-    v[0] = t.x; v[1] = t.y; v[2] = t.z; v[3] = t.w;
-  } else if constexpr (R == 2) {
-    const float2 t = *reinterpret_cast<const float2*>(p);
-    v[0] = t.x; v[1] = t.y;
-  } else {
-    v[0] = *p;
-  }
-}
-
-// acc[r][c] += sum_{k0 <= k < k1} X[k * ldx + m0 + r] * Y[k * ldy + n0 + c]: both operands
-// k-major in shared memory (a warp reads one row of each per step).
-template <int RM, int RN>
-__device__ __forceinline__ void fma_tile(float (&acc)[RM][RN], const float* X, int ldx,
-                                         const float* Y, int ldy, int m0, int n0, int k0,
-                                         int k1) {
-#pragma unroll 4
-  for (int k = k0; k < k1; ++k) {
-    float a[RM], b[RN];
-    ldv<RM>(X + k * ldx + m0, a);
-    ldv<RN>(Y + k * ldy + n0, b);
-#pragma unroll
-    for (int r = 0; r < RM; ++r)
-#pragma unroll
-      for (int c = 0; c < RN; ++c) acc[r][c] = fmaf(a[r], b[c], acc[r][c]);
-  }
-}
-
-template <int RM, int RN>
-__device__ __forceinline__ void zero(float (&acc)[RM][RN]) {
-#pragma unroll
-  for (int r = 0; r < RM; ++r)
-#pragma unroll
-    for (int c = 0; c < RN; ++c) acc[r][c] = 0.f;
-}
-
-// Resolve the chunk of this slot; returns false (after flagging) if the CTA has nothing to do.
-__device__ __forceinline__ bool resolve_slot(const Params& p, int slot, int& t0, int& L,
-                                             int& wslot) {
-  const int2 e = p.chunk_table[slot];
-  if (e.x < 0) return false;  // sentinel slot: early exit
-  if (e.x >= p.N) {
-    set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
-    return false;
-  }
-  const SeqView sv = seq_view(p, e.x);
-  const int nch = (sv.len + kChunk - 1) / kChunk;
-  if (e.y < 0 || e.y >= nch) {
-    set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
-    return false;
-  }
-  wslot = sv.first_slot + e.y;
-  if (wslot >= p.nt_max) {
-    set_status(p.status, GDN_DEV_CHUNK_OVERFLOW);
-    return false;
-  }
-  t0 = sv.start + kChunk * e.y;
-  L = min(kChunk, sv.len - kChunk * e.y);
-  return true;
-}
 
 // Shared-memory floats of the intra kernel.
 template <int D, bool CH>
@@ -405,17 +337,20 @@ template <int D>
 constexpr int scan_bv() { return D == 128 ? 32 : 16; }
 
 template <int D>
+constexpr int scan_sld() { return scan_bv<D>() + 4; }  // state row stride (fewer bank conflicts)
+
+template <int D>
 constexpr size_t scan_smem_bytes() {
-  constexpr int BV = scan_bv<D>();
-  return sizeof(float) * (2 * D * BV + 2 * D * 64 + 64 * D + 64 * 64 + 2 * 64 * BV + D) + 64;
+  constexpr int BV = scan_bv<D>(), SLD = scan_sld<D>();
+  return sizeof(float) * (2 * D * SLD + 2 * D * 64 + 64 * D + 64 * 64 + 2 * 64 * BV + D) + 64;
 }
 
 template <int D>
 __global__ void __launch_bounds__(kThr) gen_inter_kernel(Params p) {
-  constexpr int BV = scan_bv<D>();
+  constexpr int BV = scan_bv<D>(), SLD = scan_sld<D>();
   extern __shared__ __align__(16) float sm[];
-  float* S0 = sm;                    // [2][D][BV] state, double buffered
-  float* Wt = S0 + 2 * D * BV;       // [D][64] w^T
+  float* S0 = sm;                    // [2][D][SLD] state (BV columns used), double buffered
+  float* Wt = S0 + 2 * D * SLD;      // [D][64] w^T
   float* Qt = Wt + D * 64;           // [D][64] (exp(G) q)^T
   float* Kt = Qt + D * 64;           // [64][D] exp(G_L - G) k
   float* Mt = Kt + 64 * D;           // [64][64] M^T
@@ -469,16 +404,23 @@ __global__ void __launch_bounds__(kThr) gen_inter_kernel(Params p) {
   }
   for (int idx = tid; idx < D * BV; idx += kThr) {
     const int d = idx / BV, j = idx % BV;
-    S0[idx] = p.s0 ? p.s0[state_base + (size_t)(c0 + j) * D + d] : 0.f;
+    S0[d * SLD + j] = p.s0 ? p.s0[state_base + (size_t)(c0 + j) * D + d] : 0.f;
   }
   __syncthreads();
 
   bool failed = false;
   int cur = 0;
   for (int c = 0; c < nch; ++c) {
-    const float* S = S0 + cur * D * BV;
-    float* Sn = S0 + (cur ^ 1) * D * BV;
+    const float* S = S0 + cur * D * SLD;
+    float* Sn = S0 + (cur ^ 1) * D * SLD;
     float* Uc = U + (c & 1) * 64 * BV;
+    if (p.hs) {  // chunk-start state, [dv][dk] rows of the slot (for the backward pass)
+      float* hs = p.hs + slot_of(c) * D * D;
+      for (int idx = tid; idx < D * BV; idx += kThr) {
+        const int j = idx / D, d = idx % D;
+        hs[(size_t)(c0 + j) * D + d] = S[d * SLD + j];
+      }
+    }
     bool ok = mbar_wait(&bars[c & 1], (uint32_t)((c >> 1) & 1), kGenWaitIters);
     ok = ok && mbar_wait(&bars[2], (uint32_t)(c & 1), kGenWaitIters);
     if (__syncthreads_or(!ok)) {
@@ -491,13 +433,17 @@ __global__ void __launch_bounds__(kThr) gen_inter_kernel(Params p) {
       const int i0 = (tid >> 4) * 4, n0 = (tid & 15) * RN;
       float acc[4][RN];
       zero(acc);
-      fma_tile<4, RN>(acc, Wt, 64, S, BV, i0, n0, 0, D);
+      fma_tile<4, RN>(acc, Wt, 64, S, SLD, i0, n0, 0, D);
 #pragma unroll
       for (int a = 0; a < 4; ++a)
 #pragma unroll
         for (int b = 0; b < RN; ++b) Uc[(i0 + a) * BV + n0 + b] -= acc[a][b];
     }
     __syncthreads();
+    if (p.vn_out) {
+      float* vo = p.vn_out + slot_of(c) * 64 * D + c0;
+      for (int idx = tid; idx < 64 * BV; idx += kThr) vo[(idx / BV) * D + idx % BV] = Uc[idx];
+    }
     if (tid == 0 && c + 1 < nch) {
       fence_async_smem();
       issue_w(c + 1);
@@ -520,8 +466,8 @@ __global__ void __launch_bounds__(kThr) gen_inter_kernel(Params p) {
         zero(acc);
         if (t < OT) {
           const int i0 = (t >> 4) * 4, n0 = (t & 15) * RN;
-          if (i0 >= L) continue;
-          fma_tile<4, RN>(acc, Qt, 64, S, BV, i0, n0, 0, D);
+          if (i0 >= L || !p.out) continue;  // no output when only the states are wanted
+          fma_tile<4, RN>(acc, Qt, 64, S, SLD, i0, n0, 0, D);
           fma_tile<4, RN>(acc, Mt, 64, Uc, BV, i0, n0, 0, min(i0 + 4, 64));
 #pragma unroll
           for (int a = 0; a < 4; ++a) {
@@ -544,7 +490,7 @@ __global__ void __launch_bounds__(kThr) gen_inter_kernel(Params p) {
           for (int a = 0; a < 4; ++a)
 #pragma unroll
             for (int b = 0; b < RN; ++b) {
-              const int idx = (d0 + a) * BV + n0 + b;
+              const int idx = (d0 + a) * SLD + n0 + b;
               Sn[idx] = fmaf(gam[d0 + a], S[idx], acc[a][b]);
             }
         }
@@ -568,10 +514,10 @@ __global__ void __launch_bounds__(kThr) gen_inter_kernel(Params p) {
     return;
   }
   if (p.sT) {
-    const float* S = S0 + cur * D * BV;
+    const float* S = S0 + cur * D * SLD;
     for (int idx = tid; idx < D * BV; idx += kThr) {
       const int j = idx / D, d = idx % D;
-      p.sT[state_base + (size_t)(c0 + j) * D + d] = S[d * BV + j];
+      p.sT[state_base + (size_t)(c0 + j) * D + d] = S[d * SLD + j];
     }
   }
 }

@@ -202,6 +202,41 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k,
                   cudaStream_t stream);
 
 /*
+ * Workspace bytes gdn_chunk_bwd needs for this descriptor (0 if the descriptor
+ * is invalid or not supported by the backward pass).
+ */
+size_t gdn_bwd_workspace_size(const gdn_desc* desc);
+
+/*
+ * The backward pass of gdn_chunk_fwd (scalar gates; no q/k L2 norm): given the
+ * gradient of a loss with respect to out (d_out) and to final_state
+ * (d_final_state, NULL for none), the gradients with respect to q, k, v, g,
+ * beta and initial_state. It is the chunked form of the recurrence's adjoint,
+ * run as the backward kernels the FLA graph-capture RFC lists for GDN ("What
+ * needs to change": the state-gradient scan, the local dv, dq/dk/dw/dg and
+ * WY-representation gradients): a forward recompute that keeps each chunk's
+ * start state and v_new, a reverse scan over the chunks for the state
+ * gradient, and per-chunk kernels for the rest, all in fp32 arithmetic.
+ *   q, k, v, g, beta, scale, initial_state, cu_seqlens, chunk_indices
+ *                  as for gdn_chunk_fwd (the same values as the forward call)
+ *   d_out          [T, Hv, dv] in desc->out_dtype
+ *   d_final_state  fp32 [N, Hv, dv, dk] or NULL (zero)
+ *   dq, dk         fp32 [T, H, dk] (summed over the value heads of each key head)
+ *   dv             fp32 [T, Hv, dv]
+ *   dg, dbeta      fp32 [T, Hv]
+ *   d_initial_state fp32 [N, Hv, dv, dk] or NULL (not written)
+ * Rows outside the sequences are not written. desc->workspace must hold
+ * gdn_bwd_workspace_size(desc) bytes. Errors: as gdn_chunk_fwd, plus
+ * GDN_ERR_UNSUPPORTED for GDN_FLAG_CHANNEL_GATES or GDN_FLAG_QK_L2NORM.
+ */
+int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void* v,
+                  const float* g, const float* beta, float scale,
+                  const float* initial_state, const int32_t* cu_seqlens,
+                  int32_t* chunk_indices, const void* d_out, const float* d_final_state,
+                  float* dq, float* dk, float* dv, float* dg, float* dbeta,
+                  float* d_initial_state, cudaStream_t stream);
+
+/*
  * Enqueue an asynchronous copy of the device status word of the last call
  * that used desc->workspace into *host_status (pinned host memory is best).
  * The caller synchronizes the stream before reading it.
