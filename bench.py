@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--clocks-file", default=None)
+    ap.add_argument("--backward", action="store_true",
+                    help="time gdn_chunk_bwd (the backward pass) on the workload instead")
     return ap.parse_args(argv)
 
 
@@ -726,6 +728,209 @@ def run_gdn(args, ws, rank, local):
     return res
 
 
+def bwd_bytes(x):
+    """Compulsory HBM bytes of one backward call: q, k, v, g, beta, the initial state and
+    the upstream gradients in; dq, dk, dv, dg, dbeta and the initial-state gradient out."""
+    esz = 2 if x["dtype"] == "bf16" else 4
+    T, H, Hv, D, N = x["n_tokens"], x["H"], x["Hv"], x["dk"], x["N"]
+    st = N * Hv * D * D * 4
+    ins = 2 * T * H * D * esz + T * Hv * D * esz + 2 * T * Hv * 4 + st + T * Hv * D * 4 + st
+    outs = 2 * T * H * D * 4 + T * Hv * D * 4 + 2 * T * Hv * 4 + st
+    return ins + outs
+
+
+def bwd_stage_flops(x):
+    """FLOPs of the backward's three stages (64 x 64 and 64 x d products counted in full):
+    the forward recompute (intra kernel, and w S plus the state update of the scan), the
+    reverse scan (Kt dS, M^T dO, Qt^T dO, w^T dv_new) and the per-chunk kernels (the three
+    state contractions, K K^T, Q K^T, the inverse, dP, Z, T^T dv_new, T^T dw, T^T Z T^T and
+    the dq / dk products)."""
+    NT = n_chunks(x["lengths"])
+    C, D, Hv = CHUNK, x["dk"], x["Hv"]
+    intra = stage_flops(x)["intra"]
+    recompute = intra + NT * Hv * (2 * 2 * C * D * D)
+    scan = NT * Hv * (6 * C * D * D + 2 * C * C * D)
+    chunk = NT * Hv * (6 * C * D * D + 20 * C * C * D + 4 * C ** 3 + C ** 3 / 3)
+    return {"recompute": recompute, "reverse_scan": scan, "chunk_grads": chunk}
+
+
+def run_gdn_bwd(args, ws, rank, local):
+    import torch
+    from gated_delta_rule_chunk_gb300 import binding as B
+    from gated_delta_rule_chunk_gb300.build import build
+    from gated_delta_rule_chunk_gb300.inputs import WORKLOADS, make_inputs
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    build()
+    x = make_inputs(args.workload)
+    if x.get("channel_gates"):
+        raise SystemExit("the backward pass takes scalar gates")
+    gen = torch.Generator().manual_seed(77)
+    D = x["dk"]
+    do_h = torch.randn(x["T"], x["Hv"], D, generator=gen, dtype=torch.float64).float()
+    dfin_h = torch.randn(x["N"], x["Hv"], D, D, generator=gen, dtype=torch.float64).float()
+    d = {k: (x[k].to(dev) if x.get(k) is not None else None)
+         for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
+    do, dfin = do_h.to(dev), dfin_h.to(dev)
+    f32 = torch.float32
+    T, H, Hv, N = x["T"], x["H"], x["Hv"], x["N"]
+    grads = dict(dq=torch.zeros(T, H, D, dtype=f32, device=dev),
+                 dk=torch.zeros(T, H, D, dtype=f32, device=dev),
+                 dv=torch.zeros(T, Hv, D, dtype=f32, device=dev),
+                 dg=torch.zeros(T, Hv, dtype=f32, device=dev),
+                 dbeta=torch.zeros(T, Hv, dtype=f32, device=dev),
+                 d_initial_state=torch.zeros(N, Hv, D, D, dtype=f32, device=dev))
+    desc = B.make_desc(T, N, H, Hv, d["q"].dtype, f32, dk=D, dv=D)
+    wsp = torch.empty(int(B.load_library().gdn_bwd_workspace_size(__import__("ctypes").byref(desc))),
+                      dtype=torch.uint8, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def call(evs=None):
+        B.gdn_chunk_bwd(d["q"], d["k"], d["v"], d["g"], d["beta"], do, x["scale"],
+                        d["initial_state"], d["cu_seqlens"], dfin, workspace=wsp, grads=grads,
+                        stage_events=evs)
+
+    K = args.steps
+    mk = lambda n: [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(K)]
+    evs, sevs = mk(2), mk(5)
+    for row in evs + sevs:
+        for e in row:
+            e.record()
+    torch.cuda.synchronize()
+    for i in range(args.warmup):
+        flush.fill_(i & 255)
+        call()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local, args.clocks_file)
+    clocks.start()
+    barrier(ws)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(K):
+        flush.fill_((i + 1) & 255)
+        evs[i][0].record(stream)
+        call()
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(ws)
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    for i in range(K):
+        flush.fill_((i + 1) & 255)
+        sevs[i][0].record(stream)
+        call([e.cuda_event for e in sevs[i][1:]])
+    torch.cuda.synchronize()
+    ms = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
+    names = ("recompute", "reverse_scan", "chunk_grads")
+    st = {nm: statistics.mean(r[j + 1].elapsed_time(r[j + 2]) for r in sevs)
+          for j, nm in enumerate(names)}
+    ms_max = max_over_ranks(ms, ws)
+    tokens = x["n_tokens"]
+    value = ws * tokens / (ms_max / 1000.0)
+
+    # end to end through host buffers: inputs and upstream gradients in, gradients out
+    host = {k: (x[k].pin_memory() if x.get(k) is not None else None)
+            for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
+    do_p, dfin_p = do_h.pin_memory(), dfin_h.pin_memory()
+    outs_h = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in grads.items()}
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    h2d += do_p.numel() * 4 + dfin_p.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in outs_h.values())
+    e2e_ms = []
+    for i in range(3 + args.e2e_steps if args.e2e_steps > 0 else 0):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for key, t in host.items():
+            if t is not None:
+                d[key].copy_(t, non_blocking=True)
+        do.copy_(do_p, non_blocking=True)
+        dfin.copy_(dfin_p, non_blocking=True)
+        call()
+        for key, t in outs_h.items():
+            t.copy_(grads[key], non_blocking=True)
+        b.record(stream)
+        b.synchronize()
+        if i >= 3:
+            e2e_ms.append(a.elapsed_time(b))
+    e2e_val = (ws * tokens / (max_over_ranks(statistics.mean(e2e_ms), ws) / 1000.0)
+               if e2e_ms else None)
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    sf = bwd_stage_flops(x)
+    dom = max(st, key=st.get)
+    achieved = sf[dom] / (st[dom] / 1000.0) / 1e12
+    alg_b, alg_f = bwd_bytes(x), sum(sf.values())
+    t_hbm = alg_b / (peaks["hbm_gbs"] * 1e9)
+    t_tc = alg_f / (peaks["bf16_tflops"] * 1e12)
+    res = {
+        "metric": f"GDN chunk backward tokens/s, {WORKLOADS[args.workload].name}; % of roofline",
+        "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_max, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic",
+        "config": {"workload": WORKLOADS[args.workload].name, "pass": "backward",
+                   "T": T, "N": N, "H": H, "Hv": Hv, "dk": D, "dv": D, "chunk": CHUNK,
+                   "qkv_dtype": x["dtype"], "grad_dtype": "fp32", "d_out_dtype": "fp32",
+                   "kernels": "fp32 SIMT: recompute, reverse scan, per-chunk gradients",
+                   "l2": "512 MiB buffer written between timed steps (L2 is 129 MB)",
+                   "parallelism": "replicas" if ws > 1 else "single GPU",
+                   "inputs": "resident in HBM"},
+        "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved,
+                     "peak": SIMT_FP32_TFLOPS, "unit": "TFLOP/s",
+                     "frac": achieved / SIMT_FP32_TFLOPS,
+                     "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz",
+                     "algorithmic_flops_per_launch": sf[dom], "traffic": None,
+                     "traffic_source": None},
+        "path_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
+                          "algorithmic_bytes": alg_b, "algorithmic_flops": alg_f,
+                          "roofline_us_measured_peaks": 1e6 * max(t_hbm, t_tc),
+                          "us_per_call": 1000.0 * ms,
+                          "frac_of_measured": max(t_hbm, t_tc) / (ms / 1000.0),
+                          "simt_alu_us": 1e6 * alg_f / (SIMT_FP32_TFLOPS * 1e12)},
+        "stages_us": {k: 1000.0 * v for k, v in st.items()},
+        "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h,
+                "ms_per_step": statistics.mean(e2e_ms) if e2e_ms else None},
+        "gpu_launches": 7 * K,   # chunk table, intra, scan, reverse scan, 3 chunk kernels
+        "clocks": clk,
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        rate, ts, dt, cores = oracle_bwd_rate(x, do_h, dfin_h, args.cpu_seconds)
+        res["cpu_baseline"] = {
+            "value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {ts} tokens of the workload, all {Hv} value heads, backward "
+                      f"({dt:.1f} s of fp64 C on the host cores)"}
+    return res
+
+
+def oracle_bwd_rate(x, do, dfin, seconds):
+    """Time the oracle's backward on the first T_s tokens (all heads), T_s sized from a probe."""
+    import oracle
+    import torch
+
+    def run(ts):
+        cu = torch.tensor([0, ts], dtype=torch.int32)
+        sl = slice(0, ts)
+        s0 = x["initial_state"][:1] if x["initial_state"] is not None else None
+        t = time.perf_counter()
+        oracle.recurrent_backward(x["q"][sl], x["k"][sl], x["v"][sl], x["g"][sl],
+                                  x["beta"][sl], x["scale"], s0, cu, do[sl], dfin[:1])
+        return time.perf_counter() - t
+
+    oracle.build()
+    probe = min(64, x["n_tokens"])
+    dt = run(probe)
+    ts = int(max(16, min(x["n_tokens"], probe * seconds / max(dt, 1e-6))))
+    ts = max(16, ts // 16 * 16)
+    dt = run(ts)
+    return ts / dt, ts, dt, oracle.max_threads()
+
+
 def main(argv=None):
     args = parse_args(argv)
     ws, rank, local = dist_env()
@@ -745,6 +950,8 @@ def main(argv=None):
                 res = run_recurrent(args, ws, rank, local)
             elif WORKLOADS[args.workload].kind == "conv":
                 res = run_conv(args, ws, rank, local)
+            elif args.backward:
+                res = run_gdn_bwd(args, ws, rank, local)
             else:
                 res = run_gdn(args, ws, rank, local)
         if rank == 0 and res is not None:

@@ -316,7 +316,8 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   d_final_state: Optional[torch.Tensor] = None,
                   chunk_indices: Optional[torch.Tensor] = None, nt_max: int = 0,
                   workspace: Optional[torch.Tensor] = None, stream=None,
-                  return_desc: bool = False):
+                  return_desc: bool = False, grads: Optional[dict] = None,
+                  stage_events=None):
     """Backward of gdn_chunk_fwd through the C ABI (scalar gates, no L2 norm).
 
     Same inputs as the forward call plus d_out [T, Hv, d] (fp32 or bf16) and
@@ -333,7 +334,7 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
             raise ValueError(f"{name} must be a contiguous CUDA tensor")
     dev = q.device
     f32 = torch.float32
-    grads = dict(dq=torch.zeros(T, H, dk, dtype=f32, device=dev),
+    grads = grads if grads is not None else dict(dq=torch.zeros(T, H, dk, dtype=f32, device=dev),
                  dk=torch.zeros(T, H, dk, dtype=f32, device=dev),
                  dv=torch.zeros(T, Hv, dv, dtype=f32, device=dev),
                  dg=torch.zeros(T, Hv, dtype=f32, device=dev),
@@ -346,6 +347,10 @@ def gdn_chunk_bwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
         workspace = torch.empty(n, dtype=torch.uint8, device=dev)
     desc.workspace = workspace.data_ptr()
     desc.workspace_bytes = workspace.numel()
+    ev_arr = None
+    if stage_events is not None:
+        ev_arr = (ctypes.c_void_p * GDN_NUM_STAGE_EVENTS)(*[int(e) for e in stage_events])
+        desc.stage_events = ctypes.cast(ev_arr, ctypes.c_void_p)
     if scale is None:
         scale = 1.0 / math.sqrt(dk)
     rc = load_library().gdn_chunk_bwd(

@@ -326,14 +326,17 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.w = ws + L.w; p.u = f32(L.u); p.M = ws + L.M;
   p.qt = f32(L.qt); p.kt = f32(L.kt); p.gam = f32(L.gam);
   p.hs = f32(B.hs); p.vn_out = f32(B.vn);
+  cudaEvent_t* ev = d.stage_events;
   if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return GDN_ERR_LAUNCH_FAILED;
+  if (ev) cudaEventRecord(ev[0], stream);
   launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
                      (!chunk_indices || build_into_caller) ? table : nullptr,
                      const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
                      p.status, stream);
   if (nt_max > 0 && !launch_gen_intra(p, D, false, bf16, stream)) return GDN_ERR_LAUNCH_FAILED;
   if (!launch_gen_inter(p, D, stream)) return GDN_ERR_LAUNCH_FAILED;
+  if (ev) cudaEventRecord(ev[1], stream);
 
   BwdParams b{};
   b.T = d.T; b.N = d.N; b.H = d.H; b.Hv = d.Hv; b.HG = p.HG; b.nt_max = nt_max;
@@ -347,7 +350,7 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   b.dvn = f32(B.dvn); b.dhs = f32(B.dhs); b.dos = f32(B.dos); b.dw = f32(B.dw);
   b.ys = f32(B.ys); b.sdot = f32(B.sdot); b.ttdw = f32(B.ttdw);
   b.dqp = f32(B.dqp); b.dkp = f32(B.dkp);
-  if (!launch_bwd(b, D, bf16, stream)) return GDN_ERR_LAUNCH_FAILED;
+  if (!launch_bwd(b, D, bf16, stream, ev ? ev + 2 : nullptr)) return GDN_ERR_LAUNCH_FAILED;
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 

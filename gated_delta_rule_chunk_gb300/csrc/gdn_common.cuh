@@ -212,7 +212,8 @@ void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, int D,
                    float* qrn, float* krn, cudaStream_t s);
 bool launch_gen_intra(const Params& p, int D, bool channel_gates, bool bf16_inputs, cudaStream_t s);
 bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
-bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s);
+// ev: null, or two events recorded after the reverse scan and after the chunk kernels.
+bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s, cudaEvent_t* ev);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, cudaStream_t s);
 bool launch_recurrent(const RecParams& p, cudaStream_t s);

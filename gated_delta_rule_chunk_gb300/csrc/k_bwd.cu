@@ -575,7 +575,7 @@ __global__ void __launch_bounds__(kThr) bwd_reduce_kernel(BwdParams p) {
 }
 
 template <typename TIn, int D>
-bool launch_bwd_t(const BwdParams& p, cudaStream_t s) {
+bool launch_bwd_t(const BwdParams& p, cudaStream_t s, cudaEvent_t* ev) {
   constexpr int BV = bv_of<D>();
   const int s1 = (int)(scan_floats<D>() * sizeof(float));
   const int s2 = (int)(state_floats<D>() * sizeof(float));
@@ -584,20 +584,24 @@ bool launch_bwd_t(const BwdParams& p, cudaStream_t s) {
   ensure_smem_limit((const void*)bwd_state_kernel<D>, s2);
   ensure_smem_limit((const void*)bwd_chunk_kernel<TIn, D>, s3);
   bwd_scan_kernel<D><<<dim3(p.N, p.Hv, D / BV), kThr, s1, s>>>(p);
+  if (ev) cudaEventRecord(ev[0], s);
   if (p.nt_max > 0) {
     bwd_state_kernel<D><<<dim3(p.nt_max, p.Hv), kThr, s2, s>>>(p);
     bwd_chunk_kernel<TIn, D><<<dim3(p.nt_max, p.Hv), kThr, s3, s>>>(p);
     bwd_reduce_kernel<D><<<dim3(p.nt_max, p.H), kThr, 0, s>>>(p);
   }
+  if (ev) cudaEventRecord(ev[1], s);
   return cudaPeekAtLastError() == cudaSuccess;
 }
 
 }  // namespace
 
-bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s) {
+bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s, cudaEvent_t* ev) {
   if (D == 128)
-    return bf16_inputs ? launch_bwd_t<__nv_bfloat16, 128>(p, s) : launch_bwd_t<float, 128>(p, s);
-  return bf16_inputs ? launch_bwd_t<__nv_bfloat16, 64>(p, s) : launch_bwd_t<float, 64>(p, s);
+    return bf16_inputs ? launch_bwd_t<__nv_bfloat16, 128>(p, s, ev)
+                       : launch_bwd_t<float, 128>(p, s, ev);
+  return bf16_inputs ? launch_bwd_t<__nv_bfloat16, 64>(p, s, ev)
+                     : launch_bwd_t<float, 64>(p, s, ev);
 }
 
 }  // namespace gdn

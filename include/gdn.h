@@ -226,7 +226,9 @@ size_t gdn_bwd_workspace_size(const gdn_desc* desc);
  *   dg, dbeta      fp32 [T, Hv]
  *   d_initial_state fp32 [N, Hv, dv, dk] or NULL (not written)
  * Rows outside the sequences are not written. desc->workspace must hold
- * gdn_bwd_workspace_size(desc) bytes. Errors: as gdn_chunk_fwd, plus
+ * gdn_bwd_workspace_size(desc) bytes. desc->stage_events, when set, are recorded
+ * before the forward recompute and after it, after the reverse scan and after
+ * the per-chunk gradient kernels. Errors: as gdn_chunk_fwd, plus
  * GDN_ERR_UNSUPPORTED for GDN_FLAG_CHANNEL_GATES or GDN_FLAG_QK_L2NORM.
  */
 int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void* v,
