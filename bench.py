@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="target CPU time of the oracle baseline sample")
     ap.add_argument("--clocks-file", default=None)
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (smaller cases for profiling)")
     ap.add_argument("--backward", action="store_true",
                     help="time gdn_chunk_bwd (the backward pass) on the workload instead")
     return ap.parse_args(argv)
@@ -137,10 +139,10 @@ def stage_bytes(x, out_bytes=2):
 # when the source has changed since, the figure no longer applies and is not reported.
 NCU_TRAFFIC = {
     "inter": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_inter.cu",
-              "sha1": "41d43b926d39a4e76727a2bce7cf3701a61c66f4", "bytes": 195343872,
+              "sha1": "6966dd1ea35bd6053d2a9cc3f646e6897c92e6be", "bytes": 191513600,
               "profile": "profiles/tc_inter_kernel_T4096_H16_Hv32.md"},
     "intra": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_intra.cu",
-              "sha1": "3c8f81595559a68767530340128566c168a2e381", "bytes": 161003776,
+              "sha1": "6955f0345004d854d0532d6b8af22b43b6f26286", "bytes": 159259648,
               "profile": "profiles/tc_intra_kernel_T4096_H16_Hv32.md"},
 }
 NCU_WORKLOAD = 2
@@ -283,7 +285,7 @@ def run_reference(args, ws, rank):
     from gated_delta_rule_chunk_gb300.inputs import WORKLOADS, make_inputs
     if rank != 0:
         return None
-    x = make_inputs(args.workload)
+    x = make_inputs(args.workload, T=args.tokens)
     budget = 150.0 / max(1, args.steps + args.warmup)   # whole run within a few minutes
     rate0, ts, dt, cores, _ = oracle_rate(x, min(budget, args.cpu_seconds))
     import oracle
@@ -341,7 +343,7 @@ def run_recurrent(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build()
-    x = make_inputs(args.workload)
+    x = make_inputs(args.workload, T=args.tokens)
     d = {k: (x[k].to(dev) if x.get(k) is not None else None)
          for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
     out = torch.empty(x["T"], x["Hv"], 128, dtype=torch.bfloat16, device=dev)
@@ -565,7 +567,7 @@ def run_gdn(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build()
-    x = make_inputs(args.workload)
+    x = make_inputs(args.workload, T=args.tokens)
     d = {k: (x[k].to(dev) if x.get(k) is not None else None)
          for k in ("q", "k", "v", "g", "beta", "initial_state", "cu_seqlens")}
     D = x["dk"]
@@ -765,7 +767,7 @@ def run_gdn_bwd(args, ws, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     build()
-    x = make_inputs(args.workload)
+    x = make_inputs(args.workload, T=args.tokens)
     if x.get("channel_gates"):
         raise SystemExit("the backward pass takes scalar gates")
     gen = torch.Generator().manual_seed(77)
