@@ -103,8 +103,9 @@ SIMT_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def uses_tc_path(x):
-    """The bf16 tensor-core kernels serve d = 128 with scalar gates; the rest is SIMT."""
-    return x["dtype"] == "bf16" and x["dk"] == 128 and not x.get("channel_gates")
+    """The bf16 tensor-core kernels serve scalar gates (d = 64 zero-padded to 128); the
+    rest is SIMT."""
+    return x["dtype"] == "bf16" and not x.get("channel_gates")
 
 
 def stage_bytes(x, out_bytes=2):
@@ -121,8 +122,9 @@ def stage_bytes(x, out_bytes=2):
     s_in = states if x["initial_state"] is not None else 0
     g_b = T * Hv * (dk if x.get("channel_gates") else 1) * 4
     if uses_tc_path(x):
-        bridge = NT * Hv * (CHUNK * dk * 2 + CHUNK * dv * 4 + CHUNK * CHUNK * 4 + CHUNK * 4)
-        k16 = NT * H * CHUNK * dk * 2
+        # the bridge is 128 wide (a head of 64 runs zero-padded to 128)
+        bridge = NT * Hv * (CHUNK * 128 * 2 + CHUNK * 128 * 4 + CHUNK * CHUNK * 4 + CHUNK * 4)
+        k16 = NT * H * CHUNK * 128 * 2
         intra = q + k + T * Hv * dv * esz + g_b + T * Hv * 4 + bridge + k16
         inter = q + k16 + bridge + s_in + states + T * Hv * dv * out_bytes
     else:

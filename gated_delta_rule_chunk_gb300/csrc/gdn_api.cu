@@ -48,11 +48,13 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads) {
+// 3-D map of a bf16 [rows, heads, D] tensor with 64 x 1 x 64 boxes (a box at x = 64 of a
+// D = 64 tensor lies wholly outside it and reads zeros).
+bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads, int D) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)kDk, (cuuint64_t)heads, (cuuint64_t)rows};
-  const cuuint64_t strides[2] = {(cuuint64_t)kDk * 2, (cuuint64_t)heads * kDk * 2};
+  const cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)heads, (cuuint64_t)rows};
+  const cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)heads * D * 2};
   const cuuint32_t box[3] = {64, 1, 64};
   const cuuint32_t estr[3] = {1, 1, 1};
   return fn(static_cast<CUtensorMap*>(tmap), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3,
@@ -120,10 +122,10 @@ int nt_max_of(const gdn_desc* d) {
 
 bool channel_gates(const gdn_desc* d) { return (d->flags & GDN_FLAG_CHANNEL_GATES) != 0; }
 
-// The tensor-core path serves bf16 inputs with dk = 128 and a scalar gate; every
-// other case (fp32 inputs, dk = 64, per-channel gates) takes the fp32 SIMT path.
+// The tensor-core path serves bf16 inputs with a scalar gate (a head of 64 zero-padded
+// to 128); the other cases (fp32 inputs, per-channel gates) take the fp32 SIMT path.
 bool uses_tc_path(const gdn_desc* d) {
-  return d->qkv_dtype == GDN_BF16 && d->dk == kDk && !channel_gates(d);
+  return d->qkv_dtype == GDN_BF16 && !channel_gates(d);
 }
 
 // The token-serial and front-end kernels are built for dk = dv = 128 and scalar gates.
@@ -229,6 +231,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
 
   Params p{};
   p.T = d.T; p.N = d.N; p.H = d.H; p.Hv = d.Hv; p.HG = d.Hv / d.H; p.nt_max = nt_max;
+  p.D = d.dk;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.scale = scale;
   p.s0 = initial_state; p.out = out; p.sT = final_state;
   p.status = reinterpret_cast<int32_t*>(ws + L.status);
@@ -315,6 +318,7 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   // forward recompute: the SIMT intra kernel and the scan, keeping S and v_new per chunk
   Params p{};
   p.T = d.T; p.N = d.N; p.H = d.H; p.Hv = d.Hv; p.HG = d.Hv / d.H; p.nt_max = nt_max;
+  p.D = D;
   p.q = q; p.k = k; p.v = v; p.g = g; p.beta = beta; p.scale = scale;
   p.s0 = initial_state; p.out = nullptr; p.sT = nullptr;
   p.status = reinterpret_cast<int32_t*>(ws + L.status);

@@ -17,6 +17,7 @@ constexpr int kDv = 128;     // value head dimension
 // Everything a kernel needs, passed by value. Pointers are device pointers.
 struct Params {
   int T, N, H, Hv, HG, nt_max;
+  int D;                     // head size of the tensors in memory (dk = dv; 64 or 128)
   const void* q;
   const void* k;
   const void* v;
@@ -130,9 +131,10 @@ struct WsLayout {
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Layout for a problem with head size D. The tensor-core path (D = 128) stores w
-// in bf16, M as a hi/lo bf16 pair and the in-chunk gate sums G; the fp32 SIMT
-// path stores w^T, u, M^T and the decayed q / k images and exp(G_L) in fp32.
+// Layout for a problem with head size D. The tensor-core path stores w in bf16, M as
+// a hi/lo bf16 pair and the in-chunk gate sums G, always at head size 128 (a head of
+// 64 runs zero-padded to 128: the tensor maps fill the missing half with zeros); the
+// fp32 SIMT path stores w^T, u, M^T and the decayed q / k images and exp(G_L) in fp32.
 inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path, bool l2norm,
                           int D = kDk) {
   WsLayout L{};
@@ -144,8 +146,9 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
   L.chunk_table = take(sizeof(int2) * (size_t)nt_max);
   const size_t slots = (size_t)nt_max * (size_t)Hv;
   L.G = tc_path ? take(sizeof(float) * slots * kChunk) : 0;
-  L.w = take((tc_path ? 2 : 4) * slots * kChunk * D);
-  L.u = take(sizeof(float) * slots * kChunk * D);
+  const size_t Dw = tc_path ? kDk : D;
+  L.w = take((tc_path ? 2 : 4) * slots * kChunk * Dw);
+  L.u = take(sizeof(float) * slots * kChunk * Dw);
   L.M = take(4 * slots * kChunk * kChunk);
   L.k16 = tc_path ? take((size_t)nt_max * H * kChunk * kDk * 2) : 0;
   L.qt = tc_path ? 0 : take(sizeof(float) * slots * kChunk * D);
@@ -221,7 +224,7 @@ bool launch_conv_front(const ConvParams& p, cudaStream_t s);
 
 // Encode a TMA tensor map over a bf16 [rows, heads, 128] tensor with a box of
 // 64 rows x 1 head x 64 elements and the 128-byte swizzle. False on failure.
-bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads);
+bool encode_rows_tmap(void* tmap, const void* base, int rows, int heads, int D);
 // Plain 2-D tensor map over a row-major [rows, cols] bf16 or fp32 matrix (no swizzle).
 bool encode_2d_tmap(void* tmap, const void* base, bool bf16, int cols, int rows, int box_cols,
                     int box_rows);

@@ -180,7 +180,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x, hv = blockIdx.y, jb = blockIdx.z, c0 = jb * BV;
   const int h = hv / p.HG;
-  const size_t state_base = ((size_t)n * p.Hv + hv) * kDv * kDk;
+  const size_t state_base = ((size_t)n * p.Hv + hv) * p.D * p.D;  // key rows >= D are padding
   const uint32_t sbase = smem_addr(sm);
   const int g = lane >> 2, c2 = 2 * (lane & 3);
 
@@ -217,7 +217,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int d = 16 * warp + g + (e >> 1) * 8, j = 8 * nt + c2 + (e & 1);
-        S[nt][e] = p.s0 ? p.s0[state_base + (size_t)(c0 + j) * kDk + d] : 0.f;
+        S[nt][e] = (p.s0 && d < p.D) ? p.s0[state_base + (size_t)(c0 + j) * p.D + d] : 0.f;
       }
     const int mt = warp & 3, np = warp >> 2;  // X tile: token rows 16mt.., columns 16np..
     auto store_split_state = [&](int buf) {
@@ -347,7 +347,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int d = 16 * warp + g + (e >> 1) * 8, j = 8 * nt + c2 + (e & 1);
-          p.sT[state_base + (size_t)(c0 + j) * kDk + d] = S[nt][e];
+          if (d < p.D) p.sT[state_base + (size_t)(c0 + j) * p.D + d] = S[nt][e];
         }
     }
   } else if (warp < kLoadWarp) {
@@ -386,7 +386,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         float o[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) o[j] = p.scale * (e * qs[j] + m[j]);
-        const size_t oi = ((size_t)(t0 + i) * p.Hv + hv) * kDv + c0;
+        const size_t oi = ((size_t)(t0 + i) * p.Hv + hv) * p.D + c0;
         if (p.out_bf16) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + oi);
 #pragma unroll
@@ -513,9 +513,9 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 bool launch_tc_inter(const Params& p, cudaStream_t s) {
   CUtensorMap tmq;
   const int rows = p.T > 0 ? p.T : 1;  // with T = 0 no tile is ever loaded
-  if (!encode_rows_tmap(&tmq, p.q, rows, p.H)) return false;
+  if (!encode_rows_tmap(&tmq, p.q, rows, p.H, p.D)) return false;
   ensure_smem_limit((const void*)tc_inter_kernel, (int)kSmemBytes);
-  return launch_pdl(tc_inter_kernel, dim3(p.N, p.Hv, kDv / BV), dim3(kThreads), kSmemBytes, s, p,
+  return launch_pdl(tc_inter_kernel, dim3(p.N, p.Hv, p.D / BV), dim3(kThreads), kSmemBytes, s, p,
                     tmq) == cudaSuccess;
 }
 

@@ -470,8 +470,9 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 bool launch_tc_intra(const Params& p, cudaStream_t s) {
   CUtensorMap tmk, tmq, tmv;
   const int rows = p.T > 0 ? p.T : 1;  // with T = 0 every slot is a sentinel
-  if (!encode_rows_tmap(&tmk, p.k, rows, p.H) || !encode_rows_tmap(&tmq, p.q, rows, p.H) ||
-      !encode_rows_tmap(&tmv, p.v, rows, p.Hv))
+  if (!encode_rows_tmap(&tmk, p.k, rows, p.H, p.D) ||
+      !encode_rows_tmap(&tmq, p.q, rows, p.H, p.D) ||
+      !encode_rows_tmap(&tmv, p.v, rows, p.Hv, p.D))
     return false;
   ensure_smem_limit((const void*)tc_intra_kernel, (int)kSmemBytes);
   return launch_pdl(tc_intra_kernel, dim3(p.H, p.nt_max), dim3(128), kSmemBytes, s, p, tmk,
