@@ -24,6 +24,7 @@
 #include "gdn_common.cuh"
 #include "simt_tile.cuh"
 #include "tri_inverse.cuh"
+#include "umma.cuh"
 
 namespace gdn {
 
@@ -76,21 +77,33 @@ __global__ void __launch_bounds__(kThr) bwd_scan_kernel(BwdParams p) {
     const size_t sl = (size_t)(sv.first_slot + c) * p.Hv + hv;
     const int t0 = sv.start + kChunk * c;
     const int L = min(kChunk, sv.len - kChunk * c);
-    for (int idx = tid; idx < 64 * D; idx += kThr) {
-      const int r = idx / D, f = idx % D;          // Kt rows, lanes along features
-      KtT[f * 68 + r] = p.kt[sl * 64 * D + idx];
-      const int fq = idx / 64, t = idx % 64;       // Qt^T and w^T rows, lanes along tokens
-      Qr[t * LQ + fq] = p.qt[sl * 64 * D + idx];
-      Wr[t * LQ + fq] = p.wT[sl * 64 * D + idx];
+    if (tid == 0 && c > 0) {  // the next (earlier) chunk's tiles into L2 while this one runs
+      const size_t pl = sl - p.Hv;
+      bulk_prefetch_l2(p.kt + pl * 64 * D, 64 * D * 4);
+      bulk_prefetch_l2(p.qt + pl * 64 * D, 64 * D * 4);
+      bulk_prefetch_l2(p.wT + pl * 64 * D, 64 * D * 4);
+      bulk_prefetch_l2(p.MT + pl * 4096, 4096 * 4);
     }
-    for (int idx = tid; idx < 64 * 64; idx += kThr) {
-      const int i = idx >> 6, t = idx & 63;        // M^T[i][t] = M[t][i]
-      Mr[t * 68 + i] = p.MT[sl * 4096 + idx];
-    }
-    for (int idx = tid; idx < 64 * BV; idx += kThr) {
-      const int i = idx / BV, j = idx % BV;
-      dO[idx] = i < L ? ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + c0 + j) : 0.f;
-    }
+    const float* kt = p.kt + sl * 64 * D;
+    const float* qt = p.qt + sl * 64 * D;
+    const float* wt = p.wT + sl * 64 * D;
+    const float* mt = p.MT + sl * 4096;
+    // Kt rows (lanes along features) into Kt^T; Qt^T and w^T rows (lanes along tokens)
+    // into token-major tiles; M^T[i][t] = M[t][i] into M
+    staged_copy<8>(64 * D, tid, kThr, [&](int i) { return kt[i]; },
+                   [&](int i, float x) { KtT[(i % D) * 68 + i / D] = x; });
+    staged_copy<8>(64 * D, tid, kThr, [&](int i) { return qt[i]; },
+                   [&](int i, float x) { Qr[(i % 64) * LQ + i / 64] = x; });
+    staged_copy<8>(64 * D, tid, kThr, [&](int i) { return wt[i]; },
+                   [&](int i, float x) { Wr[(i % 64) * LQ + i / 64] = x; });
+    staged_copy<8>(64 * 64, tid, kThr, [&](int i) { return mt[i]; },
+                   [&](int i, float x) { Mr[(i & 63) * 68 + (i >> 6)] = x; });
+    staged_copy<8>(64 * BV, tid, kThr,
+                   [&](int i) {
+                     return i / BV < L ? ld_dout(p, ((size_t)(t0 + i / BV) * p.Hv + hv) * D + c0 + i % BV)
+                                       : 0.f;
+                   },
+                   [&](int i, float x) { dO[i] = x; });
     for (int d = tid; d < D; d += kThr) gm[d] = p.gam[sl * D + d];
     __syncthreads();
     {  // the incoming gradient is this chunk's dS_next; keep it for the chunk kernels
@@ -165,12 +178,13 @@ __global__ void __launch_bounds__(kThr) bwd_state_kernel(BwdParams p) {
   int t0, L, wslot;
   if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
   const size_t sl = (size_t)wslot * p.Hv + hv;
-  for (int idx = tid; idx < 64 * D; idx += kThr) {
-    const int i = idx / D, f = idx % D;
-    dOT[f * 68 + i] = i < L ? ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + f) : 0.f;
-    vnT[f * 68 + i] = p.vn[sl * 64 * D + idx];
-    dvT[f * 68 + i] = p.dvn[sl * 64 * D + idx];
-  }
+  staged_copy<8>(64 * D, tid, kThr,
+                 [&](int i) { return i / D < L ? ld_dout(p, ((size_t)(t0 + i / D) * p.Hv + hv) * D + i % D) : 0.f; },
+                 [&](int i, float x) { dOT[(i % D) * 68 + i / D] = x; });
+  staged_copy<8>(64 * D, tid, kThr, [&](int i) { return p.vn[sl * 64 * D + i]; },
+                 [&](int i, float x) { vnT[(i % D) * 68 + i / D] = x; });
+  staged_copy<8>(64 * D, tid, kThr, [&](int i) { return p.dvn[sl * 64 * D + i]; },
+                 [&](int i, float x) { dvT[(i % D) * 68 + i / D] = x; });
   const int i0 = (tid >> 4) * 4, d0 = (tid & 15) * RN;
   float aos[4][RN], aw[4][RN], ay[4][RN];
   zero(aos);
@@ -249,17 +263,13 @@ constexpr size_t chunk_floats() {
 // chunk past L are zero). get(i, f) returns the value of token i, feature f.
 template <typename Get>
 __device__ __forceinline__ void load_fm(float* dst, int L, int tid, Get get) {
-  for (int idx = tid; idx < 64 * 32; idx += kThr) {
-    const int i = idx >> 5, f = idx & 31;
-    dst[f * kLd + i] = i < L ? get(i, f) : 0.f;
-  }
+  staged_copy<8>(64 * 32, tid, kThr, [&](int idx) { return (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f; },
+                 [&](int idx, float x) { dst[(idx & 31) * kLd + (idx >> 5)] = x; });
 }
 template <typename Get>
 __device__ __forceinline__ void load_tm(float* dst, int L, int tid, Get get) {
-  for (int idx = tid; idx < 64 * 32; idx += kThr) {
-    const int i = idx >> 5, f = idx & 31;
-    dst[i * kLt + f] = i < L ? get(i, f) : 0.f;
-  }
+  staged_copy<8>(64 * 32, tid, kThr, [&](int idx) { return (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f; },
+                 [&](int idx, float x) { dst[(idx >> 5) * kLt + (idx & 31)] = x; });
 }
 
 template <typename TIn, int D>

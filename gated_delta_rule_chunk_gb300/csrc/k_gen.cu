@@ -60,11 +60,14 @@ __global__ void __launch_bounds__(kThr) gen_intra_kernel(Params p) {
   auto qk_row_scale = [&](const float* rn, int i) {
     return rn ? rn[(size_t)(t0 + i) * p.H + h] : 1.f;
   };
-  for (int idx = tid; idx < 64 * D; idx += kThr) {
-    const int i = idx / D, d = idx % D;
-    Kr[idx] = i < L ? ld_in<TIn>(p.k, ((size_t)(t0 + i) * p.H + h) * D + d) * qk_row_scale(p.krn, i)
-                    : 0.f;
-  }
+  staged_copy<8>(64 * D, tid, kThr,
+                 [&](int idx) {
+                   const int i = idx / D;
+                   return i < L ? ld_in<TIn>(p.k, ((size_t)(t0 + i) * p.H + h) * D + idx % D) *
+                                      qk_row_scale(p.krn, i)
+                                : 0.f;
+                 },
+                 [&](int idx, float x) { Kr[idx] = x; });
 
   for (int r = 0; r < p.HG; ++r) {
     const int hv = h * p.HG + r;
@@ -77,10 +80,12 @@ __global__ void __launch_bounds__(kThr) gen_intra_kernel(Params p) {
     for (int idx = tid; idx < 64 * 65; idx += kThr) A[idx] = 0.f;
     for (int idx = tid; idx < 64 * 64; idx += kThr) TT[idx] = 0.f;
     if constexpr (CH) {  // gate rows in (coalesced), zero past the chunk end
-      for (int idx = tid; idx < 64 * D; idx += kThr) {
-        const int i = idx / D;
-        Gc[idx] = i < L ? p.g[((size_t)(t0 + i) * p.Hv + hv) * D + idx % D] : 0.f;
-      }
+      staged_copy<8>(64 * D, tid, kThr,
+                     [&](int idx) {
+                       const int i = idx / D;
+                       return i < L ? p.g[((size_t)(t0 + i) * p.Hv + hv) * D + idx % D] : 0.f;
+                     },
+                     [&](int idx, float x) { Gc[idx] = x; });
     }
     __syncthreads();
     if constexpr (CH) {  // inclusive cumsum along the chunk, one thread per channel
@@ -107,15 +112,21 @@ __global__ void __launch_bounds__(kThr) gen_intra_kernel(Params p) {
       // ------------------------------------------------ scalar gate: k and q images [D][68]
       float* KT = E;
       float* QT = E + 68 * D;
-      {
-        const int dl = tid & 7, il = (tid >> 3) & 3, grp = tid >> 5;  // 8 groups of 8 d x 4 i
-        for (int blk = grp; blk < (D / 8) * 16; blk += kThr / 32) {
-          const int d = (blk % (D / 8)) * 8 + dl, i = (blk / (D / 8)) * 4 + il;
-          float qv = 0.f;
-          if (i < L) qv = ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + d) * qk_row_scale(p.qrn, i);
-          KT[d * 68 + i] = Kr[i * D + d];
-          QT[d * 68 + i] = qv;
-        }
+      {  // element e: lane = e % 32 covers 8 d x 4 i, e / 32 picks the (d, i) block
+        auto dof = [&](int e) { return ((e >> 5) % (D / 8)) * 8 + (e & 7); };
+        auto iof = [&](int e) { return ((e >> 5) / (D / 8)) * 4 + ((e >> 3) & 3); };
+        staged_copy<8>(64 * D, tid, kThr,
+                       [&](int e) {
+                         const int i = iof(e);
+                         return i < L ? ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + dof(e)) *
+                                            qk_row_scale(p.qrn, i)
+                                      : 0.f;
+                       },
+                       [&](int e, float x) {
+                         const int d = dof(e), i = iof(e);
+                         KT[d * 68 + i] = Kr[i * D + d];
+                         QT[d * 68 + i] = x;
+                       });
       }
       __syncthreads();
       // A and M over 4x4 tiles of the lower triangle (one tile per thread)
@@ -169,15 +180,22 @@ __global__ void __launch_bounds__(kThr) gen_intra_kernel(Params p) {
       float* FT = E + 96 * D;     // [D][96]: k_j exp(G_r - G_j), one 16-block per pair
       {
         const int dl = tid & 7, il = (tid >> 3) & 3, grp = tid >> 5;
-        for (int blk = grp; blk < (D / 8) * 12; blk += kThr / 32) {
-          const int d = (blk % (D / 8)) * 8 + dl, i = 16 + (blk / (D / 8)) * 4 + il;
-          const int ref = i & ~15;  // first row of i's block
-          const float e = __expf(Gc[i * D + d] - Gc[ref * D + d]);
-          float qv = 0.f;
-          if (i < L) qv = ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + d) * qk_row_scale(p.qrn, i);
-          EkT[d * 48 + i - 16] = Kr[i * D + d] * e;
-          EqT[d * 48 + i - 16] = qv * e;
-        }
+        auto dof = [&](int e) { return ((e >> 5) % (D / 8)) * 8 + (e & 7); };
+        auto iof = [&](int e) { return 16 + ((e >> 5) / (D / 8)) * 4 + ((e >> 3) & 3); };
+        staged_copy<8>(48 * D, tid, kThr,
+                       [&](int e) {
+                         const int i = iof(e);
+                         return i < L ? ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + dof(e)) *
+                                            qk_row_scale(p.qrn, i)
+                                      : 0.f;
+                       },
+                       [&](int e, float qv) {
+                         const int d = dof(e), i = iof(e);
+                         const int ref = i & ~15;  // first row of i's block
+                         const float ex = __expf(Gc[i * D + d] - Gc[ref * D + d]);
+                         EkT[d * 48 + i - 16] = Kr[i * D + d] * ex;
+                         EqT[d * 48 + i - 16] = qv * ex;
+                       });
         // pairs (bi, bj), bj < bi, in the order (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
         for (int blk = grp; blk < (D / 8) * 24; blk += kThr / 32) {
           const int d = (blk % (D / 8)) * 8 + dl, c = (blk / (D / 8)) * 4 + il;  // column 0..95
@@ -225,11 +243,14 @@ __global__ void __launch_bounds__(kThr) gen_intra_kernel(Params p) {
       __syncthreads();
       // q rows into E (the images are consumed)
       float* Qr = E;
-      for (int idx = tid; idx < 64 * D; idx += kThr) {
-        const int i = idx / D, d = idx % D;
-        Qr[idx] = i < L ? ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + d) * qk_row_scale(p.qrn, i)
-                        : 0.f;
-      }
+      staged_copy<8>(64 * D, tid, kThr,
+                     [&](int idx) {
+                       const int i = idx / D;
+                       return i < L ? ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + idx % D) *
+                                          qk_row_scale(p.qrn, i)
+                                    : 0.f;
+                     },
+                     [&](int idx, float x) { Qr[idx] = x; });
       __syncthreads();
       // diagonal blocks: one warp per (i, j) pair, lanes over channels
       {
@@ -308,10 +329,13 @@ __global__ void __launch_bounds__(kThr) gen_intra_kernel(Params p) {
       const int j = idx >> 6, i = idx & 63;
       TT[idx] = A[i * 65 + j] * Bt[j];
     }
-    for (int idx = tid; idx < 64 * D; idx += kThr) {
-      const int i = idx / D, d = idx % D;
-      Y[idx] = i < L ? ld_in<TIn>(p.v, ((size_t)(t0 + i) * p.Hv + hv) * D + d) : 0.f;
-    }
+    staged_copy<8>(64 * D, tid, kThr,
+                   [&](int idx) {
+                     const int i = idx / D;
+                     return i < L ? ld_in<TIn>(p.v, ((size_t)(t0 + i) * p.Hv + hv) * D + idx % D)
+                                  : 0.f;
+                   },
+                   [&](int idx, float x) { Y[idx] = x; });
     __syncthreads();
     {
       constexpr int BV = D == 128 ? 32 : 16;

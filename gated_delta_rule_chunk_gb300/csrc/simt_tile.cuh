@@ -42,6 +42,26 @@ __device__ __forceinline__ void fma_tile(float (&acc)[RM][RN], const float* X, i
   }
 }
 
+// Copy n elements with every thread keeping U loads in flight: ld(i) returns element
+// i, st(i, x) stores it (usually a transposing or converting store to shared memory).
+// A plain one-load-per-iteration loop would pay one memory latency per iteration.
+template <int U, typename Ld, typename St>
+__device__ __forceinline__ void staged_copy(int n, int tid, int nthr, Ld ld, St st) {
+  for (int base = tid; base < n; base += U * nthr) {
+    float r[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * nthr;
+      r[u] = i < n ? ld(i) : 0.f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = base + u * nthr;
+      if (i < n) st(i, r[u]);
+    }
+  }
+}
+
 template <int RM, int RN>
 __device__ __forceinline__ void zero(float (&acc)[RM][RN]) {
 #pragma unroll
