@@ -103,9 +103,10 @@ SIMT_FP32_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 
 
 def uses_tc_path(x):
-    """The bf16 tensor-core kernels serve scalar gates (d = 64 zero-padded to 128); the
-    rest is SIMT."""
-    return x["dtype"] == "bf16" and not x.get("channel_gates")
+    """bf16 inputs run on the tensor-core kernels (d = 64 zero-padded to 128; per-channel
+    gates through their own intra kernel and the scan's per-channel mode); fp32 inputs on
+    the SIMT kernels."""
+    return x["dtype"] == "bf16"
 
 
 def stage_bytes(x, out_bytes=2):
@@ -121,7 +122,13 @@ def stage_bytes(x, out_bytes=2):
     states = N * Hv * dk * dv * 4
     s_in = states if x["initial_state"] is not None else 0
     g_b = T * Hv * (dk if x.get("channel_gates") else 1) * 4
-    if uses_tc_path(x):
+    if uses_tc_path(x) and x.get("channel_gates"):
+        # per chunk and value head: w (bf16), u (fp32), M (hi/lo), the decayed k (fp16),
+        # the decayed q (bf16 hi/lo) and exp(G_L) per channel
+        bridge = NT * Hv * (16384 + 32768 + 16384 + 16384 + 32768 + 512)
+        intra = q + k + T * Hv * dv * esz + g_b + T * Hv * 4 + bridge
+        inter = bridge + s_in + states + T * Hv * dv * out_bytes
+    elif uses_tc_path(x):
         # the bridge is 128 wide (a head of 64 runs zero-padded to 128)
         bridge = NT * Hv * (CHUNK * 128 * 2 + CHUNK * 128 * 4 + CHUNK * CHUNK * 4 + CHUNK * 4)
         k16 = NT * H * CHUNK * 128 * 2

@@ -122,18 +122,17 @@ int nt_max_of(const gdn_desc* d) {
 
 bool channel_gates(const gdn_desc* d) { return (d->flags & GDN_FLAG_CHANNEL_GATES) != 0; }
 
-// The tensor-core path serves bf16 inputs with a scalar gate (a head of 64 zero-padded
-// to 128); the other cases (fp32 inputs, per-channel gates) take the fp32 SIMT path.
-bool uses_tc_path(const gdn_desc* d) {
-  return d->qkv_dtype == GDN_BF16 && !channel_gates(d);
-}
+// The tensor-core path serves bf16 inputs (a head of 64 zero-padded to 128; per-channel
+// gates through their own intra kernel and the scan's per-channel mode); fp32 inputs
+// take the fp32 SIMT path.
+bool uses_tc_path(const gdn_desc* d) { return d->qkv_dtype == GDN_BF16; }
 
 // The token-serial and front-end kernels are built for dk = dv = 128 and scalar gates.
 bool serial_shape_ok(const gdn_desc* d) { return d->dk == kDk && !channel_gates(d); }
 
 WsLayout layout_of(const gdn_desc* d) {
   return ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d),
-                   (d->flags & GDN_FLAG_QK_L2NORM) != 0, d->dk);
+                   (d->flags & GDN_FLAG_QK_L2NORM) != 0, d->dk, channel_gates(d));
 }
 
 // Workspace of the backward pass: the SIMT forward's layout, then the chunk-start
@@ -245,6 +244,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.u = reinterpret_cast<float*>(ws + L.u);
   p.M = ws + L.M;
   p.k16 = L.k16 ? ws + L.k16 : nullptr;
+  p.qimg = L.qimg ? ws + L.qimg : nullptr;
   p.qt = L.qt ? reinterpret_cast<float*>(ws + L.qt) : nullptr;
   p.kt = L.kt ? reinterpret_cast<float*>(ws + L.kt) : nullptr;
   p.gam = L.gam ? reinterpret_cast<float*>(ws + L.gam) : nullptr;
@@ -266,14 +266,15 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   const bool tc = uses_tc_path(&d);
   if (nt_max > 0) {
     if (tc) {
-      if (!launch_tc_intra(p, stream)) return GDN_ERR_LAUNCH_FAILED;
+      if (!(channel_gates(&d) ? launch_kda_intra(p, stream) : launch_tc_intra(p, stream)))
+        return GDN_ERR_LAUNCH_FAILED;
     } else if (!launch_gen_intra(p, d.dk, channel_gates(&d), bf16, stream)) {
       return GDN_ERR_LAUNCH_FAILED;
     }
   }
   if (ev) cudaEventRecord(ev[2], stream);
   if (tc) {
-    if (!launch_tc_inter(p, stream)) return GDN_ERR_LAUNCH_FAILED;
+    if (!launch_tc_inter(p, channel_gates(&d), stream)) return GDN_ERR_LAUNCH_FAILED;
   } else if (!launch_gen_inter(p, d.dk, stream)) {
     return GDN_ERR_LAUNCH_FAILED;
   }

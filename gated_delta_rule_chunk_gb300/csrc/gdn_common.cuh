@@ -35,7 +35,11 @@ struct Params {
   void* w;                   // [nt_max, Hv, 64, dk]
   float* u;                  // [nt_max, Hv, 64, dv]
   void* M;                   // [nt_max, Hv, 64, 64] (or hi/lo pair) decay-masked q.k
-  void* k16;                 // [nt_max, H] fp16 images of the chunk's k tile (tensor-core path)
+  void* k16;                 // fp16 images of the chunk's k tile (tensor-core path): per
+                             // [nt_max, H] key head, or per [nt_max, Hv] value head with
+                             // per-channel gates (the decay exp(G_L - G) applied)
+  void* qimg;                // [nt_max, Hv] bf16 hi/lo images of exp(G) q (tensor-core path,
+                             // per-channel gates)
   float* qt;                 // [nt_max, Hv, dk, 64] (exp(G) q)^T        (SIMT path)
   float* kt;                 // [nt_max, Hv, 64, dk] exp(G_L - G) k      (SIMT path)
   float* gam;                // [nt_max, Hv, dk] exp(G_L)                (SIMT path)
@@ -125,8 +129,8 @@ struct ConvParams {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qt, kt, gam, qrn, krn,
-      total;
+  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qimg, qt, kt, gam, qrn,
+      krn, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -136,7 +140,7 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // 64 runs zero-padded to 128: the tensor maps fill the missing half with zeros); the
 // fp32 SIMT path stores w^T, u, M^T and the decayed q / k images and exp(G_L) in fp32.
 inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path, bool l2norm,
-                          int D = kDk) {
+                          int D = kDk, bool channel_gates = false) {
   WsLayout L{};
   size_t o = 0;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
@@ -150,10 +154,13 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
   L.w = take((tc_path ? 2 : 4) * slots * kChunk * Dw);
   L.u = take(sizeof(float) * slots * kChunk * Dw);
   L.M = take(4 * slots * kChunk * kChunk);
-  L.k16 = tc_path ? take((size_t)nt_max * H * kChunk * kDk * 2) : 0;
+  const bool tc_ch = tc_path && channel_gates;  // per value head k images, q images, exp(G_L)
+  L.k16 = tc_path ? take((size_t)nt_max * (tc_ch ? Hv : H) * kChunk * kDk * 2) : 0;
+  L.qimg = tc_ch ? take(slots * 2 * kChunk * kDk * 2) : 0;
   L.qt = tc_path ? 0 : take(sizeof(float) * slots * kChunk * D);
   L.kt = tc_path ? 0 : take(sizeof(float) * slots * kChunk * D);
-  L.gam = tc_path ? 0 : take(sizeof(float) * slots * D);
+  L.gam = tc_path ? (tc_ch ? take(sizeof(float) * slots * kDk) : 0)
+                  : take(sizeof(float) * slots * D);
   L.qrn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
   L.krn = l2norm ? take(sizeof(float) * (size_t)T * H) : 0;
   L.total = o;
@@ -218,7 +225,8 @@ bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
 // ev: null, or two events recorded after the reverse scan and after the chunk kernels.
 bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s, cudaEvent_t* ev);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
-bool launch_tc_inter(const Params& p, cudaStream_t s);
+bool launch_tc_inter(const Params& p, bool channel_gates, cudaStream_t s);
+bool launch_kda_intra(const Params& p, cudaStream_t s);
 bool launch_recurrent(const RecParams& p, cudaStream_t s);
 bool launch_conv_front(const ConvParams& p, cudaStream_t s);
 

@@ -60,25 +60,34 @@ constexpr int kChainThreads = kChainWarps * 32;
 constexpr uint32_t kW = 0;           // w: two dk halves of [64 rows][128 B], K-major, swizzled
 constexpr uint32_t kK = 16384;       // k (fp16 image): two dk halves of [64 tokens][128 B], swizzled
 constexpr uint32_t kU = 32768;       // u block: fp32 [64][32], 16-byte chunks swizzled by row
-constexpr uint32_t kG = 40960;       // G [64]
+constexpr uint32_t kG = 40960;       // G [64] (per-channel mode: exp(G_L) [128])
 constexpr uint32_t kSlot = 41984;    // 41 x 1024
-constexpr int kRing = 3;
-constexpr uint32_t kTxRing = 2 * 8192 + 16384 + 8192 + 256;  // w, k, u, G
-// q (two buffers of two swizzled [64 rows][128 B] key-dim halves) and [M_hi; M_lo]
-// ([128 rows][128 B], swizzled) for the output MMAs.
-constexpr uint32_t kQ = kRing * kSlot;
-constexpr uint32_t kQsz = 16384;
-constexpr uint32_t kM = kQ + 2 * kQsz;
-// Operands written by the threads (no-swizzle MN-major core matrices: the K
-// group stride is the descriptor's lbo, sbo = 128 along N).
-constexpr uint32_t kSB = kM + 16384;       // 2 x [S_hi | S_lo]: N = 64, K = 128 (key dim)
 constexpr uint32_t kSBsz = 16384;
-constexpr uint32_t kVN = kSB + 2 * kSBsz;  // 2 x [vn_hi | vn_lo]: N = 64, K = 64 (tokens)
 constexpr uint32_t kVNsz = 8192;
-constexpr uint32_t kVH = kVN + 2 * kVNsz;  // vh (fp16): N = 32, K = 64 (tokens)
-constexpr uint32_t kBar = kVH + 4096;      // 19 mbarriers
-constexpr uint32_t kMisc = kBar + 256;     // TMEM base address, abort flag
-constexpr uint32_t kSmemBytes = kMisc + 16 + 1024;  // + room to align the base to 1024
+
+// The rest of the layout depends on the gate kind. Per-channel gates: the q operand is
+// the decayed q as a bf16 hi/lo pair (two 16 KB images per buffer), which the ring's
+// third slot makes room for.
+template <bool CH>
+struct Lay {
+  static constexpr int kRing = CH ? 2 : 3;
+  static constexpr uint32_t kTxRing = 2 * 8192 + 16384 + 8192 + (CH ? 512 : 256);  // w, k, u, G
+  // q (two buffers of two swizzled [64 rows][128 B] key-dim halves; hi then lo with
+  // per-channel gates) and [M_hi; M_lo] ([128 rows][128 B], swizzled) for the output MMAs.
+  static constexpr uint32_t kQ = kRing * kSlot;
+  static constexpr uint32_t kQsz = CH ? 32768 : 16384;
+  static constexpr uint32_t kM = kQ + 2 * kQsz;
+  // Operands written by the threads (no-swizzle MN-major core matrices: the K
+  // group stride is the descriptor's lbo, sbo = 128 along N).
+  static constexpr uint32_t kSB = kM + 16384;       // 2 x [S_hi | S_lo]: N = 64, K = 128
+  static constexpr uint32_t kVN = kSB + 2 * kSBsz;  // 2 x [vn_hi | vn_lo]: N = 64, K = 64
+  static constexpr uint32_t kVH = kVN + 2 * kVNsz;  // vh (fp16): N = 32, K = 64 (tokens)
+  static constexpr uint32_t kBar = kVH + 4096;      // 19 mbarriers
+  static constexpr uint32_t kMisc = kBar + 256;     // TMEM base address, abort flag
+  static constexpr uint32_t kSmemBytes = kMisc + 16 + 1024;  // + room to align the base
+};
+static_assert(Lay<true>::kSmemBytes <= 232448 && Lay<false>::kSmemBytes <= 232448,
+              "shared memory over the per-CTA limit");
 
 // mbarrier indices. Ring barriers: chunk c uses slot c % 3 with parity (c / 3) & 1;
 // double-buffered barriers: index + (c & 1) with parity (c >> 1) & 1; B_MF: one
@@ -135,32 +144,48 @@ __device__ __forceinline__ bool wait_chunk(uint64_t* bars, int base, int c,
                                            volatile int* abort_flag) {
   return wait_phase(&bars[base + (c & 1)], (uint32_t)((c >> 1) & 1), abort_flag);
 }
+template <int kRing>
 __device__ __forceinline__ bool wait_ring(uint64_t* bars, int base, int c,
                                           volatile int* abort_flag) {
   return wait_phase(&bars[base + c % kRing], (uint32_t)((c / kRing) & 1), abort_flag);
 }
 
-// Issued by one thread: the chain's copies of chunk `slot` into ring slot `st`.
+// Issued by one thread: the chain's copies of chunk `slot` into ring slot `st`. The k
+// image is per key head with a scalar gate and per value head with per-channel gates
+// (the decay is inside it); G is the in-chunk gate sum, or exp(G_L) per channel.
+template <bool CH>
 __device__ __forceinline__ void issue_ring(unsigned char* st, uint64_t* full, const Params& p,
                                            int slot, int hv, int h, int jb) {
   const size_t sl = (size_t)slot * p.Hv + hv;
   const unsigned char* wimg = static_cast<const unsigned char*>(p.w) + sl * 64 * kDk * 2;
   const unsigned char* uimg = reinterpret_cast<const unsigned char*>(p.u + sl * 64 * kDv);
-  const unsigned char* kimg =
-      static_cast<const unsigned char*>(p.k16) + ((size_t)slot * p.H + h) * 64 * kDk * 2;
-  mbar_expect_tx(full, kTxRing);
+  const unsigned char* kimg = static_cast<const unsigned char*>(p.k16) +
+                              (CH ? sl : (size_t)slot * p.H + h) * 64 * kDk * 2;
+  mbar_expect_tx(full, Lay<CH>::kTxRing);
   bulk_load(st + kW, wimg, 16384, full);
   bulk_load(st + kK, kimg, 16384, full);
   bulk_load(st + kU, uimg + jb * 8192, 8192, full);
-  bulk_load(st + kG, p.G + sl * 64, 256, full);
+  if (CH)
+    bulk_load(st + kG, p.gam + sl * 128, 512, full);
+  else
+    bulk_load(st + kG, p.G + sl * 64, 256, full);
 }
 
-// Issued by one thread: the two key-dim halves of chunk c's q tile (rows t0..t0+63).
+// Issued by one thread: chunk c's q operand. Scalar gate: the two key-dim halves of the
+// q tile (rows t0..t0+63) by tensor map; per-channel gates: the decayed q's hi and lo
+// images the intra kernel wrote for (slot, value head).
+template <bool CH>
 __device__ __forceinline__ void issue_q(unsigned char* dst, uint64_t* full, const CUtensorMap* tmq,
-                                        int h, int t0) {
-  mbar_expect_tx(full, 2 * 8192);
-  tma_load_3d(dst, tmq, 0, h, t0, full);
-  tma_load_3d(dst + 8192, tmq, 64, h, t0, full);
+                                        const Params& p, int h, int t0, int slot, int hv) {
+  if (CH) {
+    mbar_expect_tx(full, 32768);
+    bulk_load(dst, static_cast<const unsigned char*>(p.qimg) + ((size_t)slot * p.Hv + hv) * 32768,
+              32768, full);
+  } else {
+    mbar_expect_tx(full, 2 * 8192);
+    tma_load_3d(dst, tmq, 0, h, t0, full);
+    tma_load_3d(dst + 8192, tmq, 64, h, t0, full);
+  }
 }
 // Issued by one thread: the [M_hi; M_lo] image of chunk `slot`.
 __device__ __forceinline__ void issue_m(unsigned char* dst, uint64_t* full, const Params& p,
@@ -170,8 +195,13 @@ __device__ __forceinline__ void issue_m(unsigned char* dst, uint64_t* full, cons
   bulk_load(dst, static_cast<const unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2, 16384, full);
 }
 
+template <bool CH>
 __global__ void __launch_bounds__(kThreads, 1)
 tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq) {
+  using LY = Lay<CH>;
+  constexpr int kRing = LY::kRing;
+  constexpr uint32_t kQ = LY::kQ, kQsz = LY::kQsz, kM = LY::kM, kSB = LY::kSB, kVN = LY::kVN,
+                     kVH = LY::kVH, kBar = LY::kBar, kMisc = LY::kMisc;
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
@@ -243,7 +273,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       const int b = c & 1;
       unsigned char* st = sm + (c % kRing) * kSlot;
       const uint32_t st_a = sbase + (c % kRing) * kSlot;
-      wait_ring(bars, B_FULL, c, abort_flag);
+      wait_ring<kRing>(bars, B_FULL, c, abort_flag);
 
       // X = w S_hi: token rows 16mt.., columns 16np..16np+15
       float xa[2][4];
@@ -277,13 +307,13 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       if (c >= 2) wait_chunk(bars, B_MD, c - 2, abort_flag);  // vn buffer b no longer read
       {
         const float* G = reinterpret_cast<const float*>(st + kG);
-        const float gl = G[63];
         unsigned char* vn = sm + kVN + b * kVNsz;
         unsigned char* vhb = sm + kVH;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int i = 16 * mt + g + 8 * hh;
-          const float fac = expf(gl - G[i]);
+          // per-channel gates: the decay exp(G_L - G) is inside the k image
+          const float fac = CH ? 1.f : expf(G[63] - G[i]);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int j = 16 * np + 8 * q + c2;
@@ -303,11 +333,14 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 
       // S <- exp(G_L) S + K^T vh   (key rows 16*warp.., all 32 columns; fp16 operands)
       {
-        const float gam = expf(reinterpret_cast<const float*>(st + kG)[63]);
+        const float* gst = reinterpret_cast<const float*>(st + kG);
+        // scalar gate: exp(G_L) for every key row; per-channel: exp(G_L) of row d
+        const float gam0 = CH ? gst[16 * warp + g] : expf(gst[63]);
+        const float gam1 = CH ? gst[16 * warp + g + 8] : gam0;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-          for (int e = 0; e < 4; ++e) S[nt][e] *= gam;
+          for (int e = 0; e < 4; ++e) S[nt][e] *= (e >> 1) ? gam1 : gam0;
         const uint32_t kt = st_a + kK + (warp >> 2) * 8192;
         const uint32_t vhb = sbase + kVH;
 #pragma unroll
@@ -361,8 +394,9 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       const int L = min(kChunk, sv.len - kChunk * c);
       // row factor exp(G_i) / ||q_i|| straight from global memory (off the critical path)
       const size_t sl = (size_t)(sv.first_slot + c) * p.Hv + hv;
-      const float grow = p.G[sl * 64 + i];
-      const float qrow = (p.qrn && i < L) ? p.qrn[(size_t)(t0 + i) * p.H + h] : 1.f;
+      // exp(G_i) / ||q_i|| (per-channel gates: both are inside the q operand)
+      const float grow = CH ? 0.f : p.G[sl * 64 + i];
+      const float qrow = (!CH && p.qrn && i < L) ? p.qrn[(size_t)(t0 + i) * p.H + h] : 1.f;
       wait_chunk(bars, B_QSD, c, abort_flag);
       wait_chunk(bars, B_MD, c, abort_flag);
       tc_fence_after();
@@ -404,11 +438,12 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     // ring chunks issued, q tiles issued, M tiles issued
     int issued = 0, q_issued = 0, m_issued = 0;
     for (int k = 0; k < min(nch, kRing - 1); ++k) {
-      issue_ring(sm + k * kSlot, &bars[B_FULL + k], p, sv.first_slot + k, hv, h, jb);
+      issue_ring<CH>(sm + k * kSlot, &bars[B_FULL + k], p, sv.first_slot + k, hv, h, jb);
       issued = k + 1;
     }
     for (int k = 0; k < min(nch, 2); ++k) {
-      issue_q(sm + kQ + k * kQsz, &bars[B_QF + k], &tmq, h, sv.start + kChunk * k);
+      issue_q<CH>(sm + kQ + k * kQsz, &bars[B_QF + k], &tmq, p, h, sv.start + kChunk * k,
+                  sv.first_slot + k, hv);
       q_issued = k + 1;
     }
     if (nch > 0) {
@@ -418,17 +453,17 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     for (int c = 0; c < nch; ++c) {
       if (*abort_flag) break;
       if (c + kRing - 1 < nch) {  // ring slot of chunk c - 1 is free once the chain released it
-        if (c >= 1 && !wait_ring(bars, B_CD, c - 1, abort_flag)) break;
+        if (c >= 1 && !wait_ring<kRing>(bars, B_CD, c - 1, abort_flag)) break;
         const int cn = c + kRing - 1;
-        issue_ring(sm + (cn % kRing) * kSlot, &bars[B_FULL + cn % kRing], p, sv.first_slot + cn,
-                   hv, h, jb);
+        issue_ring<CH>(sm + (cn % kRing) * kSlot, &bars[B_FULL + cn % kRing], p,
+                       sv.first_slot + cn, hv, h, jb);
         issued = cn + 1;
       }
       // q buffer of chunk c - 1 is free once its D_QS completed
       if (c >= 1 && c + 1 < nch) {
         if (!wait_chunk(bars, B_QSD, c - 1, abort_flag)) break;
-        issue_q(sm + kQ + ((c + 1) & 1) * kQsz, &bars[B_QF + ((c + 1) & 1)], &tmq, h,
-                sv.start + kChunk * (c + 1));
+        issue_q<CH>(sm + kQ + ((c + 1) & 1) * kQsz, &bars[B_QF + ((c + 1) & 1)], &tmq, p, h,
+                    sv.start + kChunk * (c + 1), sv.first_slot + c + 1, hv);
         q_issued = c + 2;
       }
       // M is free once chunk c's D_M completed
@@ -464,6 +499,13 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       for (int ks = 0; ks < 8; ++ks)
         umma_bf16(tmem + b * 128, sdesc_sw128(q_a + (ks >> 2) * 8192 + 32 * (ks & 3), 16, 1024),
                   sdesc(sbb + 2048 * ks, 1024, 128), id_o, ks > 0);
+      if (CH) {  // + q_lo [S_hi | S_lo]: the decayed q is a hi/lo pair
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          umma_bf16(tmem + b * 128,
+                    sdesc_sw128(q_a + 16384 + (ks >> 2) * 8192 + 32 * (ks & 3), 16, 1024),
+                    sdesc(sbb + 2048 * ks, 1024, 128), id_o, true);
+      }
       umma_commit(&bars[B_QSD + b]);
       committed = c + 1;
     }
@@ -483,7 +525,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       const int b = c & 1;
       if (*abort_flag) break;
       wait_phase(&bars[B_MF], (uint32_t)(c & 1), abort_flag);
-      wait_ring(bars, B_CD, c, abort_flag);
+      wait_ring<kRing>(bars, B_CD, c, abort_flag);
       if (c >= 2) wait_chunk(bars, B_OD, c - 2, abort_flag);
       tc_fence_after();
       const uint32_t vnb = sbase + kVN + b * kVNsz;
@@ -508,15 +550,21 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   if (warp == kQsWarp) tmem_dealloc(tmem, kTmemCols);
 }
 
-}  // namespace
-
-bool launch_tc_inter(const Params& p, cudaStream_t s) {
+template <bool CH>
+bool launch_tc_inter_t(const Params& p, cudaStream_t s) {
   CUtensorMap tmq;
   const int rows = p.T > 0 ? p.T : 1;  // with T = 0 no tile is ever loaded
   if (!encode_rows_tmap(&tmq, p.q, rows, p.H, p.D)) return false;
-  ensure_smem_limit((const void*)tc_inter_kernel, (int)kSmemBytes);
-  return launch_pdl(tc_inter_kernel, dim3(p.N, p.Hv, p.D / BV), dim3(kThreads), kSmemBytes, s, p,
+  constexpr uint32_t smem = Lay<CH>::kSmemBytes;
+  ensure_smem_limit((const void*)tc_inter_kernel<CH>, (int)smem);
+  return launch_pdl(tc_inter_kernel<CH>, dim3(p.N, p.Hv, p.D / BV), dim3(kThreads), smem, s, p,
                     tmq) == cudaSuccess;
+}
+
+}  // namespace
+
+bool launch_tc_inter(const Params& p, bool channel_gates, cudaStream_t s) {
+  return channel_gates ? launch_tc_inter_t<true>(p, s) : launch_tc_inter_t<false>(p, s);
 }
 
 }  // namespace gdn

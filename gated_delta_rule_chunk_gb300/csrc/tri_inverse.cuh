@@ -147,11 +147,12 @@ __device__ __forceinline__ void mma_split3(float (&d)[4], const uint32_t (&ah)[4
 }
 
 // In-place inverse of I + A (64 x 64, A strictly lower triangular with zeros on and
-// above the diagonal) for a CTA of 128 threads. The four diagonal 16 x 16 blocks are
+// above the diagonal) for a CTA of 32 * kWarps threads (kWarps >= 2). The four diagonal 16 x 16 blocks are
 // inverted column by column (SIMT, fp32); block row a = 1..3 then needs two small
 // products, X = A[a, 0:a] T[0:a, 0:a] and T[a, 0:a] = -T[a, a] X, done on warp-level
 // tensor-core MMAs with the fp32 operands split into bf16 hi + lo (about 16
 // significant bits, fp32 accumulate). X: 16 rows x ld scratch.
+template <int kWarps = 4>
 __device__ inline void tri_inverse_64_tc(float* AT, int ld, float* X, int tid) {
   const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = 2 * (lane & 3);
   float col[16];
@@ -175,7 +176,7 @@ __device__ inline void tri_inverse_64_tc(float* AT, int ld, float* X, int tid) {
 #pragma unroll
   for (int a = 1; a < 4; ++a) {
     const int r0 = 16 * a;
-    for (int nt = warp; nt < 2 * a; nt += 4) {
+    for (int nt = warp; nt < 2 * a; nt += kWarps) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int ks = 0; ks < a; ++ks) {
@@ -188,7 +189,7 @@ __device__ inline void tri_inverse_64_tc(float* AT, int ld, float* X, int tid) {
       *reinterpret_cast<float2*>(&X[(g + 8) * ld + 8 * nt + c]) = make_float2(acc[2], acc[3]);
     }
     __syncthreads();
-    for (int nt = warp; nt < 2 * a; nt += 4) {
+    for (int nt = warp; nt < 2 * a; nt += kWarps) {
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
       uint32_t ah[4], al[4], bh[2], bl[2];
       frag_a_split(AT, ld, r0, r0, lane, ah, al);

@@ -84,11 +84,15 @@ def test_workspace_size(lib):
     # the bridge dominates: about 64 slots x 32 heads x 64 rows x (2 + 4 + 4 + ...) bytes
     assert a >= 64 * 32 * 64 * (128 * 2 + 128 * 4 + 64 * 4)
     assert B.gdn_workspace_size(desc(Hv=24)) == 0
-    # the SIMT path (fp32 inputs, per-channel gates) keeps fp32 w^T, u, M^T, the
-    # decayed q and k images and exp(G_L): 4 * (64 * (4 d) + 64 * 64 + d) bytes per slot
-    for dd, fl, dt in ((64, 0, torch.float32), (128, B.GDN_FLAG_CHANNEL_GATES, torch.bfloat16)):
-        n = B.gdn_workspace_size(desc(dk=dd, dv=dd, flags=fl, qkv_dtype=dt))
+    # the SIMT path (fp32 inputs) keeps fp32 w^T, u, M^T, the decayed q and k images and
+    # exp(G_L): 4 * (64 * (4 d) + 64 * 64 + d) bytes per slot
+    for dd, fl in ((64, 0), (128, B.GDN_FLAG_CHANNEL_GATES)):
+        n = B.gdn_workspace_size(desc(dk=dd, dv=dd, flags=fl, qkv_dtype=torch.float32))
         assert n >= 64 * 32 * 4 * (64 * 4 * dd + 64 * 64 + dd)
+    # bf16 with per-channel gates: the tensor-core bridge plus a k image and the decayed
+    # q's hi/lo images per value head and exp(G_L) per channel
+    n = B.gdn_workspace_size(desc(flags=B.GDN_FLAG_CHANNEL_GATES))
+    assert n >= a + 64 * 32 * (16384 + 32768 + 512) - 64 * 16 * 16384
     # bf16 with a head of 64 runs on the tensor-core kernels zero-padded to 128
     assert B.gdn_workspace_size(desc(dk=64, dv=64)) == a
 
