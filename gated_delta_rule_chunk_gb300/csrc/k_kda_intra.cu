@@ -1,5 +1,5 @@
 // Intra-chunk kernel for per-channel gates (bf16 inputs) on warp-level tensor-core
-// MMAs: one CTA of 8 warps per (chunk, value head). It writes the bridge the tensor-core
+// MMAs: one CTA of 16 warps per (chunk, value head). It writes the bridge the tensor-core
 // scan reads in its per-channel mode.
 //
 // With G the in-chunk cumulative log-decay of each key channel d (gates g <= 0, so G is
@@ -38,7 +38,8 @@ namespace gdn {
 
 namespace {
 
-constexpr int kThr = 256;
+constexpr int kThr = 512;
+constexpr int kWarps = kThr / 32;
 constexpr int LDT = 68;     // fp32 stride of the A / T tile
 constexpr int LI = 40;      // bf16 stride of image rows (80 B: ldmatrix rows conflict-free)
 constexpr int LTW = 72;     // bf16 stride of the T operand rows (144 B)
@@ -127,6 +128,7 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     tma_load_3d(sm + sV, &tmv, 0, hv, t0, bar);
     tma_load_3d(sm + sV + 8192, &tmv, 64, hv, t0, bar);
   }
+  __syncthreads();  // the barrier and the flags are initialised before anyone waits
   // gate rows (16-byte pieces; zero past the chunk end and for channels past D)
   for (int idx = tid; idx < 64 * 32; idx += kThr) {
     const int i = idx >> 5, c4 = (idx & 31) * 4;
@@ -213,9 +215,10 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
   // blocks 0-5: A of pair p, 6-11: M of pair p, 12-15: A of diagonal block b, 16-19: M
   // pairs (bi, bj), bj < bi: (1,0) (2,0) (2,1) (3,0) (3,1) (3,2)
   auto pair_bi = [](int pr) { return pr < 1 ? 1 : (pr < 3 ? 2 : 3); };
-  float acc[3][2][4];
+  constexpr int kBlkPerWarp = (20 + kWarps - 1) / kWarps;
+  float acc[kBlkPerWarp][2][4];
 #pragma unroll
-  for (int s = 0; s < 3; ++s)
+  for (int s = 0; s < kBlkPerWarp; ++s)
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -262,8 +265,8 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     }
     __syncthreads();
 #pragma unroll
-    for (int s = 0; s < 3; ++s) {
-      const int blk = warp + 8 * s;
+    for (int s = 0; s < kBlkPerWarp; ++s) {
+      const int blk = warp + kWarps * s;
       if (blk >= 20) break;
       int eR, fR;
       if (blk < 12) {
@@ -297,8 +300,8 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     const int g = lane >> 2, c = 2 * (lane & 3);
     unsigned char* mimg = sm + sM;
 #pragma unroll
-    for (int s = 0; s < 3; ++s) {
-      const int blk = warp + 8 * s;
+    for (int s = 0; s < kBlkPerWarp; ++s) {
+      const int blk = warp + kWarps * s;
       if (blk >= 20) break;
       int r0, c0;
       bool diag;
@@ -397,41 +400,43 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
   }
   __syncthreads();
 
-  const int mt = warp & 3, nh = warp >> 2;  // rows 16 mt.., columns 64 nh..64 nh + 63
+  constexpr int kNW = 128 / (kWarps / 4);  // output columns per warp (4 warps per 16-row tile)
+  constexpr int kNT = kNW / 8;              // n8 tiles per warp
+  const int mt = warp & 3, nh = warp >> 2;  // rows 16 mt.., columns kNW nh .. kNW nh + kNW - 1
   const int g = lane >> 2, c = 2 * (lane & 3);
   // ---------------- w = T diag(beta) (exp(G) k): T is lower triangular (k steps <= mt)
   {
-    float wa[8][4];
+    float wa[kNT][4];
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < kNT; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) wa[n][e] = 0.f;
     for (int ks = 0; ks <= mt; ++ks) {
       uint32_t a[4];
       load_a(a, TH, LTW, 16 * mt, 16 * ks, lane);
 #pragma unroll
-      for (int n2 = 0; n2 < 4; ++n2) {
+      for (int n2 = 0; n2 < kNT / 2; ++n2) {
         uint32_t b[4];
-        load_b_kn(b, KG, LKG, 16 * ks, 64 * nh + 16 * n2, lane);
+        load_b_kn(b, KG, LKG, 16 * ks, kNW * nh + 16 * n2, lane);
         mma_bf16(wa[2 * n2], a, b[0], b[1]);
         mma_bf16(wa[2 * n2 + 1], a, b[2], b[3]);
       }
     }
     unsigned char* wimg = reinterpret_cast<unsigned char*>(IMG + 2 * 64 * LTW);
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < kNT; ++n)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int i = 16 * mt + g + 8 * hh, col = 64 * nh + 8 * n + c;
-        *reinterpret_cast<uint32_t*>(wimg + nh * 8192 + sw_off(i, (col & 63) >> 3) + (col & 7) * 2) =
-            pack_bf16(wa[n][2 * hh], wa[n][2 * hh + 1]);
+        const int i = 16 * mt + g + 8 * hh, col = kNW * nh + 8 * n + c;
+        *reinterpret_cast<uint32_t*>(wimg + (col >> 6) * 8192 + sw_off(i, (col & 63) >> 3) +
+                                     (col & 7) * 2) = pack_bf16(wa[n][2 * hh], wa[n][2 * hh + 1]);
       }
   }
   // ---------------- u = T diag(beta) v (T hi and lo against the exact v tile)
   {
-    float ua[8][4];
+    float ua[kNT][4];
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < kNT; ++n)
 #pragma unroll
       for (int e = 0; e < 4; ++e) ua[n][e] = 0.f;
     const uint32_t vbase = smem_addr(sm + sV);
@@ -440,11 +445,11 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
       load_a(ah, TH, LTW, 16 * mt, 16 * ks, lane);
       load_a(al, TL, LTW, 16 * mt, 16 * ks, lane);
 #pragma unroll
-      for (int n2 = 0; n2 < 4; ++n2) {
+      for (int n2 = 0; n2 < kNT / 2; ++n2) {
         // B = v tile [token][value column], swizzled: rows 16 ks.., columns 16-wide group
         const int m = lane >> 3;
         const int row = 16 * ks + (lane & 7) + (m & 1) * 8;
-        const int col = 64 * nh + 16 * n2 + (m >> 1) * 8;
+        const int col = kNW * nh + 16 * n2 + (m >> 1) * 8;
         uint32_t b[4];
         ldsm_x4_t_addr(b, vbase + (col >> 6) * 8192 + sw_off(row, (col & 63) >> 3));
         mma_bf16(ua[2 * n2], ah, b[0], b[1]);
@@ -455,10 +460,10 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     }
     unsigned char* ust = sm + sG;  // the gates are consumed
 #pragma unroll
-    for (int n = 0; n < 8; ++n)
+    for (int n = 0; n < kNT; ++n)
 #pragma unroll
       for (int hh = 0; hh < 2; ++hh) {
-        const int i = 16 * mt + g + 8 * hh, col = 64 * nh + 8 * n + c;
+        const int i = 16 * mt + g + 8 * hh, col = kNW * nh + 8 * n + c;
         *reinterpret_cast<float2*>(ust + (col >> 5) * 8192 + u_offset(i, col & 31)) =
             make_float2(ua[n][2 * hh], ua[n][2 * hh + 1]);
       }
