@@ -35,6 +35,13 @@
 //   * 4 output warps (one per TMEM lane quarter; rows 16q..16q+15 of an M = 64
 //     result sit in lanes 32q..32q+15) finish chunk c's output while the chain
 //     works on chunk c + 1.
+//
+// Per-channel gates (template parameter CH): the state's key row d decays by
+// exp(G_L) of channel d; the state update's k operand is the value head's
+// exp(G_L - G) * k image (so v_new needs no row factor); the output operand is
+// exp(G) * q as a bf16 hi/lo pair written by the per-channel intra kernel (D_QS gains
+// a q_lo [S_hi | S_lo] pass and the output needs no row factor); to make room for the
+// hi/lo q buffers the ring has two slots instead of three.
 // Hand-offs use mbarriers; every wait is bounded (GDN_DEV_TIMEOUT on expiry).
 #include <cuda.h>
 

@@ -147,8 +147,9 @@ __device__ __forceinline__ void mma_split3(float (&d)[4], const uint32_t (&ah)[4
 }
 
 // In-place inverse of I + A (64 x 64, A strictly lower triangular with zeros on and
-// above the diagonal) for a CTA of 32 * kWarps threads (kWarps >= 2). The four diagonal 16 x 16 blocks are
-// inverted column by column (SIMT, fp32); block row a = 1..3 then needs two small
+// above the diagonal) for a CTA of 32 * kWarps threads (kWarps >= 2). The four
+// diagonal 16 x 16 blocks are inverted column by column (SIMT, fp32); block row
+// a = 1..3 then needs two small
 // products, X = A[a, 0:a] T[0:a, 0:a] and T[a, 0:a] = -T[a, a] X, done on warp-level
 // tensor-core MMAs with the fp32 operands split into bf16 hi + lo (about 16
 // significant bits, fp32 accumulate). X: 16 rows x ld scratch.
