@@ -135,9 +135,10 @@ WsLayout layout_of(const gdn_desc* d) {
                    (d->flags & GDN_FLAG_QK_L2NORM) != 0, d->dk, channel_gates(d));
 }
 
-// Workspace of the backward pass: the SIMT forward's layout, then the chunk-start
-// states and v_new it keeps, then the backward intermediates (per slot = chunk slot *
-// Hv + value head).
+// Workspace of the backward pass: the forward's layout (the tensor-core path's for bf16
+// inputs, the SIMT path's for fp32), then the chunk-start states and v_new the
+// recompute keeps, then the backward intermediates (per slot = chunk slot * Hv + value
+// head).
 struct BwdLayout {
   WsLayout fwd;
   size_t hs, vn, dvn, dhs, dos, dw, ys, sdot, ttdw, dqp, dkp, total;
@@ -145,7 +146,7 @@ struct BwdLayout {
 
 BwdLayout bwd_layout_of(const gdn_desc* d) {
   BwdLayout B{};
-  B.fwd = ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), false, false, d->dk);
+  B.fwd = ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d), false, d->dk);
   size_t o = B.fwd.total;
   auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
   const size_t slots = (size_t)nt_max_of(d) * d->Hv, D = (size_t)d->dk;
@@ -328,8 +329,13 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   int2* table = chunk_indices ? reinterpret_cast<int2*>(chunk_indices)
                               : reinterpret_cast<int2*>(ws + L.chunk_table);
   p.chunk_table = table;
+  const bool tc = uses_tc_path(&d);
   p.w = ws + L.w; p.u = f32(L.u); p.M = ws + L.M;
-  p.qt = f32(L.qt); p.kt = f32(L.kt); p.gam = f32(L.gam);
+  p.G = L.G ? f32(L.G) : nullptr;
+  p.k16 = L.k16 ? ws + L.k16 : nullptr;
+  p.qt = L.qt ? f32(L.qt) : nullptr;
+  p.kt = L.kt ? f32(L.kt) : nullptr;
+  p.gam = L.gam ? f32(L.gam) : nullptr;
   p.hs = f32(B.hs); p.vn_out = f32(B.vn);
   cudaEvent_t* ev = d.stage_events;
   if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
@@ -339,8 +345,13 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
                      (!chunk_indices || build_into_caller) ? table : nullptr,
                      const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
                      p.status, stream);
-  if (nt_max > 0 && !launch_gen_intra(p, D, false, bf16, stream)) return GDN_ERR_LAUNCH_FAILED;
-  if (!launch_gen_inter(p, D, stream)) return GDN_ERR_LAUNCH_FAILED;
+  if (tc) {  // the tensor-core forward kernels, storing S and v_new per chunk
+    if (nt_max > 0 && !launch_tc_intra(p, stream)) return GDN_ERR_LAUNCH_FAILED;
+    if (!launch_tc_inter(p, false, stream)) return GDN_ERR_LAUNCH_FAILED;
+  } else {
+    if (nt_max > 0 && !launch_gen_intra(p, D, false, bf16, stream)) return GDN_ERR_LAUNCH_FAILED;
+    if (!launch_gen_inter(p, D, stream)) return GDN_ERR_LAUNCH_FAILED;
+  }
   if (ev) cudaEventRecord(ev[1], stream);
 
   BwdParams b{};
@@ -350,12 +361,16 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   b.dq = dq; b.dk = dk; b.dv = dv; b.dg = dg; b.dbeta = dbeta; b.dh0 = d_initial_state;
   b.status = p.status; b.seq_info = p.seq_info; b.chunk_offsets = p.chunk_offsets;
   b.chunk_table = table;
-  b.wT = f32(L.w); b.kt = p.kt; b.qt = p.qt; b.MT = f32(L.M); b.gam = p.gam;
+  if (tc) {
+    b.wimg = ws + L.w; b.mimg = ws + L.M; b.k16 = p.k16; b.G = p.G;
+  } else {
+    b.wT = f32(L.w); b.kt = p.kt; b.qt = p.qt; b.MT = f32(L.M); b.gam = p.gam;
+  }
   b.hs = p.hs; b.vn = p.vn_out;
   b.dvn = f32(B.dvn); b.dhs = f32(B.dhs); b.dos = f32(B.dos); b.dw = f32(B.dw);
   b.ys = f32(B.ys); b.sdot = f32(B.sdot); b.ttdw = f32(B.ttdw);
   b.dqp = f32(B.dqp); b.dkp = f32(B.dkp);
-  if (!launch_bwd(b, D, bf16, stream, ev ? ev + 2 : nullptr)) return GDN_ERR_LAUNCH_FAILED;
+  if (!launch_bwd(b, D, bf16, tc, stream, ev ? ev + 2 : nullptr)) return GDN_ERR_LAUNCH_FAILED;
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 

@@ -73,12 +73,17 @@ struct BwdParams {
   const int2* seq_info;
   const int32_t* chunk_offsets;
   const int2* chunk_table;
-  // forward quantities (the general path's layout)
+  // forward quantities: the fp32 SIMT path's layout (fp32 inputs) ...
   const float* wT;           // [slot][D][64] w^T
   const float* kt;           // [slot][64][D] exp(G_L - G) k
   const float* qt;           // [slot][D][64] (exp(G) q)^T
   const float* MT;           // [slot][64][64] M^T
   const float* gam;          // [slot][D] exp(G_L)
+  // ... or the tensor-core path's bridge (bf16 inputs)
+  const void* wimg;          // [slot] bf16 w image (two swizzled [64][128 B] halves)
+  const void* mimg;          // [slot] bf16 M hi/lo image ([128][128 B], swizzled)
+  const void* k16;           // [chunk slot, key head] fp16 k image (swizzled halves)
+  const float* G;            // [slot][64] in-chunk cumulative gate
   const float* hs;           // [slot][D][D] chunk-start state, [dv][dk]
   const float* vn;           // [slot][64][D] v_new
   // backward intermediates
@@ -223,7 +228,9 @@ void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, int D,
 bool launch_gen_intra(const Params& p, int D, bool channel_gates, bool bf16_inputs, cudaStream_t s);
 bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
 // ev: null, or two events recorded after the reverse scan and after the chunk kernels.
-bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, cudaStream_t s, cudaEvent_t* ev);
+// tc_bridge: the forward quantities are the tensor-core path's bridge (bf16 inputs).
+bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, bool tc_bridge, cudaStream_t s,
+                cudaEvent_t* ev);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, bool channel_gates, cudaStream_t s);
 bool launch_kda_intra(const Params& p, cudaStream_t s);

@@ -281,6 +281,16 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       unsigned char* st = sm + (c % kRing) * kSlot;
       const uint32_t st_a = sbase + (c % kRing) * kSlot;
       wait_ring<kRing>(bars, B_FULL, c, abort_flag);
+      if (p.hs) {  // chunk-start state, [dv][dk] rows of the slot (the backward's recompute)
+        float* hs = p.hs + ((size_t)(sv.first_slot + c) * p.Hv + hv) * p.D * p.D;
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int d = 16 * warp + g + (e >> 1) * 8, j = 8 * nt + c2 + (e & 1);
+            if (d < p.D) hs[(size_t)(c0 + j) * p.D + d] = S[nt][e];
+          }
+      }
 
       // X = w S_hi: token rows 16mt.., columns 16np..16np+15
       float xa[2][4];
@@ -326,6 +336,10 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             const int j = 16 * np + 8 * q + c2;
             const float2 u2 = *reinterpret_cast<const float2*>(st + kU + u_off(i, j));
             const float v0 = u2.x - xa[q][2 * hh], v1 = u2.y - xa[q][2 * hh + 1];
+            if (p.vn_out)  // v_new of the chunk (the backward's recompute)
+              *reinterpret_cast<float2*>(
+                  p.vn_out + (((size_t)(sv.first_slot + c) * p.Hv + hv) * 64 + i) * p.D + c0 + j) =
+                  make_float2(v0, v1);
             const __nv_bfloat162 hi = __floats2bfloat162_rn(v0, v1);
             const float2 hf = __bfloat1622float2(hi);
             *reinterpret_cast<__nv_bfloat162*>(vn + mn_off(j, i, 1024)) = hi;
@@ -422,7 +436,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&bars[B_OD + b]);
-      if (lane < 16 && i < L) {
+      if (p.out && lane < 16 && i < L) {  // (no output when only the states are wanted)
         const float e = expf(grow) * qrow;
         float o[32];
 #pragma unroll

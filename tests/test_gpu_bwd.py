@@ -1,9 +1,12 @@
 """Backward pass (gdn_chunk_bwd) through the C ABI against the oracle's fp64 adjoint
-of the token recurrence, gradient by gradient.
+of the token recurrence, gradient by gradient, as max|x - x_ref| / rms(x_ref).
 
-The kernels compute in fp32 from the same stored inputs the oracle reads, so every
-gradient is held to max|x - x_ref| / rms(x_ref) <= 2e-4 (fp32 rounding accumulated
-over the chunk products and the reverse scan)."""
+fp32 inputs: the kernels compute in fp32 from the same stored inputs the oracle reads,
+so every gradient is held to 2e-4 (fp32 rounding accumulated over the chunk products and
+the reverse scan). bf16 inputs: the forward recompute runs on the tensor-core kernels
+and the reverse scan reads their bridge (w as one bf16 rounding, M as a bf16 hi/lo pair,
+k as fp16), so the gradients carry the forward path's operand precision and are held to
+the bf16 bar, 1e-2."""
 import numpy as np
 import pytest
 import torch
@@ -17,6 +20,7 @@ from gpu_helpers import ratio, to_dev
 pytestmark = pytest.mark.gpu
 
 TOL = 2e-4
+TOL_BF16 = 1e-2
 KEYS = ("dq", "dk", "dv", "dg", "dbeta", "d_initial_state")
 
 
@@ -38,7 +42,8 @@ def run_pair(x, do, dfin, **kw):
     return got, ref
 
 
-def check(x, got, ref, tol=TOL):
+def check(x, got, ref, tol=None):
+    tol = tol or (TOL if x["dtype"] == "f32" else TOL_BF16)
     cu = x["cu_seqlens"].numpy()
     rows = np.arange(int(cu[0]), int(cu[-1]))
     for key in KEYS:
@@ -46,6 +51,7 @@ def check(x, got, ref, tol=TOL):
         if key != "d_initial_state":
             a, r = a[rows], r[rows]
         e = ratio(a, r)
+        print(f"{x['dtype']} d{x['dk']} {key} {e:.2e}")
         assert e <= tol, (key, e)
 
 
