@@ -175,3 +175,14 @@ def test_full_size_workloads(wid):
     o, f = run_gpu(x)
     check(x, o, f, *run_oracle(x))
 
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("d", [64, 128])
+def test_channel_gates_with_qk_l2norm(d, dtype):
+    """Per-channel gates with the q/k L2 norm on (the row factors enter the decayed q and
+    k operands of the per-channel kernels)."""
+    x = make_inputs(9, seed=57, lengths=[70, 1, 58], H=2, Hv=4, d=d, dtype=dtype,
+                    channel_gates=True, normalise_qk=False)
+    o, f = run_gpu(x, use_qk_l2norm=True)
+    check(x, o, f, *run_oracle(x, qk_l2norm=True))
