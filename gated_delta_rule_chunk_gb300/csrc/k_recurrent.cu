@@ -247,7 +247,7 @@ recurrent_kernel(const __grid_constant__ RecParams p, const __grid_constant__ CU
 #pragma unroll
       for (int qd = 0; qd < 4; ++qd) tma_store_2d(&tm_sT, 32 * qd, row0, buf + qd * 4096);
       bulk_commit();
-      bulk_wait<0>();
+      bulk_wait_read<0>();  // the tile has left shared memory; the writes land by grid end
     }
   }
   if (fail && lane == 0) set_status(p.status, GDN_DEV_TIMEOUT);

@@ -34,8 +34,9 @@
 // the warps never wait on scattered global stores; tiles come in by TMA tensor maps
 // (128-byte swizzle), which are also the tensor-core operand layouts.
 //
-// One CTA of 4 warps per (key head, chunk); ~99 KB of shared memory and 256 TMEM
-// columns, so two CTAs share an SM and hide each other's latency.
+// One CTA of 8 warps per (key head, chunk); ~99 KB of shared memory and 256 TMEM
+// columns, so two CTAs share an SM and hide each other's latency. Warps w and w + 4
+// read the same TMEM lane quarter and split its columns.
 #include <cuda.h>
 
 #include "gdn_common.cuh"
@@ -47,6 +48,8 @@ namespace gdn {
 
 namespace {
 
+constexpr int kWarps = 8;
+constexpr int kThreads = 32 * kWarps;
 constexpr int LDT = 68;  // fp32 stride of the A/T tile (16-byte rows)
 constexpr uint32_t kWaitIters = 1u << 22;
 constexpr uint32_t kTmemCols = 256;
@@ -104,7 +107,7 @@ __device__ __forceinline__ void wait_or_flag(uint64_t* bar, uint32_t parity, vol
 // Rows L..63 of a [64 rows][128 B] tile read as zero (the tile holds the rows that
 // follow the sequence, or padding, there).
 __device__ __forceinline__ void zero_tail(unsigned char* tile, int L, int tid) {
-  for (int idx = tid; idx < (64 - L) * 8; idx += 128)
+  for (int idx = tid; idx < (64 - L) * 8; idx += kThreads)
     *reinterpret_cast<uint4*>(tile + (uint32_t)(L + (idx >> 3)) * 128u + (idx & 7) * 16u) =
         make_uint4(0u, 0u, 0u, 0u);
 }
@@ -119,7 +122,7 @@ __device__ __forceinline__ void issue_v(unsigned char* sm, uint64_t* bars, const
   tma_load_3d(dst + 8192, tmv, 64, hv, t0, bar);
 }
 
-__global__ void __launch_bounds__(128, 2)
+__global__ void __launch_bounds__(kThreads, 2)
 tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmk,
                 const __grid_constant__ CUtensorMap tmq, const __grid_constant__ CUtensorMap tmv) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
@@ -161,9 +164,9 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     for (int r = 0; r < min(p.HG, 2); ++r) issue_v(sm, bars, &tmv, h * p.HG + r, t0, r);
   }
   if (tid < 64) KR[tid] = (tid < L && p.krn) ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
-  // 1/||q|| of the row this thread forms M for (warps 2 and 3 own rows 0..63 of R)
+  // 1/||q|| of the row this thread forms M for (warps 2, 3, 6 and 7 own rows 0..63 of R)
   const int qrow = 32 * (warp & 1) + lane;
-  const float qr = (warp >= 2 && p.qrn && qrow < L) ? p.qrn[(size_t)(t0 + qrow) * p.H + h] : 1.f;
+  const float qr = ((warp & 3) >= 2 && p.qrn && qrow < L) ? p.qrn[(size_t)(t0 + qrow) * p.H + h] : 1.f;
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -233,8 +236,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const unsigned char* kt = sm + kKQ;
     unsigned char* img = sm + kAT;
 #pragma unroll
-    for (int it = 0; it < 8; ++it) {
-      const int idx = tid + it * 128;  // 1024 chunks of 8 elements
+    for (int it = 0; it < 1024 / kThreads; ++it) {
+      const int idx = tid + it * kThreads;  // 1024 chunks of 8 elements
       const int half = idx >> 9, t = (idx >> 3) & 63, ch = idx & 7;
       const uint32_t off = (uint32_t)half * 16384u + sw_off(t, ch);
       const uint4 raw = *reinterpret_cast<const uint4*>(kt + off);
@@ -268,17 +271,20 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     if (r == 0) wait_or_flag(&bars[3], 0, fail);
     tc_fence_after();
 
-    // A (warps 0-1, rows of P) into A/T; M hi/lo image (warps 2-3, rows of R) into the Q
-    // halves. Branch-free: every decay factor is formed and the mask is a select (exp of
-    // a positive exponent above the diagonal may be inf; it is never used). Eight columns
-    // per step, not unrolled, to keep the kernel's code small.
+    // A (TMEM lane quarters 0-1, rows of P) into A/T; M hi/lo image (quarters 2-3, rows of
+    // R) into the Q halves; warps w and w + 4 share a lane quarter and take columns 0..31
+    // and 32..63. Branch-free: every decay factor is formed and the mask is a select (exp
+    // of a positive exponent above the diagonal may be inf; it is never used). Eight
+    // columns per step, not unrolled, to keep the kernel's code small.
     {
       const int i = 32 * (warp & 1) + lane;
-      const uint32_t trow = tmem + ((uint32_t)(32 * warp) << 16);
+      const bool rows_p = (warp & 3) < 2;
+      const uint32_t trow = tmem + ((uint32_t)(32 * (warp & 3)) << 16);
       const float gi = G[i];
-      const float rowf = warp < 2 ? Bt[i] * KR[i] : qr;
+      const float rowf = rows_p ? Bt[i] * KR[i] : qr;
+      const int ch0 = 4 * (warp >> 2);
 #pragma unroll 2
-      for (int ch = 0; ch < 8; ++ch) {
+      for (int ch = ch0; ch < ch0 + 4; ++ch) {
         const int j = 8 * ch;
         float v[8];
         tmem_ld8(trow + j, v);
@@ -292,7 +298,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 #pragma unroll
         for (int e = 0; e < 8; ++e) d[e] = __expf(gi - gg[e]) * rowf * kk[e];
         tmem_ld_wait();
-        if (warp < 2) {  // strictly lower
+        if (rows_p) {  // strictly lower
 #pragma unroll
           for (int e = 0; e < 8; ++e) d[e] = (j + e < i) ? d[e] * v[e] : 0.f;
           *reinterpret_cast<float4*>(&AT[i * LDT + j]) = make_float4(d[0], d[1], d[2], d[3]);
@@ -318,7 +324,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       bulk_store(mimg + 8192, sm + kKQ + 24576, 8192);
       bulk_commit();
     }
-    tri_inverse_64_tc(AT, LDT, X, tid);  // ends with the CTA synchronized
+    tri_inverse_64_tc<kWarps>(AT, LDT, X, tid);  // ends with the CTA synchronized
 
     // This member's V tile (rows past the end zeroed) and the M image read out of the Q halves.
     wait_or_flag(&bars[1 + (r & 1)], (uint32_t)((r >> 1) & 1), fail);
@@ -332,7 +338,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     // T operand images: T diag(beta exp(G) / ||k||) (bf16) and T diag(beta) as a bf16
     // hi/lo pair (hi into the first Q half, lo into the second).
 #pragma unroll 1
-    for (int idx = tid; idx < 512; idx += 128) {
+    for (int idx = tid; idx < 512; idx += kThreads) {
       const int i = idx >> 3, ch = idx & 7, j0 = 8 * ch;
       const float4 x0 = *reinterpret_cast<const float4*>(&AT[i * LDT + j0]);
       const float4 x1 = *reinterpret_cast<const float4*>(&AT[i * LDT + j0 + 4]);
@@ -383,13 +389,14 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     }
     wait_or_flag(&bars[4], par, fail);
     tc_fence_after();
-    {  // w rows 16 warp .. 16 warp + 15 (TMEM lanes 32 warp ..), bf16, into the A/T region
-      const int i = 16 * warp + (lane & 15);
+    {  // w rows 16 q .. 16 q + 15 (TMEM lanes 32 q .., q = warp % 4), bf16, into the A/T
+       // region; warps w and w + 4 take column blocks 0-1 and 2-3
+      const int i = 16 * (warp & 3) + (lane & 15);
       unsigned char* img = sm + kAT;
-#pragma unroll 2
-      for (int cb = 0; cb < 4; ++cb) {
+#pragma unroll
+      for (int cb = 2 * (warp >> 2); cb < 2 * (warp >> 2) + 2; ++cb) {
         float v[32];
-        tmem_ld32(dw + ((uint32_t)(32 * warp) << 16) + 32 * cb, v);
+        tmem_ld32(dw + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * cb, v);
         tmem_ld_wait();
         if (lane < 16) {
 #pragma unroll
@@ -416,11 +423,11 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
     // u blocks (32 columns) of one half from TMEM to two staging tiles, then to global
     auto u_out = [&](uint32_t d, unsigned char* s0, unsigned char* s1, int blk0) {
-      const int i = 16 * warp + (lane & 15);
-#pragma unroll 1
-      for (int b = 0; b < 2; ++b) {
+      // rows 16 q .. 16 q + 15 (q = warp % 4); warps w and w + 4 take blocks blk0, blk0 + 1
+      const int i = 16 * (warp & 3) + (lane & 15), b = warp >> 2;
+      {
         float v[32];
-        tmem_ld32(d + ((uint32_t)(32 * warp) << 16) + 32 * b, v);
+        tmem_ld32(d + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * b, v);
         tmem_ld_wait();
         unsigned char* blk = b ? s1 : s0;
         if (lane < 16) {
@@ -475,7 +482,7 @@ bool launch_tc_intra(const Params& p, cudaStream_t s) {
       !encode_rows_tmap(&tmv, p.v, rows, p.Hv, p.D))
     return false;
   ensure_smem_limit((const void*)tc_intra_kernel, (int)kSmemBytes);
-  return launch_pdl(tc_intra_kernel, dim3(p.H, p.nt_max), dim3(128), kSmemBytes, s, p, tmk,
+  return launch_pdl(tc_intra_kernel, dim3(p.H, p.nt_max), dim3(kThreads), kSmemBytes, s, p, tmk,
                     tmq, tmv) == cudaSuccess;
 }
 
