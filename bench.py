@@ -151,7 +151,7 @@ NCU_TRAFFIC = {
               "sha1": "d8aac1d5c1abbd0da433a3e56a3067d7734e932a", "bytes": 191652352,
               "profile": "profiles/tc_inter_kernel_T4096_H16_Hv32.md"},
     "intra": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_intra.cu",
-              "sha1": "15f43310cbc0788816d610dd08576f9235a1ac92", "bytes": 159164928,
+              "sha1": "fa58a6cd13d0a4a63568e928f2d9f6acfb58eb88", "bytes": 158551808,
               "profile": "profiles/tc_intra_kernel_T4096_H16_Hv32.md"},
 }
 NCU_WORKLOAD = 2
@@ -565,6 +565,45 @@ def run_conv(args, ws, rank, local):
     return res
 
 
+def timing_variants(call, flush, stream, n):
+    """Medians (us) of the same call with L2 left warm between calls, and of the call
+    captured once in a CUDA graph and replayed, with and without the L2 flush. Reported
+    beside the headline (which flushes L2 and launches eagerly), not instead of it."""
+    import torch
+
+    def timed(fn, do_flush):
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(n)]
+        for i in range(3):
+            if do_flush:
+                flush.fill_(i & 255)
+            fn()
+        torch.cuda.synchronize()
+        for i in range(n):
+            if do_flush:
+                flush.fill_((i + 7) & 255)
+            evs[i][0].record(stream)
+            fn()
+            evs[i][1].record(stream)
+        torch.cuda.synchronize()
+        return 1000.0 * statistics.median(a.elapsed_time(b) for a, b in evs)
+
+    res = {"warm_l2_us_median": timed(call, False)}
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        call()
+        with torch.cuda.graph(graph, stream=side):
+            call()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    res["graph_replay_us_median"] = timed(graph.replay, True)
+    res["graph_replay_warm_l2_us_median"] = timed(graph.replay, False)
+    res["calls_per_variant"] = n
+    return res
+
+
 def run_gdn(args, ws, rank, local):
     import torch
     from gated_delta_rule_chunk_gb300 import binding as B
@@ -640,6 +679,8 @@ def run_gdn(args, ws, rank, local):
     ms_max = max_over_ranks(ms, ws)
     tokens = x["n_tokens"]
     value = ws * tokens / (ms_max / 1000.0)
+    variants = timing_variants(call, flush, stream, min(K, 200))
+    variants["us_median"] = 1000.0 * statistics.median(step_ms)
 
     # ---------------------------------------------------------------- e2e through host buffers
     host = {k: (x[k].pin_memory() if x.get(k) is not None else None)
@@ -722,6 +763,7 @@ def run_gdn(args, ws, rank, local):
         "path_roofline": path_roof,
         "stages_us": {k: 1000.0 * v for k, v in stage_mean.items()},
         "us_per_call_with_stage_events": 1000.0 * staged_ms,
+        "timing_variants": variants,
         "e2e": {"value": e2e_val, "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,
                 "ms_per_step": statistics.mean(e2e_ms) if e2e_ms else None},
