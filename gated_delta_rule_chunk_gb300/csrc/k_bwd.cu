@@ -224,96 +224,155 @@ __global__ void __launch_bounds__(kThr) bwd_scan_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------------- contractions with S, dS
-template <int D>
-constexpr size_t state_floats() { return (size_t)3 * D * 68 + 2 * 32 * D + kThr / 32; }
-
 // dos = dO S^T, dw = -dv_new S^T, ys = v_new dS_next^T (contractions over dv) and
-// sdot = <S, dS_next>, per (chunk slot, value head).
+// sdot = <S, dS_next>, per (chunk slot, value head), on warp-level tensor-core MMAs.
+// With the state [dv][dk] row-major, each product is A [64 tokens][dv] times B = the
+// state [dv][dk]: a dense 64 x D x D contraction. Both fp32 operands are split into a
+// bf16 hi/lo pair in shared memory (x = hi + lo, about 16 significant bits) and the
+// product takes the three terms hi*hi + hi*lo + lo*hi (a bf16 dO is exact: two terms).
+template <int D>
+constexpr size_t state_mma_bytes() {
+  return (size_t)2 * (D + 64) * (D + 8) * sizeof(__nv_bfloat16) + 64;
+}
+
+__device__ __forceinline__ float4 ld_f4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+
+// Four consecutive dO elements (bf16 or fp32) as floats.
+__device__ __forceinline__ float4 ld_dout4(const BwdParams& p, size_t idx) {
+  if (p.dout_bf16) {
+    const uint2 r = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(p.dout) + idx);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  }
+  return ld_f4(reinterpret_cast<const float*>(p.dout) + idx);
+}
+
+// bf16 hi/lo copies of `rows` fp32 rows of D columns into row-major tiles with row
+// stride D + 8 (16-byte padding: the 8 row addresses of an ldmatrix hit distinct bank
+// groups). get(r, c4) returns columns 4 c4 .. 4 c4 + 3 of row r; four loads in flight
+// per thread.
+template <int D, typename Get>
+__device__ __forceinline__ void split_rows(__nv_bfloat16* hi, __nv_bfloat16* lo, int rows, int tid,
+                                           Get get) {
+  constexpr int RS = D + 8, Q = D / 4;
+  const int n = rows * Q;
+  for (int base = tid; base < n; base += 4 * kThr) {
+    float4 v[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * kThr;
+      v[u] = idx < n ? get(idx / Q, idx % Q) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int idx = base + u * kThr;
+      if (idx < n) {
+        const int off = (idx / Q) * RS + 4 * (idx % Q);
+        uint2 h, l;
+        split_pack2(v[u].x, v[u].y, h.x, l.x);
+        split_pack2(v[u].z, v[u].w, h.y, l.y);
+        *reinterpret_cast<uint2*>(hi + off) = h;
+        *reinterpret_cast<uint2*>(lo + off) = l;
+      }
+    }
+  }
+}
+
+// out[64][D] = sign * A B, A = Ah + Al ([64][D + 8]), B = Bh + Bl ([D][D + 8], row-major
+// [k][n]); warp w owns rows 16 (w % 4).. and columns (w / 4) D/2 ..; the lo*lo term is
+// dropped, and so is every Al term when A is exact in bf16.
+template <int D>
+__device__ __forceinline__ void state_product(const __nv_bfloat16* Ah, const __nv_bfloat16* Al,
+                                              bool a_exact, const __nv_bfloat16* Bh,
+                                              const __nv_bfloat16* Bl, float sign, float* out,
+                                              int warp, int lane) {
+  constexpr int RS = D + 8, NW = D / 2, NT = NW / 8;
+  const int mt = warp & 3, n0 = (warp >> 2) * NW;
+  float acc[NT][4];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
+#pragma unroll 2
+  for (int ks = 0; ks < D / 16; ++ks) {
+    uint32_t ah[4], al[4];
+    load_a(ah, Ah, RS, 16 * mt, 16 * ks, lane);
+    if (!a_exact) load_a(al, Al, RS, 16 * mt, 16 * ks, lane);
+#pragma unroll
+    for (int np = 0; np < NT / 2; ++np) {
+      uint32_t bh[4], bl[4];
+      load_b_kn(bh, Bh, RS, 16 * ks, n0 + 16 * np, lane);
+      load_b_kn(bl, Bl, RS, 16 * ks, n0 + 16 * np, lane);
+      mma_bf16(acc[2 * np], ah, bh[0], bh[1]);
+      mma_bf16(acc[2 * np + 1], ah, bh[2], bh[3]);
+      mma_bf16(acc[2 * np], ah, bl[0], bl[1]);
+      mma_bf16(acc[2 * np + 1], ah, bl[2], bl[3]);
+      if (!a_exact) {
+        mma_bf16(acc[2 * np], al, bh[0], bh[1]);
+        mma_bf16(acc[2 * np + 1], al, bh[2], bh[3]);
+      }
+    }
+  }
+  const int g = lane >> 2, c2 = 2 * (lane & 3), r0 = 16 * mt + g;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    const int col = n0 + 8 * nt + c2;
+    *reinterpret_cast<float2*>(out + (size_t)r0 * D + col) =
+        make_float2(sign * acc[nt][0], sign * acc[nt][1]);
+    *reinterpret_cast<float2*>(out + (size_t)(r0 + 8) * D + col) =
+        make_float2(sign * acc[nt][2], sign * acc[nt][3]);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kThr) bwd_state_kernel(BwdParams p) {
-  constexpr int RN = D / 16;
-  extern __shared__ __align__(16) float sm[];
-  float* dOT = sm;                 // [D][68] dO^T
-  float* vnT = dOT + D * 68;       // [D][68] v_new^T
-  float* dvT = vnT + D * 68;       // [D][68] dv_new^T
-  float* Sb = dvT + D * 68;        // [32][D] rows of S ([dv][dk])
-  float* dSb = Sb + 32 * D;        // [32][D] rows of dS_next
-  float* red = dSb + 32 * D;       // [8] warp partials
+  constexpr int RS = D + 8;
+  extern __shared__ __align__(16) unsigned char smb[];
+  __nv_bfloat16* Bh = reinterpret_cast<__nv_bfloat16*>(smb);  // [D][RS] the state (then dS_next)
+  __nv_bfloat16* Bl = Bh + D * RS;
+  __nv_bfloat16* Ah = Bl + D * RS;                             // [64][RS] dO, dv_new, v_new
+  __nv_bfloat16* Al = Ah + 64 * RS;
+  float* red = reinterpret_cast<float*>(Al + 64 * RS);         // [8] warp partials
 
-  const int tid = threadIdx.x, hv = blockIdx.y;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, hv = blockIdx.y;
   int t0, L, wslot;
   if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
   const size_t sl = (size_t)wslot * p.Hv + hv;
-  staged_copy<8>(64 * D, tid, kThr,
-                 [&](int i) { return i / D < L ? ld_dout(p, ((size_t)(t0 + i / D) * p.Hv + hv) * D + i % D) : 0.f; },
-                 [&](int i, float x) { dOT[(i % D) * 68 + i / D] = x; });
-  staged_copy<8>(64 * D, tid, kThr, [&](int i) { return p.vn[sl * 64 * D + i]; },
-                 [&](int i, float x) { vnT[(i % D) * 68 + i / D] = x; });
-  staged_copy<8>(64 * D, tid, kThr, [&](int i) { return p.dvn[sl * 64 * D + i]; },
-                 [&](int i, float x) { dvT[(i % D) * 68 + i / D] = x; });
-  const int i0 = (tid >> 4) * 4, d0 = (tid & 15) * RN;
-  float aos[4][RN], aw[4][RN], ay[4][RN];
-  zero(aos);
-  zero(aw);
-  zero(ay);
+  const float* hs = p.hs + sl * D * D;
+  const float* dhs = p.dhs + sl * D * D;
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+
+  split_rows<D>(Bh, Bl, D, tid, [&](int r, int c4) { return ld_f4(hs + (size_t)r * D + 4 * c4); });
+  split_rows<D>(Ah, Al, 64, tid, [&](int r, int c4) {  // rows past the sequence end: zero
+    return r < L ? ld_dout4(p, ((size_t)(t0 + r) * p.Hv + hv) * D + 4 * c4) : z4;
+  });
+  __syncthreads();
+  state_product<D>(Ah, Al, p.dout_bf16 != 0, Bh, Bl, 1.f, p.dos + sl * 64 * D, warp, lane);
+  __syncthreads();
+  split_rows<D>(Ah, Al, 64, tid,
+                [&](int r, int c4) { return ld_f4(p.dvn + sl * 64 * D + (size_t)r * D + 4 * c4); });
+  __syncthreads();
+  state_product<D>(Ah, Al, false, Bh, Bl, -1.f, p.dw + sl * 64 * D, warp, lane);
+  __syncthreads();
   float sd = 0.f;
-  const float4* hs4 = reinterpret_cast<const float4*>(p.hs + sl * D * D);
-  const float4* dh4 = reinterpret_cast<const float4*>(p.dhs + sl * D * D);
-  for (int nb = 0; nb < D / 32; ++nb) {
-    __syncthreads();  // previous blocks consumed (and the transposes above written)
-    for (int idx = tid; idx < 32 * D / 4; idx += kThr) {
-      const float4 a = hs4[nb * 8 * D + idx], b = dh4[nb * 8 * D + idx];
-      reinterpret_cast<float4*>(Sb)[idx] = a;
-      reinterpret_cast<float4*>(dSb)[idx] = b;
-      sd += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
-    }
-    __syncthreads();
-#pragma unroll 2
-    for (int r = 0; r < 32; ++r) {
-      const int f = nb * 32 + r;
-      float xo[4], xw[4], xy[4], bs[RN], bd[RN];
-      ldv<4>(dOT + f * 68 + i0, xo);
-      ldv<4>(dvT + f * 68 + i0, xw);
-      ldv<4>(vnT + f * 68 + i0, xy);
-#pragma unroll
-      for (int h = 0; h < RN; h += 4) {
-        float t4[4], u4[4];
-        ldv<4>(Sb + r * D + d0 + h, t4);
-        ldv<4>(dSb + r * D + d0 + h, u4);
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          bs[h + e] = t4[e];
-          bd[h + e] = u4[e];
-        }
-      }
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < RN; ++b) {
-          aos[a][b] = fmaf(xo[a], bs[b], aos[a][b]);
-          aw[a][b] = fmaf(xw[a], bs[b], aw[a][b]);
-          ay[a][b] = fmaf(xy[a], bd[b], ay[a][b]);
-        }
-    }
-  }
-#pragma unroll
-  for (int a = 0; a < 4; ++a) {
-    const size_t row = sl * 64 * D + (size_t)(i0 + a) * D + d0;
-#pragma unroll
-    for (int b = 0; b < RN; ++b) {
-      p.dos[row + b] = aos[a][b];
-      p.dw[row + b] = -aw[a][b];
-      p.ys[row + b] = ay[a][b];
-    }
-  }
+  split_rows<D>(Bh, Bl, D, tid, [&](int r, int c4) {
+    const float4 a = ld_f4(dhs + (size_t)r * D + 4 * c4), b = ld_f4(hs + (size_t)r * D + 4 * c4);
+    sd += a.x * b.x + a.y * b.y + a.z * b.z + a.w * b.w;
+    return a;
+  });
+  split_rows<D>(Ah, Al, 64, tid,
+                [&](int r, int c4) { return ld_f4(p.vn + sl * 64 * D + (size_t)r * D + 4 * c4); });
+  __syncthreads();
+  state_product<D>(Ah, Al, false, Bh, Bl, 1.f, p.ys + sl * 64 * D, warp, lane);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) sd += __shfl_xor_sync(0xffffffffu, sd, o);
-  if ((tid & 31) == 0) red[tid >> 5] = sd;
+  if (lane == 0) red[warp] = sd;
   __syncthreads();
   if (tid == 0) {
-    float s = 0.f;
-    for (int w = 0; w < kThr / 32; ++w) s += red[w];
-    p.sdot[sl] = s;
+    float t = 0.f;
+    for (int w = 0; w < kThr / 32; ++w) t += red[w];
+    p.sdot[sl] = t;
   }
 }
 
@@ -654,7 +713,7 @@ template <typename TIn, int D, bool TC>
 bool launch_bwd_t(const BwdParams& p, cudaStream_t s, cudaEvent_t* ev) {
   constexpr int BV = bv_of<D>();
   const int s1 = (int)(scan_floats<D>() * sizeof(float));
-  const int s2 = (int)(state_floats<D>() * sizeof(float));
+  const int s2 = (int)state_mma_bytes<D>();
   const int s3 = (int)(chunk_floats() * sizeof(float));
   ensure_smem_limit((const void*)bwd_scan_kernel<D, TC>, s1);
   ensure_smem_limit((const void*)bwd_state_kernel<D>, s2);
