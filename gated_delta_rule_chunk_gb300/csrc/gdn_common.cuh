@@ -231,6 +231,7 @@ bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
 // tc_bridge: the forward quantities are the tensor-core path's bridge (bf16 inputs).
 bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, bool tc_bridge, cudaStream_t s,
                 cudaEvent_t* ev);
+bool launch_bwd_scan_tc(const BwdParams& p, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, bool channel_gates, cudaStream_t s);
 bool launch_kda_intra(const Params& p, cudaStream_t s);

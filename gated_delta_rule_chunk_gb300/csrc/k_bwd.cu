@@ -718,7 +718,11 @@ bool launch_bwd_t(const BwdParams& p, cudaStream_t s, cudaEvent_t* ev) {
   ensure_smem_limit((const void*)bwd_scan_kernel<D, TC>, s1);
   ensure_smem_limit((const void*)bwd_state_kernel<D>, s2);
   ensure_smem_limit((const void*)bwd_chunk_kernel<TIn, D>, s3);
-  bwd_scan_kernel<D, TC><<<dim3(p.N, p.Hv, D / BV), kThr, s1, s>>>(p);
+  if (TC && D == 128) {  // the tensor-core bridge at d = 128: the warp-MMA scan
+    if (!launch_bwd_scan_tc(p, s)) return false;
+  } else {
+    bwd_scan_kernel<D, TC><<<dim3(p.N, p.Hv, D / BV), kThr, s1, s>>>(p);
+  }
   if (ev) cudaEventRecord(ev[0], s);
   if (p.nt_max > 0) {
     bwd_state_kernel<D><<<dim3(p.nt_max, p.Hv), kThr, s2, s>>>(p);
