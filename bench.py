@@ -793,18 +793,29 @@ def bwd_bytes(x):
 
 
 def bwd_stage_flops(x):
-    """FLOPs of the backward's three stages (64 x 64 and 64 x d products counted in full):
+    """FLOPs of the backward's four stages (64 x 64 and 64 x d products counted in full):
     the forward recompute (intra kernel, and w S plus the state update of the scan), the
-    reverse scan (Kt dS, M^T dO, Qt^T dO, w^T dv_new) and the per-chunk kernels (the three
-    state contractions, K K^T, Q K^T, the inverse, dP, Z, T^T dv_new, T^T dw, T^T Z T^T and
-    the dq / dk products)."""
+    reverse scan (Kt dS, M^T dO, Qt^T dO, w^T dv_new), the three contractions with the
+    stored states (dO S^T, dv_new S^T, v_new dS^T) and the per-chunk kernels (K K^T, Q K^T,
+    the inverse, dP, Z, T^T dv_new, T^T dw, T^T Z T^T and the dq / dk products)."""
     NT = n_chunks(x["lengths"])
     C, D, Hv = CHUNK, x["dk"], x["Hv"]
     intra = stage_flops(x)["intra"]
     recompute = intra + NT * Hv * (2 * 2 * C * D * D)
     scan = NT * Hv * (6 * C * D * D + 2 * C * C * D)
-    chunk = NT * Hv * (6 * C * D * D + 20 * C * C * D + 4 * C ** 3 + C ** 3 / 3)
-    return {"recompute": recompute, "reverse_scan": scan, "chunk_grads": chunk}
+    state = NT * Hv * (6 * C * D * D)
+    chunk = NT * Hv * (20 * C * C * D + 4 * C ** 3 + C ** 3 / 3)
+    return {"recompute": recompute, "reverse_scan": scan, "state_products": state,
+            "chunk_grads": chunk}
+
+
+def bwd_state_bytes(x):
+    """Algorithmic bytes of the state contractions per call: per (chunk, value head) the
+    chunk-start state and its gradient (fp32 D x D each), v_new and dv_new (fp32 64 x D),
+    dO (64 x D) in; dO S^T, dw and v_new dS^T (fp32 64 x D) out."""
+    NT = n_chunks(x["lengths"])
+    D, Hv = x["dk"], x["Hv"]
+    return NT * Hv * (2 * D * D * 4 + 2 * 64 * D * 4 + 64 * D * 4 + 3 * 64 * D * 4)
 
 
 def run_gdn_bwd(args, ws, rank, local):
@@ -849,7 +860,7 @@ def run_gdn_bwd(args, ws, rank, local):
 
     K = args.steps
     mk = lambda n: [[torch.cuda.Event(enable_timing=True) for _ in range(n)] for _ in range(K)]
-    evs, sevs = mk(2), mk(5)
+    evs, sevs = mk(2), mk(6)
     for row in evs + sevs:
         for e in row:
             e.record()
@@ -878,7 +889,7 @@ def run_gdn_bwd(args, ws, rank, local):
         call([e.cuda_event for e in sevs[i][1:]])
     torch.cuda.synchronize()
     ms = statistics.mean(r[0].elapsed_time(r[1]) for r in evs)
-    names = ("recompute", "reverse_scan", "chunk_grads")
+    names = ("recompute", "reverse_scan", "state_products", "chunk_grads")
     st = {nm: statistics.mean(r[j + 1].elapsed_time(r[j + 2]) for r in sevs)
           for j, nm in enumerate(names)}
     ms_max = max_over_ranks(ms, ws)
@@ -920,6 +931,26 @@ def run_gdn_bwd(args, ws, rank, local):
     alg_b, alg_f = bwd_bytes(x), sum(sf.values())
     t_hbm = alg_b / (peaks["hbm_gbs"] * 1e9)
     t_tc = alg_f / (peaks["bf16_tflops"] * 1e12)
+    if dom == "state_products":  # warp-MMA contractions: bound by HBM
+        sb = bwd_state_bytes(x)
+        gbs = sb / (st[dom] / 1000.0) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": gbs, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
+                "algorithmic_bytes_per_launch": sb, "traffic": None, "traffic_source": None}
+    else:
+        roof = {"bound": "alu", "kernel": dom, "achieved": achieved,
+                "peak": SIMT_FP32_TFLOPS, "unit": "TFLOP/s",
+                "frac": achieved / SIMT_FP32_TFLOPS,
+                "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz",
+                "algorithmic_flops_per_launch": sf[dom], "traffic": None,
+                "traffic_source": None}
+    if x["dtype"] == "bf16":
+        kinds = ("tensor-core recompute and reverse scan" if D == 128 else
+                 "tensor-core recompute, fp32 SIMT reverse scan")
+    else:
+        kinds = "fp32 SIMT recompute and reverse scan"
+    kinds += ", warp-MMA state contractions, fp32 SIMT per-chunk gradients"
     res = {
         "metric": f"GDN chunk backward tokens/s, {WORKLOADS[args.workload].name}; % of roofline",
         "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
@@ -928,16 +959,11 @@ def run_gdn_bwd(args, ws, rank, local):
         "config": {"workload": WORKLOADS[args.workload].name, "pass": "backward",
                    "T": T, "N": N, "H": H, "Hv": Hv, "dk": D, "dv": D, "chunk": CHUNK,
                    "qkv_dtype": x["dtype"], "grad_dtype": "fp32", "d_out_dtype": "fp32",
-                   "kernels": "fp32 SIMT: recompute, reverse scan, per-chunk gradients",
+                   "kernels": kinds,
                    "l2": "512 MiB buffer written between timed steps (L2 is 129 MB)",
                    "parallelism": "replicas" if ws > 1 else "single GPU",
                    "inputs": "resident in HBM"},
-        "roofline": {"bound": "alu", "kernel": dom, "achieved": achieved,
-                     "peak": SIMT_FP32_TFLOPS, "unit": "TFLOP/s",
-                     "frac": achieved / SIMT_FP32_TFLOPS,
-                     "peak_source": "derived: 152 SMs x 128 fp32 FMA lanes x 2 FLOP x 2.07 GHz",
-                     "algorithmic_flops_per_launch": sf[dom], "traffic": None,
-                     "traffic_source": None},
+        "roofline": roof,
         "path_roofline": {"bound": "hbm" if t_hbm >= t_tc else "tensor",
                           "algorithmic_bytes": alg_b, "algorithmic_flops": alg_f,
                           "roofline_us_measured_peaks": 1e6 * max(t_hbm, t_tc),

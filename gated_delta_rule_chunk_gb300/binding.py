@@ -22,7 +22,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_BUILD_CHUNK_INDICES = 2
 GDN_FLAG_CHANNEL_GATES = 4
-GDN_NUM_STAGE_EVENTS = 4
+GDN_NUM_STAGE_EVENTS = 5
 DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table"}
 
 # Every entry point include/gdn.h declares.

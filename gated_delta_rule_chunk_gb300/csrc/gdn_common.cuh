@@ -227,7 +227,8 @@ void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, int D,
                    float* qrn, float* krn, cudaStream_t s);
 bool launch_gen_intra(const Params& p, int D, bool channel_gates, bool bf16_inputs, cudaStream_t s);
 bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
-// ev: null, or two events recorded after the reverse scan and after the chunk kernels.
+// ev: null, or three events recorded after the reverse scan, after the contractions with
+// the stored states and after the per-chunk gradient kernels.
 // tc_bridge: the forward quantities are the tensor-core path's bridge (bf16 inputs).
 bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, bool tc_bridge, cudaStream_t s,
                 cudaEvent_t* ev);

@@ -724,12 +724,13 @@ bool launch_bwd_t(const BwdParams& p, cudaStream_t s, cudaEvent_t* ev) {
     bwd_scan_kernel<D, TC><<<dim3(p.N, p.Hv, D / BV), kThr, s1, s>>>(p);
   }
   if (ev) cudaEventRecord(ev[0], s);
+  if (p.nt_max > 0) bwd_state_kernel<D><<<dim3(p.nt_max, p.Hv), kThr, s2, s>>>(p);
+  if (ev) cudaEventRecord(ev[1], s);
   if (p.nt_max > 0) {
-    bwd_state_kernel<D><<<dim3(p.nt_max, p.Hv), kThr, s2, s>>>(p);
     bwd_chunk_kernel<TIn, D><<<dim3(p.nt_max, p.Hv), kThr, s3, s>>>(p);
     bwd_reduce_kernel<D><<<dim3(p.nt_max, p.H), kThr, 0, s>>>(p);
   }
-  if (ev) cudaEventRecord(ev[1], s);
+  if (ev) cudaEventRecord(ev[2], s);
   return cudaPeekAtLastError() == cudaSuccess;
 }
 

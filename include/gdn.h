@@ -86,7 +86,7 @@ enum {
   GDN_FLAG_CHANNEL_GATES = 4u         /* g is [T, Hv, dk]: a gate per key channel */
 };
 
-enum { GDN_NUM_STAGE_EVENTS = 4 };
+enum { GDN_NUM_STAGE_EVENTS = 5 };
 
 /*
  * Problem descriptor (plain data; the pages' Python signature infers these
@@ -110,8 +110,9 @@ enum { GDN_NUM_STAGE_EVENTS = 4 };
  *                another call that may run at the same time
  *   stage_events NULL, or an array of GDN_NUM_STAGE_EVENTS cudaEvent_t that
  *                gdn_chunk_fwd records on `stream` before the first kernel and
- *                after the chunk-table, intra-chunk and inter-chunk kernels
- *                (for timing each stage; the library does not create them)
+ *                after the chunk-table, intra-chunk and inter-chunk kernels (the
+ *                first four; gdn_chunk_bwd records all five), for timing each
+ *                stage; the library does not create them
  */
 typedef struct gdn_desc {
   int32_t T;
@@ -227,8 +228,8 @@ size_t gdn_bwd_workspace_size(const gdn_desc* desc);
  *   d_initial_state fp32 [N, Hv, dv, dk] or NULL (not written)
  * Rows outside the sequences are not written. desc->workspace must hold
  * gdn_bwd_workspace_size(desc) bytes. desc->stage_events, when set, are recorded
- * before the forward recompute and after it, after the reverse scan and after
- * the per-chunk gradient kernels. Errors: as gdn_chunk_fwd, plus
+ * before the forward recompute and after it, after the reverse scan, after the
+ * contractions with the stored states and after the per-chunk gradient kernels. Errors: as gdn_chunk_fwd, plus
  * GDN_ERR_UNSUPPORTED for GDN_FLAG_CHANNEL_GATES or GDN_FLAG_QK_L2NORM.
  */
 int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void* v,
