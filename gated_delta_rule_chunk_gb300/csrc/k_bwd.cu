@@ -397,6 +397,47 @@ __device__ __forceinline__ void load_tm(float* dst, int L, int tid, Get get) {
                  [&](int idx, float x) { dst[(idx >> 5) * kLt + (idx & 31)] = x; });
 }
 
+// acc[nt] += sum_{k0 <= k < k1} X[k][m0 + r] Y[k][n0 + 8 nt + c'] over a 16 x 8 NT warp
+// tile: both operands fp32 and k-major in shared memory (row strides ldx, ldy), split into
+// bf16 hi + lo per fragment, three warp MMAs per step of 16 (hi*hi, hi*lo, lo*hi).
+// Accumulator element e of tile nt: row m0 + g + 8 (e >> 1), column n0 + 8 nt + c + (e & 1)
+// (g = lane / 4, c = 2 (lane % 4)). Reads X rows k0..k1-1, columns m0..m0+15.
+template <int NT>
+__device__ __forceinline__ void mma_kmajor(float (&acc)[NT][4], const float* X, int ldx,
+                                           const float* Y, int ldy, int m0, int n0, int k0,
+                                           int k1, int lane) {
+  const int g = lane >> 2, c = 2 * (lane & 3);
+#pragma unroll 2
+  for (int k = k0; k < k1; k += 16) {
+    uint32_t ah[4], al[4];
+    const float* xp = X + (k + c) * ldx + m0 + g;
+    split_pack2(xp[0], xp[ldx], ah[0], al[0]);
+    split_pack2(xp[8], xp[ldx + 8], ah[1], al[1]);
+    split_pack2(xp[8 * ldx], xp[9 * ldx], ah[2], al[2]);
+    split_pack2(xp[8 * ldx + 8], xp[9 * ldx + 8], ah[3], al[3]);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const float* yp = Y + (k + c) * ldy + n0 + 8 * nt + g;
+      uint32_t bh[2], bl[2];
+      split_pack2(yp[0], yp[ldy], bh[0], bl[0]);
+      split_pack2(yp[8 * ldy], yp[9 * ldy], bh[1], bl[1]);
+      mma_bf16(acc[nt], ah, bh[0], bh[1]);
+      mma_bf16(acc[nt], ah, bl[0], bl[1]);
+      mma_bf16(acc[nt], al, bh[0], bh[1]);
+    }
+  }
+}
+
+// Sum of x over the four lanes that share a row of an MMA accumulator.
+__device__ __forceinline__ float quad_sum(float x) {
+  x += __shfl_xor_sync(0xffffffffu, x, 1);
+  x += __shfl_xor_sync(0xffffffffu, x, 2);
+  return x;
+}
+
+// Per (chunk slot, value head). Every product is a warp-MMA tile product of fp32 operands in
+// shared memory (mma_kmajor); warp w owns rows 16 (w % 4).. of each result and columns
+// 32 (w / 4).. of a 64-wide one (16 (w / 4).. of a 32-wide feature block).
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   extern __shared__ __align__(16) float sm[];
@@ -422,25 +463,30 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   float* dBv = dGv + 64;           // dbeta
   float* rsk = dBv + 64;           // (T^T dw)_i . k_i
   float* wsum = rsk + 64;          // W_i = exp(G_L - G_i) k_i . (v_new dS^T)_i
-  float* pv = wsum + 64;           // [64][8] partial row dots (T^T dv_new) . v
+  float* pv = wsum + 64;           // [64][8] partial row dots (T^T dv_new) . v (slots 0-1)
   float* pk = pv + 64 * 8;         // [64][8] partial row dots (T^T dw) . k
   float* pq = pk + 64 * 8;         // [64][8] partial row dots q . (dO S^T)
   float* pw = pq + 64 * 8;         // [64][8] partial row dots k . (v_new dS^T)
 
-  const int tid = threadIdx.x, hv = blockIdx.y, h = hv / p.HG;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, hv = blockIdx.y, h = hv / p.HG;
+  const int g = lane >> 2, c = 2 * (lane & 3), mt = warp & 3, nh = warp >> 2;
+  const int r0 = 16 * mt + g;  // this thread's accumulator rows: r0 and r0 + 8
   int t0, L, wslot;
   if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
   const size_t sl = (size_t)wslot * p.Hv + hv;
   auto kin = [&](int i, int f) { return ld_in<TIn>(p.k, ((size_t)(t0 + i) * p.H + h) * D + f); };
   auto qin = [&](int i, int f) { return ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + f); };
   auto vin = [&](int i, int f) { return ld_in<TIn>(p.v, ((size_t)(t0 + i) * p.Hv + hv) * D + f); };
+  // element (row, column) of accumulator entry (nt, e) of a 64-wide and a 32-wide result
+  auto col64 = [&](int nt, int e) { return 32 * nh + 8 * nt + c + (e & 1); };
+  auto col32 = [&](int nt, int e) { return 16 * nh + 8 * nt + c + (e & 1); };
+  auto row = [&](int e) { return r0 + 8 * (e >> 1); };
 
   if (tid < 64) {
     const bool ok = tid < L;
     G[tid] = ok ? p.g[(size_t)(t0 + tid) * p.Hv + hv] : 0.f;
     bt[tid] = ok ? p.beta[(size_t)(t0 + tid) * p.Hv + hv] : 0.f;
   }
-  for (int idx = tid; idx < 64 * kLd; idx += kThr) Tm[idx] = 0.f;
   __syncthreads();
   if (tid == 0) {
     float acc = 0.f;
@@ -455,7 +501,6 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
     eL[tid] = expf(G[63] - G[tid]);
   }
   // ---------------- K K^T and Q K^T (feature blocks of 32)
-  const int ti = (tid >> 4) * 4, tj = (tid & 15) * 4;  // 4 x 4 tile of a 64 x 64 matrix
   {
     float akk[4][4], aqk[4][4];
     zero(akk);
@@ -465,24 +510,22 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       load_fm(B0, L, tid, [&](int i, int f) { return kin(i, fb * 32 + f); });
       load_fm(B1, L, tid, [&](int i, int f) { return qin(i, fb * 32 + f); });
       __syncthreads();
-      if (tj <= ti) {
-        fma_tile<4, 4>(akk, B0, kLd, B0, kLd, ti, tj, 0, 32);
-        fma_tile<4, 4>(aqk, B1, kLd, B0, kLd, ti, tj, 0, 32);
-      }
+      mma_kmajor<4>(akk, B0, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+      mma_kmajor<4>(aqk, B1, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
     }
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) {
-        const int i = ti + a, j = tj + b;
+      for (int e = 0; e < 4; ++e) {
+        const int i = row(e), j = col64(nt, e);
         const float gam = j <= i ? expf(G[i] - G[j]) : 0.f;
-        GK[i * kLd + j] = j < i ? gam * akk[a][b] : 0.f;
-        Mm[i * kLd + j] = gam * aqk[a][b];
-        Tm[i * kLd + j] = j < i ? bt[i] * gam * akk[a][b] : 0.f;  // A
+        GK[i * kLd + j] = j < i ? gam * akk[nt][e] : 0.f;
+        Mm[i * kLd + j] = gam * aqk[nt][e];
+        Tm[i * kLd + j] = j < i ? bt[i] * gam * akk[nt][e] : 0.f;  // A
       }
   }
   __syncthreads();
-  tri_inverse_64_inplace(Tm, kLd, Xs, tid, kThr);  // Tm = T, ends synchronized
+  tri_inverse_64_tc<kThr / 32>(Tm, kLd, Xs, tid);  // Tm = T, ends synchronized
   for (int idx = tid; idx < 64 * 64; idx += kThr) {
     const int i = idx >> 6, j = idx & 63;
     Tt[j * kLd + i] = Tm[i * kLd + j];
@@ -493,7 +536,6 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   {
     float adp[4][4];
     zero(adp);
-    const int j0 = (tid >> 3) * 2, n0 = (tid & 7) * 4;  // 2 x 4 tile of a 64 x 32 block
     float rv[2] = {0.f, 0.f};
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
@@ -505,31 +547,36 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       load_fm(B3, L, tid, [&](int i, int f) { return vin(i, f0 + f); });
       load_tm(R0, 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + f0 + f]; });
       __syncthreads();
-      if (tj <= ti) fma_tile<4, 4>(adp, B0, kLd, B1, kLd, ti, tj, 0, 32);
-      fma_tile<4, 4>(az, B2, kLd, B3, kLd, ti, tj, 0, 32);
-      float tu[2][4];
+      mma_kmajor<4>(adp, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+      mma_kmajor<4>(az, B2, kLd, B3, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+      float tu[2][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
       zero(tu);
-      fma_tile<2, 4>(tu, Tm, kLd, R0, kLt, j0, n0, j0, 64);  // T[i][j] = 0 for i < j
+      mma_kmajor<2>(tu, Tm, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int j = j0 + a;
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          rv[a] = fmaf(tu[a][b], B3[(n0 + b) * kLd + j], rv[a]);
-          if (j < L) p.dv[((size_t)(t0 + j) * p.Hv + hv) * D + f0 + n0 + b] = bt[j] * tu[a][b];
+        for (int e = 0; e < 4; ++e) {
+          const int j = row(e), n = col32(nt, e);
+          rv[e >> 1] = fmaf(tu[nt][e], B3[n * kLd + j], rv[e >> 1]);
+          if (j < L) p.dv[((size_t)(t0 + j) * p.Hv + hv) * D + f0 + n] = bt[j] * tu[nt][e];
         }
-      }
+    }
+    rv[0] = quad_sum(rv[0]);
+    rv[1] = quad_sum(rv[1]);
+    if ((lane & 3) == 0) {
+      pv[r0 * 8 + nh] = rv[0];
+      pv[(r0 + 8) * 8 + nh] = rv[1];
     }
 #pragma unroll
-    for (int a = 0; a < 2; ++a) pv[(j0 + a) * 8 + (tid & 7)] = rv[a];
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
-#pragma unroll
-      for (int b = 0; b < 4; ++b) dP[(ti + a) * kLd + tj + b] = (tj + b <= ti + a) ? p.scale * adp[a][b] : 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const int i = row(e), j = col64(nt, e);
+        dP[i * kLd + j] = j <= i ? p.scale * adp[nt][e] : 0.f;
+      }
   }
   // ---------------- key features: Z2, T^T dw (the dk and dbeta / dG parts)
   {
-    const int j0 = (tid >> 3) * 2, n0 = (tid & 7) * 4;
     float rk[2] = {0.f, 0.f};
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
@@ -541,52 +588,61 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       {  // Z2[i][j] = sum_d dw[i][d] exp(G_j) k[j][d]: scale column j after the sum
         float z2[4][4];
         zero(z2);
-        fma_tile<4, 4>(z2, B0, kLd, B1, kLd, ti, tj, 0, 32);
+        mma_kmajor<4>(z2, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
 #pragma unroll
-        for (int a = 0; a < 4; ++a)
+        for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-          for (int b = 0; b < 4; ++b) az[a][b] = fmaf(eG[tj + b], z2[a][b], az[a][b]);
+          for (int e = 0; e < 4; ++e) az[nt][e] = fmaf(eG[col64(nt, e)], z2[nt][e], az[nt][e]);
       }
       float tw[2][4];
       zero(tw);
-      fma_tile<2, 4>(tw, Tm, kLd, R0, kLt, j0, n0, j0, 64);
+      mma_kmajor<2>(tw, Tm, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int j = j0 + a;
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          rk[a] = fmaf(tw[a][b], B1[(n0 + b) * kLd + j], rk[a]);
-          p.ttdw[sl * 64 * D + (size_t)j * D + f0 + n0 + b] = tw[a][b];
+        for (int e = 0; e < 4; ++e) {
+          const int j = row(e), n = col32(nt, e);
+          rk[e >> 1] = fmaf(tw[nt][e], B1[n * kLd + j], rk[e >> 1]);
+          p.ttdw[sl * 64 * D + (size_t)j * D + f0 + n] = tw[nt][e];
         }
-      }
     }
-#pragma unroll
-    for (int a = 0; a < 2; ++a) pk[(j0 + a) * 8 + (tid & 7)] = rk[a];
+    rk[0] = quad_sum(rk[0]);
+    rk[1] = quad_sum(rk[1]);
+    if ((lane & 3) == 0) {
+      pk[r0 * 8 + nh] = rk[0];
+      pk[(r0 + 8) * 8 + nh] = rk[1];
+    }
   }
   // Z = (Z1 + Z2) diag(beta)
 #pragma unroll
-  for (int a = 0; a < 4; ++a)
+  for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-    for (int b = 0; b < 4; ++b) Zm[(ti + a) * kLd + tj + b] = bt[tj + b] * az[a][b];
+    for (int e = 0; e < 4; ++e) {
+      const int j = col64(nt, e);
+      Zm[row(e) * kLd + j] = bt[j] * az[nt][e];
+    }
   __syncthreads();
-  {  // Tp = Z^T T   (T[i][j] = 0 for i < j)
+  {  // Tp = Z^T T   (T[k][j] = 0 for k < j)
     float acc[4][4];
     zero(acc);
-    fma_tile<4, 4>(acc, Zm, kLd, Tm, kLd, ti, tj, tj, 64);
+    mma_kmajor<4>(acc, Zm, kLd, Tm, kLd, 16 * mt, 32 * nh, 0, 64, lane);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) Tp[(ti + a) * kLd + tj + b] = acc[a][b];
+      for (int e = 0; e < 4; ++e) Tp[row(e) * kLd + col64(nt, e)] = acc[nt][e];
   }
   __syncthreads();
   {  // dA[j][m] = -sum_l Tp[l][j] T[m][l] on the strict lower triangle (T[m][l] = 0 for l > m)
     float acc[4][4];
     zero(acc);
-    if (tj <= ti) fma_tile<4, 4>(acc, Tp, kLd, Tt, kLd, ti, tj, 0, tj + 4);
+    mma_kmajor<4>(acc, Tp, kLd, Tt, kLd, 16 * mt, 32 * nh, 0, 64, lane);
 #pragma unroll
-    for (int a = 0; a < 4; ++a)
+    for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
-      for (int b = 0; b < 4; ++b) Zm[(ti + a) * kLd + tj + b] = (tj + b < ti + a) ? -acc[a][b] : 0.f;
+      for (int e = 0; e < 4; ++e) {
+        const int i = row(e), j = col64(nt, e);
+        Zm[i * kLd + j] = j < i ? -acc[nt][e] : 0.f;
+      }
   }
   __syncthreads();
   // ---------------- row and column sums: dbeta and dG parts from A and from dP
@@ -601,11 +657,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       dg -= Zm[j * kLd + i] * bt[j] * GK[j * kLd + i];    // column of dA * A
       dg -= dP[j * kLd + i] * Mm[j * kLd + i];            // column of dP * M
     }
-    float sv = 0.f, sk = 0.f;
-    for (int c = 0; c < 8; ++c) {
-      sv += pv[i * 8 + c];
-      sk += pk[i * 8 + c];
-    }
+    const float sv = pv[i * 8] + pv[i * 8 + 1], sk = pk[i * 8] + pk[i * 8 + 1];
     rsk[i] = sk;
     dBv[i] = sv + eG[i] * sk + db;
     dGv[i] = dg + bt[i] * eG[i] * sk;
@@ -627,7 +679,6 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   }
   // ---------------- key features again: dq and dk parts of this value head
   {
-    const int i0 = (tid >> 3) * 2, d0 = (tid & 7) * 4;
     float rq[2] = {0.f, 0.f}, rw[2] = {0.f, 0.f};
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
@@ -638,38 +689,38 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       float aq[2][4], ak[2][4];
       zero(aq);
       zero(ak);
-      fma_tile<2, 4>(aq, Tp, kLd, R0, kLt, i0, d0, 0, i0 + 2);   // (PG K)[i]: j <= i
-      fma_tile<2, 4>(ak, dP, kLd, R1, kLt, i0, d0, i0, 64);      // (PG^T Q)[i]: l >= i
-      fma_tile<2, 4>(ak, GK, kLd, R0, kLt, i0, d0, 0, 64);       // (dAt + dAt^T) K
+      mma_kmajor<2>(aq, Tp, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG K)[i]
+      mma_kmajor<2>(ak, dP, kLd, R1, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG^T Q)[i]
+      mma_kmajor<2>(ak, GK, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (dAt + dAt^T) K
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        const int i = i0 + a;
-        const size_t row = sl * 64 * D + (size_t)i * D + f0 + d0;
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          const float os = p.dos[row + b], y = p.ys[row + b], tw = p.ttdw[row + b];
-          const float qv = R1[i * kLt + d0 + b], kv = R0[i * kLt + d0 + b];
-          rq[a] = fmaf(qv, os, rq[a]);
-          rw[a] = fmaf(kv, y, rw[a]);
-          p.dqp[row + b] = fmaf(p.scale * eG[i], os, aq[a][b]);
-          p.dkp[row + b] = ak[a][b] + eL[i] * y + bt[i] * eG[i] * tw;
+        for (int e = 0; e < 4; ++e) {
+          const int i = row(e), d = col32(nt, e);
+          const size_t at = sl * 64 * D + (size_t)i * D + f0 + d;
+          const float os = p.dos[at], y = p.ys[at], tw = p.ttdw[at];
+          const float qv = R1[i * kLt + d], kv = R0[i * kLt + d];
+          rq[e >> 1] = fmaf(qv, os, rq[e >> 1]);
+          rw[e >> 1] = fmaf(kv, y, rw[e >> 1]);
+          p.dqp[at] = fmaf(p.scale * eG[i], os, aq[nt][e]);
+          p.dkp[at] = ak[nt][e] + eL[i] * y + bt[i] * eG[i] * tw;
         }
-      }
     }
-#pragma unroll
-    for (int a = 0; a < 2; ++a) {
-      pq[(i0 + a) * 8 + (tid & 7)] = rq[a];
-      pw[(i0 + a) * 8 + (tid & 7)] = rw[a];
+    rq[0] = quad_sum(rq[0]);
+    rq[1] = quad_sum(rq[1]);
+    rw[0] = quad_sum(rw[0]);
+    rw[1] = quad_sum(rw[1]);
+    if ((lane & 3) == 0) {
+      pq[r0 * 8 + nh] = rq[0];
+      pq[(r0 + 8) * 8 + nh] = rq[1];
+      pw[r0 * 8 + nh] = rw[0];
+      pw[(r0 + 8) * 8 + nh] = rw[1];
     }
   }
   __syncthreads();
   if (tid < 64) {
     const int i = tid;
-    float sq = 0.f, sw = 0.f;
-    for (int c = 0; c < 8; ++c) {
-      sq += pq[i * 8 + c];
-      sw += pw[i * 8 + c];
-    }
+    const float sq = pq[i * 8] + pq[i * 8 + 1], sw = pw[i * 8] + pw[i * 8 + 1];
     wsum[i] = eL[i] * sw;
     dGv[i] += p.scale * eG[i] * sq - eL[i] * sw;
   }
