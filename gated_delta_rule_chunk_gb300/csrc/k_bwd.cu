@@ -384,17 +384,35 @@ constexpr size_t chunk_floats() {
   return (size_t)7 * 64 * kLd + 16 * kLd + 4 * 32 * kLd + 2 * 64 * kLt + 8 * 64 + 4 * 64 * 8;
 }
 
-// Load a [64 x 32] block of a token-major source as feature-major [32][kLd] (rows of the
-// chunk past L are zero). get(i, f) returns the value of token i, feature f.
+// A [64 x 32] block of a token-major source (tokens x 32 features) held in registers,
+// 8 elements per thread (element idx = tid + 256 u: token idx / 32, feature idx % 32), so
+// that the next block's loads are in flight while the current one is used.
+struct Blk {
+  float r[8];
+};
+// get(i, f) returns token i, feature f; tokens at or past L read as zero.
 template <typename Get>
-__device__ __forceinline__ void load_fm(float* dst, int L, int tid, Get get) {
-  staged_copy<8>(64 * 32, tid, kThr, [&](int idx) { return (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f; },
-                 [&](int idx, float x) { dst[(idx & 31) * kLd + (idx >> 5)] = x; });
+__device__ __forceinline__ void load_blk(Blk& b, int L, int tid, Get get) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int idx = tid + u * kThr;
+    b.r[u] = (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f;
+  }
 }
-template <typename Get>
-__device__ __forceinline__ void load_tm(float* dst, int L, int tid, Get get) {
-  staged_copy<8>(64 * 32, tid, kThr, [&](int idx) { return (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f; },
-                 [&](int idx, float x) { dst[(idx >> 5) * kLt + (idx & 31)] = x; });
+// ... stored feature-major [32][kLd] or token-major [64][kLt]
+__device__ __forceinline__ void store_fm(float* dst, const Blk& b, int tid) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int idx = tid + u * kThr;
+    dst[(idx & 31) * kLd + (idx >> 5)] = b.r[u];
+  }
+}
+__device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid) {
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    const int idx = tid + u * kThr;
+    dst[(idx >> 5) * kLt + (idx & 31)] = b.r[u];
+  }
 }
 
 // acc[nt] += sum_{k0 <= k < k1} X[k][m0 + r] Y[k][n0 + 8 nt + c'] over a 16 x 8 NT warp
@@ -501,15 +519,22 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
     eL[tid] = expf(G[63] - G[tid]);
   }
   // ---------------- K K^T and Q K^T (feature blocks of 32)
+  Blk bk, bq;  // k and q blocks (also the last stage's)
   {
     float akk[4][4], aqk[4][4];
     zero(akk);
     zero(aqk);
+    load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f); });
+    load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f); });
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
-      load_fm(B0, L, tid, [&](int i, int f) { return kin(i, fb * 32 + f); });
-      load_fm(B1, L, tid, [&](int i, int f) { return qin(i, fb * 32 + f); });
+      store_fm(B0, bk, tid);
+      store_fm(B1, bq, tid);
       __syncthreads();
+      if (fb + 1 < D / 32) {  // the next block's loads run under this block's products
+        load_blk(bk, L, tid, [&](int i, int f) { return kin(i, (fb + 1) * 32 + f); });
+        load_blk(bq, L, tid, [&](int i, int f) { return qin(i, (fb + 1) * 32 + f); });
+      }
       mma_kmajor<4>(akk, B0, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
       mma_kmajor<4>(aqk, B1, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
     }
@@ -524,6 +549,21 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
         Tm[i * kLd + j] = j < i ? bt[i] * gam * akk[nt][e] : 0.f;  // A
       }
   }
+  // value-feature blocks (dO, v_new, dv_new, v) of features f0..f0+31
+  Blk bdo, bvn, bdv, bv;
+  auto load_value_blocks = [&](int f0) {
+    load_blk(bdo, L, tid, [&](int i, int f) { return ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + f0 + f); });
+    load_blk(bvn, 64, tid, [&](int i, int f) { return p.vn[sl * 64 * D + (size_t)i * D + f0 + f]; });
+    load_blk(bdv, 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + f0 + f]; });
+    load_blk(bv, L, tid, [&](int i, int f) { return vin(i, f0 + f); });
+  };
+  // key-feature blocks (dw, k) of features f0..f0+31
+  Blk bdw, bk2;
+  auto load_key_blocks = [&](int f0) {
+    load_blk(bdw, 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + f0 + f]; });
+    load_blk(bk2, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
+  };
+  load_value_blocks(0);  // in flight during the inverse
   __syncthreads();
   tri_inverse_64_tc<kThr / 32>(Tm, kLd, Xs, tid);  // Tm = T, ends synchronized
   for (int idx = tid; idx < 64 * 64; idx += kThr) {
@@ -540,13 +580,16 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
       const int f0 = fb * 32;
-      load_fm(B0, L, tid, [&](int i, int f) {
-        return ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + f0 + f); });
-      load_fm(B1, 64, tid, [&](int i, int f) { return p.vn[sl * 64 * D + (size_t)i * D + f0 + f]; });
-      load_fm(B2, 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + f0 + f]; });
-      load_fm(B3, L, tid, [&](int i, int f) { return vin(i, f0 + f); });
-      load_tm(R0, 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + f0 + f]; });
+      store_fm(B0, bdo, tid);
+      store_fm(B1, bvn, tid);
+      store_fm(B2, bdv, tid);
+      store_fm(B3, bv, tid);
+      store_tm(R0, bdv, tid);
       __syncthreads();
+      if (fb + 1 < D / 32)
+        load_value_blocks(f0 + 32);
+      else
+        load_key_blocks(0);
       mma_kmajor<4>(adp, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
       mma_kmajor<4>(az, B2, kLd, B3, kLd, 16 * mt, 32 * nh, 0, 32, lane);
       float tu[2][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
@@ -581,10 +624,11 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
       const int f0 = fb * 32;
-      load_fm(B0, 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + f0 + f]; });
-      load_fm(B1, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
-      load_tm(R0, 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + f0 + f]; });
+      store_fm(B0, bdw, tid);
+      store_fm(B1, bk2, tid);
+      store_tm(R0, bdw, tid);
       __syncthreads();
+      if (fb + 1 < D / 32) load_key_blocks(f0 + 32);
       {  // Z2[i][j] = sum_d dw[i][d] exp(G_j) k[j][d]: scale column j after the sum
         float z2[4][4];
         zero(z2);
@@ -680,12 +724,18 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   // ---------------- key features again: dq and dk parts of this value head
   {
     float rq[2] = {0.f, 0.f}, rw[2] = {0.f, 0.f};
+    load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f); });
+    load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f); });
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
       const int f0 = fb * 32;
-      load_tm(R0, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
-      load_tm(R1, L, tid, [&](int i, int f) { return qin(i, f0 + f); });
+      store_tm(R0, bk, tid);
+      store_tm(R1, bq, tid);
       __syncthreads();
+      if (fb + 1 < D / 32) {
+        load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f0 + 32 + f); });
+        load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f0 + 32 + f); });
+      }
       float aq[2][4], ak[2][4];
       zero(aq);
       zero(ak);
