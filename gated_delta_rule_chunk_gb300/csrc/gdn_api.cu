@@ -362,7 +362,7 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   b.status = p.status; b.seq_info = p.seq_info; b.chunk_offsets = p.chunk_offsets;
   b.chunk_table = table;
   if (tc) {
-    b.wimg = ws + L.w; b.mimg = ws + L.M; b.k16 = p.k16; b.G = p.G;
+    b.wimg = ws + L.w; b.mimg = ws + L.M; b.G = p.G;
   } else {
     b.wT = f32(L.w); b.kt = p.kt; b.qt = p.qt; b.MT = f32(L.M); b.gam = p.gam;
   }

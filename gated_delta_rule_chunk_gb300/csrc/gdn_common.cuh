@@ -82,7 +82,6 @@ struct BwdParams {
   // ... or the tensor-core path's bridge (bf16 inputs)
   const void* wimg;          // [slot] bf16 w image (two swizzled [64][128 B] halves)
   const void* mimg;          // [slot] bf16 M hi/lo image ([128][128 B], swizzled)
-  const void* k16;           // [chunk slot, key head] fp16 k image (swizzled halves)
   const float* G;            // [slot][64] in-chunk cumulative gate
   const float* hs;           // [slot][D][D] chunk-start state, [dv][dk]
   const float* vn;           // [slot][64][D] v_new
@@ -232,7 +231,7 @@ bool launch_gen_inter(const Params& p, int D, cudaStream_t s);
 // tc_bridge: the forward quantities are the tensor-core path's bridge (bf16 inputs).
 bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, bool tc_bridge, cudaStream_t s,
                 cudaEvent_t* ev);
-bool launch_bwd_scan_tc(const BwdParams& p, cudaStream_t s);
+bool launch_bwd_scan_tc(const BwdParams& p, int D, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, bool channel_gates, cudaStream_t s);
 bool launch_kda_intra(const Params& p, cudaStream_t s);

@@ -44,19 +44,12 @@ __device__ __forceinline__ float ld_dout(const BwdParams& p, size_t idx) {
 template <int D>
 constexpr size_t scan_floats() {
   constexpr int BV = bv_of<D>(), SLD = BV + 4, LQ = D + 4;
-  return (size_t)D * SLD + D * 68 + 64 * 68 + 2 * 64 * LQ + 2 * 64 * BV + D + 128;
+  return (size_t)D * SLD + D * 68 + 64 * 68 + 2 * 64 * LQ + 2 * 64 * BV + D;
 }
 
-// Element (r, c) of a two-half [64][128] tile with the 128-byte swizzle (16-bit elements).
-__device__ __forceinline__ uint32_t sw_elem(int r, int c) {
-  return (uint32_t)(c >> 6) * 8192u + (uint32_t)r * 128u +
-         ((uint32_t)(((c & 63) >> 3) ^ (r & 7)) << 4) + (uint32_t)(c & 7) * 2u;
-}
-
-// TC: the forward quantities come from the tensor-core path's bridge (bf16 inputs):
-// Kt = exp(G_L - G) k from the fp16 k image, Qt = exp(G) q from q itself, w and M from
-// their bf16 images (M = hi + lo), exp(G_L) from the in-chunk gate sums.
-template <int D, bool TC>
+// fp32 SIMT reverse scan (fp32 inputs): the forward quantities are the general path's
+// fp32 tiles (Kt = exp(G_L - G) k, Qt^T = (exp(G) q)^T, w^T, M^T, exp(G_L) per key row).
+template <int D>
 __global__ void __launch_bounds__(kThr) bwd_scan_kernel(BwdParams p) {
   constexpr int BV = bv_of<D>(), SLD = BV + 4, LQ = D + 4, RN = BV / 16;
   extern __shared__ __align__(16) float sm[];
@@ -68,8 +61,6 @@ __global__ void __launch_bounds__(kThr) bwd_scan_kernel(BwdParams p) {
   float* dO = Wr + 64 * LQ;        // [64][BV]
   float* dV = dO + 64 * BV;        // [64][BV] dv_new
   float* gm = dV + 64 * BV;        // [D]
-  float* fk = gm + D;              // [64] exp(G_L - G_r) (tensor-core bridge)
-  float* fq = fk + 64;             // [64] exp(G_r)
 
   const int tid = threadIdx.x;
   const int n = blockIdx.x, hv = blockIdx.y, c0 = blockIdx.z * BV;
@@ -88,89 +79,34 @@ __global__ void __launch_bounds__(kThr) bwd_scan_kernel(BwdParams p) {
     const size_t sl = (size_t)(sv.first_slot + c) * p.Hv + hv;
     const int t0 = sv.start + kChunk * c;
     const int L = min(kChunk, sv.len - kChunk * c);
-    if constexpr (TC) {
-      const int h = hv / p.HG;
-      const float* Gc = p.G + sl * 64;
-      const unsigned char* kim =
-          static_cast<const unsigned char*>(p.k16) + ((size_t)(sv.first_slot + c) * p.H + h) * 16384;
-      const unsigned char* wim = static_cast<const unsigned char*>(p.wimg) + sl * 16384;
-      const unsigned char* mim = static_cast<const unsigned char*>(p.mimg) + sl * 16384;
-      const __nv_bfloat16* qg = reinterpret_cast<const __nv_bfloat16*>(p.q);
-      if (tid < 64) {  // row factors exp(G_L - G_r) (k) and exp(G_r) (q)
-        fk[tid] = __expf(Gc[63] - Gc[tid]);
-        fq[tid] = __expf(Gc[tid]);
-      }
-      __syncthreads();
-      // 16-byte pieces (8 elements) of row r, features 8 ch .. 8 ch + 7. The k image goes
-      // to a feature-major tile, so its lanes run along rows (conflict-free stores).
-      for (int it = tid; it < 64 * (D / 8); it += kThr) {
-        const int r = it & 63, ch = it >> 6;
-        const uint4 kr = *reinterpret_cast<const uint4*>(kim + sw_elem(r, 8 * ch));
-        const __half* kh = reinterpret_cast<const __half*>(&kr);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) KtT[(8 * ch + e) * 68 + r] = fk[r] * __half2float(kh[e]);
-      }
-      for (int it = tid; it < 64 * (D / 8); it += kThr) {
-        const int r = it / (D / 8), ch = it % (D / 8);
-        const uint4 wr = *reinterpret_cast<const uint4*>(wim + sw_elem(r, 8 * ch));
-        const uint4 qr = r < L ? *reinterpret_cast<const uint4*>(qg + ((size_t)(t0 + r) * p.H + h) * D + 8 * ch)
-                               : make_uint4(0u, 0u, 0u, 0u);
-        const __nv_bfloat16* wb = reinterpret_cast<const __nv_bfloat16*>(&wr);
-        const __nv_bfloat16* qb = reinterpret_cast<const __nv_bfloat16*>(&qr);
-        float qv[8], wv[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          qv[e] = fq[r] * __bfloat162float(qb[e]);
-          wv[e] = __bfloat162float(wb[e]);
-        }
-        float4* qd = reinterpret_cast<float4*>(Qr + r * LQ + 8 * ch);
-        float4* wd = reinterpret_cast<float4*>(Wr + r * LQ + 8 * ch);
-        qd[0] = make_float4(qv[0], qv[1], qv[2], qv[3]);
-        qd[1] = make_float4(qv[4], qv[5], qv[6], qv[7]);
-        wd[0] = make_float4(wv[0], wv[1], wv[2], wv[3]);
-        wd[1] = make_float4(wv[4], wv[5], wv[6], wv[7]);
-      }
-      for (int it = tid; it < 64 * 8; it += kThr) {  // M[t][j] = hi + lo
-        const int t = it >> 3, ch = it & 7;
-        const uint32_t so = sw_elem(t, 8 * ch);
-        const uint4 hr = *reinterpret_cast<const uint4*>(mim + so);
-        const uint4 lr = *reinterpret_cast<const uint4*>(mim + 8192 + so);
-        const __nv_bfloat16* hb = reinterpret_cast<const __nv_bfloat16*>(&hr);
-        const __nv_bfloat16* lb = reinterpret_cast<const __nv_bfloat16*>(&lr);
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-          Mr[t * 68 + 8 * ch + e] = __bfloat162float(hb[e]) + __bfloat162float(lb[e]);
-      }
-    } else {
-      if (tid == 0 && c > 0) {  // the next (earlier) chunk's tiles into L2 while this one runs
-        const size_t pl = sl - p.Hv;
-        bulk_prefetch_l2(p.kt + pl * 64 * D, 64 * D * 4);
-        bulk_prefetch_l2(p.qt + pl * 64 * D, 64 * D * 4);
-        bulk_prefetch_l2(p.wT + pl * 64 * D, 64 * D * 4);
-        bulk_prefetch_l2(p.MT + pl * 4096, 4096 * 4);
-      }
-      const float* kt = p.kt + sl * 64 * D;
-      const float* qt = p.qt + sl * 64 * D;
-      const float* wt = p.wT + sl * 64 * D;
-      const float* mt = p.MT + sl * 4096;
-      // Kt rows (lanes along features) into Kt^T; Qt^T and w^T rows (lanes along tokens)
-      // into token-major tiles; M^T[i][t] = M[t][i] into M
-      staged_copy<8>(64 * D, tid, kThr, [&](int i) { return kt[i]; },
-                     [&](int i, float x) { KtT[(i % D) * 68 + i / D] = x; });
-      staged_copy<8>(64 * D, tid, kThr, [&](int i) { return qt[i]; },
-                     [&](int i, float x) { Qr[(i % 64) * LQ + i / 64] = x; });
-      staged_copy<8>(64 * D, tid, kThr, [&](int i) { return wt[i]; },
-                     [&](int i, float x) { Wr[(i % 64) * LQ + i / 64] = x; });
-      staged_copy<8>(64 * 64, tid, kThr, [&](int i) { return mt[i]; },
-                     [&](int i, float x) { Mr[(i & 63) * 68 + (i >> 6)] = x; });
+    if (tid == 0 && c > 0) {  // the next (earlier) chunk's tiles into L2 while this one runs
+      const size_t pl = sl - p.Hv;
+      bulk_prefetch_l2(p.kt + pl * 64 * D, 64 * D * 4);
+      bulk_prefetch_l2(p.qt + pl * 64 * D, 64 * D * 4);
+      bulk_prefetch_l2(p.wT + pl * 64 * D, 64 * D * 4);
+      bulk_prefetch_l2(p.MT + pl * 4096, 4096 * 4);
     }
+    const float* kt = p.kt + sl * 64 * D;
+    const float* qt = p.qt + sl * 64 * D;
+    const float* wt = p.wT + sl * 64 * D;
+    const float* mt = p.MT + sl * 4096;
+    // Kt rows (lanes along features) into Kt^T; Qt^T and w^T rows (lanes along tokens)
+    // into token-major tiles; M^T[i][t] = M[t][i] into M
+    staged_copy<8>(64 * D, tid, kThr, [&](int i) { return kt[i]; },
+                   [&](int i, float x) { KtT[(i % D) * 68 + i / D] = x; });
+    staged_copy<8>(64 * D, tid, kThr, [&](int i) { return qt[i]; },
+                   [&](int i, float x) { Qr[(i % 64) * LQ + i / 64] = x; });
+    staged_copy<8>(64 * D, tid, kThr, [&](int i) { return wt[i]; },
+                   [&](int i, float x) { Wr[(i % 64) * LQ + i / 64] = x; });
+    staged_copy<8>(64 * 64, tid, kThr, [&](int i) { return mt[i]; },
+                   [&](int i, float x) { Mr[(i & 63) * 68 + (i >> 6)] = x; });
     staged_copy<8>(64 * BV, tid, kThr,
                    [&](int i) {
                      return i / BV < L ? ld_dout(p, ((size_t)(t0 + i / BV) * p.Hv + hv) * D + c0 + i % BV)
                                        : 0.f;
                    },
                    [&](int i, float x) { dO[i] = x; });
-    for (int d = tid; d < D; d += kThr) gm[d] = TC ? __expf(p.G[sl * 64 + 63]) : p.gam[sl * D + d];
+    for (int d = tid; d < D; d += kThr) gm[d] = p.gam[sl * D + d];
     __syncthreads();
     {  // the incoming gradient is this chunk's dS_next; keep it for the chunk kernels
       float* dh = p.dhs + sl * D * D;
@@ -816,13 +752,13 @@ bool launch_bwd_t(const BwdParams& p, cudaStream_t s, cudaEvent_t* ev) {
   const int s1 = (int)(scan_floats<D>() * sizeof(float));
   const int s2 = (int)state_mma_bytes<D>();
   const int s3 = (int)(chunk_floats() * sizeof(float));
-  ensure_smem_limit((const void*)bwd_scan_kernel<D, TC>, s1);
+  if (!TC) ensure_smem_limit((const void*)bwd_scan_kernel<D>, s1);
   ensure_smem_limit((const void*)bwd_state_kernel<D>, s2);
   ensure_smem_limit((const void*)bwd_chunk_kernel<TIn, D>, s3);
-  if (TC && D == 128) {  // the tensor-core bridge at d = 128: the warp-MMA scan
-    if (!launch_bwd_scan_tc(p, s)) return false;
+  if constexpr (TC) {  // the tensor-core bridge (bf16 inputs): the warp-MMA scan
+    if (!launch_bwd_scan_tc(p, D, s)) return false;
   } else {
-    bwd_scan_kernel<D, TC><<<dim3(p.N, p.Hv, D / BV), kThr, s1, s>>>(p);
+    bwd_scan_kernel<D><<<dim3(p.N, p.Hv, D / BV), kThr, s1, s>>>(p);
   }
   if (ev) cudaEventRecord(ev[0], s);
   if (p.nt_max > 0) bwd_state_kernel<D><<<dim3(p.nt_max, p.Hv), kThr, s2, s>>>(p);

@@ -1,5 +1,5 @@
-// Reverse scan of the backward pass on warp-level tensor-core MMAs (bf16 inputs,
-// d = 128, scalar gates): the state-gradient recurrence of the chunked gated delta
+// Reverse scan of the backward pass on warp-level tensor-core MMAs (bf16 inputs, head
+// size 128, or 64 zero-padded to 128; scalar gates): the state-gradient recurrence of the chunked gated delta
 // rule, walking the chunks of each (sequence, value head, 32-column value block) from
 // last to first.
 //
@@ -34,7 +34,7 @@ namespace gdn {
 
 namespace {
 
-constexpr int kD = 128;
+constexpr int kD = 128;  // key rows of the computed state (a head size of 64 is zero-padded)
 constexpr int BV = 32;
 constexpr int kCompWarps = 8;
 constexpr int kLoadWarp = kCompWarps;
@@ -86,7 +86,7 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
 
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmq) {
+                   const __grid_constant__ CUtensorMap tmq, int D) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
@@ -94,7 +94,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + oMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n = blockIdx.x, hv = blockIdx.y, c0 = blockIdx.z * BV, h = hv / p.HG;
-  const size_t state_base = ((size_t)n * p.Hv + hv) * kD * kD;
+  const size_t state_base = ((size_t)n * p.Hv + hv) * D * D;  // [dv][dk] with head size D
 
   if (tid == 0) {
     mbar_init(&bars[0], 1);
@@ -147,7 +147,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int d = 16 * warp + g + (e >> 1) * 8, j = 8 * nt + c2 + (e & 1);
-        dS[nt][e] = p.dfin ? p.dfin[state_base + (size_t)(c0 + j) * kD + d] : 0.f;
+        dS[nt][e] = (p.dfin && d < D) ? p.dfin[state_base + (size_t)(c0 + j) * D + d] : 0.f;
       }
     auto store_ds_split = [&]() {
       unsigned char* b = sm + oDS;
@@ -169,7 +169,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
     auto load_do = [&](int c) {
       const int t0 = sv.start + kChunk * c, L = min(kChunk, sv.len - kChunk * c);
       if (pr < L) {
-        const size_t idx = ((size_t)(t0 + pr) * p.Hv + hv) * kD + c0 + pq;
+        const size_t idx = ((size_t)(t0 + pr) * p.Hv + hv) * D + c0 + pq;
         if (p.dout_bf16) {
           const uint4 r = *reinterpret_cast<const uint4*>(
               reinterpret_cast<const __nv_bfloat16*>(p.dout) + idx);
@@ -204,13 +204,13 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
       unsigned char* st = sm + s * kSlot;
       const uint32_t st_a = sbase + s * kSlot;
       {  // the incoming gradient is this chunk's dS_next: kept for the chunk kernels
-        float* dh = p.dhs + sl * kD * kD;
+        float* dh = p.dhs + sl * D * D;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int d = 16 * warp + g + (e >> 1) * 8, j = 8 * nt + c2 + (e & 1);
-            dh[(size_t)(c0 + j) * kD + d] = dS[nt][e];
+            if (d < D) dh[(size_t)(c0 + j) * D + d] = dS[nt][e];
           }
       }
       wait_phase(&bars[s], (uint32_t)((m >> 1) & 1), abort_flag);
@@ -309,7 +309,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
             const int j = 16 * np + 8 * q + c2;
             const float v0 = fmaf(fk, x1[q][2 * hh], p.scale * x2[q][2 * hh]);
             const float v1 = fmaf(fk, x1[q][2 * hh + 1], p.scale * x2[q][2 * hh + 1]);
-            *reinterpret_cast<float2*>(p.dvn + (sl * 64 + i) * kD + c0 + j) = make_float2(v0, v1);
+            *reinterpret_cast<float2*>(p.dvn + (sl * 64 + i) * D + c0 + j) = make_float2(v0, v1);
             uint32_t hi, lo;
             split_pack2(v0, v1, hi, lo);
             *reinterpret_cast<uint32_t*>(vn + mn_off(j, i)) = hi;
@@ -362,7 +362,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int d = 16 * warp + g + (e >> 1) * 8, j = 8 * nt + c2 + (e & 1);
-          p.dh0[state_base + (size_t)(c0 + j) * kD + d] = dS[nt][e];
+          if (d < D) p.dh0[state_base + (size_t)(c0 + j) * D + d] = dS[nt][e];
         }
     }
   }
@@ -372,13 +372,17 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
 
 }  // namespace
 
-bool launch_bwd_scan_tc(const BwdParams& p, cudaStream_t s) {
+bool launch_bwd_scan_tc(const BwdParams& p, int D, cudaStream_t s) {
+  if (D != 64 && D != kD) return false;
   CUtensorMap tmk, tmq;
   const int rows = p.T > 0 ? p.T : 1;  // with T = 0 no tile is ever loaded
-  if (!encode_rows_tmap(&tmk, p.k, rows, p.H, kD) || !encode_rows_tmap(&tmq, p.q, rows, p.H, kD))
+  // With D = 64 the second key-dim half of every k and q tile lies outside the tensor and
+  // is filled with zeros, and so are the bridge's w columns 64..127: the padded rows of
+  // dS stay zero.
+  if (!encode_rows_tmap(&tmk, p.k, rows, p.H, D) || !encode_rows_tmap(&tmq, p.q, rows, p.H, D))
     return false;
   ensure_smem_limit((const void*)bwd_scan_tc_kernel, (int)kSmemBytes);
-  bwd_scan_tc_kernel<<<dim3(p.N, p.Hv, kD / BV), kThreads, kSmemBytes, s>>>(p, tmk, tmq);
+  bwd_scan_tc_kernel<<<dim3(p.N, p.Hv, D / BV), kThreads, kSmemBytes, s>>>(p, tmk, tmq, D);
   return cudaPeekAtLastError() == cudaSuccess;
 }
 
