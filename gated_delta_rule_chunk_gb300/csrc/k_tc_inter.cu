@@ -281,6 +281,18 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       unsigned char* st = sm + (c % kRing) * kSlot;
       const uint32_t st_a = sbase + (c % kRing) * kSlot;
       wait_ring<kRing>(bars, B_FULL, c, abort_flag);
+      // Row factors of this chunk, formed before X so that their latency hides under its
+      // MMAs: exp(G_L - G_i) of this thread's two v_new rows (per-channel gates: inside the
+      // k image) and the state decay of its two key rows (exp(G_L), or per channel).
+      float fac[2], gam0, gam1;
+      {
+        const float* gst = reinterpret_cast<const float*>(st + kG);
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          fac[hh] = CH ? 1.f : expf(gst[63] - gst[16 * (warp & 3) + g + 8 * hh]);
+        gam0 = CH ? gst[16 * warp + g] : expf(gst[63]);
+        gam1 = CH ? gst[16 * warp + g + 8] : gam0;
+      }
       if (p.hs) {  // chunk-start state, [dv][dk] rows of the slot (the backward's recompute)
         float* hs = p.hs + ((size_t)(sv.first_slot + c) * p.Hv + hv) * p.D * p.D;
 #pragma unroll
@@ -323,14 +335,11 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       // v_new = u - X; vn (bf16 hi|lo) for the output MMA; vh (fp16) for the state update.
       if (c >= 2) wait_chunk(bars, B_MD, c - 2, abort_flag);  // vn buffer b no longer read
       {
-        const float* G = reinterpret_cast<const float*>(st + kG);
         unsigned char* vn = sm + kVN + b * kVNsz;
         unsigned char* vhb = sm + kVH;
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int i = 16 * mt + g + 8 * hh;
-          // per-channel gates: the decay exp(G_L - G) is inside the k image
-          const float fac = CH ? 1.f : expf(G[63] - G[i]);
 #pragma unroll
           for (int q = 0; q < 2; ++q) {
             const int j = 16 * np + 8 * q + c2;
@@ -345,7 +354,7 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
             *reinterpret_cast<__nv_bfloat162*>(vn + mn_off(j, i, 1024)) = hi;
             *reinterpret_cast<uint32_t*>(vn + mn_off(32 + j, i, 1024)) =
                 pack_bf16(v0 - hf.x, v1 - hf.y);
-            *reinterpret_cast<uint32_t*>(vhb + mn_off(j, i, 512)) = pack_f16(fac * v0, fac * v1);
+            *reinterpret_cast<uint32_t*>(vhb + mn_off(j, i, 512)) = pack_f16(fac[hh] * v0, fac[hh] * v1);
           }
         }
       }
@@ -354,10 +363,6 @@ tc_inter_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 
       // S <- exp(G_L) S + K^T vh   (key rows 16*warp.., all 32 columns; fp16 operands)
       {
-        const float* gst = reinterpret_cast<const float*>(st + kG);
-        // scalar gate: exp(G_L) for every key row; per-channel: exp(G_L) of row d
-        const float gam0 = CH ? gst[16 * warp + g] : expf(gst[63]);
-        const float gam1 = CH ? gst[16 * warp + g + 8] : gam0;
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
