@@ -25,7 +25,9 @@
 // 16 KB) come in and go out as TMA tiles of 32 rows x 128 bytes with the
 // 128-byte swizzle, so each thread reads its own row from shared memory without
 // bank conflicts; the inputs of up to 8 tokens are staged in shared memory at a
-// time (cp.async), so the serial token loop waits on no global load.
+// time (cp.async), so the serial token loop waits on no global load, and the first
+// block's inputs load while the state tile is in flight (one memory round trip per
+// CTA instead of two: what a one-token decode step pays for).
 //
 // Grid: (sequence, value head, dv / 32); one warp per CTA owns 32 columns.
 #include <cuda.h>
@@ -42,13 +44,16 @@ constexpr int kCols = 32;
 constexpr int kBlk = 8;  // tokens staged per step
 constexpr uint32_t kWaitIters = 1u << 22;
 
-// One 16 KB buffer: the state tile ([4 quarters of 32 columns][32 rows][128 B],
-// swizzled) on the way in and out; in between, the staged token inputs:
-//   raw k, raw q (the input dtype) at 0 and 4096, then fp32 (normalised) k and q
-//   at 8192 and 12288; after conversion the raw region holds v (fp32 [8][32]) at 0
-//   and g, beta (fp32 [8] each) at 1024 and 1056.
+// buf (16 KB): the state tile ([4 quarters of 32 columns][32 rows][128 B], swizzled) on
+// the way in and out; in between, the staged token inputs of a block: v (fp32 [8][32]) at
+// 0, g and beta (fp32 [8] each) at 1024 and 1056, fp32 (normalised) k and q at 8192 and
+// 12288. raw: the block's k and q in the input dtype (cp.async), at 0 and 4096. The first
+// block's raw k and q, v, g and beta are loaded while the state tile is in flight.
 struct __align__(1024) RecSmem {
   unsigned char buf[16384];
+  unsigned char raw0[8192];
+  float v0[kBlk * kCols];  // v, g and beta of the first block
+  float g0[kBlk], b0[kBlk];
   uint64_t bar;
 };
 
@@ -60,6 +65,25 @@ __device__ __forceinline__ float warp_sum(float x) {
 
 __device__ __forceinline__ void cp_async8(void* smem, const void* gmem) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(smem_u32(smem)), "l"(gmem));
+}
+
+// v of this CTA's 32 columns for the block's tokens, g and beta of token `lane`.
+__device__ __forceinline__ void load_vgb(const RecParams& p, int blk, int nb, int hv, int c0,
+                                         int lane, bool bf16, float (&vr)[kBlk], float& gr,
+                                         float& br) {
+#pragma unroll
+  for (int tt = 0; tt < kBlk; ++tt) {
+    const size_t tv = (size_t)(blk + tt) * p.Hv + hv;
+    vr[tt] = tt < nb ? (bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.v)[tv * kDv + c0 + lane])
+                             : static_cast<const float*>(p.v)[tv * kDv + c0 + lane])
+                     : 0.f;
+  }
+  gr = br = 0.f;
+  if (lane < nb) {
+    const size_t tv = (size_t)(blk + lane) * p.Hv + hv;
+    gr = p.g[tv];
+    br = p.beta[tv];
+  }
 }
 
 __device__ __forceinline__ float4 raw4(const unsigned char* p, bool bf16) {
@@ -94,16 +118,50 @@ recurrent_kernel(const __grid_constant__ RecParams p, const __grid_constant__ CU
   const int row0 = (n * p.Hv + hv) * kDv + c0;  // first state row (= value column) of this CTA
   bool fail = false;
 
+  // Inputs of a block of up to kBlk tokens: raw k and q by cp.async (lane l: elements
+  // 4l..4l+3 of each token), v of this CTA's columns and g, beta into registers.
+  auto issue_raw = [&](int blk, int nb, unsigned char* rk, unsigned char* rq) {
+    for (int tt = 0; tt < nb; ++tt) {
+      const size_t e = ((size_t)(blk + tt) * p.H + h) * kDk + 4 * lane;
+      const unsigned char* kg = static_cast<const unsigned char*>(p.k) + e * esz;
+      const unsigned char* qg = static_cast<const unsigned char*>(p.q) + e * esz;
+      unsigned char* kd = rk + tt * kDk * esz + 4 * lane * esz;
+      unsigned char* qd = rq + tt * kDk * esz + 4 * lane * esz;
+      if (bf16) {
+        cp_async8(kd, kg);
+        cp_async8(qd, qg);
+      } else {
+        cp_async16(kd, kg, true);
+        cp_async16(qd, qg, true);
+      }
+    }
+    cp_async_commit();
+  };
+
+
   // ---------------------------------------------------------------- state in
   float s[kDk];
-  if (p.s0) {
-    if (lane == 0) {
-      mbar_init(&sm.bar, 1);
-      mbar_init_fence();
-      mbar_expect_tx(&sm.bar, 16384);
+  if (p.s0 && lane == 0) {
+    mbar_init(&sm.bar, 1);
+    mbar_init_fence();
+    mbar_expect_tx(&sm.bar, 16384);
 #pragma unroll
-      for (int qd = 0; qd < 4; ++qd) tma_load_2d(buf + qd * 4096, &tm_s0, 32 * qd, row0, &sm.bar);
+    for (int qd = 0; qd < 4; ++qd) tma_load_2d(buf + qd * 4096, &tm_s0, 32 * qd, row0, &sm.bar);
+  }
+  // The first block's inputs are loaded while the state tile is in flight.
+  if (len > 0) {
+    const int nb0 = min(kBlk, len);
+    issue_raw(start, nb0, sm.raw0, sm.raw0 + 4096);
+    float vr[kBlk], gr, br;
+    load_vgb(p, start, nb0, hv, c0, lane, bf16, vr, gr, br);
+#pragma unroll
+    for (int tt = 0; tt < kBlk; ++tt) sm.v0[tt * kCols + lane] = vr[tt];
+    if (lane < kBlk) {
+      sm.g0[lane] = gr;
+      sm.b0[lane] = br;
     }
+  }
+  if (p.s0) {
     __syncwarp();
     fail = !mbar_wait(&sm.bar, 0, kWaitIters);
 #pragma unroll
@@ -131,42 +189,21 @@ recurrent_kernel(const __grid_constant__ RecParams p, const __grid_constant__ CU
   float* bs = reinterpret_cast<float*>(buf + 1056);
   for (int blk = start; blk < start + len; blk += kBlk) {
     const int nb = min(kBlk, start + len - blk);
-    // raw k and q of the block (lane l: elements 4l..4l+3 of each token)
-    for (int tt = 0; tt < nb; ++tt) {
-      const size_t e = ((size_t)(blk + tt) * p.H + h) * kDk + 4 * lane;
-      const unsigned char* kg = static_cast<const unsigned char*>(p.k) + e * esz;
-      const unsigned char* qg = static_cast<const unsigned char*>(p.q) + e * esz;
-      unsigned char* kd = buf + tt * kDk * esz + 4 * lane * esz;
-      unsigned char* qd = buf + 4096 + tt * kDk * esz + 4 * lane * esz;
-      if (bf16) {
-        cp_async8(kd, kg);
-        cp_async8(qd, qg);
-      } else {
-        cp_async16(kd, kg, true);
-        cp_async16(qd, qg, true);
-      }
-    }
-    cp_async_commit();
-    // v of this CTA's columns, g and beta of the block
+    // raw k and q of the block (the first block's were issued before the state came in)
+    const bool first = blk == start;
+    const unsigned char* rk = sm.raw0;
+    const unsigned char* rq = sm.raw0 + 4096;
     float vr[kBlk], gr = 0.f, br = 0.f;
-#pragma unroll
-    for (int tt = 0; tt < kBlk; ++tt) {
-      const size_t tv = (size_t)(blk + tt) * p.Hv + hv;
-      vr[tt] = tt < nb ? (bf16 ? __bfloat162float(static_cast<const __nv_bfloat16*>(p.v)[tv * kDv + c0 + lane])
-                               : static_cast<const float*>(p.v)[tv * kDv + c0 + lane])
-                       : 0.f;
-    }
-    if (lane < nb) {
-      const size_t tv = (size_t)(blk + lane) * p.Hv + hv;
-      gr = p.g[tv];
-      br = p.beta[tv];
+    if (!first) {
+      issue_raw(blk, nb, sm.raw0, sm.raw0 + 4096);
+      load_vgb(p, blk, nb, hv, c0, lane, bf16, vr, gr, br);
     }
     cp_async_wait<0>();
     __syncwarp();
     // fp32 (normalised) k and q
     for (int tt = 0; tt < nb; ++tt) {
-      float4 kv = raw4(buf + tt * kDk * esz + 4 * lane * esz, bf16);
-      float4 qv = raw4(buf + 4096 + tt * kDk * esz + 4 * lane * esz, bf16);
+      float4 kv = raw4(rk + tt * kDk * esz + 4 * lane * esz, bf16);
+      float4 qv = raw4(rq + tt * kDk * esz + 4 * lane * esz, bf16);
       if (p.l2norm) {
         const float rk = 1.f / sqrtf(warp_sum(kv.x * kv.x + kv.y * kv.y + kv.z * kv.z + kv.w * kv.w) + p.eps);
         const float rq = 1.f / sqrtf(warp_sum(qv.x * qv.x + qv.y * qv.y + qv.z * qv.z + qv.w * qv.w) + p.eps);
@@ -176,7 +213,15 @@ recurrent_kernel(const __grid_constant__ RecParams p, const __grid_constant__ CU
       *reinterpret_cast<float4*>(buf + 8192 + tt * 512 + 16 * lane) = kv;
       *reinterpret_cast<float4*>(buf + 12288 + tt * 512 + 16 * lane) = qv;
     }
-    __syncwarp();  // the raw region is read; it now holds v, g and beta
+    __syncwarp();
+    if (first) {  // (staged while the state came in)
+#pragma unroll
+      for (int tt = 0; tt < kBlk; ++tt) vr[tt] = sm.v0[tt * kCols + lane];
+      if (lane < kBlk) {
+        gr = sm.g0[lane];
+        br = sm.b0[lane];
+      }
+    }
 #pragma unroll
     for (int tt = 0; tt < kBlk; ++tt) vs[tt * kCols + lane] = vr[tt];
     if (lane < kBlk) {
