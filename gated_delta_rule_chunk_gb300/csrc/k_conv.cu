@@ -163,20 +163,10 @@ conv_kernel(const __grid_constant__ ConvParams p, const __grid_constant__ CUtens
     }
   };
   const int qkc = p.H * kDk;
-  bool stale = true;  // the window is filled at the first row of each sequence run
-  for (int t = t0; t < t1; ++t) {
-    if (n >= p.N) break;  // rows past the last sequence are not part of any
-    if (t >= sb.y) {      // next sequence (skipping empty ones)
-      while (n < p.N && seq_bounds(p, n).y <= t) ++n;
-      if (n >= p.N) break;
-      sb = seq_bounds(p, n);
-      stale = true;
-    }
-    if (t < sb.x) continue;  // a row before the sequence (no sequence owns it)
-    if (stale) {
-      fill(t);
-      stale = false;
-    }
+  // One output row: the taps in order, SiLU, the optional L2 norm of a q or k head, the
+  // store (in place in the tile when the tile is stored whole), then the window slides
+  // (slot D - 2 takes the current row).
+  auto emit = [&](int t) {
     float cur[4], y[4];
     smem4(t, cur);
 #pragma unroll
@@ -214,11 +204,33 @@ conv_kernel(const __grid_constant__ ConvParams p, const __grid_constant__ CUtens
     } else {
       store4(p.v, (size_t)t * (p.Hv * kDv) + (c - 2 * qkc), p.bf16, y);
     }
-    // slide the window (slot D - 2 takes the current row)
 #pragma unroll
     for (int j = 0; j < D - 1; ++j)
 #pragma unroll
       for (int e = 0; e < 4; ++e) win[j][e] = j + 1 < D - 1 ? win[j + 1][e] : cur[e];
+  };
+  if (n < p.N && t0 >= sb.x && t0 + kTile <= sb.y) {
+    // the common case: one sequence owns every row of the tile (no per-row checks)
+    fill(t0);
+#pragma unroll 1
+    for (int t = t0; t < t0 + kTile; ++t) emit(t);
+  } else {
+    bool stale = true;  // the window is filled at the first row of each sequence run
+    for (int t = t0; t < t1; ++t) {
+      if (n >= p.N) break;  // rows past the last sequence are not part of any
+      if (t >= sb.y) {      // next sequence (skipping empty ones)
+        while (n < p.N && seq_bounds(p, n).y <= t) ++n;
+        if (n >= p.N) break;
+        sb = seq_bounds(p, n);
+        stale = true;
+      }
+      if (t < sb.x) continue;  // a row before the sequence (no sequence owns it)
+      if (stale) {
+        fill(t);
+        stale = false;
+      }
+      emit(t);
+    }
   }
   if (whole) {
     fence_async_smem();
