@@ -148,7 +148,7 @@ def stage_bytes(x, out_bytes=2):
 # when the source has changed since, the figure no longer applies and is not reported.
 NCU_TRAFFIC = {
     "inter": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_inter.cu",
-              "sha1": "d8aac1d5c1abbd0da433a3e56a3067d7734e932a", "bytes": 191652352,
+              "sha1": "63d5119fe47d7a59b863db1c8453f0884706c9dc", "bytes": 191537920,
               "profile": "profiles/tc_inter_kernel_T4096_H16_Hv32.md"},
     "intra": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_intra.cu",
               "sha1": "fa58a6cd13d0a4a63568e928f2d9f6acfb58eb88", "bytes": 158551808,
