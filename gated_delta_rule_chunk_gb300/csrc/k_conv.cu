@@ -212,7 +212,7 @@ conv_kernel(const __grid_constant__ ConvParams p, const __grid_constant__ CUtens
   if (n < p.N && t0 >= sb.x && t0 + kTile <= sb.y) {
     // the common case: one sequence owns every row of the tile (no per-row checks)
     fill(t0);
-#pragma unroll 1
+#pragma unroll 3
     for (int t = t0; t < t0 + kTile; ++t) emit(t);
   } else {
     bool stale = true;  // the window is filled at the first row of each sequence run
