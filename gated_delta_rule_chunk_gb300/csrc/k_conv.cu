@@ -181,7 +181,7 @@ conv_kernel(const __grid_constant__ ConvParams p, const __grid_constant__ CUtens
       float ss = y[0] * y[0] + y[1] * y[1] + y[2] * y[2] + y[3] * y[3];
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-      const float r = 1.f / sqrtf(ss + p.eps);
+      const float r = rsqrtf(ss + p.eps);
 #pragma unroll
       for (int e = 0; e < 4; ++e) y[e] *= r;
     }
