@@ -672,6 +672,18 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
         load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f0 + 32 + f); });
         load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f0 + 32 + f); });
       }
+      // the epilogue's inputs (dO S^T, v_new dS^T, T^T dw of this thread's elements) are
+      // loaded before the products, which cover their latency
+      float2 os2[2][2], y2[2][2], tw2[2][2];
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+          const size_t at = sl * 64 * D + (size_t)(r0 + 8 * hh) * D + f0 + col32(nt, 0);
+          os2[nt][hh] = *reinterpret_cast<const float2*>(p.dos + at);
+          y2[nt][hh] = *reinterpret_cast<const float2*>(p.ys + at);
+          tw2[nt][hh] = *reinterpret_cast<const float2*>(p.ttdw + at);
+        }
       float aq[2][4], ak[2][4];
       zero(aq);
       zero(ak);
@@ -681,15 +693,24 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int i = row(e), d = col32(nt, e);
+        for (int hh = 0; hh < 2; ++hh) {
+          const int i = r0 + 8 * hh, d = col32(nt, 0);
           const size_t at = sl * 64 * D + (size_t)i * D + f0 + d;
-          const float os = p.dos[at], y = p.ys[at], tw = p.ttdw[at];
-          const float qv = R1[i * kLt + d], kv = R0[i * kLt + d];
-          rq[e >> 1] = fmaf(qv, os, rq[e >> 1]);
-          rw[e >> 1] = fmaf(kv, y, rw[e >> 1]);
-          p.dqp[at] = fmaf(p.scale * eG[i], os, aq[nt][e]);
-          p.dkp[at] = ak[nt][e] + eL[i] * y + bt[i] * eG[i] * tw;
+          const float os[2] = {os2[nt][hh].x, os2[nt][hh].y};
+          const float y[2] = {y2[nt][hh].x, y2[nt][hh].y};
+          const float tw[2] = {tw2[nt][hh].x, tw2[nt][hh].y};
+          float dq[2], dk[2];
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int e = 2 * hh + u;
+            const float qv = R1[i * kLt + d + u], kv = R0[i * kLt + d + u];
+            rq[hh] = fmaf(qv, os[u], rq[hh]);
+            rw[hh] = fmaf(kv, y[u], rw[hh]);
+            dq[u] = fmaf(p.scale * eG[i], os[u], aq[nt][e]);
+            dk[u] = ak[nt][e] + eL[i] * y[u] + bt[i] * eG[i] * tw[u];
+          }
+          *reinterpret_cast<float2*>(p.dqp + at) = make_float2(dq[0], dq[1]);
+          *reinterpret_cast<float2*>(p.dkp + at) = make_float2(dk[0], dk[1]);
         }
     }
     rq[0] = quad_sum(rq[0]);
