@@ -436,18 +436,24 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   auto col32 = [&](int nt, int e) { return 16 * nh + 8 * nt + c + (e & 1); };
   auto row = [&](int e) { return r0 + 8 * (e >> 1); };
 
-  if (tid < 64) {
-    const bool ok = tid < L;
-    G[tid] = ok ? p.g[(size_t)(t0 + tid) * p.Hv + hv] : 0.f;
-    bt[tid] = ok ? p.beta[(size_t)(t0 + tid) * p.Hv + hv] : 0.f;
-  }
-  __syncthreads();
-  if (tid == 0) {
-    float acc = 0.f;
-    for (int i = 0; i < 64; ++i) {
-      acc += G[i];
-      G[i] = acc;
+  if (warp == 0) {  // G: inclusive in-chunk cumsum of g (two rows per lane, shuffle scan)
+    const bool ok0 = lane < L, ok1 = lane + 32 < L;
+    float g0 = ok0 ? p.g[(size_t)(t0 + lane) * p.Hv + hv] : 0.f;
+    float g1 = ok1 ? p.g[(size_t)(t0 + lane + 32) * p.Hv + hv] : 0.f;
+    bt[lane] = ok0 ? p.beta[(size_t)(t0 + lane) * p.Hv + hv] : 0.f;
+    bt[lane + 32] = ok1 ? p.beta[(size_t)(t0 + lane + 32) * p.Hv + hv] : 0.f;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_up_sync(0xffffffffu, g0, o);
+      const float y1 = __shfl_up_sync(0xffffffffu, g1, o);
+      if (lane >= o) {
+        g0 += y0;
+        g1 += y1;
+      }
     }
+    g1 += __shfl_sync(0xffffffffu, g0, 31);
+    G[lane] = g0;
+    G[lane + 32] = g1;
   }
   __syncthreads();
   if (tid < 64) {
@@ -646,8 +652,9 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   // PG = dP * Gamma (lower incl.), Tp = PG^T, GK = dAt + dAt^T with dAt = dA * beta_i Gamma_ij
   for (int idx = tid; idx < 64 * 64; idx += kThr) {
     const int i = idx >> 6, j = idx & 63;
-    const float gij = j <= i ? expf(G[i] - G[j]) : 0.f;
-    const float gji = i <= j ? expf(G[j] - G[i]) : 0.f;
+    const float ex = expf(j <= i ? G[i] - G[j] : G[j] - G[i]);  // one of the two is used
+    const float gij = j <= i ? ex : 0.f;
+    const float gji = i <= j ? ex : 0.f;
     const float pg = dP[i * kLd + j] * gij;
     Tp[j * kLd + i] = pg;
     GK[i * kLd + j] = Zm[i * kLd + j] * bt[i] * gij + Zm[j * kLd + i] * bt[j] * gji;
@@ -732,17 +739,32 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
     dGv[i] += p.scale * eG[i] * sq - eL[i] * sw;
   }
   __syncthreads();
-  if (tid == 0) {  // exp(G_L) terms go to the last row (G is flat past the chunk end)
-    float s = 0.f;
-    for (int i = 0; i < 64; ++i) s += wsum[i];
-    dGv[63] += s + expf(G[63]) * p.sdot[sl];
-    float acc = 0.f;  // dg = reverse in-chunk cumsum of dG
-    for (int i = 63; i >= 0; --i) {
-      acc += dGv[i];
-      if (i < L) {
-        p.dg[(size_t)(t0 + i) * p.Hv + hv] = acc;
-        p.dbeta[(size_t)(t0 + i) * p.Hv + hv] = dBv[i];
+  if (warp == 0) {  // rows lane and lane + 32, fixed shuffle orders
+    // exp(G_L) terms go to the last row (G is flat past the chunk end)
+    float sw = wsum[lane] + wsum[lane + 32];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, o);
+    float d0 = dGv[lane], d1 = dGv[lane + 32];
+    if (lane == 31) d1 += sw + expf(G[63]) * p.sdot[sl];
+    // dg = reverse in-chunk cumsum of dG: suffix sums within each half, then the upper
+    // half's total added to the lower half
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y0 = __shfl_down_sync(0xffffffffu, d0, o);
+      const float y1 = __shfl_down_sync(0xffffffffu, d1, o);
+      if (lane + o < 32) {
+        d0 += y0;
+        d1 += y1;
       }
+    }
+    d0 += __shfl_sync(0xffffffffu, d1, 0);
+    if (lane < L) {
+      p.dg[(size_t)(t0 + lane) * p.Hv + hv] = d0;
+      p.dbeta[(size_t)(t0 + lane) * p.Hv + hv] = dBv[lane];
+    }
+    if (lane + 32 < L) {
+      p.dg[(size_t)(t0 + lane + 32) * p.Hv + hv] = d1;
+      p.dbeta[(size_t)(t0 + lane + 32) * p.Hv + hv] = dBv[lane + 32];
     }
   }
 }
