@@ -21,6 +21,8 @@
 //   dg   = reverse in-chunk cumsum of dG,  dS_0 = the scan's last dS.
 // Each step is the derivative of one forward equation; together they equal the
 // token-by-token adjoint of the recurrence.
+#include <type_traits>
+
 #include "gdn_common.cuh"
 #include "simt_tile.cuh"
 #include "tri_inverse.cuh"
@@ -356,7 +358,10 @@ __device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid) {
 // bf16 hi + lo per fragment, three warp MMAs per step of 16 (hi*hi, hi*lo, lo*hi).
 // Accumulator element e of tile nt: row m0 + g + 8 (e >> 1), column n0 + 8 nt + c + (e & 1)
 // (g = lane / 4, c = 2 (lane % 4)). Reads X rows k0..k1-1, columns m0..m0+15.
-template <int NT>
+// AX / BX: the X / Y operand holds values exact in bf16 (the bf16 inputs k, q, v), whose
+// lo halves are zero: the terms with them are skipped (two MMAs per step, or one when both
+// are exact).
+template <int NT, bool AX = false, bool BX = false>
 __device__ __forceinline__ void mma_kmajor(float (&acc)[NT][4], const float* X, int ldx,
                                            const float* Y, int ldy, int m0, int n0, int k0,
                                            int k1, int lane) {
@@ -376,8 +381,8 @@ __device__ __forceinline__ void mma_kmajor(float (&acc)[NT][4], const float* X, 
       split_pack2(yp[0], yp[ldy], bh[0], bl[0]);
       split_pack2(yp[8 * ldy], yp[9 * ldy], bh[1], bl[1]);
       mma_bf16(acc[nt], ah, bh[0], bh[1]);
-      mma_bf16(acc[nt], ah, bl[0], bl[1]);
-      mma_bf16(acc[nt], al, bh[0], bh[1]);
+      if (!BX) mma_bf16(acc[nt], ah, bl[0], bl[1]);
+      if (!AX) mma_bf16(acc[nt], al, bh[0], bh[1]);
     }
   }
 }
@@ -394,6 +399,7 @@ __device__ __forceinline__ float quad_sum(float x) {
 // 32 (w / 4).. of a 64-wide one (16 (w / 4).. of a 32-wide feature block).
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
+  constexpr bool kX = std::is_same<TIn, __nv_bfloat16>::value;  // k, q, v exact in bf16
   extern __shared__ __align__(16) float sm[];
   float* Tm = sm;                  // T = (I + A)^-1, row-major
   float* Tt = Tm + 64 * kLd;       // T^T
@@ -477,8 +483,8 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
         load_blk(bk, L, tid, [&](int i, int f) { return kin(i, (fb + 1) * 32 + f); });
         load_blk(bq, L, tid, [&](int i, int f) { return qin(i, (fb + 1) * 32 + f); });
       }
-      mma_kmajor<4>(akk, B0, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
-      mma_kmajor<4>(aqk, B1, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+      mma_kmajor<4, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+      mma_kmajor<4, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
     }
 #pragma unroll
     for (int nt = 0; nt < 4; ++nt)
@@ -533,7 +539,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       else
         load_key_blocks(0);
       mma_kmajor<4>(adp, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
-      mma_kmajor<4>(az, B2, kLd, B3, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+      mma_kmajor<4, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 32 * nh, 0, 32, lane);
       float tu[2][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
       zero(tu);
       mma_kmajor<2>(tu, Tm, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);
@@ -574,7 +580,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       {  // Z2[i][j] = sum_d dw[i][d] exp(G_j) k[j][d]: scale column j after the sum
         float z2[4][4];
         zero(z2);
-        mma_kmajor<4>(z2, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+        mma_kmajor<4, false, kX>(z2, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
@@ -694,9 +700,9 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       float aq[2][4], ak[2][4];
       zero(aq);
       zero(ak);
-      mma_kmajor<2>(aq, Tp, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG K)[i]
-      mma_kmajor<2>(ak, dP, kLd, R1, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG^T Q)[i]
-      mma_kmajor<2>(ak, GK, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (dAt + dAt^T) K
+      mma_kmajor<2, false, kX>(aq, Tp, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG K)[i]
+      mma_kmajor<2, false, kX>(ak, dP, kLd, R1, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG^T Q)[i]
+      mma_kmajor<2, false, kX>(ak, GK, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (dAt + dAt^T) K
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
