@@ -931,6 +931,7 @@ def run_gdn_bwd(args, ws, rank, local):
     alg_b, alg_f = bwd_bytes(x), sum(sf.values())
     t_hbm = alg_b / (peaks["hbm_gbs"] * 1e9)
     t_tc = alg_f / (peaks["bf16_tflops"] * 1e12)
+    tensor_stage = x["dtype"] == "bf16" or dom in ("state_products", "chunk_grads")
     if dom == "state_products":  # warp-MMA contractions: bound by HBM
         sb = bwd_state_bytes(x)
         gbs = sb / (st[dom] / 1000.0) / 1e9
@@ -938,6 +939,16 @@ def run_gdn_bwd(args, ws, rank, local):
                 "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"],
                 "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)",
                 "algorithmic_bytes_per_launch": sb, "traffic": None, "traffic_source": None}
+    elif tensor_stage:
+        # fp32 products run as three bf16 warp MMAs (hi*hi + hi*lo + lo*hi): the peak is a
+        # third of the measured bf16 tensor rate
+        peak3 = peaks["bf16_tflops"] / 3.0
+        roof = {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak3,
+                "unit": "TFLOP/s", "frac": achieved / peak3,
+                "peak_source": f"{peak_src} (MEASURED_PEAKS.json bf16_tflops) / 3: fp32 "
+                               "products as three bf16 MMAs",
+                "algorithmic_flops_per_launch": sf[dom], "traffic": None,
+                "traffic_source": None, "fp32_fma_frac": achieved / SIMT_FP32_TFLOPS}
     else:
         roof = {"bound": "alu", "kernel": dom, "achieved": achieved,
                 "peak": SIMT_FP32_TFLOPS, "unit": "TFLOP/s",
@@ -950,7 +961,7 @@ def run_gdn_bwd(args, ws, rank, local):
                  "tensor-core recompute, fp32 SIMT reverse scan")
     else:
         kinds = "fp32 SIMT recompute and reverse scan"
-    kinds += ", warp-MMA state contractions, fp32 SIMT per-chunk gradients"
+    kinds += ", warp-MMA state contractions and per-chunk gradients"
     res = {
         "metric": f"GDN chunk backward tokens/s, {WORKLOADS[args.workload].name}; % of roofline",
         "value": value, "unit": "tokens/s", "n_gpus": ws, "steps": K, "warmup": args.warmup,
