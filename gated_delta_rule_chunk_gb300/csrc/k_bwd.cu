@@ -188,22 +188,22 @@ __device__ __forceinline__ float4 ld_dout4(const BwdParams& p, size_t idx) {
 
 // bf16 hi/lo copies of `rows` fp32 rows of D columns into row-major tiles with row
 // stride D + 8 (16-byte padding: the 8 row addresses of an ldmatrix hit distinct bank
-// groups). get(r, c4) returns columns 4 c4 .. 4 c4 + 3 of row r; four loads in flight
+// groups). get(r, c4) returns columns 4 c4 .. 4 c4 + 3 of row r; eight loads in flight
 // per thread.
 template <int D, typename Get>
 __device__ __forceinline__ void split_rows(__nv_bfloat16* hi, __nv_bfloat16* lo, int rows, int tid,
                                            Get get) {
   constexpr int RS = D + 8, Q = D / 4;
   const int n = rows * Q;
-  for (int base = tid; base < n; base += 4 * kThr) {
-    float4 v[4];
+  for (int base = tid; base < n; base += 8 * kThr) {
+    float4 v[8];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int idx = base + u * kThr;
       v[u] = idx < n ? get(idx / Q, idx % Q) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
+    for (int u = 0; u < 8; ++u) {
       const int idx = base + u * kThr;
       if (idx < n) {
         const int off = (idx / Q) * RS + 4 * (idx % Q);
