@@ -153,13 +153,21 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     *reinterpret_cast<uint4*>(sm + sK + part * 8192 + (uint32_t)(L + (rem >> 3)) * 128u +
                               (rem & 7) * 16u) = make_uint4(0u, 0u, 0u, 0u);
   }
-  if (tid < 128) {  // inclusive cumsum along the chunk, one thread per channel
-    float acc = 0.f;
-#pragma unroll 8
-    for (int i = 0; i < 64; ++i) {
-      acc += G[i * 128 + tid];
-      G[i * 128 + tid] = acc;
+  {  // inclusive cumsum along the chunk: four threads per channel, 16 rows each, then each
+     // segment adds the totals of the segments before it (in order), through X as scratch
+    const int chn = tid & 127, seg = tid >> 7;
+    float x[16], acc = 0.f;
+#pragma unroll
+    for (int r = 0; r < 16; ++r) {
+      acc += G[(16 * seg + r) * 128 + chn];
+      x[r] = acc;
     }
+    X[seg * 128 + chn] = acc;
+    __syncthreads();
+    float off = 0.f;
+    for (int s2 = 0; s2 < seg; ++s2) off += X[s2 * 128 + chn];
+#pragma unroll
+    for (int r = 0; r < 16; ++r) G[(16 * seg + r) * 128 + chn] = x[r] + off;
   }
   for (int idx = tid; idx < 16384 / 16; idx += kThr)
     reinterpret_cast<uint4*>(sm + sM)[idx] = make_uint4(0u, 0u, 0u, 0u);
