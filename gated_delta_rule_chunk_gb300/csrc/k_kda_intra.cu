@@ -56,8 +56,11 @@ constexpr int R_EK = 0, R_EQ = 64, R_DK = 128, R_DQ = 192, R_FD = 256, R_FO = 32
 constexpr uint32_t sK = 0;                         // k, q, v tiles (TMA, 128-byte swizzle)
 constexpr uint32_t sQ = 16384;
 constexpr uint32_t sV = 32768;
-constexpr uint32_t sG = 49152;                     // fp32 [64][128]; later the u staging
-constexpr uint32_t sIMG = sG + 32768;              // images; later T operands and w staging
+// The gates' row stride: 132 floats, so that the rows a warp reads in one step fall in
+// different shared-memory banks (with 128 every row starts in bank 0).
+constexpr int GS = 132;
+constexpr uint32_t sG = 49152;                     // fp32 [64][GS]; later the u staging
+constexpr uint32_t sIMG = sG + 64 * GS * 4;        // images; later T operands and w staging
 constexpr uint32_t sIMGsz = 2 * R_IMG * LI * 2;
 constexpr uint32_t sKG = sIMG + sIMGsz;            // bf16 [64][LKG]: exp(G) k / ||k||
 constexpr uint32_t sAT = sKG + 64 * LKG * 2;       // fp32 [64][LDT]: A, then T
@@ -67,6 +70,7 @@ constexpr uint32_t sVec = sM + 16384;              // beta, 1/||k||, 1/||q||, fl
 constexpr uint32_t sBar = sVec + 4 * 256;
 constexpr uint32_t kSmemBytes = sBar + 64 + 1024;
 static_assert(2 * 64 * LTW * 2 + 16384 <= sIMGsz, "T operands and w staging exceed the image region");
+static_assert(kSmemBytes <= 232448, "shared memory over the per-CTA limit");
 
 __device__ __forceinline__ uint32_t sw_off(int r, int ch) {
   return (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4);
@@ -133,7 +137,7 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
   for (int idx = tid; idx < 64 * 32; idx += kThr) {
     const int i = idx >> 5, c4 = (idx & 31) * 4;
     const bool ok = i < L && c4 < p.D;
-    cp_async16(G + i * 128 + c4, p.g + (((size_t)(ok ? t0 + i : t0) * p.Hv + hv) * p.D + (ok ? c4 : 0)),
+    cp_async16(G + i * GS + c4, p.g + (((size_t)(ok ? t0 + i : t0) * p.Hv + hv) * p.D + (ok ? c4 : 0)),
                ok);
   }
   cp_async_commit();
@@ -159,7 +163,7 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     float x[16], acc = 0.f;
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
-      acc += G[(16 * seg + r) * 128 + chn];
+      acc += G[(16 * seg + r) * GS + chn];
       x[r] = acc;
     }
     X[seg * 128 + chn] = acc;
@@ -167,7 +171,7 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     float off = 0.f;
     for (int s2 = 0; s2 < seg; ++s2) off += X[s2 * 128 + chn];
 #pragma unroll
-    for (int r = 0; r < 16; ++r) G[(16 * seg + r) * 128 + chn] = x[r] + off;
+    for (int r = 0; r < 16; ++r) G[(16 * seg + r) * GS + chn] = x[r] + off;
   }
   for (int idx = tid; idx < 16384 / 16; idx += kThr)
     reinterpret_cast<uint4*>(sm + sM)[idx] = make_uint4(0u, 0u, 0u, 0u);
@@ -177,7 +181,7 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
     int bad = 0;
 #pragma unroll
     for (int b = 0; b < 4; ++b)
-      if (G[16 * b * 128 + tid] - G[(16 * b + 15) * 128 + tid] > kDiagRange) bad |= 1 << b;
+      if (G[16 * b * GS + tid] - G[(16 * b + 15) * GS + tid] > kDiagRange) bad |= 1 << b;
     if (bad) atomicOr(&flags[0], bad);
   }
 
@@ -193,8 +197,8 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
         const int f = 8 * ch + e;
-        const float gi0 = G[i * 128 + f], gi1 = G[i * 128 + f + 1];
-        const float gl0 = G[63 * 128 + f], gl1 = G[63 * 128 + f + 1];
+        const float gi0 = G[i * GS + f], gi1 = G[i * GS + f + 1];
+        const float gl0 = G[63 * GS + f], gl1 = G[63 * GS + f + 1];
         const float k0 = kx[e] * KR[i], k1 = kx[e + 1] * KR[i];
         kt[e >> 1] = pack_f16(__expf(gl0 - gi0) * k0, __expf(gl1 - gi1) * k1);
         const float e0 = __expf(gi0), e1 = __expf(gi1);
@@ -207,7 +211,7 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
       *reinterpret_cast<uint4*>(img + 32768 + off) = make_uint4(ql[0], ql[1], ql[2], ql[3]);
       *reinterpret_cast<uint4*>(KG + i * LKG + 8 * ch) = make_uint4(kg[0], kg[1], kg[2], kg[3]);
     }
-    for (int f = tid; f < 128; f += kThr) p.gam[sl * 128 + f] = __expf(G[63 * 128 + f]);
+    for (int f = tid; f < 128; f += kThr) p.gam[sl * 128 + f] = __expf(G[63 * GS + f]);
     fence_async_smem();
     __syncthreads();
     if (tid == 0) {
@@ -262,8 +266,8 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
       uint32_t hi[4], lo[4];
 #pragma unroll
       for (int e = 0; e < 8; e += 2) {
-        const float gs0 = G[src * 128 + f0 + e], gs1 = G[src * 128 + f0 + e + 1];
-        const float gr0 = G[ref * 128 + f0 + e], gr1 = G[ref * 128 + f0 + e + 1];
+        const float gs0 = G[src * GS + f0 + e], gs1 = G[src * GS + f0 + e + 1];
+        const float gr0 = G[ref * GS + f0 + e], gr1 = G[ref * GS + f0 + e + 1];
         const float d0 = ref_first ? gs0 - gr0 : gr0 - gs0;
         const float d1 = ref_first ? gs1 - gr1 : gr1 - gs1;
         split_pack2(x[e] * rs * __expf(d0), x[e + 1] * rs * __expf(d1), hi[e >> 1], lo[e >> 1]);
@@ -364,7 +368,7 @@ kda_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUten
       const int i = 16 * b + ii, j = 16 * b + rem;
       float sk = 0.f, sq = 0.f;
       for (int d = lane; d < 128; d += 32) {
-        const float e = __expf(G[i * 128 + d] - G[j * 128 + d]) * tile_elem(sm + sK, j, d);
+        const float e = __expf(G[i * GS + d] - G[j * GS + d]) * tile_elem(sm + sK, j, d);
         sk = fmaf(tile_elem(sm + sK, i, d), e, sk);
         sq = fmaf(tile_elem(sm + sQ, i, d), e, sq);
       }
