@@ -116,15 +116,15 @@ conv_kernel(const __grid_constant__ ConvParams p, const __grid_constant__ CUtens
     mbar_expect_tx(bar, (uint32_t)(kRows * 128 * esz));
     tma_load_2d(tile, &tm_x, c_w, t0 - (D - 1), bar);
   }
-  __syncwarp();
-  const bool loaded = mbar_wait(bar, 0, 1u << 22);
-  if (!loaded && lane == 0) set_status(p.status, GDN_DEV_TIMEOUT);
   const bool qk = c_w < 2 * p.H * kDk;  // q or k head
-  float w[4][D];
+  float w[4][D];  // this thread's taps, loaded while the tile is in flight
 #pragma unroll
   for (int e = 0; e < 4; ++e)
 #pragma unroll
     for (int j = 0; j < D; ++j) w[e][j] = p.w[(size_t)(c + e) * D + j];
+  __syncwarp();
+  const bool loaded = mbar_wait(bar, 0, 1u << 22);
+  if (!loaded && lane == 0) set_status(p.status, GDN_DEV_TIMEOUT);
 
   auto row_ptr = [&](int t) { return tile + (t - t0 + D - 1) * 128 * esz + 4 * lane * esz; };
   auto smem4 = [&](int t, float (&o)[4]) {
