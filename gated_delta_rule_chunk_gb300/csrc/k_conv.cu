@@ -122,6 +122,13 @@ conv_kernel(const __grid_constant__ ConvParams p, const __grid_constant__ CUtens
   for (int e = 0; e < 4; ++e)
 #pragma unroll
     for (int j = 0; j < D; ++j) w[e][j] = p.w[(size_t)(c + e) * D + j];
+  // the sequences owning the tile's rows (cu_seqlens reads, also while the tile is in flight)
+  int n = seq_of(p, t0);
+  int2 sb = n < p.N ? seq_bounds(p, n) : make_int2(p.T, p.T);
+  // the TMA store may write the whole tile only if a sequence owns every row of it
+  const int lo = p.cu ? min(max(p.cu[0], 0), p.T) : 0;
+  const int hi = p.cu ? min(max(p.cu[p.N], 0), p.T) : p.T;
+  const bool whole = t0 >= lo && t1 <= hi;
   __syncwarp();
   const bool loaded = mbar_wait(bar, 0, 1u << 22);
   if (!loaded && lane == 0) set_status(p.status, GDN_DEV_TIMEOUT);
@@ -139,12 +146,6 @@ conv_kernel(const __grid_constant__ ConvParams p, const __grid_constant__ CUtens
       o[0] = f.x; o[1] = f.y; o[2] = f.z; o[3] = f.w;
     }
   };
-  int n = seq_of(p, t0);
-  int2 sb = n < p.N ? seq_bounds(p, n) : make_int2(p.T, p.T);
-  // the TMA store may write the whole tile only if a sequence owns every row of it
-  const int lo = p.cu ? min(max(p.cu[0], 0), p.T) : 0;
-  const int hi = p.cu ? min(max(p.cu[p.N], 0), p.T) : p.T;
-  const bool whole = t0 >= lo && t1 <= hi;
   float win[D > 1 ? D - 1 : 1][4];  // win[j]: input at row t - (D - 1) + j
   auto fill = [&](int t) {
 #pragma unroll
