@@ -235,9 +235,30 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------------- CPU oracle
-def oracle_rate(x, seconds: float, max_tokens=None):
+def cpu_model() -> str:
+    """The host CPU's name (x86 model name, or the Arm implementer/part of the cores)."""
+    try:
+        info = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    fields = {}
+    for line in info.splitlines():
+        if ":" in line:
+            k, v = line.split(":", 1)
+            fields.setdefault(k.strip(), v.strip())
+    if "model name" in fields:
+        return fields["model name"]
+    arm_parts = {"0xd4f": "Arm Neoverse V2", "0xd40": "Arm Neoverse V1", "0xd0c": "Arm Neoverse N1"}
+    part = fields.get("CPU part")
+    if part:
+        return f"{arm_parts.get(part, 'Arm core')} (implementer {fields.get('CPU implementer', '?')}, part {part})"
+    return "unknown"
+
+
+def oracle_rate(x, seconds: float, max_tokens=None, nthreads: int = 0):
     """Time the CPU oracle on the first T_s tokens of the workload (all heads).
-    T_s is sized from a short probe so the timed sample takes about `seconds`."""
+    T_s is sized from a short probe so the timed sample takes about `seconds`.
+    nthreads: 0 = every core the process may use, else that many threads."""
     import oracle
     import torch
 
@@ -247,7 +268,7 @@ def oracle_rate(x, seconds: float, max_tokens=None):
         s0 = x["initial_state"][:1] if x["initial_state"] is not None else None
         t = time.perf_counter()
         oracle.recurrent_forward(x["q"][sl], x["k"][sl], x["v"][sl], x["g"][sl], x["beta"][sl],
-                                 x["scale"], s0, cu)
+                                 x["scale"], s0, cu, nthreads=nthreads)
         return time.perf_counter() - t
 
     oracle.build()
@@ -261,7 +282,7 @@ def oracle_rate(x, seconds: float, max_tokens=None):
     while dt < 0.8 * seconds and ts == limit:  # the whole workload is shorter: repeat it
         dt += run(ts)
         reps += 1
-    return reps * ts / dt, ts, dt, oracle.max_threads(), reps
+    return reps * ts / dt, ts, dt, (nthreads or oracle.max_threads()), reps
 
 
 # --------------------------------------------------------------------- distributed plumbing
@@ -441,6 +462,7 @@ def run_recurrent(args, ws, rank, local):
         rate, ts, dt, cores, reps = oracle_rate(x, args.cpu_seconds)
         res["cpu_baseline"] = {
             "value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+            "cpu_model": cpu_model(),
             "sample": f"first {ts} tokens as one sequence, all {x['Hv']} value heads, "
                       f"run {reps} times ({dt:.1f} s of fp64 C on the host cores)"}
     return res
@@ -775,9 +797,15 @@ def run_gdn(args, ws, rank, local):
         rate, ts, dt, cores, reps = oracle_rate(x, args.cpu_seconds)
         what = (f"the whole workload ({ts} tokens), all {x['Hv']} value heads, run {reps} times"
                 if reps > 1 else f"first {ts} tokens of the workload, all {x['Hv']} value heads")
+        # the same oracle on one thread, on a shorter sample
+        rate1, ts1, dt1, _, _ = oracle_rate(x, max(1.0, args.cpu_seconds / 4), nthreads=1)
         res["cpu_baseline"] = {
             "value": rate, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-            "sample": f"{what} ({dt:.1f} s of fp64 C on the host cores)"}
+            "sample": f"{what} ({dt:.1f} s of fp64 C on the host cores)",
+            "cpu_model": cpu_model(),
+            "value_1thread": rate1,
+            "sample_1thread": f"first {ts1} tokens, all {x['Hv']} value heads, one thread "
+                              f"({dt1:.1f} s)"}
     return res
 
 
