@@ -322,33 +322,39 @@ constexpr size_t chunk_floats() {
   return (size_t)7 * 64 * kLd + 16 * kLd + 4 * 32 * kLd + 2 * 64 * kLt + 8 * 64 + 4 * 64 * 8;
 }
 
+// Threads of the per-chunk kernel: 16 warps, each owning a 16 x 16 tile of every 64 x 64
+// result and a 16 x 8 tile of every 64 x 32 one, so that four warps per SM sub-partition
+// cover the latency of the shared-memory operand loads and the MMAs.
+constexpr int kThrC = 512;
+constexpr int kBlkU = 64 * 32 / kThrC;
+
 // A [64 x 32] block of a token-major source (tokens x 32 features) held in registers,
-// 8 elements per thread (element idx = tid + 256 u: token idx / 32, feature idx % 32), so
-// that the next block's loads are in flight while the current one is used.
+// kBlkU elements per thread (element idx = tid + kThrC u: token idx / 32, feature idx % 32),
+// so that the next block's loads are in flight while the current one is used.
 struct Blk {
-  float r[8];
+  float r[kBlkU];
 };
 // get(i, f) returns token i, feature f; tokens at or past L read as zero.
 template <typename Get>
 __device__ __forceinline__ void load_blk(Blk& b, int L, int tid, Get get) {
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int idx = tid + u * kThr;
+  for (int u = 0; u < kBlkU; ++u) {
+    const int idx = tid + u * kThrC;
     b.r[u] = (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f;
   }
 }
 // ... stored feature-major [32][kLd] or token-major [64][kLt]
 __device__ __forceinline__ void store_fm(float* dst, const Blk& b, int tid) {
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int idx = tid + u * kThr;
+  for (int u = 0; u < kBlkU; ++u) {
+    const int idx = tid + u * kThrC;
     dst[(idx & 31) * kLd + (idx >> 5)] = b.r[u];
   }
 }
 __device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid) {
 #pragma unroll
-  for (int u = 0; u < 8; ++u) {
-    const int idx = tid + u * kThr;
+  for (int u = 0; u < kBlkU; ++u) {
+    const int idx = tid + u * kThrC;
     dst[(idx >> 5) * kLt + (idx & 31)] = b.r[u];
   }
 }
@@ -396,9 +402,9 @@ __device__ __forceinline__ float quad_sum(float x) {
 
 // Per (chunk slot, value head). Every product is a warp-MMA tile product of fp32 operands in
 // shared memory (mma_kmajor); warp w owns rows 16 (w % 4).. of each result and columns
-// 32 (w / 4).. of a 64-wide one (16 (w / 4).. of a 32-wide feature block).
+// 16 (w / 4).. of a 64-wide one (8 (w / 4).. of a 32-wide feature block).
 template <typename TIn, int D>
-__global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
+__global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   constexpr bool kX = std::is_same<TIn, __nv_bfloat16>::value;  // k, q, v exact in bf16
   extern __shared__ __align__(16) float sm[];
   float* Tm = sm;                  // T = (I + A)^-1, row-major
@@ -423,7 +429,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   float* dBv = dGv + 64;           // dbeta
   float* rsk = dBv + 64;           // (T^T dw)_i . k_i
   float* wsum = rsk + 64;          // W_i = exp(G_L - G_i) k_i . (v_new dS^T)_i
-  float* pv = wsum + 64;           // [64][8] partial row dots (T^T dv_new) . v (slots 0-1)
+  float* pv = wsum + 64;           // [64][8] partial row dots (T^T dv_new) . v (slots 0-3)
   float* pk = pv + 64 * 8;         // [64][8] partial row dots (T^T dw) . k
   float* pq = pk + 64 * 8;         // [64][8] partial row dots q . (dO S^T)
   float* pw = pq + 64 * 8;         // [64][8] partial row dots k . (v_new dS^T)
@@ -438,8 +444,8 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   auto qin = [&](int i, int f) { return ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + f); };
   auto vin = [&](int i, int f) { return ld_in<TIn>(p.v, ((size_t)(t0 + i) * p.Hv + hv) * D + f); };
   // element (row, column) of accumulator entry (nt, e) of a 64-wide and a 32-wide result
-  auto col64 = [&](int nt, int e) { return 32 * nh + 8 * nt + c + (e & 1); };
-  auto col32 = [&](int nt, int e) { return 16 * nh + 8 * nt + c + (e & 1); };
+  auto col64 = [&](int nt, int e) { return 16 * nh + 8 * nt + c + (e & 1); };
+  auto col32 = [&](int nt, int e) { return 8 * nh + 8 * nt + c + (e & 1); };
   auto row = [&](int e) { return r0 + 8 * (e >> 1); };
 
   if (warp == 0) {  // G: inclusive in-chunk cumsum of g (two rows per lane, shuffle scan)
@@ -469,7 +475,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   // ---------------- K K^T and Q K^T (feature blocks of 32)
   Blk bk, bq;  // k and q blocks (also the last stage's)
   {
-    float akk[4][4], aqk[4][4];
+    float akk[2][4], aqk[2][4];
     zero(akk);
     zero(aqk);
     load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f); });
@@ -483,11 +489,11 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
         load_blk(bk, L, tid, [&](int i, int f) { return kin(i, (fb + 1) * 32 + f); });
         load_blk(bq, L, tid, [&](int i, int f) { return qin(i, (fb + 1) * 32 + f); });
       }
-      mma_kmajor<4, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
-      mma_kmajor<4, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+      mma_kmajor<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+      mma_kmajor<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
     }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = row(e), j = col64(nt, e);
@@ -513,16 +519,16 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   };
   load_value_blocks(0);  // in flight during the inverse
   __syncthreads();
-  tri_inverse_64_tc<kThr / 32>(Tm, kLd, Xs, tid);  // Tm = T, ends synchronized
-  for (int idx = tid; idx < 64 * 64; idx += kThr) {
+  tri_inverse_64_tc<kThrC / 32>(Tm, kLd, Xs, tid);  // Tm = T, ends synchronized
+  for (int idx = tid; idx < 64 * 64; idx += kThrC) {
     const int i = idx >> 6, j = idx & 63;
     Tt[j * kLd + i] = Tm[i * kLd + j];
   }
   // ---------------- value features: dP, Z1, T^T dv_new (dv and the dbeta part)
-  float az[4][4];
+  float az[2][4];
   zero(az);
   {
-    float adp[4][4];
+    float adp[2][4];
     zero(adp);
     float rv[2] = {0.f, 0.f};
     for (int fb = 0; fb < D / 32; ++fb) {
@@ -538,13 +544,13 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
         load_value_blocks(f0 + 32);
       else
         load_key_blocks(0);
-      mma_kmajor<4>(adp, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
-      mma_kmajor<4, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 32 * nh, 0, 32, lane);
-      float tu[2][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
+      mma_kmajor<2>(adp, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+      mma_kmajor<2, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+      float tu[1][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
       zero(tu);
-      mma_kmajor<2>(tu, Tm, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);
+      mma_kmajor<1>(tu, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 1; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = row(e), n = col32(nt, e);
@@ -559,7 +565,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       pv[(r0 + 8) * 8 + nh] = rv[1];
     }
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = row(e), j = col64(nt, e);
@@ -578,19 +584,19 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       __syncthreads();
       if (fb + 1 < D / 32) load_key_blocks(f0 + 32);
       {  // Z2[i][j] = sum_d dw[i][d] exp(G_j) k[j][d]: scale column j after the sum
-        float z2[4][4];
+        float z2[2][4];
         zero(z2);
-        mma_kmajor<4, false, kX>(z2, B0, kLd, B1, kLd, 16 * mt, 32 * nh, 0, 32, lane);
+        mma_kmajor<2, false, kX>(z2, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 32, lane);
 #pragma unroll
-        for (int nt = 0; nt < 4; ++nt)
+        for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) az[nt][e] = fmaf(eG[col64(nt, e)], z2[nt][e], az[nt][e]);
       }
-      float tw[2][4];
+      float tw[1][4];
       zero(tw);
-      mma_kmajor<2>(tw, Tm, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);
+      mma_kmajor<1>(tw, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 1; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = row(e), n = col32(nt, e);
@@ -607,7 +613,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   }
   // Z = (Z1 + Z2) diag(beta)
 #pragma unroll
-  for (int nt = 0; nt < 4; ++nt)
+  for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = col64(nt, e);
@@ -615,21 +621,21 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
     }
   __syncthreads();
   {  // Tp = Z^T T   (T[k][j] = 0 for k < j)
-    float acc[4][4];
+    float acc[2][4];
     zero(acc);
-    mma_kmajor<4>(acc, Zm, kLd, Tm, kLd, 16 * mt, 32 * nh, 0, 64, lane);
+    mma_kmajor<2>(acc, Zm, kLd, Tm, kLd, 16 * mt, 16 * nh, 0, 64, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) Tp[row(e) * kLd + col64(nt, e)] = acc[nt][e];
   }
   __syncthreads();
   {  // dA[j][m] = -sum_l Tp[l][j] T[m][l] on the strict lower triangle (T[m][l] = 0 for l > m)
-    float acc[4][4];
+    float acc[2][4];
     zero(acc);
-    mma_kmajor<4>(acc, Tp, kLd, Tt, kLd, 16 * mt, 32 * nh, 0, 64, lane);
+    mma_kmajor<2>(acc, Tp, kLd, Tt, kLd, 16 * mt, 16 * nh, 0, 64, lane);
 #pragma unroll
-    for (int nt = 0; nt < 4; ++nt)
+    for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int i = row(e), j = col64(nt, e);
@@ -649,14 +655,15 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       dg -= Zm[j * kLd + i] * bt[j] * GK[j * kLd + i];    // column of dA * A
       dg -= dP[j * kLd + i] * Mm[j * kLd + i];            // column of dP * M
     }
-    const float sv = pv[i * 8] + pv[i * 8 + 1], sk = pk[i * 8] + pk[i * 8 + 1];
+    const float sv = (pv[i * 8] + pv[i * 8 + 1]) + (pv[i * 8 + 2] + pv[i * 8 + 3]);
+    const float sk = (pk[i * 8] + pk[i * 8 + 1]) + (pk[i * 8 + 2] + pk[i * 8 + 3]);
     rsk[i] = sk;
     dBv[i] = sv + eG[i] * sk + db;
     dGv[i] = dg + bt[i] * eG[i] * sk;
   }
   __syncthreads();
   // PG = dP * Gamma (lower incl.), Tp = PG^T, GK = dAt + dAt^T with dAt = dA * beta_i Gamma_ij
-  for (int idx = tid; idx < 64 * 64; idx += kThr) {
+  for (int idx = tid; idx < 64 * 64; idx += kThrC) {
     const int i = idx >> 6, j = idx & 63;
     const float ex = expf(j <= i ? G[i] - G[j] : G[j] - G[i]);  // one of the two is used
     const float gij = j <= i ? ex : 0.f;
@@ -666,7 +673,7 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
     GK[i * kLd + j] = Zm[i * kLd + j] * bt[i] * gij + Zm[j * kLd + i] * bt[j] * gji;
   }
   __syncthreads();
-  for (int idx = tid; idx < 64 * 64; idx += kThr) {
+  for (int idx = tid; idx < 64 * 64; idx += kThrC) {
     const int i = idx >> 6, j = idx & 63;
     dP[i * kLd + j] = Tp[j * kLd + i];
   }
@@ -687,9 +694,9 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
       }
       // the epilogue's inputs (dO S^T, v_new dS^T, T^T dw of this thread's elements) are
       // loaded before the products, which cover their latency
-      float2 os2[2][2], y2[2][2], tw2[2][2];
+      float2 os2[1][2], y2[1][2], tw2[1][2];
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 1; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const size_t at = sl * 64 * D + (size_t)(r0 + 8 * hh) * D + f0 + col32(nt, 0);
@@ -697,14 +704,14 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
           y2[nt][hh] = *reinterpret_cast<const float2*>(p.ys + at);
           tw2[nt][hh] = *reinterpret_cast<const float2*>(p.ttdw + at);
         }
-      float aq[2][4], ak[2][4];
+      float aq[1][4], ak[1][4];
       zero(aq);
       zero(ak);
-      mma_kmajor<2, false, kX>(aq, Tp, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG K)[i]
-      mma_kmajor<2, false, kX>(ak, dP, kLd, R1, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (PG^T Q)[i]
-      mma_kmajor<2, false, kX>(ak, GK, kLd, R0, kLt, 16 * mt, 16 * nh, 0, 64, lane);  // (dAt + dAt^T) K
+      mma_kmajor<1, false, kX>(aq, Tp, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);  // (PG K)[i]
+      mma_kmajor<1, false, kX>(ak, dP, kLd, R1, kLt, 16 * mt, 8 * nh, 0, 64, lane);  // (PG^T Q)[i]
+      mma_kmajor<1, false, kX>(ak, GK, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);  // (dAt + dAt^T) K
 #pragma unroll
-      for (int nt = 0; nt < 2; ++nt)
+      for (int nt = 0; nt < 1; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           const int i = r0 + 8 * hh, d = col32(nt, 0);
@@ -740,7 +747,8 @@ __global__ void __launch_bounds__(kThr) bwd_chunk_kernel(BwdParams p) {
   __syncthreads();
   if (tid < 64) {
     const int i = tid;
-    const float sq = pq[i * 8] + pq[i * 8 + 1], sw = pw[i * 8] + pw[i * 8 + 1];
+    const float sq = (pq[i * 8] + pq[i * 8 + 1]) + (pq[i * 8 + 2] + pq[i * 8 + 3]);
+    const float sw = (pw[i * 8] + pw[i * 8 + 1]) + (pw[i * 8 + 2] + pw[i * 8 + 3]);
     wsum[i] = eL[i] * sw;
     dGv[i] += p.scale * eG[i] * sq - eL[i] * sw;
   }
@@ -813,7 +821,7 @@ bool launch_bwd_t(const BwdParams& p, cudaStream_t s, cudaEvent_t* ev) {
   if (p.nt_max > 0) bwd_state_kernel<D><<<dim3(p.nt_max, p.Hv), kThr, s2, s>>>(p);
   if (ev) cudaEventRecord(ev[1], s);
   if (p.nt_max > 0) {
-    bwd_chunk_kernel<TIn, D><<<dim3(p.nt_max, p.Hv), kThr, s3, s>>>(p);
+    bwd_chunk_kernel<TIn, D><<<dim3(p.nt_max, p.Hv), kThrC, s3, s>>>(p);
     bwd_reduce_kernel<D><<<dim3(p.nt_max, p.H), kThr, 0, s>>>(p);
   }
   if (ev) cudaEventRecord(ev[2], s);
