@@ -319,7 +319,7 @@ constexpr int kLd = 68;    // row stride of the 64 x 64 matrices and feature-maj
 constexpr int kLt = 36;    // row stride of the token-major 64 x 32 blocks
 
 constexpr size_t chunk_floats() {
-  return (size_t)7 * 64 * kLd + 16 * kLd + 4 * 32 * kLd + 2 * 64 * kLt + 8 * 64 + 4 * 64 * 8;
+  return (size_t)7 * 64 * kLd + 16 * kLd + 4 * 32 * kLd + 64 * kLt + 8 * 64 + 4 * 64 * 8;
 }
 
 // Threads of the per-chunk kernel: 16 warps, each owning a 16 x 16 tile of every 64 x 64
@@ -351,11 +351,11 @@ __device__ __forceinline__ void store_fm(float* dst, const Blk& b, int tid) {
     dst[(idx & 31) * kLd + (idx >> 5)] = b.r[u];
   }
 }
-__device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid) {
+__device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid, int ld = kLt) {
 #pragma unroll
   for (int u = 0; u < kBlkU; ++u) {
     const int idx = tid + u * kThrC;
-    dst[(idx >> 5) * kLt + (idx & 31)] = b.r[u];
+    dst[(idx >> 5) * ld + (idx & 31)] = b.r[u];
   }
 }
 
@@ -401,8 +401,11 @@ __device__ __forceinline__ float quad_sum(float x) {
 }
 
 // Per (chunk slot, value head). Every product is a warp-MMA tile product of fp32 operands in
-// shared memory (mma_kmajor); warp w owns rows 16 (w % 4).. of each result and columns
-// 16 (w / 4).. of a 64-wide one (8 (w / 4).. of a 32-wide feature block).
+// shared memory (mma_kmajor). Warp w owns rows 16 mt.. of each result, mt = w / 4, and
+// columns 16 nh.. of a 64-wide one (8 nh.. of a 32-wide feature block), nh = (w - mt) % 4:
+// the warps of one SM sub-partition (w % 4) then hold every row block and every column
+// block once, so that the products that skip the zero triangle of T, of the gate-masked
+// matrices or of the lower-triangular results load the sub-partitions evenly.
 template <typename TIn, int D>
 __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   constexpr bool kX = std::is_same<TIn, __nv_bfloat16>::value;  // k, q, v exact in bf16
@@ -419,9 +422,8 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   float* B1 = B0 + 32 * kLd;
   float* B2 = B1 + 32 * kLd;
   float* B3 = B2 + 32 * kLd;
-  float* R0 = B3 + 32 * kLd;       // [64][kLt] token-major blocks
-  float* R1 = R0 + 64 * kLt;
-  float* G = R1 + 64 * kLt;        // [64] in-chunk cumulative gate
+  float* R0 = B3 + 32 * kLd;       // [64][kLt] token-major block (dv_new, then dw)
+  float* G = R0 + 64 * kLt;        // [64] in-chunk cumulative gate
   float* eG = G + 64;              // exp(G)
   float* eL = eG + 64;             // exp(G_L - G)
   float* bt = eL + 64;             // beta
@@ -435,10 +437,11 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   float* pw = pq + 64 * 8;         // [64][8] partial row dots k . (v_new dS^T)
 
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, hv = blockIdx.y, h = hv / p.HG;
-  const int g = lane >> 2, c = 2 * (lane & 3), mt = warp & 3, nh = warp >> 2;
+  const int g = lane >> 2, c = 2 * (lane & 3), mt = warp >> 2, nh = (warp - mt) & 3;
   const int r0 = 16 * mt + g;  // this thread's accumulator rows: r0 and r0 + 8
   int t0, L, wslot;
   if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
+  const bool lower = nh <= mt;  // this warp's 64-wide tile meets the lower triangle
   const size_t sl = (size_t)wslot * p.Hv + hv;
   auto kin = [&](int i, int f) { return ld_in<TIn>(p.k, ((size_t)(t0 + i) * p.H + h) * D + f); };
   auto qin = [&](int i, int f) { return ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + f); };
@@ -448,6 +451,9 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   auto col32 = [&](int nt, int e) { return 8 * nh + 8 * nt + c + (e & 1); };
   auto row = [&](int e) { return r0 + 8 * (e >> 1); };
 
+  Blk bk, bq;  // k and q blocks; the first ones are in flight during the gate scan
+  load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f); });
+  load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f); });
   if (warp == 0) {  // G: inclusive in-chunk cumsum of g (two rows per lane, shuffle scan)
     const bool ok0 = lane < L, ok1 = lane + 32 < L;
     float g0 = ok0 ? p.g[(size_t)(t0 + lane) * p.Hv + hv] : 0.f;
@@ -473,13 +479,10 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     eL[tid] = expf(G[63] - G[tid]);
   }
   // ---------------- K K^T and Q K^T (feature blocks of 32)
-  Blk bk, bq;  // k and q blocks (also the last stage's)
   {
     float akk[2][4], aqk[2][4];
     zero(akk);
     zero(aqk);
-    load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f); });
-    load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f); });
     for (int fb = 0; fb < D / 32; ++fb) {
       __syncthreads();
       store_fm(B0, bk, tid);
@@ -489,8 +492,10 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
         load_blk(bk, L, tid, [&](int i, int f) { return kin(i, (fb + 1) * 32 + f); });
         load_blk(bq, L, tid, [&](int i, int f) { return qin(i, (fb + 1) * 32 + f); });
       }
-      mma_kmajor<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
-      mma_kmajor<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+      if (lower) {  // both are masked to the lower triangle
+        mma_kmajor<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+        mma_kmajor<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+      }
     }
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
@@ -544,11 +549,11 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
         load_value_blocks(f0 + 32);
       else
         load_key_blocks(0);
-      mma_kmajor<2>(adp, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+      if (lower) mma_kmajor<2>(adp, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 32, lane);
       mma_kmajor<2, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 16 * nh, 0, 32, lane);
       float tu[1][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
       zero(tu);
-      mma_kmajor<1>(tu, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);
+      mma_kmajor<1>(tu, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 16 * mt, 64, lane);
 #pragma unroll
       for (int nt = 0; nt < 1; ++nt)
 #pragma unroll
@@ -594,7 +599,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       }
       float tw[1][4];
       zero(tw);
-      mma_kmajor<1>(tw, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);
+      mma_kmajor<1>(tw, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 16 * mt, 64, lane);
 #pragma unroll
       for (int nt = 0; nt < 1; ++nt)
 #pragma unroll
@@ -623,7 +628,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   {  // Tp = Z^T T   (T[k][j] = 0 for k < j)
     float acc[2][4];
     zero(acc);
-    mma_kmajor<2>(acc, Zm, kLd, Tm, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+    mma_kmajor<2>(acc, Zm, kLd, Tm, kLd, 16 * mt, 16 * nh, 16 * nh, 64, lane);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -633,7 +638,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   {  // dA[j][m] = -sum_l Tp[l][j] T[m][l] on the strict lower triangle (T[m][l] = 0 for l > m)
     float acc[2][4];
     zero(acc);
-    mma_kmajor<2>(acc, Tp, kLd, Tt, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+    if (lower) mma_kmajor<2>(acc, Tp, kLd, Tt, kLd, 16 * mt, 16 * nh, 0, 16 * nh + 16, lane);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -643,6 +648,16 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       }
   }
   __syncthreads();
+  // k and q of the dq / dk stage, 64 features a pass (the first pass's loads are in flight
+  // during the row sums and the PG pass)
+  Blk bq2;
+  auto load_kq64 = [&](int f0) {
+    load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
+    load_blk(bk2, L, tid, [&](int i, int f) { return kin(i, f0 + 32 + f); });
+    load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f0 + f); });
+    load_blk(bq2, L, tid, [&](int i, int f) { return qin(i, f0 + 32 + f); });
+  };
+  load_kq64(0);
   // ---------------- row and column sums: dbeta and dG parts from A and from dP
   if (tid < 64) {
     const int i = tid;
@@ -677,44 +692,45 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     const int i = idx >> 6, j = idx & 63;
     dP[i * kLd + j] = Tp[j * kLd + i];
   }
-  // ---------------- key features again: dq and dk parts of this value head
+  // ---------------- key features again: dq and dk parts of this value head, 64 features a
+  // pass; the token-major k and q tiles take the T and T^T buffers, dead from here on
   {
+    float* Rk = Tm;
+    float* Rq = Tt;
     float rq[2] = {0.f, 0.f}, rw[2] = {0.f, 0.f};
-    load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f); });
-    load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f); });
-    for (int fb = 0; fb < D / 32; ++fb) {
+    for (int fp = 0; fp < D / 64; ++fp) {
       __syncthreads();
-      const int f0 = fb * 32;
-      store_tm(R0, bk, tid);
-      store_tm(R1, bq, tid);
+      const int f0 = fp * 64;
+      store_tm(Rk, bk, tid, kLd);
+      store_tm(Rk + 32, bk2, tid, kLd);
+      store_tm(Rq, bq, tid, kLd);
+      store_tm(Rq + 32, bq2, tid, kLd);
       __syncthreads();
-      if (fb + 1 < D / 32) {
-        load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f0 + 32 + f); });
-        load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f0 + 32 + f); });
-      }
+      if (fp + 1 < D / 64) load_kq64(f0 + 64);
       // the epilogue's inputs (dO S^T, v_new dS^T, T^T dw of this thread's elements) are
       // loaded before the products, which cover their latency
-      float2 os2[1][2], y2[1][2], tw2[1][2];
+      float2 os2[2][2], y2[2][2], tw2[2][2];
 #pragma unroll
-      for (int nt = 0; nt < 1; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const size_t at = sl * 64 * D + (size_t)(r0 + 8 * hh) * D + f0 + col32(nt, 0);
+          const size_t at = sl * 64 * D + (size_t)(r0 + 8 * hh) * D + f0 + col64(nt, 0);
           os2[nt][hh] = *reinterpret_cast<const float2*>(p.dos + at);
           y2[nt][hh] = *reinterpret_cast<const float2*>(p.ys + at);
           tw2[nt][hh] = *reinterpret_cast<const float2*>(p.ttdw + at);
         }
-      float aq[1][4], ak[1][4];
+      float aq[2][4], ak[2][4];
       zero(aq);
       zero(ak);
-      mma_kmajor<1, false, kX>(aq, Tp, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);  // (PG K)[i]
-      mma_kmajor<1, false, kX>(ak, dP, kLd, R1, kLt, 16 * mt, 8 * nh, 0, 64, lane);  // (PG^T Q)[i]
-      mma_kmajor<1, false, kX>(ak, GK, kLd, R0, kLt, 16 * mt, 8 * nh, 0, 64, lane);  // (dAt + dAt^T) K
+      // PG is lower triangular: (PG K)[i] takes tokens j <= i, (PG^T Q)[i] tokens j >= i
+      mma_kmajor<2, false, kX>(aq, Tp, kLd, Rk, kLd, 16 * mt, 16 * nh, 0, 16 * mt + 16, lane);
+      mma_kmajor<2, false, kX>(ak, dP, kLd, Rq, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
+      mma_kmajor<2, false, kX>(ak, GK, kLd, Rk, kLd, 16 * mt, 16 * nh, 0, 64, lane);  // (dAt + dAt^T) K
 #pragma unroll
-      for (int nt = 0; nt < 1; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const int i = r0 + 8 * hh, d = col32(nt, 0);
+          const int i = r0 + 8 * hh, d = col64(nt, 0);
           const size_t at = sl * 64 * D + (size_t)i * D + f0 + d;
           const float os[2] = {os2[nt][hh].x, os2[nt][hh].y};
           const float y[2] = {y2[nt][hh].x, y2[nt][hh].y};
@@ -723,7 +739,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int e = 2 * hh + u;
-            const float qv = R1[i * kLt + d + u], kv = R0[i * kLt + d + u];
+            const float qv = Rq[i * kLd + d + u], kv = Rk[i * kLd + d + u];
             rq[hh] = fmaf(qv, os[u], rq[hh]);
             rw[hh] = fmaf(kv, y[u], rw[hh]);
             dq[u] = fmaf(p.scale * eG[i], os[u], aq[nt][e]);
