@@ -315,11 +315,10 @@ __global__ void __launch_bounds__(kThr) bwd_state_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------------- per-chunk gradients
-constexpr int kLd = 68;    // row stride of the 64 x 64 matrices and feature-major blocks
-constexpr int kLt = 36;    // row stride of the token-major 64 x 32 blocks
+constexpr int kLd = 68;    // row stride of the 64 x 64 matrices and the 64-wide blocks
 
 constexpr size_t chunk_floats() {
-  return (size_t)7 * 64 * kLd + 16 * kLd + 4 * 32 * kLd + 64 * kLt + 8 * 64 + 4 * 64 * 8;
+  return (size_t)12 * 64 * kLd + 16 * kLd + 8 * 64 + 4 * 64 * 8;
 }
 
 // Threads of the per-chunk kernel: 16 warps, each owning a 16 x 16 tile of every 64 x 64
@@ -343,7 +342,7 @@ __device__ __forceinline__ void load_blk(Blk& b, int L, int tid, Get get) {
     b.r[u] = (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f;
   }
 }
-// ... stored feature-major [32][kLd] or token-major [64][kLt]
+// ... stored feature-major (32 rows of stride kLd) or token-major (64 rows of stride ld)
 __device__ __forceinline__ void store_fm(float* dst, const Blk& b, int tid) {
 #pragma unroll
   for (int u = 0; u < kBlkU; ++u) {
@@ -351,7 +350,7 @@ __device__ __forceinline__ void store_fm(float* dst, const Blk& b, int tid) {
     dst[(idx & 31) * kLd + (idx >> 5)] = b.r[u];
   }
 }
-__device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid, int ld = kLt) {
+__device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid, int ld) {
 #pragma unroll
   for (int u = 0; u < kBlkU; ++u) {
     const int idx = tid + u * kThrC;
@@ -402,7 +401,7 @@ __device__ __forceinline__ float quad_sum(float x) {
 
 // Per (chunk slot, value head). Every product is a warp-MMA tile product of fp32 operands in
 // shared memory (mma_kmajor). Warp w owns rows 16 mt.. of each result, mt = w / 4, and
-// columns 16 nh.. of a 64-wide one (8 nh.. of a 32-wide feature block), nh = (w - mt) % 4:
+// columns 16 nh.. (of 64 tokens or of a pass of 64 features), nh = (w - mt) % 4:
 // the warps of one SM sub-partition (w % 4) then hold every row block and every column
 // block once, so that the products that skip the zero triangle of T, of the gate-masked
 // matrices or of the lower-triangular results load the sub-partitions evenly.
@@ -418,12 +417,12 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   float* Zm = dP + 64 * kLd;       // Z; later dA
   float* Tp = Zm + 64 * kLd;       // scratch: Z^T T; later (dP * Gamma)^T
   float* Xs = Tp + 64 * kLd;       // [16][kLd] scratch of the inverse
-  float* B0 = Xs + 16 * kLd;       // [32][kLd] feature-major blocks
-  float* B1 = B0 + 32 * kLd;
-  float* B2 = B1 + 32 * kLd;
-  float* B3 = B2 + 32 * kLd;
-  float* R0 = B3 + 32 * kLd;       // [64][kLt] token-major block (dv_new, then dw)
-  float* G = R0 + 64 * kLt;        // [64] in-chunk cumulative gate
+  float* B0 = Xs + 16 * kLd;       // [64][kLd] feature-major blocks of 64 features
+  float* B1 = B0 + 64 * kLd;
+  float* B2 = B1 + 64 * kLd;
+  float* B3 = B2 + 64 * kLd;
+  float* R0 = B3 + 64 * kLd;       // [64][kLd] token-major block (dv_new, then dw)
+  float* G = R0 + 64 * kLd;        // [64] in-chunk cumulative gate
   float* eG = G + 64;              // exp(G)
   float* eL = eG + 64;             // exp(G_L - G)
   float* bt = eL + 64;             // beta
@@ -446,14 +445,21 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   auto kin = [&](int i, int f) { return ld_in<TIn>(p.k, ((size_t)(t0 + i) * p.H + h) * D + f); };
   auto qin = [&](int i, int f) { return ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + f); };
   auto vin = [&](int i, int f) { return ld_in<TIn>(p.v, ((size_t)(t0 + i) * p.Hv + hv) * D + f); };
-  // element (row, column) of accumulator entry (nt, e) of a 64-wide and a 32-wide result
+  // element (row, column) of accumulator entry (nt, e) of a 64-wide result
   auto col64 = [&](int nt, int e) { return 16 * nh + 8 * nt + c + (e & 1); };
-  auto col32 = [&](int nt, int e) { return 8 * nh + 8 * nt + c + (e & 1); };
   auto row = [&](int e) { return r0 + 8 * (e >> 1); };
 
-  Blk bk, bq;  // k and q blocks; the first ones are in flight during the gate scan
-  load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f); });
-  load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f); });
+  // k and q of features f0..f0+63 (two blocks each); the first ones are in flight during
+  // the gate scan
+  Blk bk[2], bq[2];
+  auto load_kq64 = [&](int f0) {
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      load_blk(bk[h], L, tid, [&](int i, int f) { return kin(i, f0 + 32 * h + f); });
+      load_blk(bq[h], L, tid, [&](int i, int f) { return qin(i, f0 + 32 * h + f); });
+    }
+  };
+  load_kq64(0);
   if (warp == 0) {  // G: inclusive in-chunk cumsum of g (two rows per lane, shuffle scan)
     const bool ok0 = lane < L, ok1 = lane + 32 < L;
     float g0 = ok0 ? p.g[(size_t)(t0 + lane) * p.Hv + hv] : 0.f;
@@ -478,23 +484,23 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     eG[tid] = expf(G[tid]);
     eL[tid] = expf(G[63] - G[tid]);
   }
-  // ---------------- K K^T and Q K^T (feature blocks of 32)
+  // ---------------- K K^T and Q K^T (64 features a pass)
   {
     float akk[2][4], aqk[2][4];
     zero(akk);
     zero(aqk);
-    for (int fb = 0; fb < D / 32; ++fb) {
+    for (int fp = 0; fp < D / 64; ++fp) {
       __syncthreads();
-      store_fm(B0, bk, tid);
-      store_fm(B1, bq, tid);
-      __syncthreads();
-      if (fb + 1 < D / 32) {  // the next block's loads run under this block's products
-        load_blk(bk, L, tid, [&](int i, int f) { return kin(i, (fb + 1) * 32 + f); });
-        load_blk(bq, L, tid, [&](int i, int f) { return qin(i, (fb + 1) * 32 + f); });
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        store_fm(B0 + 32 * h * kLd, bk[h], tid);
+        store_fm(B1 + 32 * h * kLd, bq[h], tid);
       }
+      __syncthreads();
+      if (fp + 1 < D / 64) load_kq64(64 * (fp + 1));  // in flight under this pass's products
       if (lower) {  // both are masked to the lower triangle
-        mma_kmajor<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
-        mma_kmajor<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+        mma_kmajor<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+        mma_kmajor<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
       }
     }
 #pragma unroll
@@ -508,19 +514,27 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
         Tm[i * kLd + j] = j < i ? bt[i] * gam * akk[nt][e] : 0.f;  // A
       }
   }
-  // value-feature blocks (dO, v_new, dv_new, v) of features f0..f0+31
-  Blk bdo, bvn, bdv, bv;
+  // value-feature blocks (dO, v_new, dv_new, v) of features f0..f0+63, two blocks each
+  Blk bdo[2], bvn[2], bdv[2], bv[2];
   auto load_value_blocks = [&](int f0) {
-    load_blk(bdo, L, tid, [&](int i, int f) { return ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + f0 + f); });
-    load_blk(bvn, 64, tid, [&](int i, int f) { return p.vn[sl * 64 * D + (size_t)i * D + f0 + f]; });
-    load_blk(bdv, 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + f0 + f]; });
-    load_blk(bv, L, tid, [&](int i, int f) { return vin(i, f0 + f); });
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int fh = f0 + 32 * h;
+      load_blk(bdo[h], L, tid, [&](int i, int f) { return ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + fh + f); });
+      load_blk(bvn[h], 64, tid, [&](int i, int f) { return p.vn[sl * 64 * D + (size_t)i * D + fh + f]; });
+      load_blk(bdv[h], 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + fh + f]; });
+      load_blk(bv[h], L, tid, [&](int i, int f) { return vin(i, fh + f); });
+    }
   };
-  // key-feature blocks (dw, k) of features f0..f0+31
-  Blk bdw, bk2;
+  // key-feature blocks (dw, k) of features f0..f0+63: dw, and k into bk
+  Blk bdw[2];
   auto load_key_blocks = [&](int f0) {
-    load_blk(bdw, 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + f0 + f]; });
-    load_blk(bk2, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int fh = f0 + 32 * h;
+      load_blk(bdw[h], 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + fh + f]; });
+      load_blk(bk[h], L, tid, [&](int i, int f) { return kin(i, fh + f); });
+    }
   };
   load_value_blocks(0);  // in flight during the inverse
   __syncthreads();
@@ -536,29 +550,32 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     float adp[2][4];
     zero(adp);
     float rv[2] = {0.f, 0.f};
-    for (int fb = 0; fb < D / 32; ++fb) {
+    for (int fp = 0; fp < D / 64; ++fp) {
       __syncthreads();
-      const int f0 = fb * 32;
-      store_fm(B0, bdo, tid);
-      store_fm(B1, bvn, tid);
-      store_fm(B2, bdv, tid);
-      store_fm(B3, bv, tid);
-      store_tm(R0, bdv, tid);
+      const int f0 = fp * 64;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        store_fm(B0 + 32 * h * kLd, bdo[h], tid);
+        store_fm(B1 + 32 * h * kLd, bvn[h], tid);
+        store_fm(B2 + 32 * h * kLd, bdv[h], tid);
+        store_fm(B3 + 32 * h * kLd, bv[h], tid);
+        store_tm(R0 + 32 * h, bdv[h], tid, kLd);
+      }
       __syncthreads();
-      if (fb + 1 < D / 32)
-        load_value_blocks(f0 + 32);
+      if (fp + 1 < D / 64)
+        load_value_blocks(f0 + 64);
       else
         load_key_blocks(0);
-      if (lower) mma_kmajor<2>(adp, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 32, lane);
-      mma_kmajor<2, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 16 * nh, 0, 32, lane);
-      float tu[1][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
+      if (lower) mma_kmajor<2>(adp, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+      mma_kmajor<2, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+      float tu[2][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
       zero(tu);
-      mma_kmajor<1>(tu, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 16 * mt, 64, lane);
+      mma_kmajor<2>(tu, Tm, kLd, R0, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
 #pragma unroll
-      for (int nt = 0; nt < 1; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int j = row(e), n = col32(nt, e);
+          const int j = row(e), n = col64(nt, e);
           rv[e >> 1] = fmaf(tu[nt][e], B3[n * kLd + j], rv[e >> 1]);
           if (j < L) p.dv[((size_t)(t0 + j) * p.Hv + hv) * D + f0 + n] = bt[j] * tu[nt][e];
         }
@@ -580,31 +597,34 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   // ---------------- key features: Z2, T^T dw (the dk and dbeta / dG parts)
   {
     float rk[2] = {0.f, 0.f};
-    for (int fb = 0; fb < D / 32; ++fb) {
+    for (int fp = 0; fp < D / 64; ++fp) {
       __syncthreads();
-      const int f0 = fb * 32;
-      store_fm(B0, bdw, tid);
-      store_fm(B1, bk2, tid);
-      store_tm(R0, bdw, tid);
+      const int f0 = fp * 64;
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        store_fm(B0 + 32 * h * kLd, bdw[h], tid);
+        store_fm(B1 + 32 * h * kLd, bk[h], tid);
+        store_tm(R0 + 32 * h, bdw[h], tid, kLd);
+      }
       __syncthreads();
-      if (fb + 1 < D / 32) load_key_blocks(f0 + 32);
+      if (fp + 1 < D / 64) load_key_blocks(f0 + 64);
       {  // Z2[i][j] = sum_d dw[i][d] exp(G_j) k[j][d]: scale column j after the sum
         float z2[2][4];
         zero(z2);
-        mma_kmajor<2, false, kX>(z2, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 32, lane);
+        mma_kmajor<2, false, kX>(z2, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 64, lane);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) az[nt][e] = fmaf(eG[col64(nt, e)], z2[nt][e], az[nt][e]);
       }
-      float tw[1][4];
+      float tw[2][4];
       zero(tw);
-      mma_kmajor<1>(tw, Tm, kLd, R0, kLt, 16 * mt, 8 * nh, 16 * mt, 64, lane);
+      mma_kmajor<2>(tw, Tm, kLd, R0, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
 #pragma unroll
-      for (int nt = 0; nt < 1; ++nt)
+      for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int j = row(e), n = col32(nt, e);
+          const int j = row(e), n = col64(nt, e);
           rk[e >> 1] = fmaf(tw[nt][e], B1[n * kLd + j], rk[e >> 1]);
           p.ttdw[sl * 64 * D + (size_t)j * D + f0 + n] = tw[nt][e];
         }
@@ -648,15 +668,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       }
   }
   __syncthreads();
-  // k and q of the dq / dk stage, 64 features a pass (the first pass's loads are in flight
-  // during the row sums and the PG pass)
-  Blk bq2;
-  auto load_kq64 = [&](int f0) {
-    load_blk(bk, L, tid, [&](int i, int f) { return kin(i, f0 + f); });
-    load_blk(bk2, L, tid, [&](int i, int f) { return kin(i, f0 + 32 + f); });
-    load_blk(bq, L, tid, [&](int i, int f) { return qin(i, f0 + f); });
-    load_blk(bq2, L, tid, [&](int i, int f) { return qin(i, f0 + 32 + f); });
-  };
+  // k and q of the dq / dk stage's first pass: in flight during the row sums and the PG pass
   load_kq64(0);
   // ---------------- row and column sums: dbeta and dG parts from A and from dP
   if (tid < 64) {
@@ -701,10 +713,11 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     for (int fp = 0; fp < D / 64; ++fp) {
       __syncthreads();
       const int f0 = fp * 64;
-      store_tm(Rk, bk, tid, kLd);
-      store_tm(Rk + 32, bk2, tid, kLd);
-      store_tm(Rq, bq, tid, kLd);
-      store_tm(Rq + 32, bq2, tid, kLd);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        store_tm(Rk + 32 * h, bk[h], tid, kLd);
+        store_tm(Rq + 32 * h, bq[h], tid, kLd);
+      }
       __syncthreads();
       if (fp + 1 < D / 64) load_kq64(f0 + 64);
       // the epilogue's inputs (dO S^T, v_new dS^T, T^T dw of this thread's elements) are
