@@ -328,34 +328,39 @@ constexpr int kThrC = 512;
 constexpr int kBlkU = 64 * 32 / kThrC;
 
 // A [64 x 32] block of a token-major source (tokens x 32 features) held in registers,
-// kBlkU elements per thread (element idx = tid + kThrC u: token idx / 32, feature idx % 32),
-// so that the next block's loads are in flight while the current one is used.
+// kBlkU elements per thread, so that the next block's loads are in flight while the current
+// one is used. Warp w, lane l holds token 4 w + l / 8 and features l % 8 + 8 u: each load
+// instruction reads four 8-feature runs, and the 32 lanes of a feature-major store fall in
+// 32 distinct banks (4 f + t, row stride kLd = 4 mod 32).
 struct Blk {
   float r[kBlkU];
 };
+__device__ __forceinline__ int blk_token(int tid) { return 4 * (tid >> 5) + ((tid & 31) >> 3); }
+__device__ __forceinline__ int blk_feature(int tid, int u) { return (tid & 7) + 8 * u; }
 // get(i, f) returns token i, feature f; tokens at or past L read as zero.
 template <typename Get>
 __device__ __forceinline__ void load_blk(Blk& b, int L, int tid, Get get) {
+  const int t = blk_token(tid);
 #pragma unroll
-  for (int u = 0; u < kBlkU; ++u) {
-    const int idx = tid + u * kThrC;
-    b.r[u] = (idx >> 5) < L ? get(idx >> 5, idx & 31) : 0.f;
-  }
+  for (int u = 0; u < kBlkU; ++u) b.r[u] = t < L ? get(t, blk_feature(tid, u)) : 0.f;
 }
 // ... stored feature-major (32 rows of stride kLd) or token-major (64 rows of stride ld)
 __device__ __forceinline__ void store_fm(float* dst, const Blk& b, int tid) {
+  const int t = blk_token(tid);
 #pragma unroll
-  for (int u = 0; u < kBlkU; ++u) {
-    const int idx = tid + u * kThrC;
-    dst[(idx & 31) * kLd + (idx >> 5)] = b.r[u];
-  }
+  for (int u = 0; u < kBlkU; ++u) dst[blk_feature(tid, u) * kLd + t] = b.r[u];
 }
 __device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid, int ld) {
+  const int t = blk_token(tid);
 #pragma unroll
-  for (int u = 0; u < kBlkU; ++u) {
-    const int idx = tid + u * kThrC;
-    dst[(idx >> 5) * ld + (idx & 31)] = b.r[u];
-  }
+  for (int u = 0; u < kBlkU; ++u) dst[t * ld + blk_feature(tid, u)] = b.r[u];
+}
+// Element (i, j) of a 64 x 64 pass over index idx: each warp covers an 8 x 4 patch, so that
+// both [i][j] and [j][i] accesses (row stride kLd) are at most two-way bank conflicts.
+__device__ __forceinline__ void patch_ij(int idx, int& i, int& j) {
+  const int blk = idx >> 5, l = idx & 31;
+  i = 8 * (blk & 7) + (l & 7);
+  j = 4 * (blk >> 3) + (l >> 3);
 }
 
 // acc[nt] += sum_{k0 <= k < k1} X[k][m0 + r] Y[k][n0 + 8 nt + c'] over a 16 x 8 NT warp
@@ -540,7 +545,8 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   __syncthreads();
   tri_inverse_64_tc<kThrC / 32>(Tm, kLd, Xs, tid);  // Tm = T, ends synchronized
   for (int idx = tid; idx < 64 * 64; idx += kThrC) {
-    const int i = idx >> 6, j = idx & 63;
+    int i, j;
+    patch_ij(idx, i, j);
     Tt[j * kLd + i] = Tm[i * kLd + j];
   }
   // ---------------- value features: dP, Z1, T^T dv_new (dv and the dbeta part)
@@ -691,7 +697,8 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   __syncthreads();
   // PG = dP * Gamma (lower incl.), Tp = PG^T, GK = dAt + dAt^T with dAt = dA * beta_i Gamma_ij
   for (int idx = tid; idx < 64 * 64; idx += kThrC) {
-    const int i = idx >> 6, j = idx & 63;
+    int i, j;
+    patch_ij(idx, i, j);
     const float ex = expf(j <= i ? G[i] - G[j] : G[j] - G[i]);  // one of the two is used
     const float gij = j <= i ? ex : 0.f;
     const float gji = i <= j ? ex : 0.f;
@@ -701,7 +708,8 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   }
   __syncthreads();
   for (int idx = tid; idx < 64 * 64; idx += kThrC) {
-    const int i = idx >> 6, j = idx & 63;
+    int i, j;
+    patch_ij(idx, i, j);
     dP[i * kLd + j] = Tp[j * kLd + i];
   }
   // ---------------- key features again: dq and dk parts of this value head, 64 features a
