@@ -677,10 +677,12 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   // k and q of the dq / dk stage's first pass: in flight during the row sums and the PG pass
   load_kq64(0);
   // ---------------- row and column sums: dbeta and dG parts from A and from dP
-  if (tid < 64) {
-    const int i = tid;
+  {  // eight threads per row i, each over columns j = 8 m + sub, then a fixed shuffle sum
+    const int i = tid >> 3, sub = tid & 7;
     float db = 0.f, dg = 0.f;
-    for (int j = 0; j < 64; ++j) {
+#pragma unroll
+    for (int m = 0; m < 8; ++m) {
+      const int j = 8 * m + sub;
       const float da = Zm[i * kLd + j], gk = GK[i * kLd + j];
       db = fmaf(da, gk, db);
       dg = fmaf(da, bt[i] * gk, dg);                      // row of dA * A
@@ -688,11 +690,18 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       dg -= Zm[j * kLd + i] * bt[j] * GK[j * kLd + i];    // column of dA * A
       dg -= dP[j * kLd + i] * Mm[j * kLd + i];            // column of dP * M
     }
-    const float sv = (pv[i * 8] + pv[i * 8 + 1]) + (pv[i * 8 + 2] + pv[i * 8 + 3]);
-    const float sk = (pk[i * 8] + pk[i * 8 + 1]) + (pk[i * 8 + 2] + pk[i * 8 + 3]);
-    rsk[i] = sk;
-    dBv[i] = sv + eG[i] * sk + db;
-    dGv[i] = dg + bt[i] * eG[i] * sk;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      db += __shfl_xor_sync(0xffffffffu, db, o);
+      dg += __shfl_xor_sync(0xffffffffu, dg, o);
+    }
+    if (sub == 0) {
+      const float sv = (pv[i * 8] + pv[i * 8 + 1]) + (pv[i * 8 + 2] + pv[i * 8 + 3]);
+      const float sk = (pk[i * 8] + pk[i * 8 + 1]) + (pk[i * 8 + 2] + pk[i * 8 + 3]);
+      rsk[i] = sk;
+      dBv[i] = sv + eG[i] * sk + db;
+      dGv[i] = dg + bt[i] * eG[i] * sk;
+    }
   }
   __syncthreads();
   // PG = dP * Gamma (lower incl.), Tp = PG^T, GK = dAt + dAt^T with dAt = dA * beta_i Gamma_ij
