@@ -315,11 +315,14 @@ __global__ void __launch_bounds__(kThr) bwd_state_kernel(BwdParams p) {
 }
 
 // ---------------------------------------------------------------- per-chunk gradients
-constexpr int kLd = 68;    // row stride of the 64 x 64 matrices and the 64-wide blocks
+constexpr int kLd = 72;    // row stride (8 mod 32) of the 64 x 64 matrices and the 64-wide blocks
 
 constexpr size_t chunk_floats() {
-  return (size_t)12 * 64 * kLd + 16 * kLd + 8 * 64 + 4 * 64 * 8;
+  return (size_t)11 * 64 * kLd + 16 * kLd + 8 * 64 + 4 * 64 * 8;
 }
+// On a GB300 a launch of this kernel with 219,392 B of dynamic shared memory ran and one with
+// 231,936 B was refused (the per-block total also holds about 4 KB beyond the dynamic size).
+static_assert(chunk_floats() * sizeof(float) <= 219392, "per-chunk kernel shared memory");
 
 // Threads of the per-chunk kernel: 16 warps, each owning a 16 x 16 tile of every 64 x 64
 // result and a 16 x 8 tile of every 64 x 32 one, so that four warps per SM sub-partition
@@ -330,8 +333,8 @@ constexpr int kBlkU = 64 * 32 / kThrC;
 // A [64 x 32] block of a token-major source (tokens x 32 features) held in registers,
 // kBlkU elements per thread, so that the next block's loads are in flight while the current
 // one is used. Warp w, lane l holds token 4 w + l / 8 and features l % 8 + 8 u: each load
-// instruction reads four 8-feature runs, and the 32 lanes of a feature-major store fall in
-// 32 distinct banks (4 f + t, row stride kLd = 4 mod 32).
+// instruction reads four 8-feature runs, and the 32 lanes of a token-major store fall in
+// 32 distinct banks (8 t + f, row stride 8 mod 32; a feature-major store is two-way).
 struct Blk {
   float r[kBlkU];
 };
@@ -363,33 +366,40 @@ __device__ __forceinline__ void patch_ij(int idx, int& i, int& j) {
   j = 4 * (blk >> 3) + (l >> 3);
 }
 
-// acc[nt] += sum_{k0 <= k < k1} X[k][m0 + r] Y[k][n0 + 8 nt + c'] over a 16 x 8 NT warp
-// tile: both operands fp32 and k-major in shared memory (row strides ldx, ldy), split into
-// bf16 hi + lo per fragment, three warp MMAs per step of 16 (hi*hi, hi*lo, lo*hi).
+// acc[nt] += sum_{k0 <= k < k1} A[m0 + r][k] B[n0 + 8 nt + c'][k] over a 16 x 8 NT warp tile:
+// both operands fp32 in shared memory with k contiguous (row strides lda, ldb = 8 mod 32, so
+// that the 64-bit fragment loads of each half-warp fall in distinct banks), split into bf16
+// hi + lo per fragment, three warp MMAs per step of 16 (hi*hi, hi*lo, lo*hi).
 // Accumulator element e of tile nt: row m0 + g + 8 (e >> 1), column n0 + 8 nt + c + (e & 1)
-// (g = lane / 4, c = 2 (lane % 4)). Reads X rows k0..k1-1, columns m0..m0+15.
-// AX / BX: the X / Y operand holds values exact in bf16 (the bf16 inputs k, q, v), whose
+// (g = lane / 4, c = 2 (lane % 4)).
+// AX / BX: the A / B operand holds values exact in bf16 (the bf16 inputs k, q, v), whose
 // lo halves are zero: the terms with them are skipped (two MMAs per step, or one when both
 // are exact).
 template <int NT, bool AX = false, bool BX = false>
-__device__ __forceinline__ void mma_kmajor(float (&acc)[NT][4], const float* X, int ldx,
-                                           const float* Y, int ldy, int m0, int n0, int k0,
-                                           int k1, int lane) {
+__device__ __forceinline__ void mma_rowk(float (&acc)[NT][4], const float* A, int lda,
+                                         const float* B, int ldb, int m0, int n0, int k0,
+                                         int k1, int lane) {
   const int g = lane >> 2, c = 2 * (lane & 3);
 #pragma unroll 2
   for (int k = k0; k < k1; k += 16) {
+    const float* ap = A + (m0 + g) * lda + k + c;
+    const float2 a0 = *reinterpret_cast<const float2*>(ap);
+    const float2 a1 = *reinterpret_cast<const float2*>(ap + 8 * lda);
+    const float2 a2 = *reinterpret_cast<const float2*>(ap + 8);
+    const float2 a3 = *reinterpret_cast<const float2*>(ap + 8 * lda + 8);
     uint32_t ah[4], al[4];
-    const float* xp = X + (k + c) * ldx + m0 + g;
-    split_pack2(xp[0], xp[ldx], ah[0], al[0]);
-    split_pack2(xp[8], xp[ldx + 8], ah[1], al[1]);
-    split_pack2(xp[8 * ldx], xp[9 * ldx], ah[2], al[2]);
-    split_pack2(xp[8 * ldx + 8], xp[9 * ldx + 8], ah[3], al[3]);
+    split_pack2(a0.x, a0.y, ah[0], al[0]);
+    split_pack2(a1.x, a1.y, ah[1], al[1]);
+    split_pack2(a2.x, a2.y, ah[2], al[2]);
+    split_pack2(a3.x, a3.y, ah[3], al[3]);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const float* yp = Y + (k + c) * ldy + n0 + 8 * nt + g;
+      const float* bp = B + (n0 + 8 * nt + g) * ldb + k + c;
+      const float2 b0 = *reinterpret_cast<const float2*>(bp);
+      const float2 b1 = *reinterpret_cast<const float2*>(bp + 8);
       uint32_t bh[2], bl[2];
-      split_pack2(yp[0], yp[ldy], bh[0], bl[0]);
-      split_pack2(yp[8 * ldy], yp[9 * ldy], bh[1], bl[1]);
+      split_pack2(b0.x, b0.y, bh[0], bl[0]);
+      split_pack2(b1.x, b1.y, bh[1], bl[1]);
       mma_bf16(acc[nt], ah, bh[0], bh[1]);
       if (!BX) mma_bf16(acc[nt], ah, bl[0], bl[1]);
       if (!AX) mma_bf16(acc[nt], al, bh[0], bh[1]);
@@ -405,7 +415,9 @@ __device__ __forceinline__ float quad_sum(float x) {
 }
 
 // Per (chunk slot, value head). Every product is a warp-MMA tile product of fp32 operands in
-// shared memory (mma_kmajor). Warp w owns rows 16 mt.. of each result, mt = w / 4, and
+// shared memory stored with the contraction index contiguous (mma_rowk): token-major blocks
+// for the sums over features, feature-major blocks and transposed matrices for the sums over
+// tokens. Warp w owns rows 16 mt.. of each result, mt = w / 4, and
 // columns 16 nh.. (of 64 tokens or of a pass of 64 features), nh = (w - mt) % 4:
 // the warps of one SM sub-partition (w % 4) then hold every row block and every column
 // block once, so that the products that skip the zero triangle of T, of the gate-masked
@@ -419,15 +431,15 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   float* GK = Tt + 64 * kLd;       // Gamma * K K^T (strict lower); later dAt + dAt^T
   float* Mm = GK + 64 * kLd;       // Gamma * Q K^T (lower incl.)
   float* dP = Mm + 64 * kLd;       // scale dO v_new^T (lower incl.); later dP * Gamma
-  float* Zm = dP + 64 * kLd;       // Z; later dA
-  float* Tp = Zm + 64 * kLd;       // scratch: Z^T T; later (dP * Gamma)^T
+  float* Zm = dP + 64 * kLd;       // Z^T; later dA
+  float* Tp = Zm + 64 * kLd;       // scratch: (Z^T T)^T; later (dP * Gamma)^T
+  float* R0 = Tp;                  // before that, the feature-major block (dv_new, then dw)
   float* Xs = Tp + 64 * kLd;       // [16][kLd] scratch of the inverse
-  float* B0 = Xs + 16 * kLd;       // [64][kLd] feature-major blocks of 64 features
+  float* B0 = Xs + 16 * kLd;       // [64][kLd] token-major blocks of 64 features
   float* B1 = B0 + 64 * kLd;
   float* B2 = B1 + 64 * kLd;
   float* B3 = B2 + 64 * kLd;
-  float* R0 = B3 + 64 * kLd;       // [64][kLd] token-major block (dv_new, then dw)
-  float* G = R0 + 64 * kLd;        // [64] in-chunk cumulative gate
+  float* G = B3 + 64 * kLd;        // [64] in-chunk cumulative gate
   float* eG = G + 64;              // exp(G)
   float* eL = eG + 64;             // exp(G_L - G)
   float* bt = eL + 64;             // beta
@@ -498,14 +510,14 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       __syncthreads();
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        store_fm(B0 + 32 * h * kLd, bk[h], tid);
-        store_fm(B1 + 32 * h * kLd, bq[h], tid);
+        store_tm(B0 + 32 * h, bk[h], tid, kLd);
+        store_tm(B1 + 32 * h, bq[h], tid, kLd);
       }
       __syncthreads();
       if (fp + 1 < D / 64) load_kq64(64 * (fp + 1));  // in flight under this pass's products
       if (lower) {  // both are masked to the lower triangle
-        mma_kmajor<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
-        mma_kmajor<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+        mma_rowk<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+        mma_rowk<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
       }
     }
 #pragma unroll
@@ -561,28 +573,28 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       const int f0 = fp * 64;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        store_fm(B0 + 32 * h * kLd, bdo[h], tid);
-        store_fm(B1 + 32 * h * kLd, bvn[h], tid);
-        store_fm(B2 + 32 * h * kLd, bdv[h], tid);
-        store_fm(B3 + 32 * h * kLd, bv[h], tid);
-        store_tm(R0 + 32 * h, bdv[h], tid, kLd);
+        store_tm(B0 + 32 * h, bdo[h], tid, kLd);
+        store_tm(B1 + 32 * h, bvn[h], tid, kLd);
+        store_tm(B2 + 32 * h, bdv[h], tid, kLd);
+        store_tm(B3 + 32 * h, bv[h], tid, kLd);
+        store_fm(R0 + 32 * h * kLd, bdv[h], tid);
       }
       __syncthreads();
       if (fp + 1 < D / 64)
         load_value_blocks(f0 + 64);
       else
         load_key_blocks(0);
-      if (lower) mma_kmajor<2>(adp, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 64, lane);
-      mma_kmajor<2, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+      if (lower) mma_rowk<2>(adp, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+      mma_rowk<2, false, kX>(az, B2, kLd, B3, kLd, 16 * mt, 16 * nh, 0, 64, lane);
       float tu[2][4];  // (T^T dv_new)[j][n]: T[i][j] = 0 for i < j
       zero(tu);
-      mma_kmajor<2>(tu, Tm, kLd, R0, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
+      mma_rowk<2>(tu, Tt, kLd, R0, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = row(e), n = col64(nt, e);
-          rv[e >> 1] = fmaf(tu[nt][e], B3[n * kLd + j], rv[e >> 1]);
+          rv[e >> 1] = fmaf(tu[nt][e], B3[j * kLd + n], rv[e >> 1]);
           if (j < L) p.dv[((size_t)(t0 + j) * p.Hv + hv) * D + f0 + n] = bt[j] * tu[nt][e];
         }
     }
@@ -608,16 +620,16 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       const int f0 = fp * 64;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        store_fm(B0 + 32 * h * kLd, bdw[h], tid);
-        store_fm(B1 + 32 * h * kLd, bk[h], tid);
-        store_tm(R0 + 32 * h, bdw[h], tid, kLd);
+        store_tm(B0 + 32 * h, bdw[h], tid, kLd);
+        store_tm(B1 + 32 * h, bk[h], tid, kLd);
+        store_fm(R0 + 32 * h * kLd, bdw[h], tid);
       }
       __syncthreads();
       if (fp + 1 < D / 64) load_key_blocks(f0 + 64);
       {  // Z2[i][j] = sum_d dw[i][d] exp(G_j) k[j][d]: scale column j after the sum
         float z2[2][4];
         zero(z2);
-        mma_kmajor<2, false, kX>(z2, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 64, lane);
+        mma_rowk<2, false, kX>(z2, B0, kLd, B1, kLd, 16 * mt, 16 * nh, 0, 64, lane);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -625,13 +637,13 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       }
       float tw[2][4];
       zero(tw);
-      mma_kmajor<2>(tw, Tm, kLd, R0, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
+      mma_rowk<2>(tw, Tt, kLd, R0, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const int j = row(e), n = col64(nt, e);
-          rk[e >> 1] = fmaf(tw[nt][e], B1[n * kLd + j], rk[e >> 1]);
+          rk[e >> 1] = fmaf(tw[nt][e], B1[j * kLd + n], rk[e >> 1]);
           p.ttdw[sl * 64 * D + (size_t)j * D + f0 + n] = tw[nt][e];
         }
     }
@@ -642,29 +654,30 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       pk[(r0 + 8) * 8 + nh] = rk[1];
     }
   }
-  // Z = (Z1 + Z2) diag(beta)
+  // Z = (Z1 + Z2) diag(beta), stored transposed
 #pragma unroll
   for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
       const int j = col64(nt, e);
-      Zm[row(e) * kLd + j] = bt[j] * az[nt][e];
+      Zm[j * kLd + row(e)] = bt[j] * az[nt][e];
     }
   __syncthreads();
-  {  // Tp = Z^T T   (T[k][j] = 0 for k < j)
+  {  // Z^T T (T[k][n] = 0 for k < n), stored transposed
     float acc[2][4];
     zero(acc);
-    mma_kmajor<2>(acc, Zm, kLd, Tm, kLd, 16 * mt, 16 * nh, 16 * nh, 64, lane);
+    mma_rowk<2>(acc, Zm, kLd, Tt, kLd, 16 * mt, 16 * nh, 16 * nh, 64, lane);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) Tp[row(e) * kLd + col64(nt, e)] = acc[nt][e];
+      for (int e = 0; e < 4; ++e) Tp[col64(nt, e) * kLd + row(e)] = acc[nt][e];
   }
   __syncthreads();
-  {  // dA[j][m] = -sum_l Tp[l][j] T[m][l] on the strict lower triangle (T[m][l] = 0 for l > m)
+  {  // dA[j][m] = -sum_l (Z^T T)[l][j] T[m][l] on the strict lower triangle (T[m][l] = 0 for
+     // l > m)
     float acc[2][4];
     zero(acc);
-    if (lower) mma_kmajor<2>(acc, Tp, kLd, Tt, kLd, 16 * mt, 16 * nh, 0, 16 * nh + 16, lane);
+    if (lower) mma_rowk<2>(acc, Tp, kLd, Tm, kLd, 16 * mt, 16 * nh, 0, 16 * nh + 16, lane);
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -722,7 +735,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     dP[i * kLd + j] = Tp[j * kLd + i];
   }
   // ---------------- key features again: dq and dk parts of this value head, 64 features a
-  // pass; the token-major k and q tiles take the T and T^T buffers, dead from here on
+  // pass; the feature-major k and q tiles take the T and T^T buffers, dead from here on
   {
     float* Rk = Tm;
     float* Rq = Tt;
@@ -732,8 +745,8 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       const int f0 = fp * 64;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        store_tm(Rk + 32 * h, bk[h], tid, kLd);
-        store_tm(Rq + 32 * h, bq[h], tid, kLd);
+        store_fm(Rk + 32 * h * kLd, bk[h], tid);
+        store_fm(Rq + 32 * h * kLd, bq[h], tid);
       }
       __syncthreads();
       if (fp + 1 < D / 64) load_kq64(f0 + 64);
@@ -753,9 +766,9 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       zero(aq);
       zero(ak);
       // PG is lower triangular: (PG K)[i] takes tokens j <= i, (PG^T Q)[i] tokens j >= i
-      mma_kmajor<2, false, kX>(aq, Tp, kLd, Rk, kLd, 16 * mt, 16 * nh, 0, 16 * mt + 16, lane);
-      mma_kmajor<2, false, kX>(ak, dP, kLd, Rq, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
-      mma_kmajor<2, false, kX>(ak, GK, kLd, Rk, kLd, 16 * mt, 16 * nh, 0, 64, lane);  // (dAt + dAt^T) K
+      mma_rowk<2, false, kX>(aq, dP, kLd, Rk, kLd, 16 * mt, 16 * nh, 0, 16 * mt + 16, lane);
+      mma_rowk<2, false, kX>(ak, Tp, kLd, Rq, kLd, 16 * mt, 16 * nh, 16 * mt, 64, lane);
+      mma_rowk<2, false, kX>(ak, GK, kLd, Rk, kLd, 16 * mt, 16 * nh, 0, 64, lane);  // (dAt + dAt^T) K
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
@@ -769,7 +782,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
 #pragma unroll
           for (int u = 0; u < 2; ++u) {
             const int e = 2 * hh + u;
-            const float qv = Rq[i * kLd + d + u], kv = Rk[i * kLd + d + u];
+            const float qv = Rq[(d + u) * kLd + i], kv = Rk[(d + u) * kLd + i];
             rq[hh] = fmaf(qv, os[u], rq[hh]);
             rw[hh] = fmaf(kv, y[u], rw[hh]);
             dq[u] = fmaf(p.scale * eG[i], os[u], aq[nt][e]);
