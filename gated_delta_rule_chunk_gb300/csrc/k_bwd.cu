@@ -592,10 +592,14 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = row(e), n = col64(nt, e);
-          rv[e >> 1] = fmaf(tu[nt][e], B3[j * kLd + n], rv[e >> 1]);
-          if (j < L) p.dv[((size_t)(t0 + j) * p.Hv + hv) * D + f0 + n] = bt[j] * tu[nt][e];
+        for (int hh = 0; hh < 2; ++hh) {  // entries 2 hh, 2 hh + 1: adjacent columns
+          const int j = r0 + 8 * hh, n = col64(nt, 0);
+          const float t0v = tu[nt][2 * hh], t1v = tu[nt][2 * hh + 1];
+          rv[hh] = fmaf(t0v, B3[j * kLd + n], rv[hh]);
+          rv[hh] = fmaf(t1v, B3[j * kLd + n + 1], rv[hh]);
+          if (j < L)
+            *reinterpret_cast<float2*>(p.dv + ((size_t)(t0 + j) * p.Hv + hv) * D + f0 + n) =
+                make_float2(bt[j] * t0v, bt[j] * t1v);
         }
     }
     rv[0] = quad_sum(rv[0]);
@@ -641,10 +645,12 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const int j = row(e), n = col64(nt, e);
-          rk[e >> 1] = fmaf(tw[nt][e], B1[j * kLd + n], rk[e >> 1]);
-          p.ttdw[sl * 64 * D + (size_t)j * D + f0 + n] = tw[nt][e];
+        for (int hh = 0; hh < 2; ++hh) {  // entries 2 hh, 2 hh + 1: adjacent columns
+          const int j = r0 + 8 * hh, n = col64(nt, 0);
+          const float t0v = tw[nt][2 * hh], t1v = tw[nt][2 * hh + 1];
+          rk[hh] = fmaf(t0v, B1[j * kLd + n], rk[hh]);
+          rk[hh] = fmaf(t1v, B1[j * kLd + n + 1], rk[hh]);
+          *reinterpret_cast<float2*>(p.ttdw + sl * 64 * D + (size_t)j * D + f0 + n) = make_float2(t0v, t1v);
         }
     }
     rk[0] = quad_sum(rk[0]);
@@ -848,17 +854,19 @@ __global__ void __launch_bounds__(kThr) bwd_reduce_kernel(BwdParams p) {
   const int tid = threadIdx.x, h = blockIdx.y;
   int t0, L, wslot;
   if (!resolve_slot(p, blockIdx.x, t0, L, wslot)) return;
-  for (int idx = tid; idx < L * D; idx += kThr) {
+  for (int idx = 4 * tid; idx < L * D; idx += 4 * kThr) {  // four features at a time
     const int i = idx / D, d = idx % D;
-    float sq = 0.f, sk = 0.f;
+    float4 sq = make_float4(0.f, 0.f, 0.f, 0.f), sk = sq;
     for (int r = 0; r < p.HG; ++r) {
       const size_t at = ((size_t)wslot * p.Hv + h * p.HG + r) * 64 * D + idx;
-      sq += p.dqp[at];
-      sk += p.dkp[at];
+      const float4 a = *reinterpret_cast<const float4*>(p.dqp + at);
+      const float4 b = *reinterpret_cast<const float4*>(p.dkp + at);
+      sq.x += a.x; sq.y += a.y; sq.z += a.z; sq.w += a.w;
+      sk.x += b.x; sk.y += b.y; sk.z += b.z; sk.w += b.w;
     }
     const size_t o = ((size_t)(t0 + i) * p.H + h) * D + d;
-    p.dq[o] = sq;
-    p.dk[o] = sk;
+    *reinterpret_cast<float4*>(p.dq + o) = sq;
+    *reinterpret_cast<float4*>(p.dk + o) = sk;
   }
 }
 
