@@ -358,6 +358,33 @@ __device__ __forceinline__ void store_tm(float* dst, const Blk& b, int tid, int 
 #pragma unroll
   for (int u = 0; u < kBlkU; ++u) dst[t * ld + blk_feature(tid, u)] = b.r[u];
 }
+// A [64 x 32] block held as one 4-feature vector per thread: warp w, lane l holds token
+// 4 w + l / 8 and features 4 (l % 8) .. 4 (l % 8) + 3 (one vector load); for blocks stored
+// token-major only, where each eight lanes write one contiguous 128-byte row segment.
+struct Blk4 {
+  float4 v;
+};
+template <typename TIn>
+__device__ __forceinline__ float4 ld_in4(const void* base, size_t idx) {
+  if constexpr (std::is_same<TIn, __nv_bfloat16>::value) {
+    const uint2 r = *reinterpret_cast<const uint2*>(reinterpret_cast<const __nv_bfloat16*>(base) + idx);
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&r.y));
+    return make_float4(a.x, a.y, b.x, b.y);
+  } else {
+    return *reinterpret_cast<const float4*>(reinterpret_cast<const float*>(base) + idx);
+  }
+}
+// get(i, f) returns features f..f+3 of token i; tokens at or past L read as zero.
+template <typename Get>
+__device__ __forceinline__ void load_blk4(Blk4& b, int L, int tid, Get get) {
+  const int t = blk_token(tid);
+  b.v = t < L ? get(t, 4 * (tid & 7)) : make_float4(0.f, 0.f, 0.f, 0.f);
+}
+__device__ __forceinline__ void store_tm4(float* dst, const Blk4& b, int tid, int ld) {
+  *reinterpret_cast<float4*>(dst + blk_token(tid) * ld + 4 * (tid & 7)) = b.v;
+}
+
 // Element (i, j) of a 64 x 64 pass over index idx: each warp covers an 8 x 4 patch, so that
 // both [i][j] and [j][i] accesses (row stride kLd) are at most two-way bank conflicts.
 __device__ __forceinline__ void patch_ij(int idx, int& i, int& j) {
@@ -461,22 +488,23 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
   const size_t sl = (size_t)wslot * p.Hv + hv;
   auto kin = [&](int i, int f) { return ld_in<TIn>(p.k, ((size_t)(t0 + i) * p.H + h) * D + f); };
   auto qin = [&](int i, int f) { return ld_in<TIn>(p.q, ((size_t)(t0 + i) * p.H + h) * D + f); };
-  auto vin = [&](int i, int f) { return ld_in<TIn>(p.v, ((size_t)(t0 + i) * p.Hv + hv) * D + f); };
   // element (row, column) of accumulator entry (nt, e) of a 64-wide result
   auto col64 = [&](int nt, int e) { return 16 * nh + 8 * nt + c + (e & 1); };
   auto row = [&](int e) { return r0 + 8 * (e >> 1); };
 
-  // k and q of features f0..f0+63 (two blocks each); the first ones are in flight during
-  // the gate scan
-  Blk bk[2], bq[2];
-  auto load_kq64 = [&](int f0) {
+  const size_t krow = (size_t)p.H * D, vrow = (size_t)p.Hv * D;  // token strides
+  const size_t kbase = ((size_t)t0 * p.H + h) * D, vbase = ((size_t)t0 * p.Hv + hv) * D;
+  // k and q of features f0..f0+63 (two blocks each) for the first stage, token-major only
+  // (vector loads); the first ones are in flight during the gate scan
+  Blk4 k4[2], q4[2];
+  auto load_kq4 = [&](int f0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      load_blk(bk[h], L, tid, [&](int i, int f) { return kin(i, f0 + 32 * h + f); });
-      load_blk(bq[h], L, tid, [&](int i, int f) { return qin(i, f0 + 32 * h + f); });
+    for (int hh = 0; hh < 2; ++hh) {
+      load_blk4(k4[hh], L, tid, [&](int i, int f) { return ld_in4<TIn>(p.k, kbase + i * krow + f0 + 32 * hh + f); });
+      load_blk4(q4[hh], L, tid, [&](int i, int f) { return ld_in4<TIn>(p.q, kbase + i * krow + f0 + 32 * hh + f); });
     }
   };
-  load_kq64(0);
+  load_kq4(0);
   if (warp == 0) {  // G: inclusive in-chunk cumsum of g (two rows per lane, shuffle scan)
     const bool ok0 = lane < L, ok1 = lane + 32 < L;
     float g0 = ok0 ? p.g[(size_t)(t0 + lane) * p.Hv + hv] : 0.f;
@@ -509,12 +537,12 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     for (int fp = 0; fp < D / 64; ++fp) {
       __syncthreads();
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        store_tm(B0 + 32 * h, bk[h], tid, kLd);
-        store_tm(B1 + 32 * h, bq[h], tid, kLd);
+      for (int hh = 0; hh < 2; ++hh) {
+        store_tm4(B0 + 32 * hh, k4[hh], tid, kLd);
+        store_tm4(B1 + 32 * hh, q4[hh], tid, kLd);
       }
       __syncthreads();
-      if (fp + 1 < D / 64) load_kq64(64 * (fp + 1));  // in flight under this pass's products
+      if (fp + 1 < D / 64) load_kq4(64 * (fp + 1));  // in flight under this pass's products
       if (lower) {  // both are masked to the lower triangle
         mma_rowk<2, kX, kX>(akk, B0, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
         mma_rowk<2, kX, kX>(aqk, B1, kLd, B0, kLd, 16 * mt, 16 * nh, 0, 64, lane);
@@ -531,26 +559,29 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
         Tm[i * kLd + j] = j < i ? bt[i] * gam * akk[nt][e] : 0.f;  // A
       }
   }
-  // value-feature blocks (dO, v_new, dv_new, v) of features f0..f0+63, two blocks each
-  Blk bdo[2], bvn[2], bdv[2], bv[2];
+  // value-feature blocks (dO, v_new, dv_new, v) of features f0..f0+63, two blocks each;
+  // dv_new is also stored feature-major (scalar element map), the others by vectors
+  Blk4 bdo[2], bvn[2], bv[2];
+  Blk bdv[2];
   auto load_value_blocks = [&](int f0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int fh = f0 + 32 * h;
-      load_blk(bdo[h], L, tid, [&](int i, int f) { return ld_dout(p, ((size_t)(t0 + i) * p.Hv + hv) * D + fh + f); });
-      load_blk(bvn[h], 64, tid, [&](int i, int f) { return p.vn[sl * 64 * D + (size_t)i * D + fh + f]; });
-      load_blk(bdv[h], 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + fh + f]; });
-      load_blk(bv[h], L, tid, [&](int i, int f) { return vin(i, fh + f); });
+    for (int hh = 0; hh < 2; ++hh) {
+      const int fh = f0 + 32 * hh;
+      load_blk4(bdo[hh], L, tid, [&](int i, int f) { return ld_dout4(p, vbase + i * vrow + fh + f); });
+      load_blk4(bvn[hh], 64, tid, [&](int i, int f) { return ld_f4(p.vn + sl * 64 * D + (size_t)i * D + fh + f); });
+      load_blk(bdv[hh], 64, tid, [&](int i, int f) { return p.dvn[sl * 64 * D + (size_t)i * D + fh + f]; });
+      load_blk4(bv[hh], L, tid, [&](int i, int f) { return ld_in4<TIn>(p.v, vbase + i * vrow + fh + f); });
     }
   };
-  // key-feature blocks (dw, k) of features f0..f0+63: dw, and k into bk
+  // key-feature blocks (dw, k) of features f0..f0+63: dw (also stored feature-major), and k
+  // by vectors into k4
   Blk bdw[2];
   auto load_key_blocks = [&](int f0) {
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-      const int fh = f0 + 32 * h;
-      load_blk(bdw[h], 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + fh + f]; });
-      load_blk(bk[h], L, tid, [&](int i, int f) { return kin(i, fh + f); });
+    for (int hh = 0; hh < 2; ++hh) {
+      const int fh = f0 + 32 * hh;
+      load_blk(bdw[hh], 64, tid, [&](int i, int f) { return p.dw[sl * 64 * D + (size_t)i * D + fh + f]; });
+      load_blk4(k4[hh], L, tid, [&](int i, int f) { return ld_in4<TIn>(p.k, kbase + i * krow + fh + f); });
     }
   };
   load_value_blocks(0);  // in flight during the inverse
@@ -573,10 +604,10 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       const int f0 = fp * 64;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        store_tm(B0 + 32 * h, bdo[h], tid, kLd);
-        store_tm(B1 + 32 * h, bvn[h], tid, kLd);
+        store_tm4(B0 + 32 * h, bdo[h], tid, kLd);
+        store_tm4(B1 + 32 * h, bvn[h], tid, kLd);
         store_tm(B2 + 32 * h, bdv[h], tid, kLd);
-        store_tm(B3 + 32 * h, bv[h], tid, kLd);
+        store_tm4(B3 + 32 * h, bv[h], tid, kLd);
         store_fm(R0 + 32 * h * kLd, bdv[h], tid);
       }
       __syncthreads();
@@ -625,7 +656,7 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         store_tm(B0 + 32 * h, bdw[h], tid, kLd);
-        store_tm(B1 + 32 * h, bk[h], tid, kLd);
+        store_tm4(B1 + 32 * h, k4[h], tid, kLd);
         store_fm(R0 + 32 * h * kLd, bdw[h], tid);
       }
       __syncthreads();
@@ -693,7 +724,17 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
       }
   }
   __syncthreads();
-  // k and q of the dq / dk stage's first pass: in flight during the row sums and the PG pass
+  // k and q of features f0..f0+63 (two blocks each) for the dq / dk stage, stored
+  // feature-major (scalar element map); the first pass's are in flight during the row sums
+  // and the PG pass
+  Blk bk[2], bq[2];
+  auto load_kq64 = [&](int f0) {
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      load_blk(bk[hh], L, tid, [&](int i, int f) { return kin(i, f0 + 32 * hh + f); });
+      load_blk(bq[hh], L, tid, [&](int i, int f) { return qin(i, f0 + 32 * hh + f); });
+    }
+  };
   load_kq64(0);
   // ---------------- row and column sums: dbeta and dG parts from A and from dP
   {  // eight threads per row i, each over columns j = 8 m + sub, then a fixed shuffle sum
