@@ -764,7 +764,8 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     }
   }
   __syncthreads();
-  // PG = dP * Gamma (lower incl.), Tp = PG^T, GK = dAt + dAt^T with dAt = dA * beta_i Gamma_ij
+  // PG = dP * Gamma (lower incl.) into dP and, transposed, into Tp; GK = dAt + dAt^T with
+  // dAt = dA * beta_i Gamma_ij
   for (int idx = tid; idx < 64 * 64; idx += kThrC) {
     int i, j;
     patch_ij(idx, i, j);
@@ -772,15 +773,11 @@ __global__ void __launch_bounds__(kThrC) bwd_chunk_kernel(BwdParams p) {
     const float gij = j <= i ? ex : 0.f;
     const float gji = i <= j ? ex : 0.f;
     const float pg = dP[i * kLd + j] * gij;
+    dP[i * kLd + j] = pg;  // in place: this pass reads dP at (i, j) only
     Tp[j * kLd + i] = pg;
     GK[i * kLd + j] = Zm[i * kLd + j] * bt[i] * gij + Zm[j * kLd + i] * bt[j] * gji;
   }
-  __syncthreads();
-  for (int idx = tid; idx < 64 * 64; idx += kThrC) {
-    int i, j;
-    patch_ij(idx, i, j);
-    dP[i * kLd + j] = Tp[j * kLd + i];
-  }
+  // (the dq / dk stage's first barrier orders these writes before its products)
   // ---------------- key features again: dq and dk parts of this value head, 64 features a
   // pass; the feature-major k and q tiles take the T and T^T buffers, dead from here on
   {
