@@ -324,9 +324,9 @@ constexpr size_t chunk_floats() {
 // 231,936 B was refused (the per-block total also holds about 4 KB beyond the dynamic size).
 static_assert(chunk_floats() * sizeof(float) <= 219392, "per-chunk kernel shared memory");
 
-// Threads of the per-chunk kernel: 16 warps, each owning a 16 x 16 tile of every 64 x 64
-// result and a 16 x 8 tile of every 64 x 32 one, so that four warps per SM sub-partition
-// cover the latency of the shared-memory operand loads and the MMAs.
+// Threads of the per-chunk kernel: 16 warps, each owning a 16 x 16 tile of every 64-wide
+// result, so that four warps per SM sub-partition cover the latency of the shared-memory
+// operand loads and the MMAs.
 constexpr int kThrC = 512;
 constexpr int kBlkU = 64 * 32 / kThrC;
 
