@@ -84,9 +84,10 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, volat
   return false;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ CUtensorMap tmk,
-                   const __grid_constant__ CUtensorMap tmq, int D) {
+                   const __grid_constant__ CUtensorMap tmq) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
@@ -140,6 +141,11 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
   } else {
     const int g = lane >> 2, c2 = 2 * (lane & 3), i8 = lane >> 3;
     const int mt = warp & 3, np = warp >> 2;  // dv_new tile: token rows 16mt.., columns 16np..
+    // With a head size of 64 the upper key half is zero (the k tile reads the TMA fill there):
+    // K dS contracts over D key rows only, and the warps whose dS rows lie past D (never
+    // stored, never read) skip their products. They still take every barrier.
+    constexpr int nks = D / 16;
+    const bool live = 16 * warp < D;  // always at D = 128
     // dS: key rows 16 warp + g (+8), value columns 8 nt + c2 (+1)
     float dS[4][4];
 #pragma unroll
@@ -240,6 +246,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
         for (int e = 0; e < 4; ++e) x1[q][e] = x2[q][e] = 0.f;
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
+        if (ks >= nks) break;
         uint32_t a[4], bh[4], bl[4];
         const int row = 16 * mt + (lane & 7) + (i8 & 1) * 8;
         const int col = (16 * ks + (i8 >> 1) * 8) & 63;
@@ -281,6 +288,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
       const int arow = 16 * (warp & 3) + (i8 & 1) * 8;  // this warp's key rows in its half
 #pragma unroll
       for (int ks = 0; ks < 4; ++ks) {
+        if (!live) break;
         uint32_t a[4];
         const int t = 16 * ks + (i8 >> 1) * 8 + (lane & 7);
         ldsm_x4_t_addr(a, st_a + sQ + (warp >> 2) * 8192 + sw_chunk(t, arow));
@@ -320,7 +328,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
       named_sync(1, kCompThreads);  // dv_new visible to every warp
 
       // dS <- exp(G_L) dS + scale Q^T (exp(G) dO) - w^T dv_new
-      {
+      if (live) {
         float y2[4][4];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt)
@@ -354,7 +362,7 @@ bwd_scan_tc_kernel(const __grid_constant__ BwdParams p, const __grid_constant__ 
       if (lane == 0) mbar_arrive(&bars[2 + s]);  // this warp is done with the ring slot
       // split of the updated dS for the next chunk (every warp has passed this chunk's
       // K dS, so the buffer is free; the next chunk's first barrier publishes it)
-      if (m + 1 < nch) store_ds_split();
+      if (m + 1 < nch && live) store_ds_split();
     }
     if (p.dh0) {
 #pragma unroll
@@ -381,8 +389,13 @@ bool launch_bwd_scan_tc(const BwdParams& p, int D, cudaStream_t s) {
   // dS stay zero.
   if (!encode_rows_tmap(&tmk, p.k, rows, p.H, D) || !encode_rows_tmap(&tmq, p.q, rows, p.H, D))
     return false;
-  ensure_smem_limit((const void*)bwd_scan_tc_kernel, (int)kSmemBytes);
-  bwd_scan_tc_kernel<<<dim3(p.N, p.Hv, D / BV), kThreads, kSmemBytes, s>>>(p, tmk, tmq, D);
+  if (D == kD) {
+    ensure_smem_limit((const void*)bwd_scan_tc_kernel<kD>, (int)kSmemBytes);
+    bwd_scan_tc_kernel<kD><<<dim3(p.N, p.Hv, D / BV), kThreads, kSmemBytes, s>>>(p, tmk, tmq);
+  } else {
+    ensure_smem_limit((const void*)bwd_scan_tc_kernel<64>, (int)kSmemBytes);
+    bwd_scan_tc_kernel<64><<<dim3(p.N, p.Hv, D / BV), kThreads, kSmemBytes, s>>>(p, tmk, tmq);
+  }
   return cudaPeekAtLastError() == cudaSuccess;
 }
 
