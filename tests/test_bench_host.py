@@ -22,6 +22,26 @@ def test_headline_roofline_arithmetic():
     assert bench.n_chunks(x["lengths"]) == 64
 
 
+def test_backward_roofline_arithmetic():
+    # T = 4096, H = 16, Hv = 32, d = 128, bf16 q/k/v, fp32 upstream and output gradients
+    x = make_inputs(2)
+    # in: q, k (2 x 16 MiB bf16), v (32 MiB), g and beta (1 MiB), the initial state and
+    # d_final (2 MiB each), dO (64 MiB fp32); out: dq, dk (64 MiB), dv (64 MiB), dg and
+    # dbeta (1 MiB), d_initial_state (2 MiB). The in and out parts equal the end-to-end
+    # copies bench.py counts from its tensors (host to device also carries cu_seqlens, 8 B).
+    assert bench.bwd_bytes(x) == 139460608 + 137363456
+    # per (chunk, value head): S and dS (64 KiB each), v_new and dv_new (32 KiB each),
+    # dO (32 KiB) in, three 64 x 128 fp32 results out: 320 KiB, over 64 chunks x 32 heads
+    assert bench.bwd_state_bytes(x) == 2048 * 327680
+    f = bench.bwd_stage_flops(x)
+    # ten 64 x 64 x 128 products, two 64 x 64 x 64 ones and the triangular inverse per
+    # (chunk, value head): 2048 x (10485760 + 1048576 + 87381.33)
+    assert abs(f["chunk_grads"] - 23801277098.67) < 1.0
+    # the reverse scan: three 64 x 128 x 128 products and one 64 x 64 x 128 per step
+    assert f["reverse_scan"] == 2048 * (6 * 64 * 128 * 128 + 2 * 64 * 64 * 128)
+    assert f["state_products"] == 2048 * 6291456
+
+
 def _free_port():
     s = socket.socket()
     s.bind(("127.0.0.1", 0))
