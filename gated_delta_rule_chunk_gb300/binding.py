@@ -23,7 +23,8 @@ GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_BUILD_CHUNK_INDICES = 2
 GDN_FLAG_CHANNEL_GATES = 4
 GDN_NUM_STAGE_EVENTS = 5
-DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table"}
+DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table",
+                   8: "on-chip wait timed out", 16: "non-finite state or output"}
 
 # Every entry point include/gdn.h declares.
 EXPORTED = ("gdn_check_desc", "gdn_nt_max", "gdn_workspace_size", "gdn_build_chunk_indices",

@@ -234,6 +234,8 @@ bool launch_bwd(const BwdParams& p, int D, bool bf16_inputs, bool tc_bridge, cud
 bool launch_bwd_scan_tc(const BwdParams& p, int D, cudaStream_t s);
 bool launch_tc_intra(const Params& p, cudaStream_t s);
 bool launch_tc_inter(const Params& p, bool channel_gates, cudaStream_t s);
+// The scalar-gate scan (k_scan.cu); launch_tc_inter routes scalar gates to it.
+bool launch_scan(const Params& p, cudaStream_t s);
 bool launch_kda_intra(const Params& p, cudaStream_t s);
 bool launch_recurrent(const RecParams& p, cudaStream_t s);
 bool launch_conv_front(const ConvParams& p, cudaStream_t s);

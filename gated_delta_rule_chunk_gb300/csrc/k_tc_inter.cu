@@ -590,7 +590,7 @@ bool launch_tc_inter_t(const Params& p, cudaStream_t s) {
 }  // namespace
 
 bool launch_tc_inter(const Params& p, bool channel_gates, cudaStream_t s) {
-  return channel_gates ? launch_tc_inter_t<true>(p, s) : launch_tc_inter_t<false>(p, s);
+  return channel_gates ? launch_tc_inter_t<true>(p, s) : launch_scan(p, s);
 }
 
 }  // namespace gdn

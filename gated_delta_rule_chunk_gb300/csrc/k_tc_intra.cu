@@ -27,7 +27,9 @@
 //   w: two 64-column halves, each [64 rows][128 B] with the 128-byte swizzle
 //      (16-byte chunk c of row r stored at chunk c ^ (r % 8));
 //   M: [128 rows: hi then lo][128 B], same swizzle;
-//   u: [dv/32 blocks][64 rows][32 fp32], 16-byte chunk c of row r at c ^ (r % 8);
+//   u: [dv/32 blocks][32 columns][64 tokens] fp32 (each block stored column-major, the
+//      scan's chain reads two tokens of one column at a time), 32-byte group c of column j
+//      at c ^ (j % 8);
 //   k (once per key head): fp16, scaled by 1/||k|| when the L2 norm is on, zero past
 //      the sequence end, two 64-column halves of [64 rows][128 B] with the 128-byte swizzle.
 // Each image is assembled in shared memory and written with bulk copies (TMA), so
@@ -71,9 +73,10 @@ static_assert(kX + 16 * LDT * 4 <= kTW, "shared-memory layout overlaps");
 __device__ __forceinline__ uint32_t sw_off(int r, int ch) {
   return (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4);
 }
-// Byte offset of fp32 element (r, j), j < 32, in a [rows][32] tile with 16-byte chunks swizzled.
-__device__ __forceinline__ uint32_t u_offset(int r, int j) {
-  return (uint32_t)r * 128u + ((uint32_t)((j >> 2) ^ (r & 7)) << 4) + (uint32_t)(j & 3) * 4u;
+// Byte offset of fp32 element (column j < 32, token i < 64) in a u block stored column-major,
+// [32 columns][64 tokens], with the 32-byte groups of each column swizzled by the column.
+__device__ __forceinline__ uint32_t u_offset(int j, int i) {
+  return (uint32_t)j * 256u + ((uint32_t)((i >> 3) ^ (j & 7)) << 5) + (uint32_t)(i & 7) * 4u;
 }
 
 __device__ __forceinline__ bool resolve(const Params& p, int slot, int& t0, int& L, int& wslot) {
@@ -430,11 +433,9 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         tmem_ld32(d + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * b, v);
         tmem_ld_wait();
         unsigned char* blk = b ? s1 : s0;
-        if (lane < 16) {
+        if (lane < 16) {  // one column per store: the 16 lanes write 16 tokens of it
 #pragma unroll
-          for (int q = 0; q < 8; ++q)
-            *reinterpret_cast<float4*>(blk + u_offset(i, 4 * q)) =
-                make_float4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+          for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(blk + u_offset(j, i)) = v[j];
         }
       }
       fence_async_smem();

@@ -104,15 +104,6 @@ __device__ inline void tri_inverse_64_inplace(float* AT, int ld, float* X, int t
 
 namespace gdn {
 
-// fp32 pair -> bf16 hi pair and bf16 lo pair (x = hi + lo to about 16 bits).
-__device__ __forceinline__ void split_pack2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
-  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
-  const float2 hf = __bfloat1622float2(h);
-  const __nv_bfloat162 l = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
-  hi = *reinterpret_cast<const uint32_t*>(&h);
-  lo = *reinterpret_cast<const uint32_t*>(&l);
-}
-
 // Split A fragment (16 x 16 at (r0, c0)) of a row-major fp32 tile with stride ld.
 __device__ __forceinline__ void frag_a_split(const float* base, int ld, int r0, int c0, int lane,
                                              uint32_t (&hi)[4], uint32_t (&lo)[4]) {

@@ -22,6 +22,21 @@ def test_headline_roofline_arithmetic():
     assert bench.n_chunks(x["lengths"]) == 64
 
 
+def test_stage_boundary_bytes():
+    # Headline shape: the scan reads q and k (2 x 16 MiB bf16), w and u in bf16 (2 x 32 MiB:
+    # 64 chunks x 32 value heads x 64 x 128 x 2 B each), G (64 x 32 x 64 x 4 B = 0.5 MiB)
+    # and the initial state (2 MiB), and writes out (32 MiB bf16) and the final state
+    # (2 MiB); the intra stage reads q, k, v (32 MiB), g and beta (0.5 MiB each) and writes
+    # w, u and G. 132.5 MiB (138.9 MB) for the scan.
+    x = make_inputs(2)
+    sb = bench.survey_stage_bytes(x)
+    MiB = 1 << 20
+    assert sb["inter"] == 32 * MiB + 64 * MiB + MiB // 2 + 4 * MiB + 32 * MiB
+    assert sb["intra"] == 32 * MiB + 32 * MiB + MiB + 64 * MiB + MiB // 2
+    # the whole call's compulsory bytes are what the two stages exchange with the caller
+    assert bench.algorithmic_bytes(x) == 32 * MiB + 32 * MiB + 32 * MiB + MiB + 4 * MiB
+
+
 def test_backward_roofline_arithmetic():
     # T = 4096, H = 16, Hv = 32, d = 128, bf16 q/k/v, fp32 upstream and output gradients
     x = make_inputs(2)
