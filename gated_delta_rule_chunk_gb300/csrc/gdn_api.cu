@@ -246,6 +246,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.M = ws + L.M;
   p.k16 = L.k16 ? ws + L.k16 : nullptr;
   p.qimg = L.qimg ? ws + L.qimg : nullptr;
+  p.q16 = L.q16 ? ws + L.q16 : nullptr;
   p.qt = L.qt ? reinterpret_cast<float*>(ws + L.qt) : nullptr;
   p.kt = L.kt ? reinterpret_cast<float*>(ws + L.kt) : nullptr;
   p.gam = L.gam ? reinterpret_cast<float*>(ws + L.gam) : nullptr;
@@ -333,6 +334,7 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.w = ws + L.w; p.u = f32(L.u); p.M = ws + L.M;
   p.G = L.G ? f32(L.G) : nullptr;
   p.k16 = L.k16 ? ws + L.k16 : nullptr;
+  p.q16 = L.q16 ? ws + L.q16 : nullptr;
   p.qt = L.qt ? f32(L.qt) : nullptr;
   p.kt = L.kt ? f32(L.kt) : nullptr;
   p.gam = L.gam ? f32(L.gam) : nullptr;

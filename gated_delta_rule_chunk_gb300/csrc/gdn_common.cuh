@@ -40,6 +40,8 @@ struct Params {
                              // per-channel gates (the decay exp(G_L - G) applied)
   void* qimg;                // [nt_max, Hv] bf16 hi/lo images of exp(G) q (tensor-core path,
                              // per-channel gates)
+  void* q16;                 // [nt_max, H] fp16 images of the chunk's q tile, 1/||q|| applied
+                             // (tensor-core path, scalar gates)
   float* qt;                 // [nt_max, Hv, dk, 64] (exp(G) q)^T        (SIMT path)
   float* kt;                 // [nt_max, Hv, 64, dk] exp(G_L - G) k      (SIMT path)
   float* gam;                // [nt_max, Hv, dk] exp(G_L)                (SIMT path)
@@ -133,8 +135,8 @@ struct ConvParams {
 
 // Byte offsets of the workspace regions (each 256-byte aligned).
 struct WsLayout {
-  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qimg, qt, kt, gam, qrn,
-      krn, total;
+  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qimg, q16, qt, kt, gam,
+      qrn, krn, total;
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -161,6 +163,7 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
   const bool tc_ch = tc_path && channel_gates;  // per value head k images, q images, exp(G_L)
   L.k16 = tc_path ? take((size_t)nt_max * (tc_ch ? Hv : H) * kChunk * kDk * 2) : 0;
   L.qimg = tc_ch ? take(slots * 2 * kChunk * kDk * 2) : 0;
+  L.q16 = (tc_path && !channel_gates) ? take((size_t)nt_max * H * kChunk * kDk * 2) : 0;
   L.qt = tc_path ? 0 : take(sizeof(float) * slots * kChunk * D);
   L.kt = tc_path ? 0 : take(sizeof(float) * slots * kChunk * D);
   L.gam = tc_path ? (tc_ch ? take(sizeof(float) * slots * kDk) : 0)

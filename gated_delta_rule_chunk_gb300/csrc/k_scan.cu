@@ -15,23 +15,24 @@
 //   output (lags the chain by one chunk):
 //                     o = scale (diag(exp(G) / ||q||) Q S + M v_new)
 //
-// Warp roles (5 warps; warp w runs on SM sub-partition w % 4):
+// Warp roles (8 warps; warp w runs on SM sub-partition w % 4):
 //   * warps 0, 1 (chain): warp r owns the 16 value columns 16r..16r+15 of the block with
 //     all 128 key rows, as fp32 MMA accumulators of S^T. Because S^T sits in the
 //     accumulator layout of m16n8 tiles, pairs of its n-tiles are directly the A
 //     fragments of the next product (as are those of X^T), so the chain never moves the
 //     state through shared memory: two dependent warp-MMA groups per chunk (64 m16n8k16
 //     each), with w (bf16) and the fp16 k image as the shared-memory operands.
-//   * warps 2, 3 (output): each takes two 16-token row tiles of the chunk (tiles {0, 3}
-//     and {1, 2}, which balances the triangular M product) for all 32 columns:
-//     Q S with fp16 operands (q converted from bf16 in registers, the chain's fp16 copy
-//     of S) and M v_new as three bf16 products of hi/lo pairs (hi*hi + hi*lo + lo*hi).
+//   * warps 2, 3, 6, 7 (output): each takes one 16-token row tile of the chunk for all 32
+//     columns (warps 2 and 6, which share a sub-partition, tiles 0 and 3; warps 3 and 7
+//     tiles 1 and 2, which balances the triangular M product between the two):
+//     Q S with fp16 operands (the intra kernel's fp16 q image, the chain's fp16 copy of
+//     S) and M v_new as three bf16 products of hi/lo pairs (hi*hi + hi*lo + lo*hi).
 //     They run on the two sub-partitions the chain leaves free, so the two roles do not
 //     share a tensor unit (no tcgen05 anywhere in this kernel).
 //   * warp 4 (loads): one thread issues every copy: a 3-slot ring of what the chain
 //     reads (w, k, the u block, G; bulk copies of images the intra kernel wrote in this
-//     kernel's layout) and a double buffer of what the output warps read (the q tile by
-//     tensor map with the 128-byte swizzle, and the [M_hi; M_lo] image).
+//     kernel's layout) and a double buffer of what the output warps read (the fp16 q
+//     image and the [M_hi; M_lo] image).
 // The chain hands each chunk's fp16 S and bf16 hi/lo v_new to the output warps through a
 // double-buffered shared tile (stmatrix). Precision (CPU emulation against the fp64
 // oracle at the headline distributions): w S with bf16 operands, the state update with
@@ -122,11 +123,6 @@ __device__ __forceinline__ void stsm_x4(uint32_t saddr, uint32_t r0, uint32_t r1
                : "memory");
 }
 
-// bf16 pair -> fp16 pair (round to nearest even).
-__device__ __forceinline__ uint32_t bf2_to_h2(uint32_t x) {
-  return pack_f16(__uint_as_float(x << 16), __uint_as_float(x & 0xffff0000u));
-}
-
 // Bounded wait for the phase of `bar` with parity `parity`. Gives up after a bounded
 // number of polls (raising the abort flag), and at once when the flag is already raised.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
@@ -153,7 +149,7 @@ __device__ __forceinline__ bool wait_bar_sleep(uint64_t* bar, uint32_t parity,
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMap tmq) {
+scan_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   unsigned char* sm = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const uint32_t sbase = smem_addr(sm);
@@ -241,6 +237,13 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
           }
       }
 
+      // this thread's u values, loaded before the X product so their latency hides
+      float2 uu[8][2];
+#pragma unroll
+      for (int nt = 0; nt < 8; ++nt)
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh)
+          uu[nt][hh] = *reinterpret_cast<const float2*>(st + rU + u_blk(rb + g + 8 * hh, 8 * nt + c2));
       // X^T = S^T w^T: columns 16r.., tokens 0..63 (8 n-tiles), keys in 8 steps of 16
       float X[8][4];
 #pragma unroll
@@ -271,8 +274,7 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
       for (int nt = 0; nt < 8; ++nt)
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-          const float2 u2 =
-              *reinterpret_cast<const float2*>(st + rU + u_blk(rb + g + 8 * hh, 8 * nt + c2));
+          const float2 u2 = uu[nt][hh];
           X[nt][2 * hh] = u2.x - X[nt][2 * hh];
           X[nt][2 * hh + 1] = u2.y - X[nt][2 * hh + 1];
         }
@@ -369,36 +371,16 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
     const int mts[kMT] = {ow < 2 ? ow : 5 - ow};
     float chk = 0.f;  // stays 0 unless an output is non-finite (x * 0 is NaN for inf, NaN)
     const uint32_t ost = sbase + kOST + ow * kOSTsz;
-    // 1/||q|| of this thread's rows, loaded one chunk ahead (1 without the L2 norm)
-    float qrn_next[kMT][2];
-    auto load_qrn = [&](int cc) {
-#pragma unroll
-      for (int mi = 0; mi < kMT; ++mi)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          const int i = 16 * mts[mi] + g + 8 * hh;
-          qrn_next[mi][hh] = (p.qrn && cc < nch && i < sv.len - kChunk * cc)
-                                 ? p.qrn[(size_t)(sv.start + kChunk * cc + i) * p.H + h]
-                                 : 1.f;
-        }
-    };
-    load_qrn(0);
     // (no output wanted: the backward's recompute keeps only states and v_new, and the
     // chain then makes no hand-off)
     for (int c = 0; has_out && c < nch; ++c) {
       const int b = c & 1;
       const int t0 = sv.start + kChunk * c;
       const int L = min(kChunk, sv.len - kChunk * c);
-      float qr[kMT][2];
-#pragma unroll
-      for (int mi = 0; mi < kMT; ++mi)
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) qr[mi][hh] = qrn_next[mi][hh];
-      load_qrn(c + 1);
       wait_bar(&bars[B_QF + b], (uint32_t)((c >> 1) & 1), abort_flag);
       wait_bar(&bars[B_SF + b], (uint32_t)((c >> 1) & 1), abort_flag);
       const uint32_t qa = sbase + kQM + b * kQMsz, sva = sbase + kSV + b * kSVsz;
-      // row factors scale exp(G_i) / ||q_i|| of this thread's rows
+      // row factors scale exp(G_i) of this thread's rows (1/||q_i|| is inside the q image)
       float f[kMT][2];
       {
         const float* Gs = reinterpret_cast<const float*>(sm + kSV + b * kSVsz + vG);
@@ -406,7 +388,7 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
         for (int mi = 0; mi < kMT; ++mi)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
-            f[mi][hh] = p.scale * __expf(Gs[16 * mts[mi] + g + 8 * hh]) * qr[mi][hh];
+            f[mi][hh] = p.scale * __expf(Gs[16 * mts[mi] + g + 8 * hh]);
       }
       const int m = lane >> 3;
       const int arow = (lane & 7) + (m & 1) * 8;   // A fragment row inside a 16-row tile
@@ -421,7 +403,7 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
             qs[mi][nt][e] = 0.f;
             mv[mi][nt][e] = 0.f;
           }
-      // Q S (fp16): A = q rows (converted from bf16), B = the chain's fp16 S^T rows. The
+      // Q S (fp16): A = the fp16 q image's rows, B = the chain's fp16 S^T rows. The
       // output warps' loops stay compact: run once per chunk, unrolled code does not stay
       // in the instruction cache.
 #pragma unroll 2
@@ -434,8 +416,6 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
         for (int mi = 0; mi < kMT; ++mi) {
           uint32_t a[4];
           ldsm_x4_addr(a, qa + qQ + half_img(16 * mts[mi] + arow, 2 * ks + (m >> 1)));
-#pragma unroll
-          for (int e = 0; e < 4; ++e) a[e] = bf2_to_h2(a[e]);
           mma_f16(qs[mi][0], a, bs[0][0], bs[0][1]);
           mma_f16(qs[mi][1], a, bs[0][2], bs[0][3]);
           mma_f16(qs[mi][2], a, bs[1][0], bs[1][1]);
@@ -542,8 +522,8 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
       uint64_t* full = &bars[B_QF + (cc & 1)];
       const size_t sl = ((size_t)sv.first_slot + cc) * p.Hv + hv;
       mbar_expect_tx(full, kQMsz);
-      tma_load_3d(dst + qQ, &tmq, 0, h, sv.start + kChunk * cc, full);
-      tma_load_3d(dst + qQ + 8192, &tmq, 64, h, sv.start + kChunk * cc, full);
+      bulk_load(dst + qQ, static_cast<const unsigned char*>(p.q16) +
+                              (((size_t)sv.first_slot + cc) * p.H + h) * 16384, 16384, full);
       bulk_load(dst + qM, static_cast<const unsigned char*>(p.M) + sl * 16384, 16384, full);
     };
     int issued = 0, qm_issued = 0;
@@ -581,12 +561,9 @@ scan_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtensorMa
 }  // namespace
 
 bool launch_scan(const Params& p, cudaStream_t s) {
-  CUtensorMap tmq;
-  const int rows = p.T > 0 ? p.T : 1;  // with T = 0 no tile is ever loaded
-  if (!encode_rows_tmap(&tmq, p.q, rows, p.H, p.D)) return false;
   ensure_smem_limit((const void*)scan_kernel, (int)kSmemBytes);
-  return launch_pdl(scan_kernel, dim3(p.N, p.Hv, p.D / BV), dim3(kThreads), kSmemBytes, s, p,
-                    tmq) == cudaSuccess;
+  return launch_pdl(scan_kernel, dim3(p.N, p.Hv, p.D / BV), dim3(kThreads), kSmemBytes, s,
+                    p) == cudaSuccess;
 }
 
 }  // namespace gdn

@@ -30,8 +30,9 @@
 //   u: [dv/32 blocks][32 columns][64 tokens] fp32 (each block stored column-major, the
 //      scan's chain reads two tokens of one column at a time), 32-byte group c of column j
 //      at c ^ (j % 8);
-//   k (once per key head): fp16, scaled by 1/||k|| when the L2 norm is on, zero past
-//      the sequence end, two 64-column halves of [64 rows][128 B] with the 128-byte swizzle.
+//   k and q (once per key head): fp16, scaled by 1/||k|| and 1/||q|| when the L2 norm is
+//      on, zero past the sequence end, two 64-column halves of [64 rows][128 B] with the
+//      128-byte swizzle.
 // Each image is assembled in shared memory and written with bulk copies (TMA), so
 // the warps never wait on scattered global stores; tiles come in by TMA tensor maps
 // (128-byte swizzle), which are also the tensor-core operand layouts.
@@ -137,6 +138,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   float* Bt = G + 64;   // beta
   float* KR = G + 128;  // 1/||k|| (1 when the norm is off)
   float* FW = G + 192;  // beta exp(G) / ||k||: column factor of the w operand
+  float* QR = G + 256;  // 1/||q|| (1 when the norm is off)
   // mbarriers: 0 k/q landed, 1-2 v buffers landed, 3 [P; R] done, 4 w done, 5 and 6 the
   // two column halves of u done (one completion per value head for 4-6)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
@@ -167,6 +169,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     for (int r = 0; r < min(p.HG, 2); ++r) issue_v(sm, bars, &tmv, h * p.HG + r, t0, r);
   }
   if (tid < 64) KR[tid] = (tid < L && p.krn) ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
+  else if (tid < 128)
+    QR[tid - 64] = (tid - 64 < L && p.qrn) ? p.qrn[(size_t)(t0 + tid - 64) * p.H + h] : 1.f;
   // 1/||q|| of the row this thread forms M for (warps 2, 3, 6 and 7 own rows 0..63 of R)
   const int qrow = 32 * (warp & 1) + lane;
   const float qr = ((warp & 3) >= 2 && p.qrn && qrow < L) ? p.qrn[(size_t)(t0 + qrow) * p.H + h] : 1.f;
@@ -235,19 +239,20 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     umma_commit(&bars[3]);
   }
 
-  {  // fp16 image of the (normalised) k tile, assembled in the A/T region
-    const unsigned char* kt = sm + kKQ;
-    unsigned char* img = sm + kAT;
+  // fp16 images of the (normalised) k and q tiles, assembled in turn in the A/T region,
+  // each two halves of [64 rows][128 B] with the 128-byte swizzle; the scan reads them
+  // with one bulk copy each.
+  auto f16_image = [&](const unsigned char* src, unsigned char* img, const float* rowf) {
 #pragma unroll
     for (int it = 0; it < 1024 / kThreads; ++it) {
       const int idx = tid + it * kThreads;  // 1024 chunks of 8 elements
       const int half = idx >> 9, t = (idx >> 3) & 63, ch = idx & 7;
       const uint32_t off = (uint32_t)half * 16384u + sw_off(t, ch);
-      const uint4 raw = *reinterpret_cast<const uint4*>(kt + off);
+      const uint4 raw = *reinterpret_cast<const uint4*>(src + off);
       const uint32_t* rw = reinterpret_cast<const uint32_t*>(&raw);
       uint4 v;
       uint32_t* o = reinterpret_cast<uint32_t*>(&v);
-      const float sc = KR[t];
+      const float sc = rowf[t];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&rw[e]));
@@ -255,13 +260,26 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       }
       *reinterpret_cast<uint4*>(img + (uint32_t)half * 8192u + sw_off(t, ch)) = v;
     }
-  }
+  };
+  f16_image(sm + kKQ, sm + kAT, KR);
   fence_async_smem();
   __syncthreads();
   if (tid == 0) {
     bulk_store(static_cast<unsigned char*>(p.k16) + ((size_t)wslot * p.H + h) * 64 * kDk * 2,
                sm + kAT, 16384);
     bulk_commit();
+    if (p.q16) bulk_wait_read<0>();  // the staging region is reused for q
+  }
+  if (p.q16) {
+    __syncthreads();
+    f16_image(sm + kKQ + 8192, sm + kAT, QR);
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      bulk_store(static_cast<unsigned char*>(p.q16) + ((size_t)wslot * p.H + h) * 64 * kDk * 2,
+                 sm + kAT, 16384);
+      bulk_commit();
+    }
   }
 
   for (int r = 0; r < p.HG; ++r) {
