@@ -22,6 +22,7 @@ GDN_F32, GDN_BF16 = 0, 1
 GDN_FLAG_QK_L2NORM = 1
 GDN_FLAG_BUILD_CHUNK_INDICES = 2
 GDN_FLAG_CHANNEL_GATES = 4
+GDN_FLAG_WORKSPACE_GUARDS = 8
 GDN_NUM_STAGE_EVENTS = 5
 DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table",
                    8: "on-chip wait timed out", 16: "non-finite state or output"}
@@ -29,6 +30,7 @@ DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table
 # Every entry point include/gdn.h declares.
 EXPORTED = ("gdn_check_desc", "gdn_nt_max", "gdn_workspace_size", "gdn_build_chunk_indices",
             "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string", "gdn_chunk_fwd_noalloc",
+            "gdn_noalloc_read_status", "gdn_test_scan_timeout", "gdn_workspace_regions",
             "gdn_recurrent_fwd", "gdn_conv_front", "gdn_bwd_workspace_size", "gdn_chunk_bwd")
 GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -77,6 +79,12 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_chunk_fwd.restype = ctypes.c_int
         lib.gdn_chunk_fwd_noalloc.argtypes = lib.gdn_chunk_fwd.argtypes
         lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
+        lib.gdn_noalloc_read_status.argtypes = [vp, vp]
+        lib.gdn_noalloc_read_status.restype = ctypes.c_int
+        lib.gdn_test_scan_timeout.argtypes = [ctypes.c_uint32]
+        lib.gdn_test_scan_timeout.restype = None
+        lib.gdn_workspace_regions.argtypes = [P(GdnDesc), vp, vp, ctypes.c_int]
+        lib.gdn_workspace_regions.restype = ctypes.c_int
         lib.gdn_recurrent_fwd.argtypes = [P(GdnDesc), vp, vp, vp, vp, vp, ctypes.c_float, vp,
                                           vp, vp, vp, vp]
         lib.gdn_recurrent_fwd.restype = ctypes.c_int
@@ -177,7 +185,7 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
                   build_chunk_indices: bool = False, nt_max: int = 0,
                   out: Optional[torch.Tensor] = None, final_state: Optional[torch.Tensor] = None,
                   workspace: Optional[torch.Tensor] = None, stream=None,
-                  stage_events=None, return_desc: bool = False):
+                  stage_events=None, return_desc: bool = False, extra_flags: int = 0):
     """Chunked gated-delta-rule forward through the C ABI.
 
     q, k [T, H, d]; v [T, Hv, d] with d = 128 or 64 (fp32 or bf16, CUDA,
@@ -191,7 +199,7 @@ def gdn_chunk_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: torch.Te
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
     flags = (GDN_FLAG_QK_L2NORM if use_qk_l2norm else 0) | (
         GDN_FLAG_BUILD_CHUNK_INDICES if build_chunk_indices else 0) | (
-        GDN_FLAG_CHANNEL_GATES if g.dim() == 3 else 0)
+        GDN_FLAG_CHANNEL_GATES if g.dim() == 3 else 0) | extra_flags
     out_dtype = out_dtype or (out.dtype if out is not None else q.dtype)
     desc = make_desc(T, N, H, Hv, q.dtype, out_dtype, nt_max=nt_max, flags=flags,
                      l2norm_eps=l2norm_eps, dk=dk, dv=dv)
@@ -406,3 +414,30 @@ def gdn_chunk_fwd_noalloc(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, g: 
     if rc != 0:
         raise GdnError(rc, "gdn_chunk_fwd_noalloc")
     return out, final_state
+
+
+def gdn_noalloc_read_status(stream=None) -> int:
+    """Device status word of the last gdn_chunk_fwd_noalloc call on the current device
+    (it lives in the library's static scratch; synchronizes the stream)."""
+    host = torch.zeros(1, dtype=torch.int32).pin_memory()
+    rc = load_library().gdn_noalloc_read_status(_ptr(host), _stream_handle(stream))
+    if rc != 0:
+        raise GdnError(rc, "gdn_noalloc_read_status")
+    (torch.cuda.current_stream() if stream is None else stream).synchronize()
+    return int(host.item())
+
+
+def gdn_test_scan_timeout(polls: int) -> None:
+    """Testing hook: with polls > 0 the bf16 scan waits that many polls on an event that
+    never happens and takes its timeout path (GDN_DEV_TIMEOUT); 0 turns it off."""
+    load_library().gdn_test_scan_timeout(int(polls))
+
+
+def gdn_workspace_regions(desc: GdnDesc):
+    """[(begin, end)] byte ranges of the workspace regions for this descriptor."""
+    b = (ctypes.c_size_t * 16)()
+    e = (ctypes.c_size_t * 16)()
+    n = load_library().gdn_workspace_regions(ctypes.byref(desc), b, e, 16)
+    if n < 0:
+        raise GdnError(n, "gdn_workspace_regions")
+    return [(int(b[i]), int(e[i])) for i in range(n)]

@@ -5,6 +5,7 @@
 
 #include <cuda.h>
 
+#include <atomic>
 #include <map>
 #include <mutex>
 #include <utility>
@@ -14,6 +15,12 @@
 using namespace gdn;
 
 namespace gdn {
+
+namespace {
+std::atomic<uint32_t> g_scan_stall_polls{0};
+}  // namespace
+
+uint32_t scan_stall_polls() { return g_scan_stall_polls.load(std::memory_order_relaxed); }
 
 void ensure_smem_limit(const void* kernel, int bytes) {
   // largest limit set so far per (kernel, device); raised when a call needs more
@@ -107,8 +114,8 @@ int check_desc_impl(const gdn_desc* d) {
   const bool dt_ok = (d->qkv_dtype == GDN_F32 || d->qkv_dtype == GDN_BF16) &&
                      (d->out_dtype == GDN_F32 || d->out_dtype == GDN_BF16);
   if (!dt_ok) return GDN_ERR_UNSUPPORTED;
-  if (d->flags &
-      ~(uint32_t)(GDN_FLAG_QK_L2NORM | GDN_FLAG_BUILD_CHUNK_INDICES | GDN_FLAG_CHANNEL_GATES))
+  if (d->flags & ~(uint32_t)(GDN_FLAG_QK_L2NORM | GDN_FLAG_BUILD_CHUNK_INDICES |
+                             GDN_FLAG_CHANNEL_GATES | GDN_FLAG_WORKSPACE_GUARDS))
     return GDN_ERR_UNSUPPORTED;
   // Index arithmetic stays within 64-bit sizes and 32-bit grid limits.
   if ((int64_t)d->T * d->Hv * kDv >= ((int64_t)1 << 40)) return GDN_ERR_BAD_SHAPE;
@@ -130,9 +137,15 @@ bool uses_tc_path(const gdn_desc* d) { return d->qkv_dtype == GDN_BF16; }
 // The token-serial and front-end kernels are built for dk = dv = 128 and scalar gates.
 bool serial_shape_ok(const gdn_desc* d) { return d->dk == kDk && !channel_gates(d); }
 
+// Guard gap after every workspace region with GDN_FLAG_WORKSPACE_GUARDS.
+constexpr size_t kGuardBytes = 4096;
+size_t guard_of(const gdn_desc* d) {
+  return (d->flags & GDN_FLAG_WORKSPACE_GUARDS) ? kGuardBytes : 0;
+}
+
 WsLayout layout_of(const gdn_desc* d) {
   return ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d),
-                   (d->flags & GDN_FLAG_QK_L2NORM) != 0, d->dk, channel_gates(d));
+                   (d->flags & GDN_FLAG_QK_L2NORM) != 0, d->dk, channel_gates(d), guard_of(d));
 }
 
 // Workspace of the backward pass: the forward's layout (the tensor-core path's for bf16
@@ -146,9 +159,14 @@ struct BwdLayout {
 
 BwdLayout bwd_layout_of(const gdn_desc* d) {
   BwdLayout B{};
-  B.fwd = ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d), false, d->dk);
+  B.fwd = ws_layout(d->T, d->N, d->H, d->Hv, nt_max_of(d), uses_tc_path(d), false, d->dk,
+                    false, guard_of(d));
   size_t o = B.fwd.total;
-  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  auto take = [&](size_t bytes) {
+    size_t at = o;
+    o = align_up(o + bytes, 256) + guard_of(d);
+    return at;
+  };
   const size_t slots = (size_t)nt_max_of(d) * d->Hv, D = (size_t)d->dk;
   const size_t mat = sizeof(float) * slots * kChunk * D, st = sizeof(float) * slots * D * D;
   B.hs = take(st);
@@ -253,6 +271,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.qrn = l2 ? reinterpret_cast<float*>(ws + L.qrn) : nullptr;
   p.krn = l2 ? reinterpret_cast<float*>(ws + L.krn) : nullptr;
   p.out_bf16 = d.out_dtype == GDN_BF16;
+  p.stall_polls = scan_stall_polls();
 
   cudaEvent_t* ev = d.stage_events;
   if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
@@ -339,6 +358,7 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.kt = L.kt ? f32(L.kt) : nullptr;
   p.gam = L.gam ? f32(L.gam) : nullptr;
   p.hs = f32(B.hs); p.vn_out = f32(B.vn);
+  p.stall_polls = scan_stall_polls();
   cudaEvent_t* ev = d.stage_events;
   if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
     return GDN_ERR_LAUNCH_FAILED;
@@ -441,6 +461,18 @@ int gdn_conv_front(const gdn_desc* desc, const void* x, const float* conv_w, int
   return cudaPeekAtLastError() == cudaSuccess ? GDN_OK : GDN_ERR_LAUNCH_FAILED;
 }
 
+int gdn_workspace_regions(const gdn_desc* desc, size_t* begin, size_t* end, int max_regions) {
+  const int rc = check_desc_impl(desc);
+  if (rc != GDN_OK) return rc;
+  if (max_regions < 0 || (max_regions > 0 && (!begin || !end))) return GDN_ERR_NULL_ARG;
+  const WsLayout L = layout_of(desc);
+  for (int i = 0; i < L.nreg && i < max_regions; ++i) {
+    begin[i] = L.rbeg[i];
+    end[i] = L.rend[i];
+  }
+  return L.nreg;
+}
+
 int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t stream) {
   int rc = check_desc_impl(desc);
   if (rc != GDN_OK) return rc;
@@ -451,6 +483,10 @@ int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t str
                       stream) != cudaSuccess)
     return GDN_ERR_LAUNCH_FAILED;
   return GDN_OK;
+}
+
+void gdn_test_scan_timeout(uint32_t polls) {
+  g_scan_stall_polls.store(polls, std::memory_order_relaxed);
 }
 
 const char* gdn_status_string(int status) {

@@ -50,6 +50,8 @@ struct Params {
   const float* qrn;          // [T, H] 1/||q|| or null
   const float* krn;          // [T, H] 1/||k|| or null
   int out_bf16;
+  uint32_t stall_polls;      // testing hook: > 0 makes the scan wait this many polls on an
+                             // event that never happens (its timeout path); 0 normally
 };
 
 // Parameters of the backward kernels (device pointers; fp32 SIMT arithmetic). Per-slot
@@ -133,10 +135,14 @@ struct ConvParams {
   int bf16, l2norm;
 };
 
-// Byte offsets of the workspace regions (each 256-byte aligned).
+// Byte offsets of the workspace regions (each 256-byte aligned), and the extent
+// [begin, end) of every region in order (for the guard-band check of the tests).
 struct WsLayout {
   size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qimg, q16, qt, kt, gam,
       qrn, krn, total;
+  static constexpr int kMaxRegions = 16;
+  int nreg;
+  size_t rbeg[kMaxRegions], rend[kMaxRegions];
 };
 
 __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -145,11 +151,21 @@ __host__ __device__ inline size_t align_up(size_t x, size_t a) { return (x + a -
 // a hi/lo bf16 pair and the in-chunk gate sums G, always at head size 128 (a head of
 // 64 runs zero-padded to 128: the tensor maps fill the missing half with zeros); the
 // fp32 SIMT path stores w^T, u, M^T and the decayed q / k images and exp(G_L) in fp32.
+// `guard` bytes are left free after every region (GDN_FLAG_WORKSPACE_GUARDS).
 inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path, bool l2norm,
-                          int D = kDk, bool channel_gates = false) {
+                          int D = kDk, bool channel_gates = false, size_t guard = 0) {
   WsLayout L{};
   size_t o = 0;
-  auto take = [&](size_t bytes) { size_t at = o; o = align_up(o + bytes, 256); return at; };
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    if (L.nreg < WsLayout::kMaxRegions) {
+      L.rbeg[L.nreg] = at;
+      L.rend[L.nreg] = at + bytes;
+      ++L.nreg;
+    }
+    o = align_up(o + bytes, 256) + guard;
+    return at;
+  };
   L.status = take(64);
   L.seq_info = take(sizeof(int2) * (size_t)N);
   L.chunk_offsets = take(sizeof(int32_t) * (size_t)(N + 1));
@@ -200,6 +216,10 @@ __device__ __forceinline__ SeqView seq_view(const P& p, int n) {
   int2 si = p.seq_info[n];
   return SeqView{si.x, si.y, p.chunk_offsets[n]};
 }
+
+// Testing hook (gdn_test_scan_timeout): polls of the scan's never-completing wait for the
+// next launches, 0 normally.
+uint32_t scan_stall_polls();
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
 // that later calls (for example under CUDA-graph capture) make no attribute call.

@@ -14,36 +14,26 @@
 // library, held until the process exits. All calls share it: two calls that
 // may run at the same time on the GPU (different streams, or different host
 // threads) race on it and must be serialized by the caller. Nothing in it
-// needs to start at zero except the status word, which every call clears.
-#include <mutex>
-
+// needs to start at zero except the status word, which every call clears; the
+// status word of the last call stays readable with gdn_noalloc_read_status.
 #include "gdn_common.cuh"
 
 namespace {
 
 constexpr size_t kScratchBytes = (size_t)GDN_NOALLOC_SCRATCH_BYTES;
-constexpr int kMaxDevices = 64;
 
 // Device storage of the scratch. In host code this name is only a stand-in
 // for the symbol: its device address comes from cudaGetSymbolAddress below.
 __device__ __align__(256) unsigned char gdn_noalloc_scratch[kScratchBytes];
 
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device, looked up once per
-// device (with that device current). Returns nullptr on failure.
+// Device address of the scratch on the current device, looked up on every call with
+// that device current (no allocation; after the first lookup on a device, which may
+// load the library's device code, it is a table lookup). Not cached, so that a device
+// reset, which reloads the module, never leaves a stale address. nullptr on failure.
 void* scratch_address() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, gdn_noalloc_scratch) != cudaSuccess || p == nullptr)
-      return nullptr;
-    g_scratch_addr[dev] = p;
-  }
-  return g_scratch_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, gdn_noalloc_scratch) != cudaSuccess) return nullptr;
+  return p;
 }
 
 }  // namespace
@@ -63,4 +53,16 @@ extern "C" int gdn_chunk_fwd_noalloc(const gdn_desc* desc, const void* q, const 
   d.workspace_bytes = kScratchBytes;
   return gdn_chunk_fwd(&d, q, k, v, g, beta, scale, initial_state, cu_seqlens, chunk_indices,
                        out, final_state, stream);
+}
+
+extern "C" int gdn_noalloc_read_status(int32_t* host_status, cudaStream_t stream) {
+  if (!host_status) return GDN_ERR_NULL_ARG;
+  const char* base = static_cast<const char*>(scratch_address());
+  if (!base) return GDN_ERR_LAUNCH_FAILED;
+  // the status word sits at the same offset in every workspace layout
+  const size_t off = gdn::ws_layout(0, 1, 1, 1, 0, true, false).status;
+  if (cudaMemcpyAsync(host_status, base + off, sizeof(int32_t), cudaMemcpyDeviceToHost,
+                      stream) != cudaSuccess)
+    return GDN_ERR_LAUNCH_FAILED;
+  return GDN_OK;
 }

@@ -6,9 +6,11 @@
 // searchsorted over the per-sequence chunk counts, with a sentinel in unused
 // slots, so no host synchronization is needed.
 //
-// One CTA of 1024 threads: (1) sanitize each sequence's [start, end) to
-// [0, T] and count its chunks, (2) exclusive-scan the counts into
-// chunk_offsets, (3) for every slot binary-search the sequence that owns it.
+// One CTA of 1024 threads: (1) sanitize the boundaries: each cu_seqlens entry is
+// clamped to [0, T] and raised to the largest entry before it (a prefix maximum), so
+// sequence n is [max(c_0..c_n), max(c_0..c_n+1)) -- never overlapping another, empty
+// where the input decreases -- and count its chunks, (2) exclusive-scan the counts
+// into chunk_offsets, (3) for every slot binary-search the sequence that owns it.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -18,25 +20,51 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
                    int2* __restrict__ table, int32_t* __restrict__ offsets,
                    int2* __restrict__ seq_info, int32_t* status) {
   __shared__ int warp_incl[32];
-  __shared__ int carry_s;
+  __shared__ int warp_max[32];
+  __shared__ int carry_s, carry_max_s;
   pdl_release();  // the intra kernel may be scheduled now; it waits for this grid's writes
   const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-  if (tid == 0) carry_s = 0;
+  if (tid == 0) {
+    carry_s = 0;
+    carry_max_s = 0;
+  }
   __syncthreads();
   int bad = 0;
   for (int base = 0; base < N; base += 1024) {
     const int n = base + tid;
+    // clamped boundaries, then the inclusive prefix maximum of the starts
+    const int a = (n < N && cu) ? cu[n] : 0;
+    const int b = n < N ? (cu ? cu[n + 1] : T) : 0;
+    int pm = min(max(a, 0), T);
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, pm, o);
+      if (lane >= o) pm = max(pm, y);
+    }
+    if (lane == 31) warp_max[wid] = pm;
+    __syncthreads();
+    if (wid == 0) {
+      int wm = warp_max[lane];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, wm, o);
+        if (lane >= o) wm = max(wm, y);
+      }
+      warp_max[lane] = wm;
+    }
+    __syncthreads();
+    pm = max(max(pm, carry_max_s), wid ? warp_max[wid - 1] : 0);
     int cnt = 0;
     if (n < N) {
-      const int a = cu ? cu[n] : 0;
-      const int b = cu ? cu[n + 1] : T;
-      const int s = min(max(a, 0), T);
-      const int e = min(max(b, s), T);
+      const int s = pm;                          // max(c_0 .. c_n)
+      const int e = max(min(max(b, 0), T), s);   // max(c_0 .. c_n+1)
       bad |= (a != s) | (b != e);
       const int len = e - s;
       cnt = (len + kChunk - 1) / kChunk;
       if (seq_info) seq_info[n] = make_int2(s, len);
     }
+    __syncthreads();
+    if (tid == 1023) carry_max_s = pm;
     int x = cnt;  // inclusive warp scan
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {

@@ -41,7 +41,9 @@
 // M or v_new alone would cost ~3e-3 each.
 //
 // Hand-offs use mbarriers; every wait is bounded (GDN_DEV_TIMEOUT on expiry, after which
-// every role runs through without waiting). A non-finite state or output (an fp16
+// every role runs through without waiting; the load thread still waits, at the full
+// bound, for each copy it issued before the CTA retires). A testing hook makes the chain
+// wait on an event that never happens, to exercise that path. A non-finite state or output (an fp16
 // operand out of range, or non-finite inputs) sets GDN_DEV_NONFINITE.
 #include <cuda.h>
 
@@ -100,7 +102,8 @@ constexpr int B_QF = 6;     // q and M of chunk c landed
 constexpr int B_QE = 8;     // every output warp done with q and M of chunk c
 constexpr int B_SF = 10;    // both chain warps wrote S and v_new of chunk c
 constexpr int B_SE = 12;    // every output warp done with the hand-off buffer of chunk c
-constexpr int kNumBars = 14;
+constexpr int B_STALL = 14; // never completes (the testing hook's wait)
+constexpr int kNumBars = 15;
 
 // Byte offset of the 16-byte chunk holding column-chunk ch of row r in a tile of
 // `rowb`-byte rows whose chunks are swizzled by row (c ^ (r % 8)).
@@ -126,8 +129,8 @@ __device__ __forceinline__ void stsm_x4(uint32_t saddr, uint32_t r0, uint32_t r1
 // Bounded wait for the phase of `bar` with parity `parity`. Gives up after a bounded
 // number of polls (raising the abort flag), and at once when the flag is already raised.
 __device__ __forceinline__ bool wait_bar(uint64_t* bar, uint32_t parity,
-                                         volatile int* abort_flag) {
-  for (uint32_t i = 0; i < kWaitIters; ++i) {
+                                         volatile int* abort_flag, uint32_t limit = kWaitIters) {
+  for (uint32_t i = 0; i < limit; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
   }
@@ -206,6 +209,9 @@ scan_kernel(const __grid_constant__ Params p) {
                 pack_f16(S[2 * ks + 1][2], S[2 * ks + 1][3]));
     };
     if (nch > 0 && has_out) store_s16(0);
+    // testing hook: a bounded wait for an event that never happens (nothing arrives on
+    // B_STALL), so that the call takes the timeout path below
+    if (p.stall_polls && nch > 0) wait_bar(&bars[B_STALL], 0, abort_flag, p.stall_polls);
     for (int c = 0; c < nch; ++c) {
       const int slot = c % kRing, b = c & 1;
       const unsigned char* st = sm + slot * kSlot;

@@ -86,7 +86,11 @@ typedef enum gdn_dev_status {
 enum {
   GDN_FLAG_QK_L2NORM = 1u,            /* normalise q and k rows: x / sqrt(sum x^2 + eps) */
   GDN_FLAG_BUILD_CHUNK_INDICES = 2u,  /* fill the caller's chunk_indices buffer */
-  GDN_FLAG_CHANNEL_GATES = 4u         /* g is [T, Hv, dk]: a gate per key channel */
+  GDN_FLAG_CHANNEL_GATES = 4u,        /* g is [T, Hv, dk]: a gate per key channel */
+  GDN_FLAG_WORKSPACE_GUARDS = 8u      /* leave a 4 KiB gap after every workspace region
+                                         (a caller may fill the workspace with a pattern
+                                         and check the gaps after the call; see
+                                         gdn_workspace_regions); results are unchanged */
 };
 
 enum { GDN_NUM_STAGE_EVENTS = 5 };
@@ -243,6 +247,19 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
                   float* d_initial_state, cudaStream_t stream);
 
 /*
+ * Host-only description of the workspace layout for this descriptor (as
+ * gdn_workspace_size computes it): writes the byte range [begin[i], end[i]) of
+ * each region the library may write, in increasing order, for the first
+ * max_regions regions, and returns the number of regions (at most 16), or a
+ * negative gdn_status for an invalid descriptor. Bytes of the workspace outside
+ * every region are never written, so with GDN_FLAG_WORKSPACE_GUARDS the 4 KiB gap
+ * after each region is a guard band a test can fill and check (the device-side
+ * substitute for an out-of-bounds checker). The layout has no counterpart in the
+ * pages.
+ */
+int gdn_workspace_regions(const gdn_desc* desc, size_t* begin, size_t* end, int max_regions);
+
+/*
  * Enqueue an asynchronous copy of the device status word of the last call
  * that used desc->workspace into *host_status (pinned host memory is best).
  * The caller synchronizes the stream before reading it.
@@ -268,8 +285,13 @@ enum { GDN_NOALLOC_SCRATCH_BYTES = 64 << 20 };
  *     Hv = 32 fits; T = 4096 with Hv = 32 does not);
  *   - calls that may overlap on the GPU (other streams or host threads) race
  *     on the array: the caller must order them;
- *   - the first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress), so make that first call outside stream capture.
+ *   - every call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress; nothing is cached, so a device reset leaves no
+ *     stale address); the first lookup on a device may load the library's
+ *     device code, so make the first call outside stream capture;
+ *   - the kernels' device status word (gdn_dev_status bits) lives in the
+ *     array: read the last call's with gdn_noalloc_read_status, not
+ *     gdn_read_status (which needs desc->workspace).
  * It calls no allocator (no cudaMalloc, cudaFree or library allocation).
  */
 int gdn_chunk_fwd_noalloc(const gdn_desc* desc, const void* q, const void* k,
@@ -277,6 +299,17 @@ int gdn_chunk_fwd_noalloc(const gdn_desc* desc, const void* q, const void* k,
                           const float* initial_state, const int32_t* cu_seqlens,
                           int32_t* chunk_indices, void* out, float* final_state,
                           cudaStream_t stream);
+
+/*
+ * Enqueue an asynchronous copy of the device status word of the last
+ * gdn_chunk_fwd_noalloc call on the current device (the one in the shared
+ * scratch array) into *host_status. Like the entry point it belongs to, it has
+ * no counterpart in the pages. The caller synchronizes the stream before
+ * reading *host_status; a call still running on another stream would race.
+ * GDN_ERR_NULL_ARG for a NULL host_status, GDN_ERR_LAUNCH_FAILED if the copy
+ * could not be enqueued.
+ */
+int gdn_noalloc_read_status(int32_t* host_status, cudaStream_t stream);
 
 /*
  * Token-serial forward of the same recurrence, for decode (one token per
@@ -350,6 +383,18 @@ int gdn_conv_front(const gdn_desc* desc, const void* x, const float* conv_w, int
                    const float* conv_state_in, const int32_t* cu_seqlens, void* q, void* k,
                    void* v, float* conv_state_out, float* snapshots, int32_t n_snapshots,
                    cudaStream_t stream);
+
+/*
+ * Testing hook (no counterpart in the pages). With polls > 0, the bf16 scan of
+ * the calls that follow (on any thread) first waits, for at most `polls`
+ * polls, on an on-chip event that never happens; the wait runs out and the scan
+ * takes its timeout path: GDN_DEV_TIMEOUT in the status word, every warp runs on
+ * without waiting, the results of that call are invalid, and every copy in
+ * flight is still waited for (at the full bound) before the kernel ends, so the
+ * device stays usable. polls = 0 (the default) turns it off. It lets a test
+ * exercise that path without a fault or a hang.
+ */
+void gdn_test_scan_timeout(uint32_t polls);
 
 /* Static description of a gdn_status value. */
 const char* gdn_status_string(int status);

@@ -59,8 +59,9 @@ def test_check_desc(lib):
     d = desc()
     d.qkv_dtype = 7
     assert B.gdn_check_desc(d) == -3
+    assert B.gdn_check_desc(desc(flags=B.GDN_FLAG_WORKSPACE_GUARDS)) == 0
     d = desc()
-    d.flags = 8
+    d.flags = 16
     assert B.gdn_check_desc(d) == -3
     assert lib.gdn_check_desc(None) == -1
 
@@ -198,3 +199,22 @@ def test_conv_front_rejects_before_enqueue(lib):
     assert f(s1=4098) == -4
     assert f(d=desc(Hv=24)) == -2
     assert f(d=desc(dk=64, dv=64)) == -3       # built for d = 128 only
+
+
+def test_workspace_regions_and_guard_bands(lib):
+    """The region list covers what the library may write, in order and without overlap;
+    the guard flag leaves 4 KiB after every region and changes nothing else."""
+    import torch
+    d0 = desc()
+    dg = desc(flags=B.GDN_FLAG_WORKSPACE_GUARDS)
+    r0, rg = B.gdn_workspace_regions(d0), B.gdn_workspace_regions(dg)
+    assert len(r0) == len(rg) >= 8
+    assert r0[0] == (0, 64)                          # the status word comes first
+    for (a0, b0), (ag, bg) in zip(r0, rg):
+        assert b0 - a0 == bg - ag                    # same region sizes
+    for i in range(len(rg) - 1):
+        assert rg[i + 1][0] - rg[i][1] >= 4096       # a guard gap after every region
+        assert r0[i + 1][0] >= r0[i][1]              # ordered, no overlap
+    assert B.gdn_workspace_size(d0) >= r0[-1][1]
+    assert B.gdn_workspace_size(dg) >= rg[-1][1] + 4096
+    assert B.gdn_workspace_size(dg) == B.gdn_workspace_size(d0) + 4096 * len(rg)

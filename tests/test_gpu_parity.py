@@ -74,6 +74,54 @@ def test_bf16_output_is_rounded_fp32_output():
     assert torch.equal(o16, o32.to(torch.bfloat16))
 
 
+def test_bf16_output_is_rounded_fp32_output_full_size():
+    """Same at the benchmarked shape (T=4096, H=16, Hv=32): the bf16 store the benchmark
+    times is the RNE rounding of the parity-tested fp32 output, bit for bit."""
+    x = make_inputs(2)
+    o32, f32 = run_gpu(x, out_dtype=torch.float32)
+    o16, f16 = run_gpu(x, out_dtype=torch.bfloat16)
+    assert torch.equal(o16, o32.to(torch.bfloat16))
+    assert torch.equal(f16, f32)
+
+
+def test_decreasing_cu_seqlens_run_as_their_prefix_maximum():
+    """A malformed cu_seqlens is sanitized to its running maximum (clamped to [0, T]):
+    [0, 100, 50, 200] runs exactly as [0, 100, 100, 200] (the middle sequence empty, no
+    two sequences overlapping), with status bit 1 and no fault."""
+    x = make_inputs(2, seed=3, T=256, H=2, Hv=4)
+    d = to_dev(x)
+    s0 = torch.randn(3, 4, 128, 128, device="cuda") * 0.02
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"], s0)
+    bad = torch.tensor([0, 100, 50, 200], dtype=torch.int32, device="cuda")
+    good = torch.tensor([0, 100, 100, 200], dtype=torch.int32, device="cuda")
+    out_b = torch.full((256, 4, 128), 7.0, device="cuda")
+    out_g = out_b.clone()
+    o, f, desc, _ = B.gdn_chunk_fwd(*args, bad, out=out_b, out_dtype=torch.float32,
+                                    return_desc=True)
+    assert B.gdn_read_status(desc) == 1
+    o2, f2, desc2, _ = B.gdn_chunk_fwd(*args, good, out=out_g, out_dtype=torch.float32,
+                                       return_desc=True)
+    assert B.gdn_read_status(desc2) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(o, o2) and torch.equal(f, f2)
+    assert torch.equal(f[1], s0[1])                     # the empty sequence passes its state
+    assert bool((o[200:] == 7.0).all())                 # rows past the last sequence untouched
+
+
+def test_nonfinite_status_bit_for_fp16_range():
+    """Values whose decayed correction exceeds the fp16 range of the tensor-core path's state
+    update (|v| ~ 1e6 here) make the state non-finite: the call completes, no fault, and the
+    status word carries GDN_DEV_NONFINITE (16); the same call on in-range values is clean."""
+    x = make_inputs(2, seed=9, T=200, H=2, Hv=4)
+    run_gpu(x, out_dtype=torch.float32)                 # asserts a clean status word
+    x["v"] = (x["v"].float() * 1e6).to(torch.bfloat16)
+    d = to_dev(x)
+    o, f, desc, _ = B.gdn_chunk_fwd(d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"],
+                                    d["initial_state"], d["cu_seqlens"],
+                                    out_dtype=torch.float32, return_desc=True)
+    assert B.gdn_read_status(desc) & 16
+
+
 @pytest.mark.parametrize("wid", [3, 4])
 def test_chunk_table_bit_exact(wid):
     x = make_inputs(wid)
@@ -251,3 +299,29 @@ def test_cuda_graph_replay_bitwise():
         call()
         torch.cuda.synchronize()
         assert torch.equal(o_g, out) and torch.equal(f_g, fin), trial
+
+
+def test_scan_wait_timeout_is_reported_and_recoverable():
+    """A bounded on-chip wait that runs out: the testing hook makes the scan wait on an event
+    that never happens; the wait gives up, the call returns with GDN_DEV_TIMEOUT in the status
+    word and no fault or hang (copies in flight drained); with the hook off, the next call on
+    the same workspace is clean and parity-green."""
+    x = make_inputs(2, seed=11, T=1024, H=4, Hv=8)
+    d = to_dev(x)
+    desc = B.make_desc(x["T"], x["N"], x["H"], x["Hv"], torch.bfloat16, torch.float32)
+    ws = B.alloc_workspace(desc, "cuda")
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"], d["initial_state"],
+            d["cu_seqlens"])
+    try:
+        B.gdn_test_scan_timeout(64)
+        _, _, desc1, _ = B.gdn_chunk_fwd(*args, workspace=ws, out_dtype=torch.float32,
+                                         return_desc=True)
+        torch.cuda.synchronize()
+        assert B.gdn_read_status(desc1) & 8
+    finally:
+        B.gdn_test_scan_timeout(0)
+    o, f, desc2, _ = B.gdn_chunk_fwd(*args, workspace=ws, out_dtype=torch.float32,
+                                     return_desc=True)
+    assert B.gdn_read_status(desc2) == 0
+    o_ref, f_ref = run_oracle(x)
+    check_parity(x, o, f, o_ref, f_ref, TOL_BF16)
