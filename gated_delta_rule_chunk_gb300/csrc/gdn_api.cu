@@ -259,6 +259,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
                               : reinterpret_cast<int2*>(ws + L.chunk_table);
   p.chunk_table = table;
   p.G = L.G ? reinterpret_cast<float*>(ws + L.G) : nullptr;
+  p.EF = L.EF ? reinterpret_cast<float*>(ws + L.EF) : nullptr;
   p.w = ws + L.w;
   p.u = reinterpret_cast<float*>(ws + L.u);
   p.M = ws + L.M;
@@ -352,6 +353,7 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   const bool tc = uses_tc_path(&d);
   p.w = ws + L.w; p.u = f32(L.u); p.M = ws + L.M;
   p.G = L.G ? f32(L.G) : nullptr;
+  p.EF = L.EF ? f32(L.EF) : nullptr;
   p.k16 = L.k16 ? ws + L.k16 : nullptr;
   p.q16 = L.q16 ? ws + L.q16 : nullptr;
   p.qt = L.qt ? f32(L.qt) : nullptr;

@@ -32,6 +32,8 @@ struct Params {
   const int32_t* chunk_offsets;  // [N + 1]
   const int2* chunk_table;   // [nt_max] (sequence, ordinal) or (-1, -1)
   float* G;                  // [nt_max, Hv, 64] in-chunk cumulative log-decay
+  float* EF;                 // [nt_max, Hv, 128] exp(G) then exp(G_L - G) (tensor-core path,
+                             // scalar gates)
   void* w;                   // [nt_max, Hv, 64, dk]
   float* u;                  // [nt_max, Hv, 64, dv]
   void* M;                   // [nt_max, Hv, 64, 64] (or hi/lo pair) decay-masked q.k
@@ -138,8 +140,8 @@ struct ConvParams {
 // Byte offsets of the workspace regions (each 256-byte aligned), and the extent
 // [begin, end) of every region in order (for the guard-band check of the tests).
 struct WsLayout {
-  size_t status, seq_info, chunk_offsets, chunk_table, G, w, u, M, k16, qimg, q16, qt, kt, gam,
-      qrn, krn, total;
+  size_t status, seq_info, chunk_offsets, chunk_table, G, EF, w, u, M, k16, qimg, q16, qt, kt,
+      gam, qrn, krn, total;
   static constexpr int kMaxRegions = 16;
   int nreg;
   size_t rbeg[kMaxRegions], rend[kMaxRegions];
@@ -172,6 +174,7 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
   L.chunk_table = take(sizeof(int2) * (size_t)nt_max);
   const size_t slots = (size_t)nt_max * (size_t)Hv;
   L.G = tc_path ? take(sizeof(float) * slots * kChunk) : 0;
+  L.EF = (tc_path && !channel_gates) ? take(sizeof(float) * slots * 2 * kChunk) : 0;
   const size_t Dw = tc_path ? kDk : D;
   L.w = take((tc_path ? 2 : 4) * slots * kChunk * Dw);
   L.u = take(sizeof(float) * slots * kChunk * Dw);

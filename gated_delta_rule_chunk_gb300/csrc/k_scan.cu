@@ -67,9 +67,9 @@ constexpr int kRing = 3;
 constexpr uint32_t rW = 0;        // w, bf16: two dk halves of [64 tokens][128 B], 128-B swizzle
 constexpr uint32_t rK = 16384;    // k, fp16: same layout
 constexpr uint32_t rU = 32768;    // u block, fp32 [32 columns][64 tokens], 32-B groups swizzled
-constexpr uint32_t rG = 40960;    // G [64]
+constexpr uint32_t rE = 40960;    // exp(G) [64], exp(G_L - G) [64]
 constexpr uint32_t kSlot = 41984;
-constexpr uint32_t kTxRing = 16384 + 16384 + 8192 + 256;
+constexpr uint32_t kTxRing = 16384 + 16384 + 8192 + 512;
 // Output operands, double-buffered: q (two dk halves of [64][128 B], swizzled, by tensor
 // map) and [M_hi; M_lo] ([128 rows][128 B], swizzled).
 constexpr uint32_t kQM = kRing * kSlot;
@@ -219,16 +219,15 @@ scan_kernel(const __grid_constant__ Params p) {
       wait_bar(&bars[B_FULL + slot], (uint32_t)((c / kRing) & 1), abort_flag);
       // row factors exp(G_L - G_i) of this thread's 16 tokens and the state decay, formed
       // first so that their latency hides under the X product
-      const float* G = reinterpret_cast<const float*>(st + rG);
-      const float gl = G[63];
+      const float* E = reinterpret_cast<const float*>(st + rE);
       float fac[8][2];
 #pragma unroll
       for (int nt = 0; nt < 8; ++nt) {
-        const float2 gg = *reinterpret_cast<const float2*>(&G[8 * nt + c2]);
-        fac[nt][0] = __expf(gl - gg.x);
-        fac[nt][1] = __expf(gl - gg.y);
+        const float2 ff = *reinterpret_cast<const float2*>(&E[64 + 8 * nt + c2]);
+        fac[nt][0] = ff.x;
+        fac[nt][1] = ff.y;
       }
-      const float gam = __expf(gl);
+      const float gam = E[63];
       const size_t slot_hv = (size_t)(sv.first_slot + c) * p.Hv + hv;
       if (p.hs) {  // chunk-start state [dv][dk] (the backward's recompute)
         float* hs = p.hs + slot_hv * p.D * p.D;
@@ -308,7 +307,7 @@ scan_kernel(const __grid_constant__ Params p) {
         }
         if (r == 0)  // the chunk's G for the output's row factors
           *reinterpret_cast<float2*>(sm + kSV + b * kSVsz + vG + 8 * lane) =
-              *reinterpret_cast<const float2*>(&G[2 * lane]);
+              *reinterpret_cast<const float2*>(&E[2 * lane]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&bars[B_SF + b]);
       }
@@ -394,7 +393,7 @@ scan_kernel(const __grid_constant__ Params p) {
         for (int mi = 0; mi < kMT; ++mi)
 #pragma unroll
           for (int hh = 0; hh < 2; ++hh)
-            f[mi][hh] = p.scale * __expf(Gs[16 * mts[mi] + g + 8 * hh]);
+            f[mi][hh] = p.scale * Gs[16 * mts[mi] + g + 8 * hh];
       }
       const int m = lane >> 3;
       const int arow = (lane & 7) + (m & 1) * 8;   // A fragment row inside a 16-row tile
@@ -521,7 +520,7 @@ scan_kernel(const __grid_constant__ Params p) {
                 16384, full);
       bulk_load(st + rU, reinterpret_cast<const unsigned char*>(p.u) + sl * 32768 +
                              blockIdx.z * 8192, 8192, full);
-      bulk_load(st + rG, p.G + sl * 64, 256, full);
+      bulk_load(st + rE, p.EF + sl * 128, 512, full);
     };
     auto issue_qm = [&](int cc) {
       unsigned char* dst = sm + kQM + (cc & 1) * kQMsz;

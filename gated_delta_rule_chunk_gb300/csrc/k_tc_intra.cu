@@ -209,10 +209,19 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     G[lane + 32] = g1;
     Bt[lane] = be0;
     Bt[lane + 32] = be1;
-    FW[lane] = be0 * expf(g0) * KR[lane];
-    FW[lane + 32] = be1 * expf(g1) * KR[lane + 32];
+    const float e0 = expf(g0), e1 = expf(g1);
+    FW[lane] = be0 * e0 * KR[lane];
+    FW[lane + 32] = be1 * e1 * KR[lane + 32];
     p.G[sl * 64 + lane] = g0;
     p.G[sl * 64 + lane + 32] = g1;
+    if (p.EF) {  // exp(G) and exp(G_L - G) for the scan (G is flat past the last row)
+      const float gl = __shfl_sync(0xffffffffu, g1, 31);
+      float* ef = p.EF + sl * 128;
+      ef[lane] = e0;
+      ef[lane + 32] = e1;
+      ef[64 + lane] = expf(gl - g0);
+      ef[96 + lane] = expf(gl - g1);
+    }
   };
   if (warp == 0) {
     load_gates(0);
