@@ -92,9 +92,9 @@ def test_workspace_size(lib):
         assert n >= 64 * 32 * 4 * (64 * 4 * dd + 64 * 64 + dd)
     # bf16 with per-channel gates: the tensor-core bridge plus a k image and the decayed
     # q's hi/lo images per value head and exp(G_L) per channel, in place of the scalar-gate
-    # path's fp16 k and q images per key head
+    # path's fp16 k and q images per key head and its exp(G), exp(G_L - G) (512 B per slot)
     n = B.gdn_workspace_size(desc(flags=B.GDN_FLAG_CHANNEL_GATES))
-    assert n >= a + 64 * 32 * (16384 + 32768 + 512) - 2 * 64 * 16 * 16384
+    assert n >= a + 64 * 32 * (16384 + 32768 + 512) - 2 * 64 * 16 * 16384 - 64 * 32 * 512
     # bf16 with a head of 64 runs on the tensor-core kernels zero-padded to 128
     assert B.gdn_workspace_size(desc(dk=64, dv=64)) == a
 
