@@ -62,13 +62,15 @@ constexpr uint32_t kKQ = 0;       // [K_h0 | Q_h0 | K_h1 | Q_h1], each [64 rows]
                                   // the Q halves later hold the M image and the u operands
 constexpr uint32_t kV = 32768;    // two buffers of [V_h0 | V_h1]
 constexpr uint32_t kAT = 65536;   // fp32 [64][LDT]: A, then T; staging of the k and w images
-constexpr uint32_t kX = kAT + 64 * LDT * 4;  // fp32 [16][LDT]: scratch of the inverse
+constexpr int LDX = 36;  // fp32 stride of the inverse's scratch (32 rows)
+constexpr uint32_t kX = kAT + 64 * LDT * 4;  // fp32 [32][LDX]: scratch of the inverse
 constexpr uint32_t kTW = 88064;   // bf16 [64][128 B], swizzled: T diag(beta exp(G)) (w operand)
 constexpr uint32_t kVec = kTW + 8192;        // 6 x fp32 [64] row vectors
 constexpr uint32_t kBar = kVec + 6 * 256;    // 7 mbarriers
 constexpr uint32_t kMisc = kBar + 64;        // TMEM base address, failure flag
 constexpr uint32_t kSmemBytes = kMisc + 16 + 1024;  // + room to align the base to 1024
-static_assert(kX + 16 * LDT * 4 <= kTW, "shared-memory layout overlaps");
+static_assert(kX + 32 * LDX * 4 <= kTW, "shared-memory layout overlaps");
+static_assert(kWarps == 8, "the triangular inverse is written for eight warps");
 
 // Byte offset of 16-byte chunk ch of row r in a [rows][128 B] tile with the 128-byte swizzle.
 __device__ __forceinline__ uint32_t sw_off(int r, int ch) {
@@ -354,7 +356,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       bulk_store(mimg + 8192, sm + kKQ + 24576, 8192);
       bulk_commit();
     }
-    tri_inverse_64_tc<kWarps>(AT, LDT, X, tid);  // ends with the CTA synchronized
+    tri_inverse_64_rd(AT, LDT, X, LDX, tid);  // ends with the CTA synchronized
 
     // This member's V tile (rows past the end zeroed) and the M image read out of the Q halves.
     wait_or_flag(&bars[1 + (r & 1)], (uint32_t)((r >> 1) & 1), fail);

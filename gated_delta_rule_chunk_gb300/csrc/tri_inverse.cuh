@@ -195,3 +195,99 @@ __device__ inline void tri_inverse_64_tc(float* AT, int ld, float* X, int tid) {
 }
 
 }  // namespace gdn
+
+namespace gdn {
+
+// In-place inverse of I + A (64 x 64, A strictly lower triangular with zeros on and above
+// the diagonal) for a CTA of 8 warps, by recursive doubling: the four diagonal 16 x 16
+// blocks by column substitution (fp32, one thread per column); then the two 32 x 32
+// diagonal blocks, T = [[T11, 0], [-T22 A21 T11, T22]] with 16 x 16 parts (both at once);
+// then the whole 64 x 64 the same way with 32 x 32 parts. Four dependent products in
+// place of the six of the block-row order, with all eight warps busy in the last level.
+// The products run on warp-level MMAs with fp32 operands split into bf16 hi + lo (about
+// 16 significant bits, fp32 accumulate). X: scratch of 32 rows x ldx fp32 (ldx >= 32).
+__device__ inline void tri_inverse_64_rd(float* AT, int ld, float* X, int ldx, int tid) {
+  const int warp = tid >> 5, lane = tid & 31, g = lane >> 2, c = 2 * (lane & 3);
+  float col[16];
+  const int base = (tid >> 4) * 16, cc = tid & 15;
+  if (tid < 64) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      float acc = 0.f;
+#pragma unroll
+      for (int m = 0; m < 16; ++m)
+        if (m < i) acc = fmaf(AT[(base + i) * ld + base + m], col[m], acc);
+      col[i] = (i < cc) ? 0.f : (i == cc ? 1.f : -acc);
+    }
+  }
+  __syncthreads();  // every diagonal block of A has been read
+  if (tid < 64) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) AT[(base + i) * ld + base + cc] = col[i];
+  }
+  __syncthreads();
+  // Level 1: blocks (1, 0) and (3, 2). Warp w < 4: pair q = w / 2 (rows r, columns o),
+  // n-tile w % 2. Y = A[r, o] T[o, o] into X columns 16 q..; then T[r, o] = -T[r, r] Y.
+  const int q = warp >> 1, n1 = warp & 1;
+  const int r1 = 16 + 32 * q, o1 = 32 * q;
+  if (warp < 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    frag_a_split(AT, ld, r1, o1, lane, ah, al);
+    frag_b_split(AT, ld, o1, o1 + 8 * n1, lane, bh, bl);
+    mma_split3(acc, ah, al, bh, bl);
+    *reinterpret_cast<float2*>(&X[g * ldx + 16 * q + 8 * n1 + c]) = make_float2(acc[0], acc[1]);
+    *reinterpret_cast<float2*>(&X[(g + 8) * ldx + 16 * q + 8 * n1 + c]) =
+        make_float2(acc[2], acc[3]);
+  }
+  __syncthreads();
+  if (warp < 4) {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    uint32_t ah[4], al[4], bh[2], bl[2];
+    frag_a_split(AT, ld, r1, r1, lane, ah, al);
+    frag_b_split(X, ldx, 0, 16 * q + 8 * n1, lane, bh, bl);
+    mma_split3(acc, ah, al, bh, bl);
+    *reinterpret_cast<float2*>(&AT[(r1 + g) * ld + o1 + 8 * n1 + c]) = make_float2(-acc[0], -acc[1]);
+    *reinterpret_cast<float2*>(&AT[(r1 + g + 8) * ld + o1 + 8 * n1 + c]) =
+        make_float2(-acc[2], -acc[3]);
+  }
+  __syncthreads();
+  // Level 2: rows 32..63, columns 0..31. Warp w: row tile m2 = w / 4 (16 rows), n-tile
+  // w % 4. Y = A21 T11 (T11[0:16, 16:32] is zero, so column tiles 2, 3 skip k-step 0)
+  // into X rows 16 m2..; then T21 = -T22 Y (T22[0:16, 16:32] is zero, so row tile 0 skips
+  // k-step 1).
+  const int m2 = warp >> 2, n2 = warp & 3;
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      if (ks == 0 && n2 >= 2) continue;
+      uint32_t ah[4], al[4], bh[2], bl[2];
+      frag_a_split(AT, ld, 32 + 16 * m2, 16 * ks, lane, ah, al);
+      frag_b_split(AT, ld, 16 * ks, 8 * n2, lane, bh, bl);
+      mma_split3(acc, ah, al, bh, bl);
+    }
+    *reinterpret_cast<float2*>(&X[(16 * m2 + g) * ldx + 8 * n2 + c]) = make_float2(acc[0], acc[1]);
+    *reinterpret_cast<float2*>(&X[(16 * m2 + g + 8) * ldx + 8 * n2 + c]) =
+        make_float2(acc[2], acc[3]);
+  }
+  __syncthreads();
+  {
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      if (ks == 1 && m2 == 0) continue;
+      uint32_t ah[4], al[4], bh[2], bl[2];
+      frag_a_split(AT, ld, 32 + 16 * m2, 32 + 16 * ks, lane, ah, al);
+      frag_b_split(X, ldx, 16 * ks, 8 * n2, lane, bh, bl);
+      mma_split3(acc, ah, al, bh, bl);
+    }
+    *reinterpret_cast<float2*>(&AT[(32 + 16 * m2 + g) * ld + 8 * n2 + c]) =
+        make_float2(-acc[0], -acc[1]);
+    *reinterpret_cast<float2*>(&AT[(32 + 16 * m2 + g + 8) * ld + 8 * n2 + c]) =
+        make_float2(-acc[2], -acc[3]);
+  }
+  __syncthreads();
+}
+
+}  // namespace gdn
