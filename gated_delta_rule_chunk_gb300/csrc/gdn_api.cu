@@ -275,15 +275,13 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.stall_polls = scan_stall_polls();
 
   cudaEvent_t* ev = d.stage_events;
-  if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
-    return GDN_ERR_LAUNCH_FAILED;
   if (ev) cudaEventRecord(ev[0], stream);
   if (l2) launch_l2norm(q, k, bf16, d.T, d.H, d.dk, eps, const_cast<float*>(p.qrn),
                         const_cast<float*>(p.krn), stream);
   launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
                      (!chunk_indices || build_into_caller) ? table : nullptr,
                      const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
-                     p.status, stream);
+                     p.status, stream, /*zero_status=*/true);  // (no separate memset)
   if (ev) cudaEventRecord(ev[1], stream);
   const bool tc = uses_tc_path(&d);
   if (nt_max > 0) {
@@ -362,13 +360,11 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.hs = f32(B.hs); p.vn_out = f32(B.vn);
   p.stall_polls = scan_stall_polls();
   cudaEvent_t* ev = d.stage_events;
-  if (cudaMemsetAsync(p.status, 0, sizeof(int32_t), stream) != cudaSuccess)
-    return GDN_ERR_LAUNCH_FAILED;
   if (ev) cudaEventRecord(ev[0], stream);
   launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
                      (!chunk_indices || build_into_caller) ? table : nullptr,
                      const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
-                     p.status, stream);
+                     p.status, stream, /*zero_status=*/true);  // (no separate memset)
   if (tc) {  // the tensor-core forward kernels, storing S and v_new per chunk
     if (nt_max > 0 && !launch_tc_intra(p, stream)) return GDN_ERR_LAUNCH_FAILED;
     if (!launch_tc_inter(p, false, stream)) return GDN_ERR_LAUNCH_FAILED;

@@ -247,7 +247,8 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 
 // Kernel launchers (one translation unit each).
 void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,
-                        int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s);
+                        int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s,
+                        bool zero_status = false);
 void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, int D, float eps,
                    float* qrn, float* krn, cudaStream_t s);
 bool launch_gen_intra(const Params& p, int D, bool channel_gates, bool bf16_inputs, cudaStream_t s);

@@ -6,7 +6,8 @@
 // searchsorted over the per-sequence chunk counts, with a sentinel in unused
 // slots, so no host synchronization is needed.
 //
-// One CTA of 1024 threads: (1) sanitize the boundaries: each cu_seqlens entry is
+// One CTA of 1024 threads: (0) in a forward or backward call, clear the call's status
+// word (in place of a separate memset), (1) sanitize the boundaries: each cu_seqlens entry is
 // clamped to [0, T] and raised to the largest entry before it (a prefix maximum), so
 // sequence n is [max(c_0..c_n), max(c_0..c_n+1)) -- never overlapping another, empty
 // where the input decreases -- and count its chunks, (2) exclusive-scan the counts
@@ -18,7 +19,7 @@ namespace gdn {
 __global__ void __launch_bounds__(1024)
 chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
                    int2* __restrict__ table, int32_t* __restrict__ offsets,
-                   int2* __restrict__ seq_info, int32_t* status) {
+                   int2* __restrict__ seq_info, int32_t* status, bool zero_status) {
   __shared__ int warp_incl[32];
   __shared__ int warp_max[32];
   __shared__ int carry_s, carry_max_s;
@@ -27,6 +28,7 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
   if (tid == 0) {
     carry_s = 0;
     carry_max_s = 0;
+    if (zero_status && status) *status = 0;  // the call's status word starts clean
   }
   __syncthreads();
   int bad = 0;
@@ -113,8 +115,10 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
 }
 
 void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,
-                        int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s) {
-  chunk_table_kernel<<<1, 1024, 0, s>>>(cu, N, T, nt_max, table, offsets, seq_info, status);
+                        int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s,
+                        bool zero_status) {
+  chunk_table_kernel<<<1, 1024, 0, s>>>(cu, N, T, nt_max, table, offsets, seq_info, status,
+                                        zero_status);
 }
 
 }  // namespace gdn

@@ -155,7 +155,19 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   int t0, L, wslot;
   if (!resolve(p, blockIdx.y, t0, L, wslot)) return;  // uniform over the CTA
 
+  // g and beta of group member r (warp 0, 2 rows per lane), loaded one member ahead of
+  // their use; the first member's loads are in flight during the setup below.
+  float gn0 = 0.f, gn1 = 0.f, bn0 = 0.f, bn1 = 0.f;
+  auto load_gates = [&](int r) {
+    const int hv = h * p.HG + r;
+    const size_t b0 = (size_t)(t0 + lane) * p.Hv + hv, b1 = (size_t)(t0 + lane + 32) * p.Hv + hv;
+    gn0 = lane < L ? p.g[b0] : 0.f;
+    gn1 = lane + 32 < L ? p.g[b1] : 0.f;
+    bn0 = lane < L ? p.beta[b0] : 0.f;
+    bn1 = lane + 32 < L ? p.beta[b1] : 0.f;
+  };
   if (warp == 0) {
+    load_gates(0);
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -181,17 +193,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  // Gates of group member r and their in-chunk inclusive cumsum (warp 0, 2 rows per
-  // lane); the next member's g and beta are loaded one member ahead.
-  float gn0 = 0.f, gn1 = 0.f, bn0 = 0.f, bn1 = 0.f;
-  auto load_gates = [&](int r) {
-    const int hv = h * p.HG + r;
-    const size_t b0 = (size_t)(t0 + lane) * p.Hv + hv, b1 = (size_t)(t0 + lane + 32) * p.Hv + hv;
-    gn0 = lane < L ? p.g[b0] : 0.f;
-    gn1 = lane + 32 < L ? p.g[b1] : 0.f;
-    bn0 = lane < L ? p.beta[b0] : 0.f;
-    bn1 = lane + 32 < L ? p.beta[b1] : 0.f;
-  };
+  // Gates of group member r and their in-chunk inclusive cumsum (warp 0, 2 rows per lane).
   auto gates = [&](int r) {
     const size_t sl = (size_t)wslot * p.Hv + h * p.HG + r;
     float g0 = gn0, g1 = gn1;
@@ -225,20 +227,15 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       ef[96 + lane] = expf(gl - g1);
     }
   };
-  if (warp == 0) {
-    load_gates(0);
-    gates(0);  // while the k and q tiles are in flight
-  }
-
   wait_or_flag(&bars[0], 0, fail);
-  if (L < kChunk) {
+  if (L < kChunk) {  // (a full chunk needs no barrier: thread 0 waited for the tiles itself)
     zero_tail(sm + kKQ, L, tid);
     zero_tail(sm + kKQ + 8192, L, tid);
     zero_tail(sm + kKQ + 16384, L, tid);
     zero_tail(sm + kKQ + 24576, L, tid);
+    fence_async_smem();
+    __syncthreads();
   }
-  fence_async_smem();
-  __syncthreads();
   if (tid == 0) {  // [P; R] = [K; Q] K^T
     tc_fence_after();
     const uint32_t id = idesc_bf16_f32(128, 64, false, false);
@@ -297,7 +294,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const int hv = h * p.HG + r;
     const size_t sl = (size_t)wslot * p.Hv + hv;
     const uint32_t par = (uint32_t)(r & 1);  // parity of this member's MMA barriers
-    if (r > 0 && warp == 0) gates(r);
+    if (warp == 0) gates(r);  // (member 0's g and beta were loaded during the setup)
     if (tid == 0) bulk_wait_read<0>();  // staging regions read out by the previous copies
     __syncthreads();
     if (r == 0) wait_or_flag(&bars[3], 0, fail);
