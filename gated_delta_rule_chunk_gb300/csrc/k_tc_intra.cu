@@ -56,6 +56,7 @@ constexpr int kThreads = 32 * kWarps;
 constexpr int LDT = 68;  // fp32 stride of the A/T tile (16-byte rows)
 constexpr uint32_t kWaitIters = 1u << 22;
 constexpr uint32_t kTmemCols = 256;
+constexpr int kMStoreThread = kThreads - 32;  // issues the M image copies (warp 7, lane 0)
 
 // Shared memory (bytes from a 1024-aligned base).
 constexpr uint32_t kKQ = 0;       // [K_h0 | Q_h0 | K_h1 | Q_h1], each [64 rows][128 B], swizzled;
@@ -154,6 +155,9 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   pdl_release();  // the inter kernel may take SMs as this grid drains
   int t0, L, wslot;
   if (!resolve(p, blockIdx.y, t0, L, wslot)) return;  // uniform over the CTA
+  // The q image is staged in the second V buffer, whose tile is loaded once the image has
+  // been read out.
+  const bool v1_late = p.q16 != nullptr && p.HG > 1;
 
   // g and beta of group member r (warp 0, 2 rows per lane), loaded one member ahead of
   // their use; the first member's loads are in flight during the setup below.
@@ -180,7 +184,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     tma_load_3d(sm + kKQ + 16384, &tmk, 64, h, t0, &bars[0]);
     tma_load_3d(sm + kKQ + 8192, &tmq, 0, h, t0, &bars[0]);
     tma_load_3d(sm + kKQ + 24576, &tmq, 64, h, t0, &bars[0]);
-    for (int r = 0; r < min(p.HG, 2); ++r) issue_v(sm, bars, &tmv, h * p.HG + r, t0, r);
+    for (int r = 0; r < min(p.HG, v1_late ? 1 : 2); ++r)
+      issue_v(sm, bars, &tmv, h * p.HG + r, t0, r);
   }
   if (tid < 64) KR[tid] = (tid < L && p.krn) ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
   else if (tid < 128)
@@ -247,9 +252,9 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     umma_commit(&bars[3]);
   }
 
-  // fp16 images of the (normalised) k and q tiles, assembled in turn in the A/T region,
-  // each two halves of [64 rows][128 B] with the 128-byte swizzle; the scan reads them
-  // with one bulk copy each.
+  // fp16 images of the (normalised) k and q tiles, assembled in the A/T region and the
+  // second V buffer, each two halves of [64 rows][128 B] with the 128-byte swizzle; the
+  // scan reads them with one bulk copy each.
   auto f16_image = [&](const unsigned char* src, unsigned char* img, const float* rowf) {
 #pragma unroll
     for (int it = 0; it < 1024 / kThreads; ++it) {
@@ -269,25 +274,16 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       *reinterpret_cast<uint4*>(img + (uint32_t)half * 8192u + sw_off(t, ch)) = v;
     }
   };
+  unsigned char* const qstage = sm + kV + 16384;
   f16_image(sm + kKQ, sm + kAT, KR);
+  if (p.q16) f16_image(sm + kKQ + 8192, qstage, QR);
   fence_async_smem();
   __syncthreads();
   if (tid == 0) {
-    bulk_store(static_cast<unsigned char*>(p.k16) + ((size_t)wslot * p.H + h) * 64 * kDk * 2,
-               sm + kAT, 16384);
+    const size_t img = ((size_t)wslot * p.H + h) * 64 * kDk * 2;
+    bulk_store(static_cast<unsigned char*>(p.k16) + img, sm + kAT, 16384);
+    if (p.q16) bulk_store(static_cast<unsigned char*>(p.q16) + img, qstage, 16384);
     bulk_commit();
-    if (p.q16) bulk_wait_read<0>();  // the staging region is reused for q
-  }
-  if (p.q16) {
-    __syncthreads();
-    f16_image(sm + kKQ + 8192, sm + kAT, QR);
-    fence_async_smem();
-    __syncthreads();
-    if (tid == 0) {
-      bulk_store(static_cast<unsigned char*>(p.q16) + ((size_t)wslot * p.H + h) * 64 * kDk * 2,
-                 sm + kAT, 16384);
-      bulk_commit();
-    }
   }
 
   for (int r = 0; r < p.HG; ++r) {
@@ -295,7 +291,10 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const size_t sl = (size_t)wslot * p.Hv + hv;
     const uint32_t par = (uint32_t)(r & 1);  // parity of this member's MMA barriers
     if (warp == 0) gates(r);  // (member 0's g and beta were loaded during the setup)
-    if (tid == 0) bulk_wait_read<0>();  // staging regions read out by the previous copies
+    if (tid == 0) {
+      bulk_wait_read<0>();  // staging regions read out by the previous copies
+      if (r == 0 && v1_late) issue_v(sm, bars, &tmv, hv + 1, t0, 1);  // into the q staging
+    }
     __syncthreads();
     if (r == 0) wait_or_flag(&bars[3], 0, fail);
     tc_fence_after();
@@ -347,7 +346,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
+    if (tid == kMStoreThread) {  // (thread 0 leads the inverse's first step)
       unsigned char* mimg = static_cast<unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2;
       bulk_store(mimg, sm + kKQ + 8192, 8192);
       bulk_store(mimg + 8192, sm + kKQ + 24576, 8192);
@@ -362,7 +361,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       zero_tail(vt, L, tid);
       zero_tail(vt + 8192, L, tid);
     }
-    if (tid == 0) bulk_wait_read<0>();
+    if (tid == kMStoreThread) bulk_wait_read<0>();  // the M image read out of the Q halves
     __syncthreads();
     // T operand images: T diag(beta exp(G) / ||k||) (bf16) and T diag(beta) as a bf16
     // hi/lo pair (hi into the first Q half, lo into the second).
@@ -488,7 +487,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   }
 
   if (tid == 0) {
-    bulk_wait<0>();  // every image written
+    bulk_wait_read<0>();  // every image read out (the grid's end completes the writes)
     for (int r = max(0, p.HG - 2); r < p.HG; ++r)  // (all V loads were consumed; bounded)
       mbar_wait(&bars[1 + (r & 1)], (uint32_t)((r >> 1) & 1), kWaitIters);
     if (*fail) set_status(p.status, GDN_DEV_TIMEOUT);
