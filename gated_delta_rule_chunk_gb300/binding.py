@@ -25,12 +25,15 @@ GDN_FLAG_CHANNEL_GATES = 4
 GDN_FLAG_WORKSPACE_GUARDS = 8
 GDN_NUM_STAGE_EVENTS = 5
 DEV_STATUS_BITS = {1: "bad cu_seqlens", 2: "chunk overflow", 4: "bad chunk table",
-                   8: "on-chip wait timed out", 16: "non-finite state or output"}
+                   8: "on-chip wait timed out", 16: "non-finite state or output",
+                   32: "index out of range (GDN_DEBUG build)"}
+GDN_DEV_DEBUG_INDEX = 32
 
 # Every entry point include/gdn.h declares.
 EXPORTED = ("gdn_check_desc", "gdn_nt_max", "gdn_workspace_size", "gdn_build_chunk_indices",
             "gdn_chunk_fwd", "gdn_read_status", "gdn_status_string", "gdn_chunk_fwd_noalloc",
             "gdn_noalloc_read_status", "gdn_test_scan_timeout", "gdn_workspace_regions",
+            "gdn_debug_build", "gdn_test_debug_poison",
             "gdn_recurrent_fwd", "gdn_conv_front", "gdn_bwd_workspace_size", "gdn_chunk_bwd")
 GDN_NOALLOC_SCRATCH_BYTES = 64 << 20
 
@@ -81,6 +84,10 @@ def load_library(path: str = LIB_PATH):
         lib.gdn_chunk_fwd_noalloc.restype = ctypes.c_int
         lib.gdn_noalloc_read_status.argtypes = [vp, vp]
         lib.gdn_noalloc_read_status.restype = ctypes.c_int
+        lib.gdn_debug_build.argtypes = []
+        lib.gdn_debug_build.restype = ctypes.c_int
+        lib.gdn_test_debug_poison.argtypes = [i32]
+        lib.gdn_test_debug_poison.restype = None
         lib.gdn_test_scan_timeout.argtypes = [ctypes.c_uint32]
         lib.gdn_test_scan_timeout.restype = None
         lib.gdn_workspace_regions.argtypes = [P(GdnDesc), vp, vp, ctypes.c_int]
@@ -431,6 +438,17 @@ def gdn_test_scan_timeout(polls: int) -> None:
     """Testing hook: with polls > 0 the bf16 scan waits that many polls on an event that
     never happens and takes its timeout path (GDN_DEV_TIMEOUT); 0 turns it off."""
     load_library().gdn_test_scan_timeout(int(polls))
+
+
+def gdn_debug_build() -> bool:
+    """Whether the loaded library is the GDN_DEBUG build (device-side index checks)."""
+    return bool(load_library().gdn_debug_build())
+
+
+def gdn_test_debug_poison(on: bool) -> None:
+    """Testing hook of the GDN_DEBUG build: aim one intra CTA's M copies one slot past the
+    end of their region, which the device check must catch (GDN_DEV_DEBUG_INDEX)."""
+    load_library().gdn_test_debug_poison(1 if on else 0)
 
 
 def gdn_workspace_regions(desc: GdnDesc):

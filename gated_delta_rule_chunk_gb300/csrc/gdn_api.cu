@@ -21,6 +21,8 @@ std::atomic<uint32_t> g_scan_stall_polls{0};
 }  // namespace
 
 uint32_t scan_stall_polls() { return g_scan_stall_polls.load(std::memory_order_relaxed); }
+std::atomic<int> g_debug_poison{0};
+int debug_poison() { return g_debug_poison.load(std::memory_order_relaxed); }
 
 void ensure_smem_limit(const void* kernel, int bytes) {
   // largest limit set so far per (kernel, device); raised when a call needs more
@@ -273,6 +275,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.krn = l2 ? reinterpret_cast<float*>(ws + L.krn) : nullptr;
   p.out_bf16 = d.out_dtype == GDN_BF16;
   p.stall_polls = scan_stall_polls();
+  p.dbg_poison = debug_poison();
 
   cudaEvent_t* ev = d.stage_events;
   if (ev) cudaEventRecord(ev[0], stream);
@@ -359,6 +362,7 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.gam = L.gam ? f32(L.gam) : nullptr;
   p.hs = f32(B.hs); p.vn_out = f32(B.vn);
   p.stall_polls = scan_stall_polls();
+  p.dbg_poison = debug_poison();
   cudaEvent_t* ev = d.stage_events;
   if (ev) cudaEventRecord(ev[0], stream);
   launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
@@ -481,6 +485,18 @@ int gdn_read_status(const gdn_desc* desc, int32_t* host_status, cudaStream_t str
                       stream) != cudaSuccess)
     return GDN_ERR_LAUNCH_FAILED;
   return GDN_OK;
+}
+
+int gdn_debug_build(void) {
+#ifdef GDN_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
+void gdn_test_debug_poison(int32_t on) {
+  g_debug_poison.store(on ? 1 : 0, std::memory_order_relaxed);
 }
 
 void gdn_test_scan_timeout(uint32_t polls) {

@@ -54,6 +54,7 @@ struct Params {
   int out_bf16;
   uint32_t stall_polls;      // testing hook: > 0 makes the scan wait this many polls on an
                              // event that never happens (its timeout path); 0 normally
+  int dbg_poison;            // testing hook of the GDN_DEBUG build (an out-of-range M slot)
 };
 
 // Parameters of the backward kernels (device pointers; fp32 SIMT arithmetic). Per-slot
@@ -209,6 +210,20 @@ __device__ __forceinline__ void set_status(int32_t* status, int bits) {
   if (status) atomicOr(status, bits);
 }
 
+// Device-side index check of the GDN_DEBUG build: returns whether an index that
+// addresses global memory is in its range, raising GDN_DEV_DEBUG_INDEX when it is not (the
+// caller then skips or redirects the access). Always true, and free, in the normal build.
+__device__ __forceinline__ bool dbg_ok(bool in_range, int32_t* status) {
+#ifdef GDN_DEBUG
+  if (!in_range) set_status(status, GDN_DEV_DEBUG_INDEX);
+  return in_range;
+#else
+  (void)in_range;
+  (void)status;
+  return true;
+#endif
+}
+
 // The (start, length) of sequence n and its first chunk slot.
 struct SeqView {
   int start, len, first_slot;
@@ -223,6 +238,8 @@ __device__ __forceinline__ SeqView seq_view(const P& p, int n) {
 // Testing hook (gdn_test_scan_timeout): polls of the scan's never-completing wait for the
 // next launches, 0 normally.
 uint32_t scan_stall_polls();
+// Testing hook of the GDN_DEBUG build (gdn_test_debug_poison), 0 normally.
+int debug_poison();
 
 // Raise a kernel's dynamic shared-memory limit once per (kernel, device), so
 // that later calls (for example under CUDA-graph capture) make no attribute call.

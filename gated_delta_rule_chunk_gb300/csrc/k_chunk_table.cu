@@ -86,7 +86,7 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
     }
     __syncthreads();
     const int excl = carry_s + (wid ? warp_incl[wid - 1] : 0) + x - cnt;
-    if (n < N) offsets[n] = excl;
+    if (n < N && dbg_ok(n <= N, status)) offsets[n] = excl;
     __syncthreads();
     if (tid == 1023) carry_s = excl + cnt;
     __syncthreads();
@@ -110,7 +110,7 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
       }
       r = make_int2(lo, s - offsets[lo]);
     }
-    table[s] = r;
+    if (dbg_ok(s < nt_max, status)) table[s] = r;
   }
 }
 

@@ -229,7 +229,8 @@ scan_kernel(const __grid_constant__ Params p) {
       }
       const float gam = E[63];
       const size_t slot_hv = (size_t)(sv.first_slot + c) * p.Hv + hv;
-      if (p.hs) {  // chunk-start state [dv][dk] (the backward's recompute)
+      // chunk-start state [dv][dk] (the backward's recompute)
+      if (p.hs && dbg_ok(slot_hv < (size_t)p.nt_max * p.Hv, p.status)) {
         float* hs = p.hs + slot_hv * p.D * p.D;
 #pragma unroll
         for (int nt = 0; nt < 16; ++nt)
@@ -283,7 +284,8 @@ scan_kernel(const __grid_constant__ Params p) {
           X[nt][2 * hh] = u2.x - X[nt][2 * hh];
           X[nt][2 * hh + 1] = u2.y - X[nt][2 * hh + 1];
         }
-      if (p.vn_out) {  // v_new [64 tokens][dv] of the chunk (the backward's recompute)
+      // v_new [64 tokens][dv] of the chunk (the backward's recompute)
+      if (p.vn_out && dbg_ok(slot_hv < (size_t)p.nt_max * p.Hv, p.status)) {
         float* vo = p.vn_out + slot_hv * 64 * p.D + c0 + rb;
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt)
@@ -474,7 +476,8 @@ scan_kernel(const __grid_constant__ Params p) {
             rs[hh] += a + b2;
             if (p.out_bf16) {
               pk[nt][hh] = pack_bf16(a, b2);
-            } else if (16 * mt + g + 8 * hh < L) {
+            } else if (16 * mt + g + 8 * hh < L &&
+                       dbg_ok(t0 + 16 * mt + g + 8 * hh < p.T, p.status)) {
               *reinterpret_cast<float2*>(static_cast<float*>(p.out) +
                                          ((size_t)(t0 + 16 * mt + g + 8 * hh) * p.Hv + hv) * p.D +
                                          c0 + 8 * nt + c2) = make_float2(a, b2);
@@ -497,7 +500,7 @@ scan_kernel(const __grid_constant__ Params p) {
             asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4];\n"
                          : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                          : "r"(st + row * 64 + ((uint32_t)(ch ^ ((row >> 1) & 3)) << 4)));
-            if (16 * mt + row < L)
+            if (16 * mt + row < L && dbg_ok(t0 + 16 * mt + row < p.T, p.status))
               *reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) +
                                         ((size_t)(t0 + 16 * mt + row) * p.Hv + hv) * p.D + c0 +
                                         8 * ch) = v;
@@ -512,7 +515,8 @@ scan_kernel(const __grid_constant__ Params p) {
       const int slot = cc % kRing;
       unsigned char* st = sm + slot * kSlot;
       uint64_t* full = &bars[B_FULL + slot];
-      const size_t wslot = (size_t)sv.first_slot + cc;
+      size_t wslot = (size_t)sv.first_slot + cc;
+      if (!dbg_ok(wslot < (size_t)p.nt_max, p.status)) wslot = 0;  // (keeps the tx count)
       const size_t sl = wslot * p.Hv + hv;
       mbar_expect_tx(full, kTxRing);
       bulk_load(st + rW, static_cast<const unsigned char*>(p.w) + sl * 16384, 16384, full);
@@ -525,10 +529,12 @@ scan_kernel(const __grid_constant__ Params p) {
     auto issue_qm = [&](int cc) {
       unsigned char* dst = sm + kQM + (cc & 1) * kQMsz;
       uint64_t* full = &bars[B_QF + (cc & 1)];
-      const size_t sl = ((size_t)sv.first_slot + cc) * p.Hv + hv;
+      size_t wslot = (size_t)sv.first_slot + cc;
+      if (!dbg_ok(wslot < (size_t)p.nt_max, p.status)) wslot = 0;  // (keeps the tx count)
+      const size_t sl = wslot * p.Hv + hv;
       mbar_expect_tx(full, kQMsz);
-      bulk_load(dst + qQ, static_cast<const unsigned char*>(p.q16) +
-                              (((size_t)sv.first_slot + cc) * p.H + h) * 16384, 16384, full);
+      bulk_load(dst + qQ, static_cast<const unsigned char*>(p.q16) + (wslot * p.H + h) * 16384,
+                16384, full);
       bulk_load(dst + qM, static_cast<const unsigned char*>(p.M) + sl * 16384, 16384, full);
     };
     int issued = 0, qm_issued = 0;

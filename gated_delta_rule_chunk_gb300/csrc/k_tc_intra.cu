@@ -158,6 +158,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   // The q image is staged in the second V buffer, whose tile is loaded once the image has
   // been read out.
   const bool v1_late = p.q16 != nullptr && p.HG > 1;
+  const size_t n_vslots = (size_t)p.nt_max * p.Hv;  // value slots of the bridge regions
 
   // g and beta of group member r (warp 0, 2 rows per lane), loaded one member ahead of
   // their use; the first member's loads are in flight during the setup below.
@@ -221,6 +222,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const float e0 = expf(g0), e1 = expf(g1);
     FW[lane] = be0 * e0 * KR[lane];
     FW[lane + 32] = be1 * e1 * KR[lane + 32];
+    if (!dbg_ok(sl < n_vslots, p.status)) return;
     p.G[sl * 64 + lane] = g0;
     p.G[sl * 64 + lane + 32] = g1;
     if (p.EF) {  // exp(G) and exp(G_L - G) for the scan (G is flat past the last row)
@@ -281,8 +283,10 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   __syncthreads();
   if (tid == 0) {
     const size_t img = ((size_t)wslot * p.H + h) * 64 * kDk * 2;
-    bulk_store(static_cast<unsigned char*>(p.k16) + img, sm + kAT, 16384);
-    if (p.q16) bulk_store(static_cast<unsigned char*>(p.q16) + img, qstage, 16384);
+    if (dbg_ok(wslot < p.nt_max && h < p.H, p.status)) {
+      bulk_store(static_cast<unsigned char*>(p.k16) + img, sm + kAT, 16384);
+      if (p.q16) bulk_store(static_cast<unsigned char*>(p.q16) + img, qstage, 16384);
+    }
     bulk_commit();
   }
 
@@ -347,9 +351,16 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     tc_fence_before();
     __syncthreads();
     if (tid == kMStoreThread) {  // (thread 0 leads the inverse's first step)
-      unsigned char* mimg = static_cast<unsigned char*>(p.M) + sl * 2 * 64 * 64 * 2;
-      bulk_store(mimg, sm + kKQ + 8192, 8192);
-      bulk_store(mimg + 8192, sm + kKQ + 24576, 8192);
+      size_t slm = sl;
+#ifdef GDN_DEBUG
+      // testing hook: one past the end of the M region (the next region follows it)
+      if (p.dbg_poison && blockIdx.x == 0 && blockIdx.y == 0) slm = n_vslots;
+#endif
+      if (dbg_ok(slm < n_vslots, p.status)) {
+        unsigned char* mimg = static_cast<unsigned char*>(p.M) + slm * 2 * 64 * 64 * 2;
+        bulk_store(mimg, sm + kKQ + 8192, 8192);
+        bulk_store(mimg + 8192, sm + kKQ + 24576, 8192);
+      }
       bulk_commit();
     }
     tri_inverse_64_rd(AT, LDT, X, LDX, tid);  // ends with the CTA synchronized
@@ -443,7 +454,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-      bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
+      if (dbg_ok(sl < n_vslots, p.status))
+        bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
       bulk_commit();
       tc_fence_after();
       issue_u_half(du1, 1, &bars[6]);
@@ -467,8 +479,10 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       tc_fence_before();
       __syncthreads();
       if (tid == 0) {
-        bulk_store(uimg + blk0 * 8192, s0, 8192);
-        bulk_store(uimg + (blk0 + 1) * 8192, s1, 8192);
+        if (dbg_ok(sl < n_vslots, p.status)) {
+          bulk_store(uimg + blk0 * 8192, s0, 8192);
+          bulk_store(uimg + (blk0 + 1) * 8192, s1, 8192);
+        }
         bulk_commit();
       }
     };

@@ -78,9 +78,12 @@ typedef enum gdn_dev_status {
   GDN_DEV_CHUNK_OVERFLOW = 2,     /* more chunks than nt_max: the excess is skipped */
   GDN_DEV_BAD_CHUNK_TABLE = 4,    /* caller table names a chunk that does not exist: skipped */
   GDN_DEV_TIMEOUT = 8,            /* a bounded on-chip wait gave up (results invalid) */
-  GDN_DEV_NONFINITE = 16          /* a state or output of the bf16 tensor-core path came out
+  GDN_DEV_NONFINITE = 16,         /* a state or output of the bf16 tensor-core path came out
                                      non-finite: an fp16 operand (state, decayed v_new) left
                                      the fp16 range, or the inputs held inf/NaN */
+  GDN_DEV_DEBUG_INDEX = 32        /* (GDN_DEBUG builds only) an index that addresses global
+                                     memory in the chunk-table, intra or scan kernel was out of
+                                     its range: that access was skipped or redirected */
 } gdn_dev_status;
 
 enum {
@@ -395,6 +398,27 @@ int gdn_conv_front(const gdn_desc* desc, const void* x, const float* conv_w, int
  * exercise that path without a fault or a hang.
  */
 void gdn_test_scan_timeout(uint32_t polls);
+
+/*
+ * 1 when this library was compiled with GDN_DEBUG (libgdn_debug.so), else 0.
+ * The GDN_DEBUG build checks, in the device code of the chunk-table, intra and
+ * scan kernels, every index that addresses a global-memory copy or store of
+ * the bf16 forward path (chunk slot, key and value head, token row) against
+ * its range before the access; an index out of range sets
+ * GDN_DEV_DEBUG_INDEX and the access is skipped (a load is redirected to the
+ * region's first slot so that its transaction count still completes).
+ */
+int gdn_debug_build(void);
+
+/*
+ * Testing hook for the GDN_DEBUG build (no counterpart in the pages; the
+ * normal build ignores it). With on != 0, in the calls that follow the intra
+ * kernel's CTA of chunk slot 0 and key head 0 aims its M image copies at value
+ * slot nt_max * Hv, one past the end of the M region (inside the workspace,
+ * whose next region follows): the device check must catch it, skip the copies
+ * and set GDN_DEV_DEBUG_INDEX. on = 0 (the default) turns it off.
+ */
+void gdn_test_debug_poison(int32_t on);
 
 /* Static description of a gdn_status value. */
 const char* gdn_status_string(int status);
