@@ -15,8 +15,10 @@
 //     A_ij = beta_i exp(G_i - G_j) P_ij (j < i);  T = (I + A)^-1 in place (fp32 diagonal
 //            blocks, off-diagonal blocks on warp MMAs with split operands)
 //     w    = (T diag(beta exp(G))) K   (bf16 T operand; tcgen05, M = 64, N = 128)
-//     u    = (T diag(beta)) V          (T operand split into bf16 hi + lo, two MMA groups
-//                                       into one accumulator)
+//     u    = (T diag(beta)) V          (formed transposed, u^T = V^T (T diag(beta))^T, M = 128
+//                                       value columns, N = 64 tokens; the T operand split
+//                                       into bf16 hi + lo, two MMA groups into one
+//                                       accumulator)
 //     M_ij = exp(G_i - G_j) R_ij (j <= i)   (stored as a bf16 hi/lo pair)
 // (1/||k|| and 1/||q|| enter as fp32 row factors when the L2 norm is on.) The hi/lo
 // split keeps about 16 significant bits where one bf16 rounding would cost ~1e-2 of
@@ -67,7 +69,7 @@ constexpr int LDX = 36;  // fp32 stride of the inverse's scratch (32 rows)
 constexpr uint32_t kX = kAT + 64 * LDT * 4;  // fp32 [32][LDX]: scratch of the inverse
 constexpr uint32_t kTW = 88064;   // bf16 [64][128 B], swizzled: T diag(beta exp(G)) (w operand)
 constexpr uint32_t kVec = kTW + 8192;        // 6 x fp32 [64] row vectors
-constexpr uint32_t kBar = kVec + 6 * 256;    // 7 mbarriers
+constexpr uint32_t kBar = kVec + 6 * 256;    // 6 mbarriers
 constexpr uint32_t kMisc = kBar + 64;        // TMEM base address, failure flag
 constexpr uint32_t kSmemBytes = kMisc + 16 + 1024;  // + room to align the base to 1024
 static_assert(kX + 32 * LDX * 4 <= kTW, "shared-memory layout overlaps");
@@ -77,12 +79,6 @@ static_assert(kWarps == 8, "the triangular inverse is written for eight warps");
 __device__ __forceinline__ uint32_t sw_off(int r, int ch) {
   return (uint32_t)r * 128u + ((uint32_t)(ch ^ (r & 7)) << 4);
 }
-// Byte offset of fp32 element (column j < 32, token i < 64) in a u block stored column-major,
-// [32 columns][64 tokens], with the 32-byte groups of each column swizzled by the column.
-__device__ __forceinline__ uint32_t u_offset(int j, int i) {
-  return (uint32_t)j * 256u + ((uint32_t)((i >> 3) ^ (j & 7)) << 5) + (uint32_t)(i & 7) * 4u;
-}
-
 __device__ __forceinline__ bool resolve(const Params& p, int slot, int& t0, int& L, int& wslot) {
   const int2 e = p.chunk_table[slot];
   if (e.x < 0) return false;  // sentinel: early exit
@@ -142,8 +138,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   float* KR = G + 128;  // 1/||k|| (1 when the norm is off)
   float* FW = G + 192;  // beta exp(G) / ||k||: column factor of the w operand
   float* QR = G + 256;  // 1/||q|| (1 when the norm is off)
-  // mbarriers: 0 k/q landed, 1-2 v buffers landed, 3 [P; R] done, 4 w done, 5 and 6 the
-  // two column halves of u done (one completion per value head for 4-6)
+  // mbarriers: 0 k/q landed, 1-2 v buffers landed, 3 [P; R] done, 4 w done, 5 u done (one
+  // completion per value head for 4 and 5)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sm + kMisc);
   volatile int* fail = reinterpret_cast<volatile int*>(sm + kMisc + 4);
@@ -177,7 +173,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     tmem_relinquish();
   }
   if (tid == 0) {
-    for (int b = 0; b < 7; ++b) mbar_init(&bars[b], 1);
+    for (int b = 0; b < 6; ++b) mbar_init(&bars[b], 1);
     mbar_init_fence();
     *fail = 0;
     mbar_expect_tx(&bars[0], 32768);
@@ -399,23 +395,16 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     }
     fence_async_smem();
     __syncthreads();
-    // TMEM: [P; R] in columns 0..63, w in 128..255, the first half of u in 64..127; the
-    // second half of u reuses w's columns once w has been read out.
-    const uint32_t dw = tmem + 128, du0 = tmem + 64, du1 = tmem + 128;
+    // TMEM: [P; R] in columns 0..63 (lanes 0..127), u^T in 64..127 (lanes 0..127), w in
+    // 128..255 (lanes 32 q .. 32 q + 15 for rows 16 q .. 16 q + 15).
+    const uint32_t dw = tmem + 128, du = tmem + 64;
     const uint32_t vb = sbase + kV + (r & 1) * 16384;
     const uint32_t id_w = idesc_bf16_f32(64, 128, false, true);
-    const uint32_t id_u = idesc_bf16_f32(64, 64, false, true);
-    auto issue_u_half = [&](uint32_t d, int half, uint64_t* bar) {
-      // u[:, 64 half ..] = T_hi V + T_lo V over the value columns of this half; B is the
-      // v tile read MN-major (N = value dim, K = tokens)
-#pragma unroll
-      for (int part = 0; part < 2; ++part)
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-          umma_bf16(d, sdesc_sw128(sbase + kKQ + 8192 + 16384 * part + 32 * ks, 16, 1024),
-                    sdesc_sw128(vb + 8192 * half + 2048 * ks, 8192, 1024), id_u, part > 0 || ks > 0);
-      umma_commit(bar);
-    };
+    // u^T = V^T T_hi^T + V^T T_lo^T: A is the v tile read MN-major (M = the 128 value
+    // columns, K = tokens), B the T_hi and T_lo images (K-major, N = 64 tokens). Row j of
+    // D (TMEM lane j) is value column j, so a thread's TMEM row is one column of the
+    // column-major u image.
+    const uint32_t id_u = idesc_bf16_f32(128, 64, true, false);
     if (tid == 0) {
       tc_fence_after();
       // w = TW K: B is the k tile read MN-major (N = key dim, K = tokens)
@@ -424,7 +413,14 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         umma_bf16(dw, sdesc_sw128(sbase + kTW + 32 * ks, 16, 1024),
                   sdesc_sw128(sbase + kKQ + 2048 * ks, 16384, 1024), id_w, ks > 0);
       umma_commit(&bars[4]);
-      issue_u_half(du0, 0, &bars[5]);
+#pragma unroll
+      for (int part = 0; part < 2; ++part)
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+          umma_bf16(du, sdesc_sw128(vb + 2048 * ks, 8192, 1024),
+                    sdesc_sw128(sbase + kKQ + 8192 + 16384 * part + 32 * ks, 16, 1024), id_u,
+                    part > 0 || ks > 0);
+      umma_commit(&bars[5]);
     }
     wait_or_flag(&bars[4], par, fail);
     tc_fence_after();
@@ -450,50 +446,42 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         }
       }
     }
+    // u^T: value column 32 q + lane (TMEM lane quarter q = warp % 4), tokens 32 th ..
+    // 32 th + 31 (th = warp / 4), into block q of the u image: blocks 0, 1 staged in this
+    // member's V buffer, 2, 3 in the Q halves (the u MMAs have read the tile and the T
+    // images there)
+    wait_or_flag(&bars[5], par, fail);
+    tc_fence_after();
+    auto u_stage = [&](int b) {
+      return b < 2 ? vt + 8192 * b : sm + kKQ + 8192 + 16384 * (b - 2);
+    };
+    {
+      const int q = warp & 3, th = warp >> 2, j = lane;
+      float v[32];
+      tmem_ld32(du + ((uint32_t)(32 * q) << 16) + 32 * th, v);
+      tmem_ld_wait();
+      unsigned char* blk = u_stage(q);
+#pragma unroll
+      for (int gi = 0; gi < 4; ++gi) {  // 8-token group 4 th + gi: 32 bytes, swizzled by j
+        const uint32_t off = (uint32_t)j * 256u + ((uint32_t)((4 * th + gi) ^ (j & 7)) << 5);
+        *reinterpret_cast<float4*>(blk + off) =
+            make_float4(v[8 * gi], v[8 * gi + 1], v[8 * gi + 2], v[8 * gi + 3]);
+        *reinterpret_cast<float4*>(blk + off + 16) =
+            make_float4(v[8 * gi + 4], v[8 * gi + 5], v[8 * gi + 6], v[8 * gi + 7]);
+      }
+    }
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
     if (tid == 0) {
-      if (dbg_ok(sl < n_vslots, p.status))
+      if (dbg_ok(sl < n_vslots, p.status)) {
         bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
-      bulk_commit();
-      tc_fence_after();
-      issue_u_half(du1, 1, &bars[6]);
-    }
-    unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
-    // u blocks (32 columns) of one half from TMEM to two staging tiles, then to global
-    auto u_out = [&](uint32_t d, unsigned char* s0, unsigned char* s1, int blk0) {
-      // rows 16 q .. 16 q + 15 (q = warp % 4); warps w and w + 4 take blocks blk0, blk0 + 1
-      const int i = 16 * (warp & 3) + (lane & 15), b = warp >> 2;
-      {
-        float v[32];
-        tmem_ld32(d + ((uint32_t)(32 * (warp & 3)) << 16) + 32 * b, v);
-        tmem_ld_wait();
-        unsigned char* blk = b ? s1 : s0;
-        if (lane < 16) {  // one column per store: the 16 lanes write 16 tokens of it
+        unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
 #pragma unroll
-          for (int j = 0; j < 32; ++j) *reinterpret_cast<float*>(blk + u_offset(j, i)) = v[j];
-        }
+        for (int b = 0; b < 4; ++b) bulk_store(uimg + b * 8192, u_stage(b), 8192);
       }
-      fence_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      if (tid == 0) {
-        if (dbg_ok(sl < n_vslots, p.status)) {
-          bulk_store(uimg + blk0 * 8192, s0, 8192);
-          bulk_store(uimg + (blk0 + 1) * 8192, s1, 8192);
-        }
-        bulk_commit();
-      }
-    };
-    // blocks 0, 1: staged in the first V half (read by the first u half only) and the
-    // w-operand image; blocks 2, 3: the second V half and the first Q half (T_hi)
-    wait_or_flag(&bars[5], par, fail);
-    tc_fence_after();
-    u_out(du0, vt, sm + kTW, 0);
-    wait_or_flag(&bars[6], par, fail);
-    tc_fence_after();
-    u_out(du1, vt + 8192, sm + kKQ + 8192, 2);
+      bulk_commit();
+    }
     if (tid == 0 && r + 2 < p.HG) {  // this V buffer serves member r + 2 once the copies read it
       bulk_wait_read<0>();
       issue_v(sm, bars, &tmv, hv + 2, t0, r + 2);
