@@ -273,6 +273,7 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.gam = L.gam ? reinterpret_cast<float*>(ws + L.gam) : nullptr;
   p.qrn = l2 ? reinterpret_cast<float*>(ws + L.qrn) : nullptr;
   p.krn = l2 ? reinterpret_cast<float*>(ws + L.krn) : nullptr;
+  p.m_f16 = 1;  // the scan takes M v_new on fp16 operands
   p.out_bf16 = d.out_dtype == GDN_BF16;
   p.stall_polls = scan_stall_polls();
   p.dbg_poison = debug_poison();

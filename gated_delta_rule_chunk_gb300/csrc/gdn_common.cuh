@@ -55,6 +55,8 @@ struct Params {
   uint32_t stall_polls;      // testing hook: > 0 makes the scan wait this many polls on an
                              // event that never happens (its timeout path); 0 normally
   int dbg_poison;            // testing hook of the GDN_DEBUG build (an out-of-range M slot)
+  int m_f16;                 // tensor-core path: the M image as an fp16 hi/lo pair (the
+                             // forward's scan), else a bf16 hi/lo pair (the backward's)
 };
 
 // Parameters of the backward kernels (device pointers; fp32 SIMT arithmetic). Per-slot

@@ -19,10 +19,11 @@
 //                                       value columns, N = 64 tokens; the T operand split
 //                                       into bf16 hi + lo, two MMA groups into one
 //                                       accumulator)
-//     M_ij = exp(G_i - G_j) R_ij (j <= i)   (stored as a bf16 hi/lo pair)
+//     M_ij = exp(G_i - G_j) R_ij (j <= i)   (stored as a hi/lo pair: fp16 halves for the
+//                                           forward's scan, bf16 halves for the backward)
 // (1/||k|| and 1/||q|| enter as fp32 row factors when the L2 norm is on.) The hi/lo
-// split keeps about 16 significant bits where one bf16 rounding would cost ~1e-2 of
-// the output's rms.
+// split keeps about 22 (fp16) or 16 (bf16) significant bits where one bf16 rounding
+// would cost ~1e-2 of the output's rms.
 //
 // The bridge is written as the exact shared-memory images the inter-chunk
 // kernel reads, so that kernel moves each with one bulk copy:
@@ -335,8 +336,13 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
 #pragma unroll
           for (int e = 0; e < 8; ++e) d[e] = (j + e <= i) ? d[e] * v[e] : 0.f;
           uint32_t hi[4], lo[4];
+          if (p.m_f16) {
 #pragma unroll
-          for (int e = 0; e < 4; ++e) split_pack2(d[2 * e], d[2 * e + 1], hi[e], lo[e]);
+            for (int e = 0; e < 4; ++e) split_pack2_f16(d[2 * e], d[2 * e + 1], hi[e], lo[e]);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) split_pack2(d[2 * e], d[2 * e + 1], hi[e], lo[e]);
+          }
           const uint32_t off = sw_off(i, ch);
           *reinterpret_cast<uint4*>(sm + kKQ + 8192 + off) = make_uint4(hi[0], hi[1], hi[2], hi[3]);
           *reinterpret_cast<uint4*>(sm + kKQ + 24576 + off) = make_uint4(lo[0], lo[1], lo[2], lo[3]);

@@ -125,6 +125,16 @@ __device__ __forceinline__ void split_pack2(float x0, float x1, uint32_t& hi, ui
   lo = *reinterpret_cast<const uint32_t*>(&l);
 }
 
+// The same with fp16 halves: x = hi + lo, hi = fp16(x), lo = fp16(x - hi), about 22
+// significant bits within the fp16 range.
+__device__ __forceinline__ void split_pack2_f16(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __half2 h = __floats2half2_rn(x0, x1);
+  const float2 hf = __half22float2(h);
+  const __half2 l = __floats2half2_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&l);
+}
+
 // x = hi + lo with hi = bf16(x) and lo = bf16(x - hi): about 16 significant bits.
 __device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
   hi = __float2bfloat16_rn(x);
