@@ -109,7 +109,7 @@ def uses_tc_path(x):
     return x["dtype"] == "bf16"
 
 
-def survey_stage_bytes(x, out_bytes=2):
+def method_stage_bytes(x, out_bytes=2):
     """Algorithmic bytes of each stage as the method defines its boundary: the intra
     stage reads q, k, v, g and beta and writes w and u (bf16) and the in-chunk gate sums
     G; the scan reads q, k, w, u, G and the initial state and writes out and the final
@@ -824,7 +824,7 @@ def run_gdn(args, ws, rank, local):
         # own fraction uses the bytes the method's stage boundary implies (w and u in bf16
         # between the stages); this implementation's bridge-level bytes and the ncu DRAM
         # count stand beside them.
-        ssb = survey_stage_bytes(x)
+        ssb = method_stage_bytes(x)
         call_gbs = alg_b / (ms / 1000.0) / 1e9
         kernels = {}
         for k in ("intra", "inter"):

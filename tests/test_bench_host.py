@@ -29,7 +29,7 @@ def test_stage_boundary_bytes():
     # (2 MiB); the intra stage reads q, k, v (32 MiB), g and beta (0.5 MiB each) and writes
     # w, u and G. 132.5 MiB (138.9 MB) for the scan.
     x = make_inputs(2)
-    sb = bench.survey_stage_bytes(x)
+    sb = bench.method_stage_bytes(x)
     MiB = 1 << 20
     assert sb["inter"] == 32 * MiB + 64 * MiB + MiB // 2 + 4 * MiB + 32 * MiB
     assert sb["intra"] == 32 * MiB + 32 * MiB + MiB + 64 * MiB + MiB // 2
