@@ -260,6 +260,9 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   int2* table = chunk_indices ? reinterpret_cast<int2*>(chunk_indices)
                               : reinterpret_cast<int2*>(ws + L.chunk_table);
   p.chunk_table = table;
+  p.seq_order = (d.N > 1 && d.N <= kMaxOrderedSeqs)
+                    ? reinterpret_cast<const int32_t*>(ws + L.seq_order)
+                    : nullptr;
   p.G = L.G ? reinterpret_cast<float*>(ws + L.G) : nullptr;
   p.EF = L.EF ? reinterpret_cast<float*>(ws + L.EF) : nullptr;
   p.w = ws + L.w;
@@ -285,7 +288,8 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
                      (!chunk_indices || build_into_caller) ? table : nullptr,
                      const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
-                     p.status, stream, /*zero_status=*/true);  // (no separate memset)
+                     p.status, stream, /*zero_status=*/true,  // (no separate memset)
+                     const_cast<int32_t*>(p.seq_order));
   if (ev) cudaEventRecord(ev[1], stream);
   const bool tc = uses_tc_path(&d);
   if (nt_max > 0) {
@@ -352,6 +356,9 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   int2* table = chunk_indices ? reinterpret_cast<int2*>(chunk_indices)
                               : reinterpret_cast<int2*>(ws + L.chunk_table);
   p.chunk_table = table;
+  p.seq_order = (d.N > 1 && d.N <= kMaxOrderedSeqs)
+                    ? reinterpret_cast<const int32_t*>(ws + L.seq_order)
+                    : nullptr;
   const bool tc = uses_tc_path(&d);
   p.w = ws + L.w; p.u = f32(L.u); p.M = ws + L.M;
   p.G = L.G ? f32(L.G) : nullptr;
@@ -369,7 +376,8 @@ int gdn_chunk_bwd(const gdn_desc* desc, const void* q, const void* k, const void
   launch_chunk_table(cu_seqlens, d.N, d.T, nt_max,
                      (!chunk_indices || build_into_caller) ? table : nullptr,
                      const_cast<int32_t*>(p.chunk_offsets), const_cast<int2*>(p.seq_info),
-                     p.status, stream, /*zero_status=*/true);  // (no separate memset)
+                     p.status, stream, /*zero_status=*/true,  // (no separate memset)
+                     const_cast<int32_t*>(p.seq_order));
   if (tc) {  // the tensor-core forward kernels, storing S and v_new per chunk
     if (nt_max > 0 && !launch_tc_intra(p, stream)) return GDN_ERR_LAUNCH_FAILED;
     if (!launch_tc_inter(p, false, stream)) return GDN_ERR_LAUNCH_FAILED;

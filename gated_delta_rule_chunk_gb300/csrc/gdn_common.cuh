@@ -31,6 +31,8 @@ struct Params {
   const int2* seq_info;      // [N] sanitized (start, length)
   const int32_t* chunk_offsets;  // [N + 1]
   const int2* chunk_table;   // [nt_max] (sequence, ordinal) or (-1, -1)
+  const int32_t* seq_order;  // [N] the sequences longest first (the scan's launch order), or
+                             // null for the given order
   float* G;                  // [nt_max, Hv, 64] in-chunk cumulative log-decay
   float* EF;                 // [nt_max, Hv, 128] exp(G) then exp(G_L - G) (tensor-core path,
                              // scalar gates)
@@ -143,8 +145,8 @@ struct ConvParams {
 // Byte offsets of the workspace regions (each 256-byte aligned), and the extent
 // [begin, end) of every region in order (for the guard-band check of the tests).
 struct WsLayout {
-  size_t status, seq_info, chunk_offsets, chunk_table, G, EF, w, u, M, k16, qimg, q16, qt, kt,
-      gam, qrn, krn, total;
+  size_t status, seq_info, chunk_offsets, chunk_table, seq_order, G, EF, w, u, M, k16, qimg,
+      q16, qt, kt, gam, qrn, krn, total;
   static constexpr int kMaxRegions = 16;
   int nreg;
   size_t rbeg[kMaxRegions], rend[kMaxRegions];
@@ -175,6 +177,7 @@ inline WsLayout ws_layout(int T, int N, int H, int Hv, int nt_max, bool tc_path,
   L.seq_info = take(sizeof(int2) * (size_t)N);
   L.chunk_offsets = take(sizeof(int32_t) * (size_t)(N + 1));
   L.chunk_table = take(sizeof(int2) * (size_t)nt_max);
+  L.seq_order = take(sizeof(int32_t) * (size_t)N);
   const size_t slots = (size_t)nt_max * (size_t)Hv;
   L.G = tc_path ? take(sizeof(float) * slots * kChunk) : 0;
   L.EF = (tc_path && !channel_gates) ? take(sizeof(float) * slots * 2 * kChunk) : 0;
@@ -265,9 +268,11 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 // Kernel launchers (one translation unit each).
+// Sequence counts up to which the chunk-table kernel also writes the longest-first order.
+constexpr int kMaxOrderedSeqs = 1024;
 void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,
                         int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s,
-                        bool zero_status = false);
+                        bool zero_status = false, int32_t* seq_order = nullptr);
 void launch_l2norm(const void* q, const void* k, bool bf16, int T, int H, int D, float eps,
                    float* qrn, float* krn, cudaStream_t s);
 bool launch_gen_intra(const Params& p, int D, bool channel_gates, bool bf16_inputs, cudaStream_t s);

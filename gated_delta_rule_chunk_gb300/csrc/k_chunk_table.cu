@@ -11,7 +11,8 @@
 // clamped to [0, T] and raised to the largest entry before it (a prefix maximum), so
 // sequence n is [max(c_0..c_n), max(c_0..c_n+1)) -- never overlapping another, empty
 // where the input decreases -- and count its chunks, (2) exclusive-scan the counts
-// into chunk_offsets, (3) for every slot binary-search the sequence that owns it.
+// into chunk_offsets, (3) for every slot binary-search the sequence that owns it, (4) for
+// up to kMaxOrderedSeqs sequences, rank them by chunk count, longest first.
 #include "gdn_common.cuh"
 
 namespace gdn {
@@ -19,8 +20,10 @@ namespace gdn {
 __global__ void __launch_bounds__(1024)
 chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
                    int2* __restrict__ table, int32_t* __restrict__ offsets,
-                   int2* __restrict__ seq_info, int32_t* status, bool zero_status) {
+                   int2* __restrict__ seq_info, int32_t* status, bool zero_status,
+                   int32_t* __restrict__ seq_order) {
   __shared__ int warp_incl[32];
+  __shared__ int cnt_s[kMaxOrderedSeqs];  // chunk counts, for the longest-first order
   __shared__ int warp_max[32];
   __shared__ int carry_s, carry_max_s;
   pdl_release();  // the intra kernel may be scheduled now; it waits for this grid's writes
@@ -64,6 +67,7 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
       const int len = e - s;
       cnt = (len + kChunk - 1) / kChunk;
       if (seq_info) seq_info[n] = make_int2(s, len);
+      if (n < kMaxOrderedSeqs) cnt_s[n] = cnt;
     }
     __syncthreads();
     if (tid == 1023) carry_max_s = pm;
@@ -97,7 +101,18 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
     if (total > nt_max) set_status(status, GDN_DEV_CHUNK_OVERFLOW);
   }
   if (bad) set_status(status, GDN_DEV_BAD_CU_SEQLENS);
-  __syncthreads();  // offsets[] (global) visible to the whole block
+  __syncthreads();  // offsets[] (global) and cnt_s visible to the whole block
+  if (seq_order && N <= kMaxOrderedSeqs && tid < N) {
+    // (4) the sequences by chunk count, longest first (ties by index): the scan's CTAs of
+    // long sequences start first, so that the short ones fill the SMs behind them
+    const int mine = cnt_s[tid];
+    int rank = 0;
+    for (int m = 0; m < N; ++m) {
+      const int o = cnt_s[m];
+      rank += (o > mine) || (o == mine && m < tid);
+    }
+    if (dbg_ok(rank < N, status)) seq_order[rank] = tid;
+  }
   if (!table) return;
   for (int s = tid; s < nt_max; s += 1024) {
     int2 r = make_int2(-1, -1);
@@ -116,9 +131,9 @@ chunk_table_kernel(const int32_t* __restrict__ cu, int N, int T, int nt_max,
 
 void launch_chunk_table(const int32_t* cu, int N, int T, int nt_max, int2* table,
                         int32_t* offsets, int2* seq_info, int32_t* status, cudaStream_t s,
-                        bool zero_status) {
+                        bool zero_status, int32_t* seq_order) {
   chunk_table_kernel<<<1, 1024, 0, s>>>(cu, N, T, nt_max, table, offsets, seq_info, status,
-                                        zero_status);
+                                        zero_status, N <= kMaxOrderedSeqs ? seq_order : nullptr);
 }
 
 }  // namespace gdn

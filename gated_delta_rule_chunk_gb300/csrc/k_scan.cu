@@ -161,10 +161,20 @@ scan_kernel(const __grid_constant__ Params p) {
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kBar);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kMisc);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int n = blockIdx.x, hv = blockIdx.y, c0 = blockIdx.z * BV;
+  // Grid (see launch_scan): one sequence: x = value head, y = value block; several: x =
+  // (value block, value head), value block fastest, so that the CTAs that share a head's
+  // images (then a sequence's) start together and meet in L2, and y + 65535 z = the
+  // sequence's rank in the longest-first order (or its index), so that long sequences
+  // start first.
+  const int nvb = p.D / BV;
+  const bool one = p.N == 1;
+  const int vb = one ? (int)blockIdx.y : (int)blockIdx.x % nvb;
+  const int hv = one ? (int)blockIdx.x : (int)blockIdx.x / nvb;
+  const int rank = one ? 0 : (int)(blockIdx.z * 65535 + blockIdx.y);
+  if (rank >= p.N) return;  // (uniform over the CTA)
+  const int c0 = vb * BV;
   const int h = hv / p.HG;
   const int g = lane >> 2, c2 = 2 * (lane & 3);
-  const size_t state_base = ((size_t)n * p.Hv + hv) * p.D * p.D;
   const bool has_out = p.out != nullptr;
 
   if (tid == 0) {
@@ -177,6 +187,8 @@ scan_kernel(const __grid_constant__ Params p) {
   }
   __syncthreads();
   pdl_wait();  // everything below reads what the chunk-table and intra kernels wrote
+  const int n = p.seq_order ? p.seq_order[rank] : rank;
+  const size_t state_base = ((size_t)n * p.Hv + hv) * p.D * p.D;
   const SeqView sv = seq_view(p, n);
   int nch = (sv.len + kChunk - 1) / kChunk;
   if (sv.first_slot + nch > p.nt_max) {
@@ -518,7 +530,7 @@ scan_kernel(const __grid_constant__ Params p) {
       bulk_load(st + rK, static_cast<const unsigned char*>(p.k16) + (wslot * p.H + h) * 16384,
                 16384, full);
       bulk_load(st + rU, reinterpret_cast<const unsigned char*>(p.u) + sl * 32768 +
-                             blockIdx.z * 8192, 8192, full);
+                             vb * 8192, 8192, full);
       bulk_load(st + rE, p.EF + sl * 128, 512, full);
     };
     auto issue_qm = [&](int cc) {
@@ -568,8 +580,10 @@ scan_kernel(const __grid_constant__ Params p) {
 
 bool launch_scan(const Params& p, cudaStream_t s) {
   ensure_smem_limit((const void*)scan_kernel, (int)kSmemBytes);
-  return launch_pdl(scan_kernel, dim3(p.N, p.Hv, p.D / BV), dim3(kThreads), kSmemBytes, s,
-                    p) == cudaSuccess;
+  const int nvb = p.D / BV;
+  const dim3 grid = p.N == 1 ? dim3(p.Hv, nvb, 1)
+                             : dim3(p.Hv * nvb, p.N < 65535 ? p.N : 65535, (p.N + 65534) / 65535);
+  return launch_pdl(scan_kernel, grid, dim3(kThreads), kSmemBytes, s, p) == cudaSuccess;
 }
 
 }  // namespace gdn
