@@ -40,7 +40,7 @@
 // the warps never wait on scattered global stores; tiles come in by TMA tensor maps
 // (128-byte swizzle), which are also the tensor-core operand layouts.
 //
-// One CTA of 8 warps per (key head, chunk); ~99 KB of shared memory and 256 TMEM
+// One CTA of 8 warps per (key head, chunk); ~113 KB of shared memory and 256 TMEM
 // columns, so two CTAs share an SM and hide each other's latency. Warps w and w + 4
 // read the same TMEM lane quarter and split its columns.
 #include <cuda.h>
@@ -65,14 +65,16 @@ constexpr int kMStoreThread = kThreads - 32;  // issues the M image copies (warp
 constexpr uint32_t kKQ = 0;       // [K_h0 | Q_h0 | K_h1 | Q_h1], each [64 rows][128 B], swizzled;
                                   // the Q halves later hold the M image and the u operands
 constexpr uint32_t kV = 32768;    // two buffers of [V_h0 | V_h1]
-constexpr uint32_t kAT = 65536;   // fp32 [64][LDT]: A, then T; staging of the k and w images
+constexpr uint32_t kAT = 65536;   // fp32 [64][LDT]: A, then T; staging of the w image
 constexpr int LDX = 36;  // fp32 stride of the inverse's scratch (32 rows)
 constexpr uint32_t kX = kAT + 64 * LDT * 4;  // fp32 [32][LDX]: scratch of the inverse
 constexpr uint32_t kTW = 88064;   // bf16 [64][128 B], swizzled: T diag(beta exp(G)) (w operand)
 constexpr uint32_t kVec = kTW + 8192;        // 6 x fp32 [64] row vectors
 constexpr uint32_t kBar = kVec + 6 * 256;    // 6 mbarriers
 constexpr uint32_t kMisc = kBar + 64;        // TMEM base address, failure flag
-constexpr uint32_t kSmemBytes = kMisc + 16 + 1024;  // + room to align the base to 1024
+constexpr uint32_t kST = kMisc + 16;         // 16 KB staging: the k image, then u blocks 2, 3
+constexpr uint32_t kSmemBytes = kST + 16384 + 1024;  // + room to align the base to 1024
+static_assert(2 * (kSmemBytes + 1024) <= 233472, "two CTAs no longer share an SM");
 static_assert(kX + 32 * LDX * 4 <= kTW, "shared-memory layout overlaps");
 static_assert(kWarps == 8, "the triangular inverse is written for eight warps");
 
@@ -274,14 +276,14 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     }
   };
   unsigned char* const qstage = sm + kV + 16384;
-  f16_image(sm + kKQ, sm + kAT, KR);
+  f16_image(sm + kKQ, sm + kST, KR);
   if (p.q16) f16_image(sm + kKQ + 8192, qstage, QR);
   fence_async_smem();
   __syncthreads();
   if (tid == 0) {
     const size_t img = ((size_t)wslot * p.H + h) * 64 * kDk * 2;
     if (dbg_ok(wslot < p.nt_max && h < p.H, p.status)) {
-      bulk_store(static_cast<unsigned char*>(p.k16) + img, sm + kAT, 16384);
+      bulk_store(static_cast<unsigned char*>(p.k16) + img, sm + kST, 16384);
       if (p.q16) bulk_store(static_cast<unsigned char*>(p.q16) + img, qstage, 16384);
     }
     bulk_commit();
@@ -292,10 +294,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const size_t sl = (size_t)wslot * p.Hv + hv;
     const uint32_t par = (uint32_t)(r & 1);  // parity of this member's MMA barriers
     if (warp == 0) gates(r);  // (member 0's g and beta were loaded during the setup)
-    if (tid == 0) {
-      bulk_wait_read<0>();  // staging regions read out by the previous copies
-      if (r == 0 && v1_late) issue_v(sm, bars, &tmv, hv + 1, t0, 1);  // into the q staging
-    }
+    // the previous member's w image read out of A/T (its u copies may still be reading)
+    if (tid == 0 && r > 0) bulk_wait_read<1>();
     __syncthreads();
     if (r == 0) wait_or_flag(&bars[3], 0, fail);
     tc_fence_after();
@@ -375,6 +375,12 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       zero_tail(vt + 8192, L, tid);
     }
     if (tid == kMStoreThread) bulk_wait_read<0>();  // the M image read out of the Q halves
+    if (tid == 0) {
+      // the k image (member 0) or the previous member's u blocks read out of the staging
+      // region, and the q image out of the second V buffer
+      bulk_wait_read<0>();
+      if (r == 0 && v1_late) issue_v(sm, bars, &tmv, hv + 1, t0, 1);  // into the q staging
+    }
     __syncthreads();
     // T operand images: T diag(beta exp(G) / ||k||) (bf16) and T diag(beta) as a bf16
     // hi/lo pair (hi into the first Q half, lo into the second).
@@ -459,7 +465,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     wait_or_flag(&bars[5], par, fail);
     tc_fence_after();
     auto u_stage = [&](int b) {
-      return b < 2 ? vt + 8192 * b : sm + kKQ + 8192 + 16384 * (b - 2);
+      return b < 2 ? vt + 8192 * b : sm + kST + 8192 * (b - 2);
     };
     {
       const int q = warp & 3, th = warp >> 2, j = lane;
@@ -479,9 +485,11 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {
-      if (dbg_ok(sl < n_vslots, p.status)) {
-        bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
+    if (tid == 0) {  // two groups: the w image (A/T is rewritten first), then the u blocks
+      const bool ok = dbg_ok(sl < n_vslots, p.status);
+      if (ok) bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
+      bulk_commit();
+      if (ok) {
         unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
 #pragma unroll
         for (int b = 0; b < 4; ++b) bulk_store(uimg + b * 8192, u_stage(b), 8192);
