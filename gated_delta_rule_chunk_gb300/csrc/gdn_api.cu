@@ -277,6 +277,8 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.qrn = l2 ? reinterpret_cast<float*>(ws + L.qrn) : nullptr;
   p.krn = l2 ? reinterpret_cast<float*>(ws + L.krn) : nullptr;
   p.m_f16 = 1;  // the scan takes M v_new on fp16 operands
+  p.cu = cu_seqlens;
+  p.early_one = d.N == 1 && (!chunk_indices || build_into_caller);
   p.out_bf16 = d.out_dtype == GDN_BF16;
   p.stall_polls = scan_stall_polls();
   p.dbg_poison = debug_poison();

@@ -38,6 +38,10 @@ struct Params {
                              // scalar gates)
   void* w;                   // [nt_max, Hv, 64, dk]
   float* u;                  // [nt_max, Hv, 64, dv]
+  const int32_t* cu;         // cu_seqlens as given (or null), read only when early_one is set
+  int early_one;             // one sequence whose chunk table this call builds: the intra
+                             // kernel maps slot s to chunk s and requests its tiles before
+                             // the table is written
   void* M;                   // [nt_max, Hv, 64, 64] (or hi/lo pair) decay-masked q.k
   void* k16;                 // fp16 images of the chunk's k tile (tensor-core path): per
                              // [nt_max, H] key head, or per [nt_max, Hv] value head with

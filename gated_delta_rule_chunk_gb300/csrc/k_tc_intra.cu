@@ -150,10 +150,25 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   // Key head fastest in the grid: CTAs resident together read all heads of the same
   // tokens (contiguous rows of q, k and v) rather than one head of many chunks.
   const int h = blockIdx.x;
-  pdl_wait();     // the chunk table (and the L2-norm factors) are written
-  pdl_release();  // the inter kernel may take SMs as this grid drains
-  int t0, L, wslot;
-  if (!resolve(p, blockIdx.y, t0, L, wslot)) return;  // uniform over the CTA
+  int t0 = 0, L = 0, wslot = 0;
+  // One sequence whose table this call builds: slot s is chunk s of the sequence, whose
+  // bounds are sanitized here exactly as the chunk-table kernel does, so the tiles (the
+  // caller's inputs) are requested while that kernel still runs. Other slots are sentinels.
+  bool early = false;
+  if (p.early_one) {
+    const int s0 = p.cu ? min(max(p.cu[0], 0), p.T) : 0;
+    const int e0 = p.cu ? max(min(max(p.cu[1], 0), p.T), s0) : p.T;
+    const int nch = (e0 - s0 + kChunk - 1) / kChunk;
+    if ((int)blockIdx.y >= nch) return;  // (the table holds a sentinel there)
+    early = true;
+    t0 = s0 + kChunk * (int)blockIdx.y;
+    L = min(kChunk, e0 - t0);
+    wslot = (int)blockIdx.y;
+  } else {
+    pdl_wait();     // the chunk table (and the L2-norm factors) are written
+    pdl_release();  // the inter kernel may take SMs as this grid drains
+    if (!resolve(p, blockIdx.y, t0, L, wslot)) return;  // uniform over the CTA
+  }
   // The q image is staged in the second V buffer, whose tile is loaded once the image has
   // been read out.
   const bool v1_late = p.q16 != nullptr && p.HG > 1;
@@ -197,6 +212,14 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (early) {
+    pdl_wait();  // the status word is cleared and the table written from here on
+    pdl_release();
+    if (tid == 0) {  // cross-check: the table maps slot s to chunk s of sequence 0
+      const int2 e = p.chunk_table[blockIdx.y];
+      if (e.x != 0 || e.y != (int)blockIdx.y) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
+    }
+  }
 
   // Gates of group member r and their in-chunk inclusive cumsum (warp 0, 2 rows per lane).
   auto gates = [&](int r) {
@@ -436,6 +459,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     }
     wait_or_flag(&bars[4], par, fail);
     tc_fence_after();
+    const bool bridge_ok = dbg_ok(sl < n_vslots, p.status);
     {  // w rows 16 q .. 16 q + 15 (TMEM lanes 32 q .., q = warp % 4), bf16, into the A/T
        // region; warps w and w + 4 take column blocks 0-1 and 2-3
       const int i = 16 * (warp & 3) + (lane & 15);
@@ -458,10 +482,18 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         }
       }
     }
+    // the w image leaves while the u^T rows are read out (its own bulk group: the next
+    // member's A overwrites the A/T region once it has been read)
+    fence_async_smem();
+    __syncthreads();
+    if (tid == 0) {
+      if (bridge_ok)
+        bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
+      bulk_commit();
+    }
     // u^T: value column 32 q + lane (TMEM lane quarter q = warp % 4), tokens 32 th ..
     // 32 th + 31 (th = warp / 4), into block q of the u image: blocks 0, 1 staged in this
-    // member's V buffer, 2, 3 in the Q halves (the u MMAs have read the tile and the T
-    // images there)
+    // member's V buffer (the u MMAs have read the tile), 2, 3 in the staging region
     wait_or_flag(&bars[5], par, fail);
     tc_fence_after();
     auto u_stage = [&](int b) {
@@ -485,11 +517,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     fence_async_smem();
     tc_fence_before();
     __syncthreads();
-    if (tid == 0) {  // two groups: the w image (A/T is rewritten first), then the u blocks
-      const bool ok = dbg_ok(sl < n_vslots, p.status);
-      if (ok) bulk_store(static_cast<unsigned char*>(p.w) + sl * 64 * kDk * 2, sm + kAT, 16384);
-      bulk_commit();
-      if (ok) {
+    if (tid == 0) {
+      if (bridge_ok) {
         unsigned char* uimg = reinterpret_cast<unsigned char*>(p.u + sl * 64 * kDv);
 #pragma unroll
         for (int b = 0; b < 4; ++b) bulk_store(uimg + b * 8192, u_stage(b), 8192);

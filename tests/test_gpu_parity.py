@@ -237,6 +237,33 @@ def test_caller_chunk_table_read_and_build():
     assert built.cpu().tolist() == ref_t
 
 
+def test_one_sequence_tiles_requested_before_the_table():
+    """One sequence whose table the call builds: the intra kernel maps slot s to chunk s
+    and requests the tiles before the chunk table is written. A caller table (read, not
+    built) takes the ordinary path; both give the same bits, for a start inside a chunk.
+    Reversed boundaries give no rows: the status reports them, no output row is written
+    and the final state is the initial one."""
+    x = make_inputs(2, seed=17, T=500, H=2, Hv=4)
+    d = to_dev(x)
+    args = (d["q"], d["k"], d["v"], d["g"], d["beta"], x["scale"], d["initial_state"])
+    cu = [37, 470]
+    cu_d = torch.tensor(cu, dtype=torch.int32, device="cuda")
+    o1, f1 = B.gdn_chunk_fwd(*args, cu_d, out_dtype=torch.float32)
+    ref_t, _, _ = build_chunk_table(cu, x["nt_max"])
+    table = torch.tensor(ref_t, dtype=torch.int32, device="cuda")
+    o2, f2 = B.gdn_chunk_fwd(*args, cu_d, chunk_indices=table, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert torch.equal(o1[37:470], o2[37:470]) and torch.equal(f1, f2)
+    o_ref, f_ref = run_oracle(dict(x, cu_seqlens=torch.tensor(cu, dtype=torch.int32)))
+    assert ratio(o1[37:470], o_ref[37:470]) <= TOL_BF16 and ratio(f1, f_ref) <= TOL_BF16
+    out = torch.full((x["T"], x["Hv"], 128), 7.0, device="cuda")
+    fin = torch.full_like(d["initial_state"], 3.0)
+    rev = torch.tensor([300, 100], dtype=torch.int32, device="cuda")
+    _, _, desc, _ = B.gdn_chunk_fwd(*args, rev, out=out, final_state=fin, return_desc=True)
+    assert B.gdn_read_status(desc) & 1
+    assert bool(torch.all(out == 7.0)) and torch.equal(fin, d["initial_state"])
+
+
 def test_status_word_reports_bad_inputs_without_fault():
     x = make_inputs(2, seed=1, T=256, H=2, Hv=2)
     d = to_dev(x)
