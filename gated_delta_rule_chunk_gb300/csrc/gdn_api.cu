@@ -279,6 +279,12 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
   p.m_f16 = 1;  // the scan takes M v_new on fp16 operands
   p.cu = cu_seqlens;
   p.early_one = d.N == 1 && (!chunk_indices || build_into_caller);
+  {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
+      p.pf_ahead = (2 * sms + d.H - 1) / d.H;  // two intra CTAs per SM, key head fastest
+  }
   p.out_bf16 = d.out_dtype == GDN_BF16;
   p.stall_polls = scan_stall_polls();
   p.dbg_poison = debug_poison();

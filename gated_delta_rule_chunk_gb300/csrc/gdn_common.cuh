@@ -39,6 +39,9 @@ struct Params {
   void* w;                   // [nt_max, Hv, 64, dk]
   float* u;                  // [nt_max, Hv, 64, dv]
   const int32_t* cu;         // cu_seqlens as given (or null), read only when early_one is set
+  int pf_ahead;              // intra kernel: > 0 prefetches into L2 the tiles of the chunk
+                             // slot this many ahead (about where the CTA that next takes its
+                             // SM will be)
   int early_one;             // one sequence whose chunk table this call builds: the intra
                              // kernel maps slot s to chunk s and requests its tiles before
                              // the table is written

@@ -220,6 +220,35 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       if (e.x != 0 || e.y != (int)blockIdx.y) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
     }
   }
+  if (tid == kMStoreThread && p.pf_ahead > 0) {
+    // L2 prefetch of the tiles of the slot about one wave ahead, which the CTA that next
+    // takes this SM is likely to hold, so that its loads hit L2
+    const int s1 = (int)blockIdx.y + p.pf_ahead;
+    int t1 = -1;
+    if (s1 < p.nt_max) {
+      const int2 e = p.chunk_table[s1];
+      if (e.x >= 0 && e.x < p.N) {
+        const SeqView sv1 = seq_view(p, e.x);
+        if (e.y >= 0 && kChunk * e.y < sv1.len) t1 = sv1.start + kChunk * e.y;
+      }
+    }
+    if (t1 >= 0) {
+#pragma unroll 1
+      for (int x = 0; x < p.D; x += 64) {  // (a head of 64 has one half)
+        tma_prefetch_3d(&tmk, x, h, t1);
+        tma_prefetch_3d(&tmq, x, h, t1);
+#pragma unroll 1
+        for (int r = 0; r < p.HG; ++r) tma_prefetch_3d(&tmv, x, h * p.HG + r, t1);
+      }
+      const int rows = min(kChunk, p.T - t1);
+      const uint32_t gb = (uint32_t)(rows * p.Hv * 4) & ~15u;
+      const size_t go = (size_t)t1 * p.Hv;
+      if (h == 0 && gb > 0 && ((go * 4) & 15) == 0) {  // every head's gates of those rows
+        bulk_prefetch_l2(p.g + go, gb);
+        bulk_prefetch_l2(p.beta + go, gb);
+      }
+    }
+  }
 
   // Gates of group member r and their in-chunk inclusive cumsum (warp 0, 2 rows per lane).
   auto gates = [&](int r) {
