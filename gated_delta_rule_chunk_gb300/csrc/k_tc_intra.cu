@@ -159,7 +159,10 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const int s0 = p.cu ? min(max(p.cu[0], 0), p.T) : 0;
     const int e0 = p.cu ? max(min(max(p.cu[1], 0), p.T), s0) : p.T;
     const int nch = (e0 - s0 + kChunk - 1) / kChunk;
-    if ((int)blockIdx.y >= nch) return;  // (the table holds a sentinel there)
+    if ((int)blockIdx.y >= nch) {  // (the table holds a sentinel there)
+      pdl_wait();  // no CTA of this grid ends before the chunk-table kernel: the scan reads
+      return;      // what that kernel wrote once this grid is done
+    }
     early = true;
     t0 = s0 + kChunk * (int)blockIdx.y;
     L = min(kChunk, e0 - t0);
