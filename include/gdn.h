@@ -76,7 +76,10 @@ typedef enum gdn_status {
 typedef enum gdn_dev_status {
   GDN_DEV_BAD_CU_SEQLENS = 1,     /* cu_seqlens not monotone or beyond T: clamped */
   GDN_DEV_CHUNK_OVERFLOW = 2,     /* more chunks than nt_max: the excess is skipped */
-  GDN_DEV_BAD_CHUNK_TABLE = 4,    /* caller table names a chunk that does not exist: skipped */
+  GDN_DEV_BAD_CHUNK_TABLE = 4,    /* caller table names a chunk that does not exist: skipped;
+                                     also set if the table built for one sequence disagrees
+                                     with the slot = chunk mapping the intra kernel assumes
+                                     when it requests its tiles early (an internal error) */
   GDN_DEV_TIMEOUT = 8,            /* a bounded on-chip wait gave up (results invalid) */
   GDN_DEV_NONFINITE = 16,         /* a state or output of the bf16 tensor-core path came out
                                      non-finite: an fp16 operand (state, decayed v_new) left
