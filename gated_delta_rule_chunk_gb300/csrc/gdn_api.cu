@@ -284,6 +284,15 @@ int gdn_chunk_fwd(const gdn_desc* desc, const void* q, const void* k, const void
     if (cudaGetDevice(&dev) == cudaSuccess &&
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && sms > 0)
       p.pf_ahead = (2 * sms + d.H - 1) / d.H;  // two intra CTAs per SM, key head fastest
+    // The intra grid's (key head, slot) CTAs fill 2 x SMs places per wave; when the last
+    // wave is partial, its slots are split by value-head halves so that it ends sooner.
+    if (sms > 0 && p.HG % 2 == 0) {
+      const long items = (long)d.H * nt_max, places = 2L * sms, tail = items % places;
+      if (items > places && tail > 0) {
+        const int ns = (int)((tail + d.H - 1) / d.H);
+        if (nt_max + ns <= 65535) p.split_slots = ns;
+      }
+    }
   }
   p.out_bf16 = d.out_dtype == GDN_BF16;
   p.stall_polls = scan_stall_polls();

@@ -42,6 +42,9 @@ struct Params {
   int pf_ahead;              // intra kernel: > 0 prefetches into L2 the tiles of the chunk
                              // slot this many ahead (about where the CTA that next takes its
                              // SM will be)
+  int split_slots;           // intra kernel: the last split_slots chunk slots are each taken
+                             // by two CTAs, one per half of the key head's value heads (the
+                             // grid's last, partial wave in smaller pieces); 0 for none
   int early_one;             // one sequence whose chunk table this call builds: the intra
                              // kernel maps slot s to chunk s and requests its tiles before
                              // the table is written

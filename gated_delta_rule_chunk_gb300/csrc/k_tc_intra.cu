@@ -150,6 +150,16 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   // Key head fastest in the grid: CTAs resident together read all heads of the same
   // tokens (contiguous rows of q, k and v) rather than one head of many chunks.
   const int h = blockIdx.x;
+  // Chunk slot and the value heads of the group this CTA takes: all of them, or for the
+  // last split_slots slots one half (two CTAs per slot, adjacent in the grid).
+  int slot = (int)blockIdx.y, r_begin = 0, nr = p.HG;
+  if (slot >= p.nt_max - p.split_slots) {
+    const int j = slot - (p.nt_max - p.split_slots);
+    slot = p.nt_max - p.split_slots + (j >> 1);
+    nr = p.HG >> 1;
+    r_begin = (j & 1) * nr;
+  }
+  const bool writes_img = r_begin == 0;  // the k and q images: once per (slot, key head)
   int t0 = 0, L = 0, wslot = 0;
   // One sequence whose table this call builds: slot s is chunk s of the sequence, whose
   // bounds are sanitized here exactly as the chunk-table kernel does, so the tiles (the
@@ -159,22 +169,22 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const int s0 = p.cu ? min(max(p.cu[0], 0), p.T) : 0;
     const int e0 = p.cu ? max(min(max(p.cu[1], 0), p.T), s0) : p.T;
     const int nch = (e0 - s0 + kChunk - 1) / kChunk;
-    if ((int)blockIdx.y >= nch) {  // (the table holds a sentinel there)
+    if (slot >= nch) {  // (the table holds a sentinel there)
       pdl_wait();  // no CTA of this grid ends before the chunk-table kernel: the scan reads
       return;      // what that kernel wrote once this grid is done
     }
     early = true;
-    t0 = s0 + kChunk * (int)blockIdx.y;
+    t0 = s0 + kChunk * slot;
     L = min(kChunk, e0 - t0);
-    wslot = (int)blockIdx.y;
+    wslot = slot;
   } else {
     pdl_wait();     // the chunk table (and the L2-norm factors) are written
     pdl_release();  // the inter kernel may take SMs as this grid drains
-    if (!resolve(p, blockIdx.y, t0, L, wslot)) return;  // uniform over the CTA
+    if (!resolve(p, slot, t0, L, wslot)) return;  // uniform over the CTA
   }
   // The q image is staged in the second V buffer, whose tile is loaded once the image has
   // been read out.
-  const bool v1_late = p.q16 != nullptr && p.HG > 1;
+  const bool v1_late = writes_img && p.q16 != nullptr && nr > 1;
   const size_t n_vslots = (size_t)p.nt_max * p.Hv;  // value slots of the bridge regions
 
   // g and beta of group member r (warp 0, 2 rows per lane), loaded one member ahead of
@@ -189,7 +199,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     bn1 = lane + 32 < L ? p.beta[b1] : 0.f;
   };
   if (warp == 0) {
-    load_gates(0);
+    load_gates(r_begin);
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -202,8 +212,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     tma_load_3d(sm + kKQ + 16384, &tmk, 64, h, t0, &bars[0]);
     tma_load_3d(sm + kKQ + 8192, &tmq, 0, h, t0, &bars[0]);
     tma_load_3d(sm + kKQ + 24576, &tmq, 64, h, t0, &bars[0]);
-    for (int r = 0; r < min(p.HG, v1_late ? 1 : 2); ++r)
-      issue_v(sm, bars, &tmv, h * p.HG + r, t0, r);
+    for (int rl = 0; rl < min(nr, v1_late ? 1 : 2); ++rl)
+      issue_v(sm, bars, &tmv, h * p.HG + r_begin + rl, t0, rl);
   }
   if (tid < 64) KR[tid] = (tid < L && p.krn) ? p.krn[(size_t)(t0 + tid) * p.H + h] : 1.f;
   else if (tid < 128)
@@ -219,14 +229,14 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     pdl_wait();  // the status word is cleared and the table written from here on
     pdl_release();
     if (tid == 0) {  // cross-check: the table maps slot s to chunk s of sequence 0
-      const int2 e = p.chunk_table[blockIdx.y];
-      if (e.x != 0 || e.y != (int)blockIdx.y) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
+      const int2 e = p.chunk_table[slot];
+      if (e.x != 0 || e.y != slot) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
     }
   }
   if (tid == kMStoreThread && p.pf_ahead > 0) {
     // L2 prefetch of the tiles of the slot about one wave ahead, which the CTA that next
     // takes this SM is likely to hold, so that its loads hit L2
-    const int s1 = (int)blockIdx.y + p.pf_ahead;
+    const int s1 = slot + p.pf_ahead;
     int t1 = -1;
     if (s1 < p.nt_max) {
       const int2 e = p.chunk_table[s1];
@@ -258,7 +268,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     const size_t sl = (size_t)wslot * p.Hv + h * p.HG + r;
     float g0 = gn0, g1 = gn1;
     const float be0 = bn0, be1 = bn1;
-    if (r + 1 < p.HG) load_gates(r + 1);
+    if (r + 1 < r_begin + nr) load_gates(r + 1);
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y0 = __shfl_up_sync(0xffffffffu, g0, o);
@@ -331,28 +341,29 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     }
   };
   unsigned char* const qstage = sm + kV + 16384;
-  f16_image(sm + kKQ, sm + kST, KR);
-  if (p.q16) f16_image(sm + kKQ + 8192, qstage, QR);
+  if (writes_img) f16_image(sm + kKQ, sm + kST, KR);
+  if (writes_img && p.q16) f16_image(sm + kKQ + 8192, qstage, QR);
   fence_async_smem();
   __syncthreads();
   if (tid == 0) {
     const size_t img = ((size_t)wslot * p.H + h) * 64 * kDk * 2;
-    if (dbg_ok(wslot < p.nt_max && h < p.H, p.status)) {
+    if (writes_img && dbg_ok(wslot < p.nt_max && h < p.H, p.status)) {
       bulk_store(static_cast<unsigned char*>(p.k16) + img, sm + kST, 16384);
       if (p.q16) bulk_store(static_cast<unsigned char*>(p.q16) + img, qstage, 16384);
     }
     bulk_commit();
   }
 
-  for (int r = 0; r < p.HG; ++r) {
+  for (int rl = 0; rl < nr; ++rl) {
+    const int r = r_begin + rl;  // (rl picks the V buffer and the barrier parities)
     const int hv = h * p.HG + r;
     const size_t sl = (size_t)wslot * p.Hv + hv;
-    const uint32_t par = (uint32_t)(r & 1);  // parity of this member's MMA barriers
+    const uint32_t par = (uint32_t)(rl & 1);  // parity of this member's MMA barriers
     if (warp == 0) gates(r);  // (member 0's g and beta were loaded during the setup)
     // the previous member's w image read out of A/T (its u copies may still be reading)
-    if (tid == 0 && r > 0) bulk_wait_read<1>();
+    if (tid == 0 && rl > 0) bulk_wait_read<1>();
     __syncthreads();
-    if (r == 0) wait_or_flag(&bars[3], 0, fail);
+    if (rl == 0) wait_or_flag(&bars[3], 0, fail);
     tc_fence_after();
 
     // A (TMEM lane quarters 0-1, rows of P) into A/T; M hi/lo image (quarters 2-3, rows of
@@ -423,8 +434,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     tri_inverse_64_rd(AT, LDT, X, LDX, tid);  // ends with the CTA synchronized
 
     // This member's V tile (rows past the end zeroed) and the M image read out of the Q halves.
-    wait_or_flag(&bars[1 + (r & 1)], (uint32_t)((r >> 1) & 1), fail);
-    unsigned char* vt = sm + kV + (r & 1) * 16384;
+    wait_or_flag(&bars[1 + (rl & 1)], (uint32_t)((rl >> 1) & 1), fail);
+    unsigned char* vt = sm + kV + (rl & 1) * 16384;
     if (L < kChunk) {
       zero_tail(vt, L, tid);
       zero_tail(vt + 8192, L, tid);
@@ -434,7 +445,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       // the k image (member 0) or the previous member's u blocks read out of the staging
       // region, and the q image out of the second V buffer
       bulk_wait_read<0>();
-      if (r == 0 && v1_late) issue_v(sm, bars, &tmv, hv + 1, t0, 1);  // into the q staging
+      if (rl == 0 && v1_late) issue_v(sm, bars, &tmv, hv + 1, t0, 1);  // into the q staging
     }
     __syncthreads();
     // T operand images: T diag(beta exp(G) / ||k||) (bf16) and T diag(beta) as a bf16
@@ -465,7 +476,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     // TMEM: [P; R] in columns 0..63 (lanes 0..127), u^T in 64..127 (lanes 0..127), w in
     // 128..255 (lanes 32 q .. 32 q + 15 for rows 16 q .. 16 q + 15).
     const uint32_t dw = tmem + 128, du = tmem + 64;
-    const uint32_t vb = sbase + kV + (r & 1) * 16384;
+    const uint32_t vb = sbase + kV + (rl & 1) * 16384;
     const uint32_t id_w = idesc_bf16_f32(64, 128, false, true);
     // u^T = V^T T_hi^T + V^T T_lo^T: A is the v tile read MN-major (M = the 128 value
     // columns, K = tokens), B the T_hi and T_lo images (K-major, N = 64 tokens). Row j of
@@ -557,16 +568,16 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       }
       bulk_commit();
     }
-    if (tid == 0 && r + 2 < p.HG) {  // this V buffer serves member r + 2 once the copies read it
+    if (tid == 0 && rl + 2 < nr) {  // this V buffer serves member r + 2 once the copies read it
       bulk_wait_read<0>();
-      issue_v(sm, bars, &tmv, hv + 2, t0, r + 2);
+      issue_v(sm, bars, &tmv, hv + 2, t0, rl + 2);
     }
   }
 
   if (tid == 0) {
     bulk_wait_read<0>();  // every image read out (the grid's end completes the writes)
-    for (int r = max(0, p.HG - 2); r < p.HG; ++r)  // (all V loads were consumed; bounded)
-      mbar_wait(&bars[1 + (r & 1)], (uint32_t)((r >> 1) & 1), kWaitIters);
+    for (int rl = max(0, nr - 2); rl < nr; ++rl)  // (all V loads were consumed; bounded)
+      mbar_wait(&bars[1 + (rl & 1)], (uint32_t)((rl >> 1) & 1), kWaitIters);
     if (*fail) set_status(p.status, GDN_DEV_TIMEOUT);
   }
   tc_fence_before();
@@ -585,7 +596,8 @@ bool launch_tc_intra(const Params& p, cudaStream_t s) {
       !encode_rows_tmap(&tmv, p.v, rows, p.Hv, p.D))
     return false;
   ensure_smem_limit((const void*)tc_intra_kernel, (int)kSmemBytes);
-  return launch_pdl(tc_intra_kernel, dim3(p.H, p.nt_max), dim3(kThreads), kSmemBytes, s, p, tmk,
+  return launch_pdl(tc_intra_kernel, dim3(p.H, p.nt_max + p.split_slots), dim3(kThreads),
+                    kSmemBytes, s, p, tmk,
                     tmq, tmv) == cudaSuccess;
 }
 

@@ -264,6 +264,21 @@ def test_one_sequence_tiles_requested_before_the_table():
     assert bool(torch.all(out == 7.0)) and torch.equal(fin, d["initial_state"])
 
 
+@pytest.mark.parametrize("H,Hv,T", [(8, 16, 2600), (4, 16, 5000), (2, 16, 9800)])
+def test_last_wave_split_by_value_heads(H, Hv, T):
+    """Shapes whose intra grid (key heads x chunk slots, two CTAs per SM) ends in a partial
+    wave, for 2, 4 and 8 value heads per key head: the slots of that wave are taken by two
+    CTAs each, one per half of the value heads. Every head still matches the oracle."""
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    x = make_inputs(2, seed=5, H=H, Hv=Hv, T=T)
+    items, places = H * x["nt_max"], 2 * sms
+    if not (items > places and items % places):
+        pytest.skip("no partial last wave for this shape on this GPU")
+    o, f = run_gpu(x, out_dtype=torch.float32)
+    o_ref, f_ref = run_oracle(x)
+    check_parity(x, o, f, o_ref, f_ref)
+
+
 def test_status_word_reports_bad_inputs_without_fault():
     x = make_inputs(2, seed=1, T=256, H=2, Hv=2)
     d = to_dev(x)
