@@ -252,8 +252,13 @@ def test_one_sequence_tiles_requested_before_the_table():
     ref_t, _, _ = build_chunk_table(cu, x["nt_max"])
     table = torch.tensor(ref_t, dtype=torch.int32, device="cuda")
     o2, f2 = B.gdn_chunk_fwd(*args, cu_d, chunk_indices=table, out_dtype=torch.float32)
+    built = torch.full_like(table, 12345)  # built into the caller's buffer: the early path
+    o3, f3 = B.gdn_chunk_fwd(*args, cu_d, chunk_indices=built, build_chunk_indices=True,
+                             out_dtype=torch.float32)
     torch.cuda.synchronize()
     assert torch.equal(o1[37:470], o2[37:470]) and torch.equal(f1, f2)
+    assert torch.equal(o1[37:470], o3[37:470]) and torch.equal(f1, f3)
+    assert built.cpu().tolist() == ref_t
     o_ref, f_ref = run_oracle(dict(x, cu_seqlens=torch.tensor(cu, dtype=torch.int32)))
     assert ratio(o1[37:470], o_ref[37:470]) <= TOL_BF16 and ratio(f1, f_ref) <= TOL_BF16
     out = torch.full((x["T"], x["Hv"], 128), 7.0, device="cuda")
