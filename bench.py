@@ -170,7 +170,7 @@ NCU_TRAFFIC = {
               "sha1": "5ca9466ac1045ce7ec35eeb70ae6c304d02d02df", "bytes": 191367936,
               "profile": "profiles/scan_kernel_T4096_H16_Hv32.md"},
     "intra": {"source": "gated_delta_rule_chunk_gb300/csrc/k_tc_intra.cu",
-              "sha1": "7a73f88928fee7c4c5899d8c512a5668ea728ff5", "bytes": 185078528,
+              "sha1": "fec6070c3e581071973e34126155a0a22ee60515", "bytes": 185078528,
               "profile": "profiles/tc_intra_kernel_T4096_H16_Hv32.md"},
 }
 NCU_WORKLOAD = 2

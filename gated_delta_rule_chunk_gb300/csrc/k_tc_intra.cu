@@ -42,7 +42,9 @@
 //
 // One CTA of 8 warps per (key head, chunk); ~113 KB of shared memory and 256 TMEM
 // columns, so two CTAs share an SM and hide each other's latency. Warps w and w + 4
-// read the same TMEM lane quarter and split its columns.
+// read the same TMEM lane quarter and split its columns. The chunk slots of the grid's
+// last, partial wave can be split (split_slots): two CTAs per slot, one per half of the
+// group's value heads, so that the wave ends sooner.
 #include <cuda.h>
 
 #include "gdn_common.cuh"
