@@ -227,15 +227,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  if (early) {
-    pdl_wait();  // the status word is cleared and the table written from here on
-    pdl_release();
-    if (tid == 0) {  // cross-check: the table maps slot s to chunk s of sequence 0
-      const int2 e = p.chunk_table[slot];
-      if (e.x != 0 || e.y != slot) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
-    }
-  }
-  if (tid == kMStoreThread && p.pf_ahead > 0) {
+  auto prefetch_next_wave = [&]() {
+    if (tid != kMStoreThread || p.pf_ahead <= 0) return;
     // L2 prefetch of the tiles of the slot about one wave ahead, which the CTA that next
     // takes this SM is likely to hold, so that its loads hit L2
     const int s1 = slot + p.pf_ahead;
@@ -263,8 +256,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
         bulk_prefetch_l2(p.beta + go, gb);
       }
     }
-  }
-
+  };
+  if (!early) prefetch_next_wave();
   // Gates of group member r and their in-chunk inclusive cumsum (warp 0, 2 rows per lane).
   auto gates = [&](int r) {
     const size_t sl = (size_t)wslot * p.Hv + h * p.HG + r;
@@ -347,6 +340,18 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   if (writes_img && p.q16) f16_image(sm + kKQ + 8192, qstage, QR);
   fence_async_smem();
   __syncthreads();
+  if (early) {
+    // (the tiles, [P; R] and the images did not need the chunk-table kernel's output)
+    pdl_wait();  // the status word is cleared and the table written from here on
+    pdl_release();
+    if (tid == 0) {  // cross-check: the table maps slot s to chunk s of sequence 0
+      const int2 e = p.chunk_table[slot];
+      if (e.x != 0 || e.y != slot) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
+    }
+  }
+  if (early) prefetch_next_wave();  // (it reads the chunk table)
+
+
   if (tid == 0) {
     const size_t img = ((size_t)wslot * p.H + h) * 64 * kDk * 2;
     if (writes_img && dbg_ok(wslot < p.nt_max && h < p.H, p.status)) {
