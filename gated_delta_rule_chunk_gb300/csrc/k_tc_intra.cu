@@ -167,6 +167,7 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   // bounds are sanitized here exactly as the chunk-table kernel does, so the tiles (the
   // caller's inputs) are requested while that kernel still runs. Other slots are sentinels.
   bool early = false;
+  int seq_s0 = 0, seq_nch = 0;  // (the one sequence's start and chunk count)
   if (p.early_one) {
     const int s0 = p.cu ? min(max(p.cu[0], 0), p.T) : 0;
     const int e0 = p.cu ? max(min(max(p.cu[1], 0), p.T), s0) : p.T;
@@ -176,6 +177,8 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
       return;      // what that kernel wrote once this grid is done
     }
     early = true;
+    seq_s0 = s0;
+    seq_nch = nch;
     t0 = s0 + kChunk * slot;
     L = min(kChunk, e0 - t0);
     wslot = slot;
@@ -233,7 +236,9 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     // takes this SM is likely to hold, so that its loads hit L2
     const int s1 = slot + p.pf_ahead;
     int t1 = -1;
-    if (s1 < p.nt_max) {
+    if (early) {  // (slot s1 is chunk s1 of the one sequence)
+      if (s1 < seq_nch) t1 = seq_s0 + kChunk * s1;
+    } else if (s1 < p.nt_max) {
       const int2 e = p.chunk_table[s1];
       if (e.x >= 0 && e.x < p.N) {
         const SeqView sv1 = seq_view(p, e.x);
@@ -341,15 +346,15 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
   fence_async_smem();
   __syncthreads();
   if (early) {
-    // (the tiles, [P; R] and the images did not need the chunk-table kernel's output)
-    pdl_wait();  // the status word is cleared and the table written from here on
+    // Nothing up to the end of this CTA reads what the chunk-table kernel writes, and only
+    // the status word is written by both: it is written here only after the wait at the
+    // end (the debug build's index checks may write it anywhere, so that build waits here).
+#ifdef GDN_DEBUG
+    pdl_wait();
+#endif
     pdl_release();
-    if (tid == 0) {  // cross-check: the table maps slot s to chunk s of sequence 0
-      const int2 e = p.chunk_table[slot];
-      if (e.x != 0 || e.y != slot) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
-    }
+    prefetch_next_wave();
   }
-  if (early) prefetch_next_wave();  // (it reads the chunk table)
 
 
   if (tid == 0) {
@@ -581,6 +586,15 @@ tc_intra_kernel(const __grid_constant__ Params p, const __grid_constant__ CUtens
     }
   }
 
+  if (early) {
+#ifndef GDN_DEBUG
+    pdl_wait();  // the status word is cleared and the table written from here on
+#endif
+    if (tid == 0) {  // cross-check: the table maps slot s to chunk s of sequence 0
+      const int2 e = p.chunk_table[slot];
+      if (e.x != 0 || e.y != slot) set_status(p.status, GDN_DEV_BAD_CHUNK_TABLE);
+    }
+  }
   if (tid == 0) {
     bulk_wait_read<0>();  // every image read out (the grid's end completes the writes)
     for (int rl = max(0, nr - 2); rl < nr; ++rl)  // (all V loads were consumed; bounded)
