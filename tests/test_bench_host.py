@@ -37,6 +37,23 @@ def test_stage_boundary_bytes():
     assert bench.algorithmic_bytes(x) == 32 * MiB + 32 * MiB + 32 * MiB + MiB + 4 * MiB
 
 
+def test_traffic_entries_are_documented_captures():
+    """Each kernel's recorded DRAM traffic names its source file and the profile summary of
+    the capture, and that summary names the source revision (SHA-1) the bytes were taken
+    on; the bytes are at least the stage's compulsory bytes (a capture cannot move less)."""
+    import re
+    x = make_inputs(bench.NCU_WORKLOAD)
+    sb = bench.method_stage_bytes(x)
+    for stage, e in bench.NCU_TRAFFIC.items():
+        assert os.path.exists(os.path.join(bench.ROOT, e["source"])), stage
+        prof = os.path.join(bench.ROOT, e["profile"])
+        assert os.path.exists(prof), stage
+        assert re.fullmatch(r"[0-9a-f]{40}", e["sha1"]), stage
+        with open(prof) as f:
+            assert e["sha1"] in f.read(), stage
+        assert e["bytes"] >= sb[stage], stage
+
+
 def test_backward_roofline_arithmetic():
     # T = 4096, H = 16, Hv = 32, d = 128, bf16 q/k/v, fp32 upstream and output gradients
     x = make_inputs(2)
